@@ -1,0 +1,348 @@
+"""Pins of the CPU oracle against things other than itself (no GPU needed).
+
+Each test checks the oracle against a value the Beam launch post prints, a
+closed form, a brute-force enumeration, or a library routine -- never
+against a retyped copy of the oracle's own formula.  Routing rule (Beam
+post, section "Mixture of Experts"): sigmoid scores over 256 experts, 8
+groups of 32 ranked by the sum of each group's two best scores, best 4
+groups kept, top-8 experts inside them, normalised weights times 2.5, no
+shared expert.
+"""
+import itertools
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+from scipy.special import expit
+
+import oracle
+from group_limited_routing_03_b300 import inputs
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+E, G, KG, K, SCALE = 256, 8, 4, 8, 2.5
+
+
+# --------------------------------------------------------------------------
+# Decoders
+# --------------------------------------------------------------------------
+def test_decode_e4m3_matches_torch_all_codes():
+    codes = torch.arange(256, dtype=torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = np.array([oracle.decode_e4m3(c) for c in range(256)])
+    np.testing.assert_array_equal(np.isnan(got), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    np.testing.assert_array_equal(got[ok], ref[ok])
+
+
+def test_decode_e2m1_matches_ocp_table():
+    # OCP Microscaling Formats spec, FP4 E2M1: the eight magnitudes.
+    table = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    for c in range(16):
+        want = table[c & 7] * (-1.0 if c & 8 else 1.0)
+        assert oracle.decode_e2m1(c) == want, c
+
+
+def test_decode_bf16_matches_torch():
+    rng = np.random.default_rng(5)
+    bits = np.concatenate([rng.integers(0, 65536, 4000), [0, 0x8000, 0x3F80, 0x7F7F, 0x0001]])
+    ref = torch.from_numpy(bits.astype(np.int32).astype(np.int16)).view(torch.bfloat16).double().numpy()
+    got = np.array([oracle.decode_bf16(int(b)) for b in bits])
+    fin = np.isfinite(ref)
+    np.testing.assert_array_equal(got[fin], ref[fin])
+
+
+# --------------------------------------------------------------------------
+# Routing
+# --------------------------------------------------------------------------
+def _rand_router(T, H, seed, bias=False):
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((T, H)).astype(np.float32)
+    w = (rng.standard_normal((E, H)) / np.sqrt(H)).astype(np.float32)
+    b = rng.uniform(0, 0.3, E).astype(np.float32) if bias else None
+    return x, w, b
+
+
+def test_scores_match_library_matmul_and_expit():
+    x, w, _ = _rand_router(16, 96, 1)
+    r = oracle.route(x, w, want_scores=True, want_logits=True)
+    lg = x.astype(np.float64) @ w.astype(np.float64).T
+    np.testing.assert_allclose(r["logits"], lg, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(r["scores"], expit(lg), rtol=1e-13, atol=0)
+
+
+def _brute_force_route(sel, s):
+    """Independent statement of the rule: enumerate all C(8,4)=70 group
+    subsets, keep one with the largest total group score (lowest indices on
+    a tie), then fully sort that subset's experts."""
+    per = E // G
+    gscore = []
+    for j in range(G):
+        top = sorted(sel[j * per:(j + 1) * per], reverse=True)
+        gscore.append(top[0] + top[1])
+    best = None
+    for sub in itertools.combinations(range(G), KG):  # lexicographic order
+        tot = sum(gscore[j] for j in sub)
+        if best is None or tot > best[0]:
+            best = (tot, sub)
+    cand = [e for j in best[1] for e in range(j * per, (j + 1) * per)]
+    chosen = sorted(cand, key=lambda e: (-sel[e], e))[:K]
+    ssum = sum(s[e] for e in chosen)
+    return chosen, [s[e] / ssum * SCALE for e in chosen], best[1]
+
+
+@pytest.mark.parametrize("use_bias", [False, True])
+def test_route_equals_brute_force_70_subsets(use_bias):
+    x, w, b = _rand_router(48, 64, 2 + use_bias, bias=use_bias)
+    r = oracle.route(x, w, b, want_scores=True)
+    n_binding = 0
+    for t in range(x.shape[0]):
+        s = r["scores"][t]
+        sel = s + (b.astype(np.float64) if b is not None else 0.0)
+        ids, wts, sub = _brute_force_route(list(sel), list(s))
+        assert list(r["ids"][t]) == ids
+        np.testing.assert_allclose(r["weights"][t], wts, rtol=1e-14)
+        glob = sorted(range(E), key=lambda e: (-sel[e], e))[:K]
+        n_binding += set(glob) != set(ids)
+    assert n_binding > 0  # group limiting changed at least one token's choice
+
+
+def test_route_ties_follow_lower_index_rule():
+    # Integer logits: x = e_0 basis vector, Wr[:, 0] small integers -> many
+    # exact ties in the scores; the brute force resolves them by lower index.
+    rng = np.random.default_rng(11)
+    H = 8
+    T = 40
+    x = np.zeros((T, H), np.float32)
+    w = np.zeros((E, H), np.float32)
+    for t in range(T):
+        x[t, t % H] = 1.0
+    w[:, :] = rng.integers(-2, 3, (E, H)).astype(np.float32)
+    r = oracle.route(x, w, want_scores=True)
+    for t in range(T):
+        s = r["scores"][t]
+        ids, wts, _ = _brute_force_route(list(s), list(s))
+        assert list(r["ids"][t]) == ids
+        np.testing.assert_allclose(r["weights"][t], wts, rtol=1e-14)
+
+
+def test_zero_input_closed_form():
+    x = np.zeros((5, 32), np.float32)
+    w = np.random.default_rng(0).standard_normal((E, 32)).astype(np.float32)
+    r = oracle.route(x, w)
+    # every score is exactly 0.5: groups 0..3 kept, experts 0..7, equal weights
+    assert (r["ids"] == np.arange(8)).all()
+    assert (r["weights"] == SCALE / 8).all()
+    assert (r["margin"] == 0).all()
+
+
+def test_group_limit_binds_designed_scores():
+    # One strong expert per group: e_j = 32j+7 with logit 3+0.1j, all others
+    # -5.  Global top-8 would take all eight strong experts; the group rule
+    # keeps groups 4..7 only, so 4 strong experts + the 4 lowest-index fillers.
+    H = 4
+    x = np.zeros((1, H), np.float32)
+    x[0, 0] = 1.0
+    c = np.full(E, -5.0)
+    for j in range(G):
+        c[32 * j + 7] = 3.0 + 0.1 * j
+    w = np.zeros((E, H), np.float32)
+    w[:, 0] = c.astype(np.float32)
+    r = oracle.route(x, w)
+    want = [231, 199, 167, 135, 128, 129, 130, 131]
+    assert list(r["ids"][0]) == want
+    cs = w[want, 0].astype(np.float64)
+    s = expit(cs)
+    np.testing.assert_allclose(r["weights"][0], s / s.sum() * SCALE, rtol=1e-14)
+    # margins: group 4th - 5th = s(3.4) - s(3.3); expert 8th - 9th = 0 (equal fillers)
+    c4, c3 = (float(np.float32(v)) for v in (3.0 + 0.1 * 4, 3.0 + 0.1 * 3))
+    np.testing.assert_allclose(r["margin_group"][0], expit(c4) - expit(c3), rtol=1e-12)
+    assert r["margin_expert"][0] == 0.0
+
+
+def test_bias_selects_but_does_not_weight():
+    # All logits 0 (s = 0.5); a bias on experts 200..203 (group 6) and
+    # 40..43 (group 1) moves the selection there; weights stay equal
+    # because they use the unbiased scores.
+    x = np.zeros((1, 8), np.float32)
+    w = np.zeros((E, 8), np.float32)
+    b = np.zeros(E, np.float32)
+    b[200:204] = [0.9, 0.8, 0.7, 0.6]
+    b[40:44] = [0.5, 0.4, 0.3, 0.2]
+    r = oracle.route(x, w, b)
+    assert list(r["ids"][0]) == [200, 201, 202, 203, 40, 41, 42, 43]
+    assert (r["weights"][0] == SCALE / 8).all()
+
+
+def test_invariants_on_tiny_workload():
+    wl = inputs.workload("tiny")
+    d = inputs.generate(wl, "cpu", experts=False)
+    r = oracle.route(d["x"].numpy(), d["router_w"].numpy(), want_scores=True)
+    ids, wts = r["ids"], r["weights"]
+    for t in range(wl.T):
+        assert len(set(ids[t])) == K
+        groups = set(int(e) // 32 for e in ids[t])
+        assert len(groups) <= KG
+        assert (wts[t] > 0).all()
+        assert abs(wts[t].sum() - SCALE) <= 1e-12
+        sel = r["scores"][t][ids[t]]
+        assert (np.diff(sel) <= 0).all()  # best first
+    # the group rule binds somewhere on this workload too
+    glob = np.argsort(-r["scores"], axis=1, kind="stable")[:, :K]
+    assert any(set(glob[t]) != set(ids[t]) for t in range(wl.T))
+
+
+# --------------------------------------------------------------------------
+# Experts and combine
+# --------------------------------------------------------------------------
+def _np_swiglu_mlp(x, wg, wu, wd):
+    a = x @ wg.T
+    u = x @ wu.T
+    return (a * expit(a) * u) @ wd.T
+
+
+def test_expert_ffn_f32_matches_numpy():
+    rng = np.random.default_rng(3)
+    H, I, n = 64, 48, 5
+    x = rng.standard_normal((n, H)).astype(np.float32)
+    wg, wu = (rng.standard_normal((I, H)) * 0.1).astype(np.float32), (rng.standard_normal((I, H)) * 0.1).astype(np.float32)
+    wd = (rng.standard_normal((H, I)) * 0.1).astype(np.float32)
+    got, h = oracle.expert_ffn(x, wg, wu, wd, want_h=True)
+    ref = _np_swiglu_mlp(*(a.astype(np.float64) for a in (x, wg, wu, wd)))
+    np.testing.assert_allclose(got, ref, rtol=1e-11, atol=1e-13)
+    a = x.astype(np.float64) @ wg.astype(np.float64).T
+    np.testing.assert_allclose(h, a * expit(a) * (x.astype(np.float64) @ wu.astype(np.float64).T), rtol=1e-11, atol=1e-14)
+
+
+def test_expert_ffn_bf16_matches_numpy():
+    rng = np.random.default_rng(4)
+    H, I, n = 32, 64, 3
+    tx = torch.from_numpy(rng.standard_normal((n, H)).astype(np.float32)).bfloat16()
+    tw = [torch.from_numpy((rng.standard_normal(s) * 0.05).astype(np.float32)).bfloat16()
+          for s in ((I, H), (I, H), (H, I))]
+    got = oracle.expert_ffn(inputs.bf16_bits(tx), *(inputs.bf16_bits(t) for t in tw))
+    ref = _np_swiglu_mlp(tx.double().numpy(), *(t.double().numpy() for t in tw))
+    np.testing.assert_allclose(got, ref, rtol=1e-11, atol=1e-13)
+
+
+def _decode_nvfp4_independent(packed, sf, g):
+    """Decode NVFP4 storage with torch's E4M3 conversion and the OCP table."""
+    table = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+    p = packed.numpy()
+    lo, hi = p & 0xF, p >> 4
+    codes = np.stack([lo, hi], -1).reshape(p.shape[0], -1)
+    val = table[codes & 7] * np.where(codes & 8, -1.0, 1.0)
+    sc = sf.view(torch.float8_e4m3fn).double().numpy()
+    return val * np.repeat(sc, 16, axis=1) * g
+
+
+def test_expert_ffn_nvfp4_matches_independent_decode():
+    rng = np.random.default_rng(6)
+    H, I, n = 64, 32, 4
+    x = torch.from_numpy(rng.standard_normal((n, H)).astype(np.float32)).bfloat16()
+    mats, dec = [], []
+    for shp in ((I, H), (I, H), (H, I)):
+        p, s, g = inputs.quantize_nvfp4(torch.from_numpy(rng.standard_normal(shp).astype(np.float32) * 0.02))
+        mats.append((p, s, g))
+        dec.append(_decode_nvfp4_independent(p, s, g))
+    got = oracle.expert_ffn(inputs.bf16_bits(x), *(m[0].numpy() for m in mats),
+                            scales=[m[1].numpy() for m in mats],
+                            global_scales=[m[2] for m in mats])
+    ref = _np_swiglu_mlp(x.double().numpy(), *dec)
+    np.testing.assert_allclose(got, ref, rtol=1e-11, atol=1e-14)
+
+
+def test_nvfp4_low_nibble_is_even_k():
+    # byte 0x72: low nibble 0x2 (E2M1 1.0) is element k=0, high 0x7 (6.0) is k=1
+    H, I = 16, 16
+    wg = np.zeros((I, H // 2), np.uint8)
+    wg[0, 0] = 0x72
+    e4m3_one = 0x38  # 1.0 in E4M3
+    sg = np.full((I, H // 16), e4m3_one, np.uint8)
+    zeros = np.zeros((I, H // 2), np.uint8)
+    wd = np.zeros((H, I // 2), np.uint8)
+    wd[0, 0] = 0x02  # Wd[0, 0] = 1.0
+    sd = np.full((H, I // 16), e4m3_one, np.uint8)
+    x = np.zeros((1, H), np.float32)
+    x[0, 1] = 1.0
+    # gate pre-activation for i=0 is Wg[0, 1] = 6.0; up is 0 -> h = 0
+    out, h = oracle.expert_ffn(x.astype(np.float32), wg, wg, wd, scales=[sg, sg, sd],
+                               global_scales=[1.0, 1.0, 1.0], want_h=True)
+    np.testing.assert_allclose(h[0, 0], 6.0 * expit(6.0) * 6.0, rtol=1e-14)
+    np.testing.assert_allclose(out[0, 0], h[0, 0], rtol=1e-14)
+
+
+def test_identical_experts_closed_form():
+    # Every expert has the same weights, so y = 2.5 * f(x) for any routing.
+    wl = inputs.workload("tiny", T=12, H=64, I=32)
+    d = inputs.generate(wl, "cpu", experts=False)
+    rng = np.random.default_rng(8)
+    wg = (rng.standard_normal((wl.I, wl.H)) * 0.1).astype(np.float32)
+    wu = (rng.standard_normal((wl.I, wl.H)) * 0.1).astype(np.float32)
+    wd = (rng.standard_normal((wl.H, wl.I)) * 0.1).astype(np.float32)
+    x = d["x"].numpy()
+    res = oracle.forward(x, d["router_w"].numpy(), None, [wg] * E, [wu] * E, [wd] * E)
+    ref = SCALE * _np_swiglu_mlp(*(a.astype(np.float64) for a in (x, wg, wu, wd)))
+    np.testing.assert_allclose(res["y"], ref, rtol=1e-11, atol=1e-13)
+
+
+def test_one_hot_scores_closed_form_output():
+    # Logits set exactly by design (x = basis vector): experts 0..3 and
+    # 32..35 get +4, the rest -4 -> ids {0..3, 32..35}, weights 2.5/8 each,
+    # y = (2.5/8) * sum of those experts' MLPs.
+    H, I = 16, 8
+    x = np.zeros((1, H), np.float32)
+    x[0, 3] = 1.0
+    wr = np.full((E, H), 0.0, np.float32)
+    wr[:, 3] = -4.0
+    chosen = [0, 1, 2, 3, 32, 33, 34, 35]
+    wr[chosen, 3] = 4.0
+    rng = np.random.default_rng(9)
+    wg = (rng.standard_normal((E, I, H)) * 0.2).astype(np.float32)
+    wu = (rng.standard_normal((E, I, H)) * 0.2).astype(np.float32)
+    wd = (rng.standard_normal((E, H, I)) * 0.2).astype(np.float32)
+    res = oracle.forward(x, wr, None, wg, wu, wd)
+    assert list(res["route"]["ids"][0]) == chosen
+    ref = sum(_np_swiglu_mlp(x.astype(np.float64), wg[e].astype(np.float64), wu[e].astype(np.float64), wd[e].astype(np.float64)) for e in chosen) * (SCALE / 8)
+    np.testing.assert_allclose(res["y"], ref, rtol=1e-11, atol=1e-14)
+
+
+def test_zero_input_gives_zero_output():
+    wl = inputs.workload("tiny", T=4)
+    d = inputs.generate(wl, "cpu")
+    x = np.zeros((4, wl.H), np.float32)
+    res = oracle.forward(x, d["router_w"].numpy(), None, d["gate"].numpy(), d["up"].numpy(), d["down"].numpy())
+    assert (res["y"] == 0).all()
+
+
+# --------------------------------------------------------------------------
+# Dispatch
+# --------------------------------------------------------------------------
+def test_dispatch_matches_numpy_stable_sort():
+    rng = np.random.default_rng(10)
+    ids = rng.integers(0, E, (300, K)).astype(np.int32)
+    d = oracle.dispatch(ids)
+    flat = ids.reshape(-1)
+    np.testing.assert_array_equal(d["counts"], np.bincount(flat, minlength=E))
+    np.testing.assert_array_equal(d["offsets"], np.concatenate([[0], np.cumsum(np.bincount(flat, minlength=E))]))
+    np.testing.assert_array_equal(d["perm"], np.argsort(flat, kind="stable"))
+    np.testing.assert_array_equal(d["perm"][d["pos"]], np.arange(flat.size))
+
+
+# --------------------------------------------------------------------------
+# Shapes printed on the pages
+# --------------------------------------------------------------------------
+def test_workload_shapes_match_published_figures():
+    with open(os.path.join(GOLDEN, "beam_moe_shapes.json")) as f:
+        g = json.load(f)
+    wl = inputs.workload("decode")
+    assert (wl.H, wl.I, wl.E) == (g["hidden_size"], g["expert_intermediate_size"], g["experts_per_moe_layer"])
+    assert (inputs.N_GROUP, inputs.TOPK_GROUP, inputs.TOP_K) == (g["groups"], g["groups_kept"], g["experts_per_token"])
+    assert wl.E // inputs.N_GROUP == g["experts_per_group"]
+    assert inputs.ROUTED_SCALE == g["routed_scale"]
+    per_expert = 3 * wl.H * wl.I  # gate, up, down
+    assert abs(per_expert - g["params_per_expert_approx"]) / g["params_per_expert_approx"] < 0.01
+    moe_layers = g["decoder_layers"] - g["dense_mlp_layers"]
+    share = moe_layers * wl.E * per_expert / g["total_params"] * 100
+    assert abs(share - g["expert_share_of_params_percent"]) < 0.1

@@ -1,0 +1,243 @@
+"""Group-limited Mixture-of-Experts block (Beam-shaped) on one B300.
+
+Thin Python binding of the C ABI in ``include/beam_moe.h``: every function
+here only marshals torch tensors (device memory, streams) into the calls of
+``libbeam_moe.so``; every step of the computation runs in the library's CUDA
+kernels.  There is no CPU fallback: a missing or unloadable library raises.
+
+The block (Beam launch post, "Willkommen Beam ..." (spke.com), section
+"Mixture of Experts"): sigmoid router over 256 experts, 8 groups of 32 ranked
+by the sum of their two best scores, best 4 groups kept, top-8 experts inside
+them, weights normalised and scaled by 2.5, SwiGLU experts, no shared expert.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "BeamError", "Shape", "shape", "workspace_size", "workspace_layout", "alloc_workspace",
+    "beam_moe_route", "beam_moe_dispatch", "beam_moe_experts", "beam_moe_forward",
+    "beam_moe_read_device_status", "beam_moe_debug_timeout", "beam_status_string", "BeamMoE",
+    "library_path", "load",
+]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "libbeam_moe.so")
+
+BEAM_OK, BEAM_ERR_INVALID_ARG, BEAM_ERR_UNSUPPORTED, BEAM_ERR_WORKSPACE = 0, 1, 2, 3
+BEAM_ERR_CUDA, BEAM_ERR_TIMEOUT, BEAM_ERR_DEVICE_CHECK = 4, 5, 6
+BEAM_F32, BEAM_BF16, BEAM_NVFP4 = 0, 1, 2
+
+
+class BeamError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {beam_status_string(code)} (status {code})")
+
+
+class Shape(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int32), ("H", ctypes.c_int32), ("I", ctypes.c_int32), ("E", ctypes.c_int32),
+                ("n_group", ctypes.c_int32), ("topk_group", ctypes.c_int32), ("top_k", ctypes.c_int32),
+                ("routed_scale", ctypes.c_float)]
+
+
+class _ExpertWeights(ctypes.Structure):
+    _fields_ = [("dtype", ctypes.c_int), ("gate", ctypes.c_void_p), ("up", ctypes.c_void_p),
+                ("down", ctypes.c_void_p), ("gate_sf", ctypes.c_void_p), ("up_sf", ctypes.c_void_p),
+                ("down_sf", ctypes.c_void_p), ("gate_gs", ctypes.c_void_p), ("up_gs", ctypes.c_void_p),
+                ("down_gs", ctypes.c_void_p)]
+
+
+class _WsLayout(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_size_t) for n in ("status", "counts", "offsets", "perm", "pos", "xp", "h", "yr",
+                                               "total")]
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load():
+    """Load libbeam_moe.so (built in-tree by ``__graft_entry__.build()``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise ImportError(f"{_LIB_PATH} is missing: build the CUDA library first (__graft_entry__.build())")
+    lib = ctypes.CDLL(_LIB_PATH)
+    vp, sz, i32, u32 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_uint32
+    sp = ctypes.POINTER(Shape)
+    lib.beam_moe_workspace_size.argtypes = [sp, i32]
+    lib.beam_moe_workspace_size.restype = sz
+    lib.beam_moe_workspace_layout.argtypes = [sp, i32, ctypes.POINTER(_WsLayout)]
+    lib.beam_moe_route.argtypes = [sp, vp, i32, vp, vp, vp, vp, vp, sz, vp]
+    lib.beam_moe_dispatch.argtypes = [sp, vp, vp, sz, vp]
+    lib.beam_moe_experts.argtypes = [sp, vp, i32, ctypes.POINTER(_ExpertWeights), vp, vp, vp, vp, sz, vp]
+    lib.beam_moe_forward.argtypes = [sp, vp, i32, vp, vp, ctypes.POINTER(_ExpertWeights), vp, vp, vp, vp, sz, vp]
+    lib.beam_moe_read_device_status.argtypes = [vp, ctypes.POINTER(u32), vp]
+    lib.beam_moe_debug_timeout.argtypes = [vp, sz, u32, vp]
+    lib.beam_status_string.argtypes = [i32]
+    lib.beam_status_string.restype = ctypes.c_char_p
+    for n in ("beam_moe_workspace_layout", "beam_moe_route", "beam_moe_dispatch", "beam_moe_experts",
+              "beam_moe_forward", "beam_moe_read_device_status", "beam_moe_debug_timeout"):
+        getattr(lib, n).restype = i32
+    _lib = lib
+    return lib
+
+
+# --------------------------------------------------------------------------
+# marshalling helpers
+# --------------------------------------------------------------------------
+def shape(T, H, I, E=256, n_group=8, topk_group=4, top_k=8, routed_scale=2.5) -> Shape:
+    return Shape(T, H, I, E, n_group, topk_group, top_k, routed_scale)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("expected a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError("tensor must live on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("tensor must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _act_dtype(t) -> int:
+    if t.dtype == torch.float32:
+        return BEAM_F32
+    if t.dtype == torch.bfloat16:
+        return BEAM_BF16
+    raise TypeError(f"activations must be float32 or bfloat16, got {t.dtype}")
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _weights(w: dict) -> _ExpertWeights:
+    ew = _ExpertWeights()
+    if w["gate"].dtype == torch.bfloat16:
+        ew.dtype = BEAM_BF16
+    elif w["gate"].dtype == torch.uint8:
+        ew.dtype = BEAM_NVFP4
+    else:
+        raise TypeError(f"expert weights must be bfloat16 or packed NVFP4 (uint8), got {w['gate'].dtype}")
+    for name in ("gate", "up", "down", "gate_sf", "up_sf", "down_sf", "gate_gs", "up_gs", "down_gs"):
+        t = w.get(name)
+        setattr(ew, name, None if t is None else _ptr(t).value)
+    return ew
+
+
+def _check(code: int, where: str):
+    if code != BEAM_OK:
+        raise BeamError(code, where)
+
+
+def _wdtype(w) -> int:
+    if isinstance(w, str):
+        return {"bf16": BEAM_BF16, "nvfp4": BEAM_NVFP4}[w]
+    return BEAM_NVFP4 if w["gate"].dtype == torch.uint8 else BEAM_BF16
+
+
+# --------------------------------------------------------------------------
+# the C ABI, one function each
+# --------------------------------------------------------------------------
+def beam_status_string(code: int) -> str:
+    return load().beam_status_string(int(code)).decode()
+
+
+def workspace_size(sh: Shape, wdtype="bf16") -> int:
+    return int(load().beam_moe_workspace_size(ctypes.byref(sh), _wdtype(wdtype)))
+
+
+def workspace_layout(sh: Shape, wdtype="bf16") -> dict:
+    lay = _WsLayout()
+    _check(load().beam_moe_workspace_layout(ctypes.byref(sh), _wdtype(wdtype), ctypes.byref(lay)),
+           "beam_moe_workspace_layout")
+    return {n: int(getattr(lay, n)) for n, _ in _WsLayout._fields_}
+
+
+def alloc_workspace(sh: Shape, wdtype="bf16", device="cuda") -> torch.Tensor:
+    """Caller-side allocation of the workspace (the library allocates none)."""
+    n = workspace_size(sh, wdtype)
+    if n == 0:
+        raise BeamError(BEAM_ERR_UNSUPPORTED, "workspace_size")
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def beam_moe_route(sh, x, router_w, router_bias, topk_ids, topk_w, workspace, stream=None):
+    _check(load().beam_moe_route(ctypes.byref(sh), _ptr(x), _act_dtype(x), _ptr(router_w), _ptr(router_bias),
+                                 _ptr(topk_ids), _ptr(topk_w), _ptr(workspace), workspace.numel(),
+                                 _stream(stream)), "beam_moe_route")
+
+
+def beam_moe_dispatch(sh, topk_ids, workspace, stream=None):
+    _check(load().beam_moe_dispatch(ctypes.byref(sh), _ptr(topk_ids), _ptr(workspace), workspace.numel(),
+                                    _stream(stream)), "beam_moe_dispatch")
+
+
+def beam_moe_experts(sh, x, weights: dict, topk_ids, topk_w, y, workspace, stream=None):
+    ew = _weights(weights)
+    _check(load().beam_moe_experts(ctypes.byref(sh), _ptr(x), _act_dtype(x), ctypes.byref(ew), _ptr(topk_ids),
+                                   _ptr(topk_w), _ptr(y), _ptr(workspace), workspace.numel(), _stream(stream)),
+           "beam_moe_experts")
+
+
+def beam_moe_forward(sh, x, router_w, router_bias, weights: dict, y, topk_ids, topk_w, workspace, stream=None):
+    ew = _weights(weights)
+    _check(load().beam_moe_forward(ctypes.byref(sh), _ptr(x), _act_dtype(x), _ptr(router_w), _ptr(router_bias),
+                                   ctypes.byref(ew), _ptr(y), _ptr(topk_ids), _ptr(topk_w), _ptr(workspace),
+                                   workspace.numel(), _stream(stream)), "beam_moe_forward")
+
+
+def beam_moe_read_device_status(workspace, stream=None):
+    """Synchronises the stream; returns (status code, where) and clears it."""
+    where = ctypes.c_uint32(0)
+    code = load().beam_moe_read_device_status(_ptr(workspace), ctypes.byref(where), _stream(stream))
+    return int(code), int(where.value)
+
+
+def beam_moe_debug_timeout(workspace, timeout_us: int, stream=None):
+    _check(load().beam_moe_debug_timeout(_ptr(workspace), workspace.numel(), int(timeout_us), _stream(stream)),
+           "beam_moe_debug_timeout")
+
+
+# --------------------------------------------------------------------------
+# convenience: one layer with its weights and workspace
+# --------------------------------------------------------------------------
+class BeamMoE:
+    """One MoE layer: router weight/bias, expert weights and a workspace sized
+    for up to ``max_tokens`` tokens, all caller-owned torch device tensors."""
+
+    def __init__(self, router_w, router_bias, weights: dict, max_tokens: int, routed_scale=2.5):
+        self.router_w, self.router_bias, self.weights = router_w, router_bias, weights
+        self.E, self.H = router_w.shape
+        self.I = weights["gate"].shape[1]
+        self.routed_scale = routed_scale
+        self.max_tokens = max_tokens
+        self.workspace = alloc_workspace(self.shape(max_tokens), _wdtype(weights), router_w.device)
+
+    def shape(self, T):
+        return shape(T, self.H, self.I, self.E, routed_scale=self.routed_scale)
+
+    def __call__(self, x, y=None, topk_ids=None, topk_w=None, stream=None):
+        T = x.shape[0]
+        if T > self.max_tokens:
+            raise ValueError(f"{T} tokens > workspace capacity {self.max_tokens}")
+        dev = x.device
+        y = torch.empty_like(x) if y is None else y
+        topk_ids = torch.empty((T, 8), dtype=torch.int32, device=dev) if topk_ids is None else topk_ids
+        topk_w = torch.empty((T, 8), dtype=torch.float32, device=dev) if topk_w is None else topk_w
+        beam_moe_forward(self.shape(T), x, self.router_w, self.router_bias, self.weights, y, topk_ids, topk_w,
+                         self.workspace, stream)
+        return y, topk_ids, topk_w

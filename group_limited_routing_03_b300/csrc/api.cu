@@ -1,0 +1,403 @@
+// api.cu -- the C ABI declared in include/beam_moe.h: argument validation,
+// workspace carve-up, TMA descriptors and the launch sequence
+//   router -> [tile histogram] -> scan -> scatter -> gather -> gate/up GEMM
+//   -> down GEMM -> combine
+// all on the caller's stream, with no host synchronisation and no allocation.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "beam_moe.h"
+#include "moe_internal.cuh"
+
+namespace beam {
+namespace {
+
+constexpr uint64_t kDefaultTimeoutNs = 1000000000ull;  // 1 s per bounded wait
+
+// ------------------------------------------------------------------ device
+struct DeviceInfo {
+  int sms = 0;
+  int smem_optin = 0;
+  int cc_major = 0;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[64];
+bool g_dev_ok[64] = {};
+
+bool device_info(DeviceInfo& out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_dev_ok[dev]) {
+    DeviceInfo d;
+    if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
+    if (cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+      return false;
+    if (cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return false;
+    g_dev[dev] = d;
+    g_dev_ok[dev] = true;
+  }
+  out = g_dev[dev];
+  return true;
+}
+
+// ------------------------------------------------------------------ TMA
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2-D row-major bf16 matrix [rows, inner]; boxes of box_rows x 64 elements,
+// 128-byte swizzle.
+bool make_bf16_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[2] = {inner, rows};
+  const cuuint64_t strides[1] = {inner * 2};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBlockK), box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// ------------------------------------------------------------------ layout
+struct Layout {
+  size_t status, counts, offsets, chunk_prefix, tile_hist, part, perm, pos, xp, h, yr, total;
+  int n_tiles, split_cap;
+};
+
+size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
+
+void make_layout(const beam_moe_shape_t& s, Layout& L) {
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align256(off + bytes);
+    return o;
+  };
+  const size_t T = static_cast<size_t>(s.T), H = static_cast<size_t>(s.H), I = static_cast<size_t>(s.I);
+  const size_t R = T * kTopK;
+  // Activation buffers hold whole 32-row TMA boxes; rows past R are never
+  // read into a used accumulator column.
+  const size_t R_pad = (R + kBoxRows - 1) / kBoxRows * kBoxRows;
+  L.n_tiles = static_cast<int>((T + kRouterTile - 1) / kRouterTile);
+  L.split_cap = router_split_cap(s.T, s.H);
+  L.status = take(16);
+  L.counts = take(kExperts * 4);
+  L.offsets = take((kExperts + 1) * 4);
+  L.chunk_prefix = take((kExperts + 1) * 4);
+  L.tile_hist = take(static_cast<size_t>(kExperts) * L.n_tiles * 4);
+  L.part = take(L.split_cap > 1 ? static_cast<size_t>(L.split_cap) * T * kExperts * 4 : 0);
+  L.perm = take(R * 4);
+  L.pos = take(R * 4);
+  L.xp = take(R_pad * H * 2);
+  L.h = take(R_pad * I * 2);
+  L.yr = take(R_pad * H * 2);
+  L.total = off;
+}
+
+// ------------------------------------------------------------------ checks
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+beam_status_t check_shape(const beam_moe_shape_t* s) {
+  if (s == nullptr) return BEAM_ERR_INVALID_ARG;
+  if (s->T < 1 || s->H < 1 || s->I < 1) return BEAM_ERR_INVALID_ARG;
+  if (s->E != kExperts || s->n_group != kGroups || s->topk_group != kGroupsKept || s->top_k != kTopK)
+    return BEAM_ERR_UNSUPPORTED;
+  if (s->H % 128 != 0 || s->I % 128 != 0 || s->H > 65536 || s->I > 65536 || s->T > (1 << 20))
+    return BEAM_ERR_UNSUPPORTED;
+  if (!std::isfinite(s->routed_scale)) return BEAM_ERR_INVALID_ARG;
+  return BEAM_OK;
+}
+
+beam_status_t check_workspace(const beam_moe_shape_t* s, const void* ws, size_t bytes, Layout& L) {
+  make_layout(*s, L);
+  if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0 || bytes < L.total) return BEAM_ERR_WORKSPACE;
+  return BEAM_OK;
+}
+
+beam_status_t check_weights(const beam_expert_weights_t* w) {
+  if (w == nullptr) return BEAM_ERR_INVALID_ARG;
+  if (w->dtype == BEAM_BF16) {
+    if (!w->gate || !w->up || !w->down) return BEAM_ERR_INVALID_ARG;
+    if (!aligned16(w->gate) || !aligned16(w->up) || !aligned16(w->down)) return BEAM_ERR_INVALID_ARG;
+    if (w->gate_sf || w->up_sf || w->down_sf || w->gate_gs || w->up_gs || w->down_gs) return BEAM_ERR_INVALID_ARG;
+    return BEAM_OK;
+  }
+  if (w->dtype == BEAM_NVFP4) return BEAM_ERR_UNSUPPORTED;
+  return BEAM_ERR_UNSUPPORTED;
+}
+
+template <typename T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
+}
+
+beam_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? BEAM_OK : BEAM_ERR_CUDA; }
+
+// ------------------------------------------------------------------ stages
+beam_status_t run_route(const beam_moe_shape_t& s, const void* x, bool x_bf16, const float* wr, const float* bias,
+                        int32_t* ids, float* w, void* ws, const Layout& L, const DeviceInfo& d,
+                        cudaStream_t stream) {
+  RouterParams p;
+  p.x = x;
+  p.wr = wr;
+  p.bias = bias;
+  p.T = s.T;
+  p.H = s.H;
+  p.scale = s.routed_scale;
+  p.splits = router_splits(s.T, s.H, d.sms);
+  if (p.splits > L.split_cap) p.splits = L.split_cap;
+  p.n_kchunks = s.H / kRouterKChunk;
+  p.n_tiles = L.n_tiles;
+  p.part = at<float>(ws, L.part);
+  p.ids = ids;
+  p.w = w;
+  p.tile_hist = at<int32_t>(ws, L.tile_hist);
+  return cuda_status(launch_router(p, x_bf16, stream));
+}
+
+beam_status_t run_dispatch(const beam_moe_shape_t& s, const int32_t* ids, void* ws, const Layout& L, int nmax,
+                           bool hist_ready, cudaStream_t stream) {
+  const int R = s.T * kTopK;
+  cudaError_t e;
+  if (!hist_ready) {
+    e = launch_tile_hist(ids, R, L.n_tiles, at<int32_t>(ws, L.tile_hist), at<uint32_t>(ws, L.status), stream);
+    if (e != cudaSuccess) return BEAM_ERR_CUDA;
+  }
+  e = launch_dispatch(ids, R, L.n_tiles, at<int32_t>(ws, L.tile_hist), at<int32_t>(ws, L.counts),
+                      at<int32_t>(ws, L.offsets), at<int32_t>(ws, L.chunk_prefix), nmax, at<int32_t>(ws, L.perm),
+                      at<int32_t>(ws, L.pos), stream);
+  return cuda_status(e);
+}
+
+int chunk_rows(int T) {
+  int n = ((T + kBoxRows - 1) / kBoxRows) * kBoxRows;
+  return n > 256 ? 256 : n;
+}
+
+uint32_t pow2_at_least(uint32_t v) {
+  uint32_t p = 32;
+  while (p < v) p <<= 1;
+  return p;
+}
+
+beam_status_t run_experts(const beam_moe_shape_t& s, const void* x, bool x_bf16, const beam_expert_weights_t* wts,
+                          const int32_t* ids, const float* w, void* y, void* ws, const Layout& L,
+                          const DeviceInfo& d, bool hist_ready, cudaStream_t stream) {
+  const int R = s.T * kTopK;
+  const uint64_t R_pad = static_cast<uint64_t>((R + kBoxRows - 1) / kBoxRows * kBoxRows);
+  const int nmax = chunk_rows(s.T);
+  beam_status_t st = run_dispatch(s, ids, ws, L, nmax, hist_ready, stream);
+  if (st != BEAM_OK) return st;
+  __nv_bfloat16* xp = at<__nv_bfloat16>(ws, L.xp);
+  __nv_bfloat16* h = at<__nv_bfloat16>(ws, L.h);
+  __nv_bfloat16* yr = at<__nv_bfloat16>(ws, L.yr);
+  if (launch_gather(x, x_bf16, s.H, at<int32_t>(ws, L.perm), R, xp, d.sms, stream) != cudaSuccess)
+    return BEAM_ERR_CUDA;
+
+  CUtensorMap m_gate, m_up, m_down, m_xp, m_h;
+  const uint64_t E = kExperts, H = s.H, I = s.I;
+  if (!make_bf16_map(&m_gate, wts->gate, H, E * I, kBlockM) || !make_bf16_map(&m_up, wts->up, H, E * I, kBlockM) ||
+      !make_bf16_map(&m_down, wts->down, I, E * H, kBlockM) ||
+      !make_bf16_map(&m_xp, xp, H, R_pad, kBoxRows) || !make_bf16_map(&m_h, h, I, R_pad, kBoxRows))
+    return BEAM_ERR_CUDA;
+
+  const size_t budget = static_cast<size_t>(d.smem_optin) - 1024 - 256;
+  for (int mode = 0; mode < 2; ++mode) {
+    GemmParams p;
+    p.counts = at<int32_t>(ws, L.counts);
+    p.offsets = at<int32_t>(ws, L.offsets);
+    p.chunk_prefix = at<int32_t>(ws, L.chunk_prefix);
+    p.m_tiles = (mode == 0 ? s.I : s.H) / kBlockM;
+    p.a_rows_per_expert = mode == 0 ? s.I : s.H;
+    p.k_blocks = (mode == 0 ? s.H : s.I) / kBlockK;
+    p.nmax = nmax;
+    const size_t sb = gemm_stage_bytes(mode, nmax);
+    int stages = static_cast<int>(budget / sb);
+    if (stages > 8) stages = 8;
+    if (stages < 2) return BEAM_ERR_UNSUPPORTED;
+    p.stages = stages;
+    p.acc_cols = static_cast<uint32_t>(mode == 0 ? 2 * nmax : nmax);
+    int acc_stages = static_cast<int>(512 / p.acc_cols);
+    if (acc_stages > 4) acc_stages = 4;
+    if (acc_stages < 1) acc_stages = 1;
+    p.acc_stages = acc_stages;
+    p.tmem_cols = pow2_at_least(static_cast<uint32_t>(acc_stages) * p.acc_cols);
+    p.out = mode == 0 ? h : yr;
+    p.out_ld = mode == 0 ? s.I : s.H;
+    p.gs0 = nullptr;
+    p.gs1 = nullptr;
+    p.status = at<uint32_t>(ws, L.status);
+    p.timeout_ns = kDefaultTimeoutNs;
+    const size_t smem = 1024 + static_cast<size_t>(stages) * sb + (2 * stages + 2 * acc_stages + 1) * 8 + 16;
+    const cudaError_t e = mode == 0 ? launch_gemm(0, m_gate, m_up, m_xp, p, d.sms, smem, stream)
+                                    : launch_gemm(1, m_down, m_down, m_h, p, d.sms, smem, stream);
+    if (e != cudaSuccess) return BEAM_ERR_CUDA;
+  }
+  return cuda_status(launch_combine(yr, at<int32_t>(ws, L.pos), w, s.T, s.H, y, x_bf16, stream));
+}
+
+}  // namespace
+}  // namespace beam
+
+using namespace beam;
+
+extern "C" {
+
+size_t beam_moe_workspace_size(const beam_moe_shape_t* shape, beam_dtype_t wdtype) {
+  if (check_shape(shape) != BEAM_OK) return 0;
+  if (wdtype != BEAM_BF16 && wdtype != BEAM_NVFP4) return 0;
+  Layout L;
+  make_layout(*shape, L);
+  return L.total;
+}
+
+beam_status_t beam_moe_workspace_layout(const beam_moe_shape_t* shape, beam_dtype_t wdtype, beam_ws_layout_t* out) {
+  const beam_status_t st = check_shape(shape);
+  if (st != BEAM_OK) return st;
+  if (out == nullptr) return BEAM_ERR_INVALID_ARG;
+  if (wdtype != BEAM_BF16 && wdtype != BEAM_NVFP4) return BEAM_ERR_UNSUPPORTED;
+  Layout L;
+  make_layout(*shape, L);
+  out->status = L.status;
+  out->counts = L.counts;
+  out->offsets = L.offsets;
+  out->perm = L.perm;
+  out->pos = L.pos;
+  out->xp = L.xp;
+  out->h = L.h;
+  out->yr = L.yr;
+  out->total = L.total;
+  return BEAM_OK;
+}
+
+beam_status_t beam_moe_route(const beam_moe_shape_t* shape, const void* x, beam_dtype_t xdtype,
+                             const float* router_w, const float* router_bias, int32_t* topk_ids, float* topk_w,
+                             void* workspace, size_t workspace_bytes, void* stream) {
+  beam_status_t st = check_shape(shape);
+  if (st != BEAM_OK) return st;
+  if (!x || !router_w || !topk_ids || !topk_w) return BEAM_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(router_w) || !aligned16(topk_ids) || !aligned16(topk_w) ||
+      (router_bias && !aligned16(router_bias)))
+    return BEAM_ERR_INVALID_ARG;
+  if (xdtype != BEAM_F32 && xdtype != BEAM_BF16) return BEAM_ERR_UNSUPPORTED;
+  Layout L;
+  st = check_workspace(shape, workspace, workspace_bytes, L);
+  if (st != BEAM_OK) return st;
+  DeviceInfo d;
+  if (!device_info(d)) return BEAM_ERR_CUDA;
+  return run_route(*shape, x, xdtype == BEAM_BF16, router_w, router_bias, topk_ids, topk_w, workspace, L, d,
+                   static_cast<cudaStream_t>(stream));
+}
+
+beam_status_t beam_moe_dispatch(const beam_moe_shape_t* shape, const int32_t* topk_ids, void* workspace,
+                                size_t workspace_bytes, void* stream) {
+  beam_status_t st = check_shape(shape);
+  if (st != BEAM_OK) return st;
+  if (!topk_ids || !aligned16(topk_ids)) return BEAM_ERR_INVALID_ARG;
+  Layout L;
+  st = check_workspace(shape, workspace, workspace_bytes, L);
+  if (st != BEAM_OK) return st;
+  DeviceInfo d;
+  if (!device_info(d)) return BEAM_ERR_CUDA;
+  return run_dispatch(*shape, topk_ids, workspace, L, chunk_rows(shape->T), false, static_cast<cudaStream_t>(stream));
+}
+
+beam_status_t beam_moe_experts(const beam_moe_shape_t* shape, const void* x, beam_dtype_t xdtype,
+                               const beam_expert_weights_t* weights, const int32_t* topk_ids, const float* topk_w,
+                               void* y, void* workspace, size_t workspace_bytes, void* stream) {
+  beam_status_t st = check_shape(shape);
+  if (st != BEAM_OK) return st;
+  if (!x || !topk_ids || !topk_w || !y) return BEAM_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(topk_ids) || !aligned16(topk_w) || !aligned16(y)) return BEAM_ERR_INVALID_ARG;
+  if (xdtype != BEAM_F32 && xdtype != BEAM_BF16) return BEAM_ERR_UNSUPPORTED;
+  st = check_weights(weights);
+  if (st != BEAM_OK) return st;
+  Layout L;
+  st = check_workspace(shape, workspace, workspace_bytes, L);
+  if (st != BEAM_OK) return st;
+  DeviceInfo d;
+  if (!device_info(d)) return BEAM_ERR_CUDA;
+  if (d.cc_major < 10) return BEAM_ERR_UNSUPPORTED;
+  return run_experts(*shape, x, xdtype == BEAM_BF16, weights, topk_ids, topk_w, y, workspace, L, d, false,
+                     static_cast<cudaStream_t>(stream));
+}
+
+beam_status_t beam_moe_forward(const beam_moe_shape_t* shape, const void* x, beam_dtype_t xdtype,
+                               const float* router_w, const float* router_bias, const beam_expert_weights_t* weights,
+                               void* y, int32_t* topk_ids, float* topk_w, void* workspace, size_t workspace_bytes,
+                               void* stream) {
+  beam_status_t st = check_shape(shape);
+  if (st != BEAM_OK) return st;
+  if (!x || !router_w || !topk_ids || !topk_w || !y) return BEAM_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(router_w) || !aligned16(topk_ids) || !aligned16(topk_w) || !aligned16(y) ||
+      (router_bias && !aligned16(router_bias)))
+    return BEAM_ERR_INVALID_ARG;
+  if (xdtype != BEAM_F32 && xdtype != BEAM_BF16) return BEAM_ERR_UNSUPPORTED;
+  st = check_weights(weights);
+  if (st != BEAM_OK) return st;
+  Layout L;
+  st = check_workspace(shape, workspace, workspace_bytes, L);
+  if (st != BEAM_OK) return st;
+  DeviceInfo d;
+  if (!device_info(d)) return BEAM_ERR_CUDA;
+  if (d.cc_major < 10) return BEAM_ERR_UNSUPPORTED;
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  st = run_route(*shape, x, xdtype == BEAM_BF16, router_w, router_bias, topk_ids, topk_w, workspace, L, d, cs);
+  if (st != BEAM_OK) return st;
+  return run_experts(*shape, x, xdtype == BEAM_BF16, weights, topk_ids, topk_w, y, workspace, L, d, true, cs);
+}
+
+beam_status_t beam_moe_read_device_status(void* workspace, uint32_t* where, void* stream) {
+  if (workspace == nullptr) return BEAM_ERR_WORKSPACE;
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  uint32_t word[4] = {0, 0, 0, 0};
+  if (cudaStreamSynchronize(cs) != cudaSuccess) return BEAM_ERR_CUDA;
+  if (cudaMemcpy(word, workspace, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return BEAM_ERR_CUDA;
+  if (cudaMemset(workspace, 0, sizeof(word)) != cudaSuccess) return BEAM_ERR_CUDA;
+  if (where != nullptr) *where = word[1];
+  return static_cast<beam_status_t>(word[0]);
+}
+
+beam_status_t beam_moe_debug_timeout(void* workspace, size_t workspace_bytes, uint32_t timeout_us, void* stream) {
+  if (workspace == nullptr || workspace_bytes < 16 || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return BEAM_ERR_WORKSPACE;
+  if (timeout_us == 0 || timeout_us > 10000000u) return BEAM_ERR_INVALID_ARG;
+  return cuda_status(launch_debug_timeout(static_cast<uint32_t*>(workspace), static_cast<uint64_t>(timeout_us) * 1000ull,
+                                          static_cast<cudaStream_t>(stream)));
+}
+
+const char* beam_status_string(beam_status_t status) {
+  switch (status) {
+    case BEAM_OK: return "ok";
+    case BEAM_ERR_INVALID_ARG: return "invalid argument (null, misaligned or out-of-range value)";
+    case BEAM_ERR_UNSUPPORTED: return "unsupported shape or data type";
+    case BEAM_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case BEAM_ERR_CUDA: return "CUDA runtime or launch error";
+    case BEAM_ERR_TIMEOUT: return "device: a bounded wait ran out";
+    case BEAM_ERR_DEVICE_CHECK: return "device: a consistency check failed (e.g. an expert id out of range)";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

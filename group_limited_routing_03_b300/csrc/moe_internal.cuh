@@ -1,0 +1,87 @@
+// moe_internal.cuh -- constants, parameter blocks and host-side launchers
+// shared by the CUDA sources of the MoE library (not part of the C ABI).
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+namespace beam {
+
+constexpr int kExperts = 256;      // E
+constexpr int kGroups = 8;         // groups of 32 contiguous experts
+constexpr int kGroupsKept = 4;     // best groups kept
+constexpr int kTopK = 8;           // experts per token
+constexpr int kRouterTile = 32;    // tokens per router CTA (= one dispatch tile)
+constexpr int kRouterKChunk = 32;  // hidden elements per router k-step
+constexpr int kTileRoutes = kRouterTile * kTopK;  // routes per dispatch tile (256)
+constexpr int kBlockM = 128;       // weight rows per MMA tile (TMEM lanes)
+constexpr int kBlockK = 64;        // K elements per pipeline stage (128 bytes of bf16)
+constexpr int kBoxRows = 32;       // token rows per TMA box of the activation operand
+constexpr int kMaxSmsForSizing = 256;  // bound on the SM count used to size the workspace
+
+// ---------------------------------------------------------------------------
+// Router
+// ---------------------------------------------------------------------------
+struct RouterParams {
+  const void* x;        // [T, H] f32 or bf16
+  const float* wr;      // [E, H]
+  const float* bias;    // [E] or null
+  int T, H;
+  float scale;
+  int splits;           // K splits (1: fused selection in the GEMM CTA)
+  int n_kchunks;        // H / kRouterKChunk
+  int n_tiles;          // ceil(T / kRouterTile)
+  float* part;          // [splits, T, E] partial logits when splits > 1
+  int32_t* ids;         // [T, 8]
+  float* w;             // [T, 8]
+  int32_t* tile_hist;   // [E, n_tiles] routes of tile per expert
+};
+
+// ---------------------------------------------------------------------------
+// Grouped GEMM (gate/up with SwiGLU epilogue, or down)
+// ---------------------------------------------------------------------------
+struct GemmParams {
+  const int32_t* counts;        // [E]
+  const int32_t* offsets;       // [E+1]
+  const int32_t* chunk_prefix;  // [E+1] exclusive scan of ceil(counts / nmax)
+  int m_tiles;                  // weight rows per expert / kBlockM
+  int a_rows_per_expert;        // I (gate/up) or H (down)
+  int k_blocks;                 // K / kBlockK
+  int nmax;                     // tokens per chunk (multiple of kBoxRows, <= 256)
+  int stages;                   // shared-memory pipeline depth
+  int acc_stages;               // TMEM accumulator buffers
+  uint32_t acc_cols;            // TMEM columns per accumulator buffer
+  uint32_t tmem_cols;           // TMEM columns allocated (power of two)
+  __nv_bfloat16* out;           // h [R, I] or yr [R, H], perm order
+  int out_ld;                   // I or H
+  const float* gs0;             // NVFP4 global scales (gate or down) [E], else null
+  const float* gs1;             // NVFP4 global scale (up) [E], else null
+  uint32_t* status;
+  uint64_t timeout_ns;
+};
+
+// ---------------------------------------------------------------------------
+// Host launchers (each returns cudaGetLastError() of its launches)
+// ---------------------------------------------------------------------------
+int router_splits(int T, int H, int num_sms);
+int router_split_cap(int T, int H);
+
+cudaError_t launch_router(const RouterParams& p, bool x_bf16, cudaStream_t stream);
+cudaError_t launch_tile_hist(const int32_t* ids, int R, int n_tiles, int32_t* tile_hist,
+                             uint32_t* status, cudaStream_t stream);
+cudaError_t launch_dispatch(const int32_t* ids, int R, int n_tiles, int32_t* tile_hist,
+                            int32_t* counts, int32_t* offsets, int32_t* chunk_prefix, int nmax,
+                            int32_t* perm, int32_t* pos, cudaStream_t stream);
+cudaError_t launch_gather(const void* x, bool x_bf16, int H, const int32_t* perm, int R,
+                          __nv_bfloat16* xp, int num_sms, cudaStream_t stream);
+cudaError_t launch_gemm(int mode, const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b,
+                        const GemmParams& p, int grid, size_t smem_bytes, cudaStream_t stream);
+size_t gemm_stage_bytes(int mode, int nmax);
+cudaError_t launch_combine(const __nv_bfloat16* yr, const int32_t* pos, const float* w, int T, int H,
+                           void* y, bool y_bf16, cudaStream_t stream);
+cudaError_t launch_debug_timeout(uint32_t* status, uint64_t timeout_ns, cudaStream_t stream);
+
+}  // namespace beam

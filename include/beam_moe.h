@@ -1,0 +1,165 @@
+/*
+ * beam_moe.h -- C ABI of a single-GPU (B300, sm_103a) implementation of the
+ * group-limited Mixture-of-Experts block of the Beam model.
+ *
+ * Source of the operation (two translations of one launch post):
+ *   "Willkommen Beam: ein offenes 501B-Modell, das Sie besitzen, anpassen und
+ *   skalieren können" (spke.com), section "Mixture of Experts", and the
+ *   Chinese "Reflection 发布 501B 开放模型 Beam，支持自托管定制与扩展"
+ *   (sihot.dev), section 混合专家.  The post fixes: 256 experts, each a
+ *   SwiGLU MLP (intermediate 2560, hidden 5120); sigmoid router scores;
+ *   8 groups of 32 ranked by the sum of each group's two best scores; the
+ *   best 4 groups kept; the top-8 experts inside them; no shared expert;
+ *   expert outputs combined with the normalised router weights times 2.5.
+ *   Section "Residual Stream" of the same post: the router and the SwiGLU
+ *   product are computed in FP32.
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers, owned by the caller, row-major,
+ *     16-byte aligned.  The library allocates no memory and keeps no state
+ *     between calls other than a per-device cache of kernel attributes.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls
+ *     only enqueue work; none synchronises the host except
+ *     beam_moe_read_device_status.
+ *   - Argument, shape and alignment errors are detected on the host before
+ *     anything is enqueued (BEAM_ERR_INVALID_ARG / BEAM_ERR_UNSUPPORTED /
+ *     BEAM_ERR_WORKSPACE).  A failed launch returns BEAM_ERR_CUDA.  Errors the
+ *     kernels detect (a bounded wait that ran out) are written to a status
+ *     word inside the workspace; read it with beam_moe_read_device_status.
+ *   - Two calls that run concurrently must use distinct workspaces.
+ *
+ * Supported shape: E = 256, n_group = 8, topk_group = 4, top_k = 8,
+ * H % 128 == 0, I % 128 == 0, 1 <= T <= 1048576.  routed_scale is any finite
+ * value (2.5 for Beam).
+ */
+#ifndef BEAM_MOE_H
+#define BEAM_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  BEAM_OK = 0,
+  BEAM_ERR_INVALID_ARG = 1,  /* null / misaligned pointer, negative size */
+  BEAM_ERR_UNSUPPORTED = 2,  /* shape or dtype outside the supported set */
+  BEAM_ERR_WORKSPACE = 3,    /* workspace null, misaligned or too small */
+  BEAM_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
+  BEAM_ERR_TIMEOUT = 5,      /* device: a bounded wait ran out (status word) */
+  BEAM_ERR_DEVICE_CHECK = 6  /* device: a kernel's own consistency check failed */
+} beam_status_t;
+
+typedef enum { BEAM_F32 = 0, BEAM_BF16 = 1, BEAM_NVFP4 = 2 } beam_dtype_t;
+
+/* Layer shape.  T tokens, hidden H, expert intermediate I, E experts in
+ * n_group contiguous groups (group j = experts [j*E/n_group, (j+1)*E/n_group)),
+ * topk_group groups kept, top_k experts per token, combine scale. */
+typedef struct {
+  int32_t T, H, I, E, n_group, topk_group, top_k;
+  float routed_scale;
+} beam_moe_shape_t;
+
+/* Expert weights, all experts stacked, linear-layer orientation [out, in]:
+ *   BF16 : gate [E, I, H], up [E, I, H], down [E, H, I]  (bf16 elements)
+ *   NVFP4: gate/up [E, I, H/2], down [E, H, I/2] bytes, two E2M1 codes per
+ *          byte, the even K index in the low nibble; *_sf = E4M3 block scales
+ *          [E, I, H/16] / [E, H, I/16], one per 16 consecutive K elements;
+ *          *_gs = FP32 global scale per expert and matrix [E].
+ *          Element value = e2m1 * e4m3 * global.
+ * Pointers the dtype does not use must be NULL. */
+typedef struct {
+  beam_dtype_t dtype; /* BEAM_BF16 or BEAM_NVFP4 */
+  const void* gate;
+  const void* up;
+  const void* down;
+  const uint8_t* gate_sf;
+  const uint8_t* up_sf;
+  const uint8_t* down_sf;
+  const float* gate_gs;
+  const float* up_gs;
+  const float* down_gs;
+} beam_expert_weights_t;
+
+/* Where the intermediates of the last call live inside the workspace (byte
+ * offsets from its start); for inspection by tests and tools.
+ *   counts int32[E]        routes per expert
+ *   offsets int32[E+1]     exclusive prefix sum of counts
+ *   perm int32[T*top_k]    route ids r = t*top_k + k grouped by expert,
+ *                          ascending r inside an expert
+ *   pos int32[T*top_k]     inverse of perm: perm[pos[r]] == r
+ *   xp bf16[T*top_k, H]    token rows in perm order
+ *   h bf16[T*top_k, I]     SwiGLU activations in perm order
+ *   yr bf16[T*top_k, H]    expert outputs in perm order (before weighting)
+ *   status uint32[4]       device status word (code, where, 0, 0) */
+typedef struct {
+  size_t status, counts, offsets, perm, pos, xp, h, yr, total;
+} beam_ws_layout_t;
+
+/* Bytes of workspace beam_moe_forward / beam_moe_experts need for `shape`
+ * with expert weights of type `wdtype` (0 on an unsupported shape).  The
+ * same workspace serves beam_moe_route and beam_moe_dispatch. */
+size_t beam_moe_workspace_size(const beam_moe_shape_t* shape, beam_dtype_t wdtype);
+
+/* Fill `layout` for `shape`; returns BEAM_OK or BEAM_ERR_UNSUPPORTED. */
+beam_status_t beam_moe_workspace_layout(const beam_moe_shape_t* shape, beam_dtype_t wdtype,
+                                        beam_ws_layout_t* layout);
+
+/* Routing only (Beam post, "Mixture of Experts"): for every token t
+ *   s[e]   = sigmoid(sum_h x[t,h] * router_w[e,h])        (FP32)
+ *   sel[e] = s[e] + router_bias[e]   (bias 0 when router_bias == NULL; it
+ *            steers the selection only, as in DeepSeek-V3's scheme)
+ *   group score = sum of the two largest sel in the group; keep the
+ *   topk_group best groups (ties: lower group index); take the top_k largest
+ *   sel among their experts (ties: lower expert index), best first.
+ *   topk_ids[t,k] = chosen expert; topk_w[t,k] = s[id] / sum_k s * scale.
+ * x: [T, H] FP32 or BF16 (xdtype); router_w: FP32 [E, H]; router_bias:
+ * FP32 [E] or NULL; topk_ids: int32 [T, top_k]; topk_w: FP32 [T, top_k].
+ * Also leaves per-tile expert histograms in the workspace for dispatch. */
+beam_status_t beam_moe_route(const beam_moe_shape_t* shape, const void* x, beam_dtype_t xdtype,
+                             const float* router_w, const float* router_bias, int32_t* topk_ids,
+                             float* topk_w, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Dispatch only: from topk_ids [T, top_k] build counts, offsets, perm and
+ * pos in the workspace (see beam_ws_layout_t), deterministic order. */
+beam_status_t beam_moe_dispatch(const beam_moe_shape_t* shape, const int32_t* topk_ids,
+                                void* workspace, size_t workspace_bytes, void* stream);
+
+/* Experts and combine for a given routing:
+ *   y[t,:] = sum_k topk_w[t,k] * FFN_{topk_ids[t,k]}(x[t,:]),  k = 0..top_k-1
+ *   FFN_e(v) = Wd[e] (silu(Wg[e] v) * (Wu[e] v)),  SwiGLU product in FP32,
+ *   FP32 accumulation, activations rounded to BF16 between the matmuls.
+ * No shared-expert term.  y has x's dtype ([T, H]). */
+beam_status_t beam_moe_experts(const beam_moe_shape_t* shape, const void* x, beam_dtype_t xdtype,
+                               const beam_expert_weights_t* weights, const int32_t* topk_ids,
+                               const float* topk_w, void* y, void* workspace,
+                               size_t workspace_bytes, void* stream);
+
+/* The whole block: beam_moe_route followed by beam_moe_experts. */
+beam_status_t beam_moe_forward(const beam_moe_shape_t* shape, const void* x, beam_dtype_t xdtype,
+                               const float* router_w, const float* router_bias,
+                               const beam_expert_weights_t* weights, void* y, int32_t* topk_ids,
+                               float* topk_w, void* workspace, size_t workspace_bytes,
+                               void* stream);
+
+/* Synchronises `stream`, returns the device status word of `workspace`
+ * (BEAM_OK when no kernel reported a problem) and clears it.  `where`
+ * (nullable) receives the code of the wait that gave up. */
+beam_status_t beam_moe_read_device_status(void* workspace, uint32_t* where, void* stream);
+
+/* Test hook for the bounded-wait machinery: launches one CTA that waits on
+ * an mbarrier nothing ever arrives on, with a limit of `timeout_us`
+ * microseconds; the kernel then records BEAM_ERR_TIMEOUT in the workspace
+ * status word and returns normally. */
+beam_status_t beam_moe_debug_timeout(void* workspace, size_t workspace_bytes, uint32_t timeout_us,
+                                     void* stream);
+
+/* Static description of a status code. */
+const char* beam_status_string(beam_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* BEAM_MOE_H */

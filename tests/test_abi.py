@@ -1,0 +1,132 @@
+"""The C-ABI library loads, exports every declared entry point, and rejects
+bad arguments on the host before touching a GPU (no compute calls here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import group_limited_routing_03_b300 as moe
+from group_limited_routing_03_b300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "beam_moe.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return moe.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(beam_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("beam_moe_route", "beam_moe_forward", "beam_moe_experts", "beam_moe_dispatch",
+                     "beam_moe_workspace_size", "beam_moe_workspace_layout", "beam_moe_read_device_status",
+                     "beam_status_string"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in beam_moe.h but not exported"
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        assert moe.beam_status_string(code)
+    assert moe.beam_status_string(99) == "unknown status"
+
+
+def _shape(**kw):
+    base = dict(T=64, H=5120, I=2560)
+    base.update(kw)
+    return moe.shape(**base)
+
+
+def test_workspace_size_and_layout(lib):
+    sh = _shape()
+    n = moe.workspace_size(sh)
+    lay = moe.workspace_layout(sh)
+    assert lay["total"] == n
+    R = 64 * 8
+    assert lay["xp"] + R * 5120 * 2 <= lay["h"]
+    assert lay["h"] + R * 2560 * 2 <= lay["yr"]
+    assert lay["yr"] + R * 5120 * 2 <= n
+    for k in ("status", "counts", "offsets", "perm", "pos", "xp", "h", "yr"):
+        assert lay[k] % 256 == 0
+    assert lay["status"] == 0
+
+
+@pytest.mark.parametrize("bad", [dict(E=128), dict(n_group=4), dict(topk_group=2), dict(top_k=6),
+                                 dict(H=5000), dict(I=2500), dict(T=(1 << 20) + 1)])
+def test_unsupported_shapes(lib, bad):
+    assert moe.workspace_size(_shape(**bad)) == 0
+    with pytest.raises(moe.BeamError) as ei:
+        moe.workspace_layout(_shape(**bad))
+    assert ei.value.code == moe.BEAM_ERR_UNSUPPORTED
+
+
+def _route_raw(lib, sh, x=0x10000, xdt=moe.BEAM_BF16, wr=0x20000, bias=None, ids=0x30000, w=0x40000,
+               ws=0x100000, nbytes=None):
+    if nbytes is None:
+        nbytes = moe.workspace_size(sh)
+    return lib.beam_moe_route(ctypes.byref(sh), x, xdt, wr, bias, ids, w, ws, nbytes, None)
+
+
+def test_route_argument_errors(lib):
+    sh = _shape()
+    assert _route_raw(lib, sh, x=None) == moe.BEAM_ERR_INVALID_ARG
+    assert _route_raw(lib, sh, x=0x10008) == moe.BEAM_ERR_INVALID_ARG  # misaligned
+    assert _route_raw(lib, sh, xdt=moe.BEAM_NVFP4) == moe.BEAM_ERR_UNSUPPORTED
+    assert _route_raw(lib, sh, ws=None) == moe.BEAM_ERR_WORKSPACE
+    assert _route_raw(lib, sh, ws=0x100080) == moe.BEAM_ERR_WORKSPACE  # not 256-aligned
+    assert _route_raw(lib, sh, nbytes=1024) == moe.BEAM_ERR_WORKSPACE
+    bad = _shape(T=0)
+    assert _route_raw(lib, bad) == moe.BEAM_ERR_INVALID_ARG
+    sh_nan = _shape(routed_scale=float("nan"))
+    assert _route_raw(lib, sh_nan) == moe.BEAM_ERR_INVALID_ARG
+
+
+def test_forward_weight_errors(lib):
+    sh = _shape()
+    ew = moe._ExpertWeights()
+    ew.dtype = moe.BEAM_BF16
+    ew.gate, ew.up, ew.down = 0x1000, 0x2000, None
+    n = moe.workspace_size(sh)
+    rc = lib.beam_moe_forward(ctypes.byref(sh), 0x10000, moe.BEAM_BF16, 0x20000, None, ctypes.byref(ew), 0x50000,
+                              0x30000, 0x40000, 0x100000, n, None)
+    assert rc == moe.BEAM_ERR_INVALID_ARG
+    ew.down = 0x3000
+    ew.gate_sf = 0x4000  # a scale pointer with BF16 weights
+    rc = lib.beam_moe_forward(ctypes.byref(sh), 0x10000, moe.BEAM_BF16, 0x20000, None, ctypes.byref(ew), 0x50000,
+                              0x30000, 0x40000, 0x100000, n, None)
+    assert rc == moe.BEAM_ERR_INVALID_ARG
+    rc = lib.beam_moe_forward(ctypes.byref(sh), 0x10000, moe.BEAM_BF16, 0x20000, None, None, 0x50000, 0x30000,
+                              0x40000, 0x100000, n, None)
+    assert rc == moe.BEAM_ERR_INVALID_ARG
+
+
+def test_debug_timeout_argument_errors(lib):
+    assert lib.beam_moe_debug_timeout(None, 4096, 100, None) == moe.BEAM_ERR_WORKSPACE
+    assert lib.beam_moe_debug_timeout(0x100000, 4096, 0, None) == moe.BEAM_ERR_INVALID_ARG
+
+
+def test_binding_refuses_host_tensors(lib):
+    import torch
+
+    with pytest.raises(ValueError):
+        moe._ptr(torch.zeros(4))
+
+
+def test_missing_library_fails_loudly(tmp_path, monkeypatch):
+    monkeypatch.setattr(moe, "_LIB_PATH", str(tmp_path / "absent.so"))
+    monkeypatch.setattr(moe, "_lib", None)
+    with pytest.raises(ImportError):
+        moe.load()

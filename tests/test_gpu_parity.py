@@ -1,0 +1,184 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle on the
+same seeded inputs.  Rules are stated in parity_helpers."""
+import gc
+
+import numpy as np
+import pytest
+import torch
+
+import group_limited_routing_03_b300 as moe
+import oracle
+from group_limited_routing_03_b300 import inputs
+from parity_helpers import (Y_TOL, compare_routing, host_act, oracle_route, oracle_y, rel_err,
+                            seeded_routing)
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from group_limited_routing_03_b300 import _build
+
+    _build.build()
+    moe.load()
+    yield
+    gc.collect()
+    torch.cuda.empty_cache()
+
+
+def _gpu_inputs(wl, *, cpu_gen=False):
+    """Inputs on the GPU; for small workloads drawn on the CPU then copied."""
+    if cpu_gen:
+        d = inputs.generate(wl, "cpu")
+        out = {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+        return out, d
+    return inputs.generate(wl, DEV), None
+
+
+def _bf16_weights(d):
+    return {k: d[k].to(torch.bfloat16).contiguous() for k in ("gate", "up", "down")}
+
+
+def _run_forward(wl, d, weights):
+    sh = moe.shape(wl.T, wl.H, wl.I)
+    ws = moe.alloc_workspace(sh, "nvfp4" if wl.w_dtype == "nvfp4" else "bf16")
+    y = torch.empty((wl.T, wl.H), dtype=d["x"].dtype, device=DEV)
+    ids = torch.empty((wl.T, 8), dtype=torch.int32, device=DEV)
+    w = torch.empty((wl.T, 8), dtype=torch.float32, device=DEV)
+    moe.beam_moe_forward(sh, d["x"], d["router_w"], d.get("bias"), weights, y, ids, w, ws)
+    code, where = moe.beam_moe_read_device_status(ws)
+    assert code == 0, f"device status {code} where {where}"
+    return y, ids, w, ws
+
+
+# ---------------------------------------------------------------------------
+# whole block, small shapes (every token compared)
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("T,H,I,x_dtype", [(128, 256, 128, "f32"), (1, 256, 128, "bf16"), (33, 256, 128, "bf16"),
+                                           (300, 384, 256, "bf16"), (77, 1024, 512, "f32")])
+def test_forward_small_all_tokens(T, H, I, x_dtype):
+    wl = inputs.workload("tiny", T=T, H=H, I=I, x_dtype=x_dtype, seed=T + H)
+    dg, dc = _gpu_inputs(wl, cpu_gen=True)
+    y, ids, w, _ = _run_forward(wl, dg, _bf16_weights(dg))
+    ref = oracle_route(dg)
+    safe = compare_routing(ids.cpu().numpy(), w.cpu().numpy(), ref)
+    tok = np.nonzero(safe)[0]
+    # oracle on the FP32 originals of the expert weights (the GPU gets BF16 copies)
+    ow = {k: dc[k].numpy() for k in ("gate", "up", "down")}
+    y_ref = oracle_y(dg, tok, ref["ids"][tok], ref["weights"][tok], oracle_weights=ow)
+    err = rel_err(y.cpu().double().numpy()[tok], y_ref)
+    assert err <= Y_TOL["bf16"], err
+
+
+def test_zero_input_exact():
+    wl = inputs.workload("tiny", T=40, x_dtype="bf16")
+    dg, _ = _gpu_inputs(wl, cpu_gen=True)
+    dg["x"] = torch.zeros_like(dg["x"])
+    y, ids, w, _ = _run_forward(wl, dg, _bf16_weights(dg))
+    assert (ids.cpu() == torch.arange(8, dtype=torch.int32)).all()
+    assert (w.cpu() == 2.5 / 8).all()
+    assert (y.cpu() == 0).all()
+
+
+# ---------------------------------------------------------------------------
+# dispatch and experts with a routing drawn independently of the router
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("T,hot", [(1000, None), (3000, (5, 77, 200)), (1, None), (37, (0, 1, 2, 3, 4, 5, 6, 7))])
+def test_dispatch_matches_oracle(T, hot):
+    ids, _ = seeded_routing(T, seed=T, hot=hot)
+    sh = moe.shape(T, 256, 128)
+    ws = moe.alloc_workspace(sh)
+    moe.beam_moe_dispatch(sh, ids.to(DEV), ws)
+    lay = moe.workspace_layout(sh)
+    torch.cuda.synchronize()
+    R = T * 8
+
+    def view(off, n):
+        return ws[off:off + 4 * n].view(torch.int32).cpu().numpy()
+
+    ref = oracle.dispatch(ids.numpy())
+    np.testing.assert_array_equal(view(lay["counts"], 256), ref["counts"])
+    np.testing.assert_array_equal(view(lay["offsets"], 257), ref["offsets"])
+    np.testing.assert_array_equal(view(lay["perm"], R), ref["perm"])
+    np.testing.assert_array_equal(view(lay["pos"], R), ref["pos"])
+
+
+@pytest.mark.parametrize("T,H,I,hot", [(600, 256, 128, (3, 77, 130, 131, 200, 201, 254, 255)),
+                                       (300, 512, 256, (9,)), (17, 256, 384, None)])
+def test_experts_given_routing(T, H, I, hot):
+    """Experts + combine on a seeded routing; `hot` experts get every token,
+    so they run several 256-token chunks."""
+    wl = inputs.workload("tiny", T=T, H=H, I=I, x_dtype="bf16", w_dtype="bf16", seed=7 + T)
+    dg, _ = _gpu_inputs(wl, cpu_gen=True)
+    ids, w = seeded_routing(T, seed=T + 1, hot=hot)
+    sh = moe.shape(T, H, I)
+    ws = moe.alloc_workspace(sh)
+    y = torch.empty((T, H), dtype=torch.bfloat16, device=DEV)
+    moe.beam_moe_experts(sh, dg["x"], _bf16_weights(dg), ids.to(DEV), w.to(DEV), y, ws)
+    assert moe.beam_moe_read_device_status(ws)[0] == 0
+    tok = np.arange(T)
+    y_ref = oracle_y(dg, tok, ids.numpy(), w.numpy().astype(np.float64))
+    assert rel_err(y.cpu().double().numpy(), y_ref) <= Y_TOL["bf16"]
+
+
+def test_identical_experts_closed_form():
+    """All experts share one weight set, so y = 2.5 * f(x) whatever the routing."""
+    T, H, I = 200, 256, 256
+    wl = inputs.workload("tiny", T=T, H=H, I=I, x_dtype="bf16", w_dtype="bf16", seed=99)
+    dg, _ = _gpu_inputs(wl, cpu_gen=True)
+    for k in ("gate", "up", "down"):
+        dg[k] = dg[k][:1].expand_as(dg[k]).contiguous()
+    y, ids, w, _ = _run_forward(wl, dg, dg)
+    x = host_act(dg["x"])
+    f = oracle.expert_ffn(x, *(host_act(dg[k][0]) for k in ("gate", "up", "down")))
+    assert rel_err(y.cpu().double().numpy(), 2.5 * f) <= Y_TOL["bf16"]
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    sh = moe.shape(8, 256, 128)
+    ws = moe.alloc_workspace(sh)
+    moe.beam_moe_debug_timeout(ws, 2000)
+    code, where = moe.beam_moe_read_device_status(ws)
+    assert code == moe.BEAM_ERR_TIMEOUT and where == 9
+    assert moe.beam_moe_read_device_status(ws)[0] == 0  # cleared
+    wl = inputs.workload("tiny", T=8, x_dtype="bf16")
+    dg, _ = _gpu_inputs(wl, cpu_gen=True)
+    _run_forward(wl, dg, _bf16_weights(dg))  # the context is still usable
+
+
+# ---------------------------------------------------------------------------
+# full-size workloads: routing on every token, outputs on sampled tokens
+# ---------------------------------------------------------------------------
+def _sample_tokens(T, ids_ref, n, seed, hot_expert=None):
+    rng = np.random.default_rng(seed)
+    pick = {0, T - 1}
+    if hot_expert is not None:
+        pick.add(int(np.nonzero((ids_ref == hot_expert).any(1))[0][0]))
+    while len(pick) < n:
+        pick.add(int(rng.integers(0, T)))
+    return np.array(sorted(pick))
+
+
+@pytest.mark.parametrize("name,n_sample", [("decode", 8), ("prefill", 4), ("skew", 4)])
+def test_full_size_workloads(name, n_sample):
+    wl = inputs.workload(name)
+    torch.cuda.empty_cache()
+    dg = inputs.generate(wl, DEV)
+    y, ids, w, ws = _run_forward(wl, dg, dg)
+    ref = oracle_route(dg)
+    bias = None if dg.get("bias") is None else dg["bias"].cpu().numpy()
+    safe = compare_routing(ids.cpu().numpy(), w.cpu().numpy(), ref, bias=bias)
+    counts = np.bincount(ref["ids"].reshape(-1), minlength=256)
+    if name == "skew":
+        assert counts.max() > 10 * counts.mean()
+    hot = int(np.argmax(counts))
+    tok = _sample_tokens(wl.T, ref["ids"], n_sample, seed=wl.seed, hot_expert=hot)
+    tok = tok[safe[tok]]
+    y_ref = oracle_y(dg, tok, ref["ids"][tok], ref["weights"][tok])
+    err = rel_err(y.cpu()[tok].double().numpy(), y_ref)
+    print(f"{name}: near-ties {(~safe).sum()} of {wl.T}; sampled {len(tok)} tokens; rel err {err:.3e}")
+    assert err <= Y_TOL[wl.w_dtype], err
+    del dg, y, ws
+    gc.collect()
+    torch.cuda.empty_cache()

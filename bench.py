@@ -1,0 +1,434 @@
+#!/usr/bin/env python
+"""Benchmark of the group-limited MoE block (Beam shapes) on B300.
+
+One step = one forward of the whole block (router, dispatch, gather, gate/up
+GEMM + SwiGLU, down GEMM, combine) over one batch of synthetic tokens, with
+every input already resident in HBM.  The headline workload is the decode
+layer (T=64, H=5120, I=2560, 256 BF16 experts); the prefill layer (T=8192)
+is measured the same way and reported under "prefill".
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+With N > 1 (torchrun) every rank runs an independent replica on its own GPU
+(the block does not shard); the barrier and the max-over-ranks time are the
+only collectives.  ``--impl reference`` times the CPU oracle (the plain FP64
+definition) on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+METRIC = "MoE-layer tokens/s (T=64 decode, T=8192 prefill); % HBM / tensor-core roofline"
+STAGES = ("route", "dispatch", "gather", "gate_up", "down", "combine")
+
+
+# ---------------------------------------------------------------------------
+# environment
+# ---------------------------------------------------------------------------
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return dict(hbm=float(p["hbm_gbs"]), bf16=float(p["bf16_tflops"]),
+                    bf16_sustained=float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), source="measured")
+    return dict(hbm=6400.0, bf16=1800.0, bf16_sustained=1400.0, source="fallback")
+
+
+class ClockSampler:
+    """Samples SM clock and clock-event reasons through NVML while running."""
+
+    REASONS = {
+        "gpu_idle": 0x1, "applications_clocks_setting": 0x2, "sw_power_cap": 0x4, "hw_slowdown": 0x8,
+        "sync_boost": 0x10, "sw_thermal_slowdown": 0x20, "hw_thermal_slowdown": 0x40,
+        "hw_power_brake_slowdown": 0x80, "display_clock_setting": 0x100,
+    }
+
+    def __init__(self, index: int, period_s: float = 0.01):
+        self.period = period_s
+        self.samples = []
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._thread = None
+        try:
+            import pynvml
+
+            pynvml.nvmlInit()
+            self._nvml = pynvml
+            self._h = pynvml.nvmlDeviceGetHandleByIndex(index)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self._h, pynvml.NVML_CLOCK_SM)
+        except Exception:  # NVML unavailable: report no clocks
+            self._nvml = None
+
+    def _run(self):
+        nv = self._nvml
+        while not self._stop.is_set():
+            try:
+                mhz = nv.nvmlDeviceGetClockInfo(self._h, nv.NVML_CLOCK_SM)
+                reasons = nv.nvmlDeviceGetCurrentClocksEventReasons(self._h)
+                self.samples.append((mhz, reasons))
+            except Exception:
+                pass
+            time.sleep(self.period)
+
+    def __enter__(self):
+        if self._nvml is not None:
+            self._thread = threading.Thread(target=self._run, daemon=True)
+            self._thread.start()
+        return self
+
+    def __exit__(self, *exc):
+        self._stop.set()
+        if self._thread is not None:
+            self._thread.join()
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0}
+        mhz = [s[0] for s in self.samples]
+        active = 0
+        for _, r in self.samples:
+            active |= int(r)
+        names = [n for n, bit in self.REASONS.items() if active & bit and n != "gpu_idle"]
+        return {"sm_mhz": float(statistics.median(mhz)), "sm_max_mhz": self.max_mhz, "reasons": names,
+                "samples": len(mhz)}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def make_layer(wl, dev):
+    import group_limited_routing_03_b300 as moe
+    from group_limited_routing_03_b300 import inputs
+
+    d = inputs.generate(wl, dev)
+    sh = moe.shape(wl.T, wl.H, wl.I)
+    ws = moe.alloc_workspace(sh, "nvfp4" if wl.w_dtype == "nvfp4" else "bf16", dev)
+    y = torch.empty((wl.T, wl.H), dtype=d["x"].dtype, device=dev)
+    ids = torch.empty((wl.T, 8), dtype=torch.int32, device=dev)
+    w = torch.empty((wl.T, 8), dtype=torch.float32, device=dev)
+    call = moe.ForwardCall(sh, d["x"], d["router_w"], d.get("bias"), d, y, ids, w, ws)
+    return d, sh, ws, y, ids, w, call
+
+
+def measure(wl, steps, warmup, dev, world, sampler_index):
+    """Device-timed steps through the per-stage C-ABI calls, events between
+    the stages on the launching stream.  Returns a dict of timings."""
+    import group_limited_routing_03_b300 as moe
+
+    d, sh, ws, y, ids, w, call = make_layer(wl, dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        for i in range(len(STAGES)):
+            call.stage(i)
+    torch.cuda.synchronize()
+    code, where = moe.beam_moe_read_device_status(ws)
+    if code != 0:
+        raise RuntimeError(f"device status {code} at {where} during warm-up")
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(STAGES) + 1)] for _ in range(steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(sampler_index) as clk:
+        for k in range(steps):
+            ev = evs[k]
+            ev[0].record(stream)
+            for i in range(len(STAGES)):
+                call.stage(i)
+                ev[i + 1].record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    total_ms = evs[0][0].elapsed_time(evs[-1][-1])
+    stage_ms = [statistics.fmean(ev[i].elapsed_time(ev[i + 1]) for ev in evs) for i in range(len(STAGES))]
+    code, where = moe.beam_moe_read_device_status(ws)
+    if code != 0:
+        raise RuntimeError(f"device status {code} at {where} in the timed region")
+    ids_h = ids.cpu()
+    touched = int(torch.unique(ids_h).numel())
+    launches = sum(moe.beam_moe_stage_kernel_count(sh, i) for i in range(len(STAGES)))
+    out = dict(total_ms=total_ms, stage_ms=stage_ms, touched=touched, launches_per_step=launches,
+               clocks=clk.summary(), counts=torch.bincount(ids_h.reshape(-1).long(), minlength=256))
+    return out, (d, sh, ws, y, ids, w, call)
+
+
+def measure_e2e(wl, state, steps, warmup, dev):
+    """Same step through the public call with host buffers: pinned x copied in,
+    y / ids / weights copied out, every step, inside the timed region."""
+    d, sh, ws, y, ids, w, call = state
+    x_dev = d["x"]
+    x_host = x_dev.cpu().pin_memory()
+    y_host = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+    ids_host = torch.empty(ids.shape, dtype=ids.dtype).pin_memory()
+    w_host = torch.empty(w.shape, dtype=w.dtype).pin_memory()
+    stream = torch.cuda.current_stream()
+
+    def step():
+        x_dev.copy_(x_host, non_blocking=True)
+        call.run()
+        y_host.copy_(y, non_blocking=True)
+        ids_host.copy_(ids, non_blocking=True)
+        w_host.copy_(w, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    h2d = x_host.numel() * x_host.element_size()
+    d2h = sum(t.numel() * t.element_size() for t in (y_host, ids_host, w_host))
+    return ms, h2d, d2h
+
+
+def weight_bytes_per_expert(wl):
+    if wl.w_dtype == "nvfp4":
+        return 3 * wl.H * wl.I // 2 + 3 * wl.H * wl.I // 16 + 12
+    return 3 * wl.H * wl.I * 2
+
+
+def traffic_record(kernel: str, workload: str):
+    """Per-launch DRAM bytes of `kernel` from the committed ncu summary, if the
+    kernel source is unchanged since the capture (else None)."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)
+    ent = rec.get(workload, {}).get(kernel)
+    if not ent:
+        return None
+    src = os.path.join(ROOT, "group_limited_routing_03_b300", "csrc", ent["source"])
+    if not os.path.exists(src) or hashlib.sha256(open(src, "rb").read()).hexdigest() != ent["sha256"]:
+        return None
+    return float(ent["dram_bytes_per_launch"])
+
+
+def roofline(wl, m, pk):
+    """Dominant kernel: the gate/up GEMM (2/3 of the weight bytes and FLOPs)."""
+    R = wl.T * 8
+    ms = m["stage_ms"][STAGES.index("gate_up")]
+    wbytes = m["touched"] * 2 * wl.I * wl.H * 2
+    act_bytes = R * wl.H * 2 + R * wl.I * 2
+    flops = 2.0 * R * 2 * wl.I * wl.H
+    gbs = (wbytes + act_bytes) / (ms * 1e-3) / 1e9
+    tfs = flops / (ms * 1e-3) / 1e12
+    hbm = dict(bound="hbm", achieved=round(gbs, 1), peak=pk["hbm"], unit="GB/s", frac=round(gbs / pk["hbm"], 4),
+               traffic=traffic_record("moe_gemm_gate_up", wl.name), kernel="moe_gemm_kernel<0> (gate/up + SwiGLU)",
+               algorithmic_bytes=wbytes + act_bytes, launch_ms=round(ms, 4), peak_source=pk["source"])
+    tc = dict(bound="tensor", achieved=round(tfs, 1), peak=pk["bf16"], unit="TFLOP/s", frac=round(tfs / pk["bf16"], 4),
+              traffic=hbm["traffic"], kernel=hbm["kernel"], algorithmic_flops=flops, launch_ms=round(ms, 4),
+              peak_source=pk["source"])
+    return hbm, tc
+
+
+def step_numbers(wl, m, steps):
+    R = wl.T * 8
+    ms = m["total_ms"] / steps
+    wbytes = m["touched"] * weight_bytes_per_expert(wl)
+    xb = 2 if wl.x_dtype == "bf16" else 4
+    bytes_alg = wbytes + wl.T * wl.H * xb * 2 + wl.E * wl.H * 4
+    flops = 2.0 * R * 3 * wl.I * wl.H + 2.0 * wl.T * wl.E * wl.H
+    return dict(ms_per_step=round(ms, 4), tokens_per_s=wl.T / (ms * 1e-3),
+                step_gbs=round(bytes_alg / (ms * 1e-3) / 1e9, 1), step_tflops=round(flops / (ms * 1e-3) / 1e12, 1),
+                touched_experts=m["touched"], stage_ms={s: round(v, 4) for s, v in zip(STAGES, m["stage_ms"])})
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline / reference arm)
+# ---------------------------------------------------------------------------
+def oracle_sample(wl, d, budget_s=12.0, max_tokens=None):
+    """Time the FP64 oracle on a bounded sample of the workload: routing of all
+    T tokens, then whole tokens (8 experts + combine) one by one until the
+    budget is spent.  Host copies of the inputs are made outside the timing."""
+    import numpy as np
+
+    import oracle
+    from group_limited_routing_03_b300 import inputs  # noqa: F401
+
+    def host(t):
+        t = t.detach().cpu().contiguous()
+        return t.view(torch.int16).numpy().view(np.uint16) if t.dtype == torch.bfloat16 else t.numpy()
+
+    x = host(d["x"])
+    wr = d["router_w"].cpu().numpy()
+    b = None if d.get("bias") is None else d["bias"].cpu().numpy()
+    threads = oracle.default_threads()
+    t0 = time.perf_counter()
+    r = oracle.route(x, wr, b, threads=threads)
+    t_route = time.perf_counter() - t0
+    order = np.random.default_rng(wl.seed).permutation(wl.T)
+    done, t_ffn = 0, 0.0
+    for t in order[: (max_tokens or wl.T)]:
+        mats = {}
+        for e in r["ids"][t]:
+            e = int(e)
+            if wl.w_dtype == "nvfp4":
+                mats[e] = ([d[n][e].cpu().numpy() for n in ("gate", "up", "down")],
+                           dict(scales=[d[n + "_sf"][e].cpu().numpy() for n in ("gate", "up", "down")],
+                                global_scales=[float(d[n + "_gs"][e]) for n in ("gate", "up", "down")]))
+            else:
+                mats[e] = ([host(d[n][e]) for n in ("gate", "up", "down")], {})
+        t1 = time.perf_counter()
+        o = np.stack([oracle.expert_ffn(x[t:t + 1], *mats[int(e)][0], threads=threads, **mats[int(e)][1])[0]
+                      for e in r["ids"][t]])[None]
+        oracle.combine(r["weights"][t:t + 1], o)
+        t_ffn += time.perf_counter() - t1
+        done += 1
+        if t_ffn + t_route * done / wl.T >= budget_s:
+            break
+    sec = t_route * done / wl.T + t_ffn
+    return dict(value=done / sec, unit="tokens/s", cores=threads, kind="oracle",
+                sample=f"{wl.name}: routing of all {wl.T} tokens (time pro-rated to the sample), then "
+                       f"{done} whole tokens (8 experts each, FP64) on {threads} threads; {sec:.2f} s of CPU time")
+
+
+def run_reference(args, rank, world):
+    """Reference arm: the CPU oracle on the host cores (rank 0 only)."""
+    if rank != 0:
+        return
+    from group_limited_routing_03_b300 import inputs
+
+    wl = inputs.workload(args.workload)
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    d = inputs.generate(wl, dev)
+    per_step = []
+    for k in range(args.warmup + args.steps):
+        res = oracle_sample(wl, d, budget_s=1e9, max_tokens=1)
+        if k >= args.warmup:
+            per_step.append(1.0 / res["value"])
+    sec = sum(per_step)
+    value = args.steps / sec
+    cores = res["cores"]
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sec / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{wl.name} T={wl.T} H={wl.H} I={wl.I} E=256 {wl.w_dtype} experts",
+                       "T": wl.T, "H": wl.H, "I": wl.I},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": f"each step: routing of {wl.T} tokens pro-rated to one token plus one whole "
+                                       f"token through its 8 experts and the combine, FP64"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(v, world):
+    if world == 1:
+        return v
+    import torch.distributed as dist
+
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="decode")
+    ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    from group_limited_routing_03_b300 import _build, inputs
+
+    _build.build()
+    pk = peaks()
+    wl = inputs.workload(args.workload)
+    m, state = measure(wl, args.steps, args.warmup, dev, world, torch.cuda.current_device())
+    total_ms = max_over_ranks(m["total_ms"], world)
+    sn = step_numbers(wl, m, args.steps)
+    value = wl.T * args.steps * world / (total_ms * 1e-3)
+    hbm, tc = roofline(wl, m, pk)
+
+    e2e = None
+    if not args.no_e2e:
+        e_ms, h2d, d2h = measure_e2e(wl, state, args.steps, args.warmup, dev)
+        e_ms = max_over_ranks(e_ms, world)
+        e2e = {"value": wl.T * args.steps * world / (e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = oracle_sample(wl, state[0])
+    del state
+    torch.cuda.empty_cache()
+
+    prefill = None
+    if not args.no_prefill:
+        pw = inputs.workload("prefill")
+        pm, pstate = measure(pw, max(3, args.steps // 2), args.warmup, dev, world, torch.cuda.current_device())
+        p_ms = max_over_ranks(pm["total_ms"], world)
+        psn = step_numbers(pw, pm, max(3, args.steps // 2))
+        phbm, ptc = roofline(pw, pm, pk)
+        prefill = dict(value=pw.T * max(3, args.steps // 2) * world / (p_ms * 1e-3), unit="tokens/s",
+                       config={"workload": "prefill T=8192 H=5120 I=2560 E=256 bf16 experts", "T": pw.T},
+                       roofline=ptc, roofline_hbm=phbm, clocks=pm["clocks"], **psn)
+        del pstate
+        torch.cuda.empty_cache()
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{wl.name} T={wl.T} H={wl.H} I={wl.I} E=256 {wl.w_dtype} experts, FP32 router",
+                   "T": wl.T, "H": wl.H, "I": wl.I, "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+                   "l2": "no flush: each step streams the touched experts' weights "
+                         f"({m['touched']} x {weight_bytes_per_expert(wl) / 1e6:.1f} MB), far larger than L2"},
+        "roofline": hbm, "roofline_tensor": tc, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": m["launches_per_step"] * args.steps, "clocks": m["clocks"],
+        "step": sn, "prefill": prefill,
+    }
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

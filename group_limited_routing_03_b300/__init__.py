@@ -19,7 +19,8 @@ import torch
 
 __all__ = [
     "BeamError", "Shape", "shape", "workspace_size", "workspace_layout", "alloc_workspace",
-    "beam_moe_route", "beam_moe_dispatch", "beam_moe_experts", "beam_moe_forward",
+    "beam_moe_route", "beam_moe_dispatch", "beam_moe_experts", "beam_moe_forward", "beam_moe_forward_stage",
+    "ForwardCall", "STAGES", "beam_moe_stage_kernel_count",
     "beam_moe_read_device_status", "beam_moe_debug_timeout", "beam_status_string", "BeamMoE",
     "library_path", "load",
 ]
@@ -51,6 +52,15 @@ class _ExpertWeights(ctypes.Structure):
                 ("down_gs", ctypes.c_void_p)]
 
 
+class _Args(ctypes.Structure):
+    _fields_ = [("x", ctypes.c_void_p), ("xdtype", ctypes.c_int), ("router_w", ctypes.c_void_p),
+                ("router_bias", ctypes.c_void_p), ("weights", ctypes.POINTER(_ExpertWeights)),
+                ("y", ctypes.c_void_p), ("topk_ids", ctypes.c_void_p), ("topk_w", ctypes.c_void_p)]
+
+
+STAGES = ("route", "dispatch", "gather", "gate_up", "down", "combine")
+
+
 class _WsLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in ("status", "counts", "offsets", "perm", "pos", "xp", "h", "yr",
                                                "total")]
@@ -80,12 +90,16 @@ def load():
     lib.beam_moe_dispatch.argtypes = [sp, vp, vp, sz, vp]
     lib.beam_moe_experts.argtypes = [sp, vp, i32, ctypes.POINTER(_ExpertWeights), vp, vp, vp, vp, sz, vp]
     lib.beam_moe_forward.argtypes = [sp, vp, i32, vp, vp, ctypes.POINTER(_ExpertWeights), vp, vp, vp, vp, sz, vp]
+    lib.beam_moe_forward_stage.argtypes = [sp, ctypes.POINTER(_Args), i32, vp, sz, vp]
     lib.beam_moe_read_device_status.argtypes = [vp, ctypes.POINTER(u32), vp]
+    lib.beam_moe_stage_kernel_count.argtypes = [sp, i32]
+    lib.beam_moe_stage_kernel_count.restype = ctypes.c_int32
     lib.beam_moe_debug_timeout.argtypes = [vp, sz, u32, vp]
     lib.beam_status_string.argtypes = [i32]
     lib.beam_status_string.restype = ctypes.c_char_p
     for n in ("beam_moe_workspace_layout", "beam_moe_route", "beam_moe_dispatch", "beam_moe_experts",
-              "beam_moe_forward", "beam_moe_read_device_status", "beam_moe_debug_timeout"):
+              "beam_moe_forward", "beam_moe_forward_stage", "beam_moe_read_device_status",
+              "beam_moe_debug_timeout"):
         getattr(lib, n).restype = i32
     _lib = lib
     return lib
@@ -144,6 +158,8 @@ def _check(code: int, where: str):
 
 
 def _wdtype(w) -> int:
+    if isinstance(w, int):
+        return w
     if isinstance(w, str):
         return {"bf16": BEAM_BF16, "nvfp4": BEAM_NVFP4}[w]
     return BEAM_NVFP4 if w["gate"].dtype == torch.uint8 else BEAM_BF16
@@ -198,6 +214,49 @@ def beam_moe_forward(sh, x, router_w, router_bias, weights: dict, y, topk_ids, t
     _check(load().beam_moe_forward(ctypes.byref(sh), _ptr(x), _act_dtype(x), _ptr(router_w), _ptr(router_bias),
                                    ctypes.byref(ew), _ptr(y), _ptr(topk_ids), _ptr(topk_w), _ptr(workspace),
                                    workspace.numel(), _stream(stream)), "beam_moe_forward")
+
+
+class ForwardCall:
+    """The marshalled arguments of one forward call, reusable across calls.
+
+    ``stage(i)`` enqueues step i of the forward (``STAGES[i]``) through
+    beam_moe_forward_stage; ``run()`` enqueues all of them through
+    beam_moe_forward.  The tensors must stay alive while the object is used."""
+
+    def __init__(self, sh, x, router_w, router_bias, weights: dict, y, topk_ids, topk_w, workspace, stream=None):
+        self.sh = sh
+        self._ew = _weights(weights)
+        self._args = _Args(_ptr(x).value, _act_dtype(x), _ptr(router_w).value,
+                           None if router_bias is None else _ptr(router_bias).value, ctypes.pointer(self._ew),
+                           _ptr(y).value, _ptr(topk_ids).value, _ptr(topk_w).value)
+        self._keep = (x, router_w, router_bias, weights, y, topk_ids, topk_w, workspace)
+        self._ws = _ptr(workspace)
+        self._ws_bytes = workspace.numel()
+        self._stream = _stream(stream)
+        self._lib = load()
+
+    def stage(self, i: int):
+        _check(self._lib.beam_moe_forward_stage(ctypes.byref(self.sh), ctypes.byref(self._args), int(i), self._ws,
+                                                self._ws_bytes, self._stream), f"beam_moe_forward_stage({i})")
+
+    def run(self):
+        a = self._args
+        _check(self._lib.beam_moe_forward(ctypes.byref(self.sh), a.x, a.xdtype, a.router_w, a.router_bias,
+                                          a.weights, a.y, a.topk_ids, a.topk_w, self._ws, self._ws_bytes,
+                                          self._stream), "beam_moe_forward")
+
+
+def beam_moe_forward_stage(sh, stage: int, x, router_w, router_bias, weights: dict, y, topk_ids, topk_w,
+                           workspace, stream=None):
+    ForwardCall(sh, x, router_w, router_bias, weights, y, topk_ids, topk_w, workspace, stream).stage(stage)
+
+
+def beam_moe_stage_kernel_count(sh, stage: int) -> int:
+    """Kernels the library launches for stage ``stage`` of a forward of ``sh``."""
+    n = int(load().beam_moe_stage_kernel_count(ctypes.byref(sh), int(stage)))
+    if n < 0:
+        raise BeamError(BEAM_ERR_UNSUPPORTED, "beam_moe_stage_kernel_count")
+    return n
 
 
 def beam_moe_read_device_status(workspace, stream=None):

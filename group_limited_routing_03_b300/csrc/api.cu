@@ -201,60 +201,117 @@ uint32_t pow2_at_least(uint32_t v) {
   return p;
 }
 
-beam_status_t run_experts(const beam_moe_shape_t& s, const void* x, bool x_bf16, const beam_expert_weights_t* wts,
-                          const int32_t* ids, const float* w, void* y, void* ws, const Layout& L,
-                          const DeviceInfo& d, bool hist_ready, cudaStream_t stream) {
+beam_status_t run_gather(const beam_moe_shape_t& s, const void* x, bool x_bf16, void* ws, const Layout& L,
+                         const DeviceInfo& d, cudaStream_t stream) {
+  const int R = s.T * kTopK;
+  return cuda_status(launch_gather(x, x_bf16, s.H, at<int32_t>(ws, L.perm), R, at<__nv_bfloat16>(ws, L.xp), d.sms,
+                                   stream));
+}
+
+// mode 0: gate/up (+SwiGLU) -> h; mode 1: down -> yr.
+beam_status_t run_gemm(int mode, const beam_moe_shape_t& s, const beam_expert_weights_t* wts, void* ws,
+                       const Layout& L, const DeviceInfo& d, cudaStream_t stream) {
   const int R = s.T * kTopK;
   const uint64_t R_pad = static_cast<uint64_t>((R + kBoxRows - 1) / kBoxRows * kBoxRows);
   const int nmax = chunk_rows(s.T);
-  beam_status_t st = run_dispatch(s, ids, ws, L, nmax, hist_ready, stream);
-  if (st != BEAM_OK) return st;
   __nv_bfloat16* xp = at<__nv_bfloat16>(ws, L.xp);
   __nv_bfloat16* h = at<__nv_bfloat16>(ws, L.h);
   __nv_bfloat16* yr = at<__nv_bfloat16>(ws, L.yr);
-  if (launch_gather(x, x_bf16, s.H, at<int32_t>(ws, L.perm), R, xp, d.sms, stream) != cudaSuccess)
-    return BEAM_ERR_CUDA;
-
-  CUtensorMap m_gate, m_up, m_down, m_xp, m_h;
   const uint64_t E = kExperts, H = s.H, I = s.I;
-  if (!make_bf16_map(&m_gate, wts->gate, H, E * I, kBlockM) || !make_bf16_map(&m_up, wts->up, H, E * I, kBlockM) ||
-      !make_bf16_map(&m_down, wts->down, I, E * H, kBlockM) ||
-      !make_bf16_map(&m_xp, xp, H, R_pad, kBoxRows) || !make_bf16_map(&m_h, h, I, R_pad, kBoxRows))
-    return BEAM_ERR_CUDA;
-
-  const size_t budget = static_cast<size_t>(d.smem_optin) - 1024 - 256;
-  for (int mode = 0; mode < 2; ++mode) {
-    GemmParams p;
-    p.counts = at<int32_t>(ws, L.counts);
-    p.offsets = at<int32_t>(ws, L.offsets);
-    p.chunk_prefix = at<int32_t>(ws, L.chunk_prefix);
-    p.m_tiles = (mode == 0 ? s.I : s.H) / kBlockM;
-    p.a_rows_per_expert = mode == 0 ? s.I : s.H;
-    p.k_blocks = (mode == 0 ? s.H : s.I) / kBlockK;
-    p.nmax = nmax;
-    const size_t sb = gemm_stage_bytes(mode, nmax);
-    int stages = static_cast<int>(budget / sb);
-    if (stages > 8) stages = 8;
-    if (stages < 2) return BEAM_ERR_UNSUPPORTED;
-    p.stages = stages;
-    p.acc_cols = static_cast<uint32_t>(mode == 0 ? 2 * nmax : nmax);
-    int acc_stages = static_cast<int>(512 / p.acc_cols);
-    if (acc_stages > 4) acc_stages = 4;
-    if (acc_stages < 1) acc_stages = 1;
-    p.acc_stages = acc_stages;
-    p.tmem_cols = pow2_at_least(static_cast<uint32_t>(acc_stages) * p.acc_cols);
-    p.out = mode == 0 ? h : yr;
-    p.out_ld = mode == 0 ? s.I : s.H;
-    p.gs0 = nullptr;
-    p.gs1 = nullptr;
-    p.status = at<uint32_t>(ws, L.status);
-    p.timeout_ns = kDefaultTimeoutNs;
-    const size_t smem = 1024 + static_cast<size_t>(stages) * sb + (2 * stages + 2 * acc_stages + 1) * 8 + 16;
-    const cudaError_t e = mode == 0 ? launch_gemm(0, m_gate, m_up, m_xp, p, d.sms, smem, stream)
-                                    : launch_gemm(1, m_down, m_down, m_h, p, d.sms, smem, stream);
-    if (e != cudaSuccess) return BEAM_ERR_CUDA;
+  CUtensorMap ma0, ma1, mb;
+  if (mode == 0) {
+    if (!make_bf16_map(&ma0, wts->gate, H, E * I, kBlockM) || !make_bf16_map(&ma1, wts->up, H, E * I, kBlockM) ||
+        !make_bf16_map(&mb, xp, H, R_pad, kBoxRows))
+      return BEAM_ERR_CUDA;
+  } else {
+    if (!make_bf16_map(&ma0, wts->down, I, E * H, kBlockM) || !make_bf16_map(&mb, h, I, R_pad, kBoxRows))
+      return BEAM_ERR_CUDA;
+    ma1 = ma0;
   }
-  return cuda_status(launch_combine(yr, at<int32_t>(ws, L.pos), w, s.T, s.H, y, x_bf16, stream));
+  GemmParams p;
+  p.counts = at<int32_t>(ws, L.counts);
+  p.offsets = at<int32_t>(ws, L.offsets);
+  p.chunk_prefix = at<int32_t>(ws, L.chunk_prefix);
+  p.m_tiles = (mode == 0 ? s.I : s.H) / kBlockM;
+  p.a_rows_per_expert = mode == 0 ? s.I : s.H;
+  p.k_blocks = (mode == 0 ? s.H : s.I) / kBlockK;
+  p.nmax = nmax;
+  const size_t budget = static_cast<size_t>(d.smem_optin) - 1024 - 256;
+  const size_t sb = gemm_stage_bytes(mode, nmax);
+  int stages = static_cast<int>(budget / sb);
+  if (stages > 8) stages = 8;
+  if (stages < 2) return BEAM_ERR_UNSUPPORTED;
+  p.stages = stages;
+  p.acc_cols = static_cast<uint32_t>(mode == 0 ? 2 * nmax : nmax);
+  int acc_stages = static_cast<int>(512 / p.acc_cols);
+  if (acc_stages > 4) acc_stages = 4;
+  if (acc_stages < 1) acc_stages = 1;
+  p.acc_stages = acc_stages;
+  p.tmem_cols = pow2_at_least(static_cast<uint32_t>(acc_stages) * p.acc_cols);
+  p.out = mode == 0 ? h : yr;
+  p.out_ld = mode == 0 ? s.I : s.H;
+  p.gs0 = nullptr;
+  p.gs1 = nullptr;
+  p.status = at<uint32_t>(ws, L.status);
+  p.timeout_ns = kDefaultTimeoutNs;
+  const size_t smem = 1024 + static_cast<size_t>(stages) * sb + (2 * stages + 2 * acc_stages + 1) * 8 + 16;
+  return cuda_status(launch_gemm(mode, ma0, ma1, mb, p, d.sms, smem, stream));
+}
+
+beam_status_t run_combine(const beam_moe_shape_t& s, const float* w, void* y, bool y_bf16, void* ws, const Layout& L,
+                          cudaStream_t stream) {
+  return cuda_status(
+      launch_combine(at<__nv_bfloat16>(ws, L.yr), at<int32_t>(ws, L.pos), w, s.T, s.H, y, y_bf16, stream));
+}
+
+beam_status_t run_experts(const beam_moe_shape_t& s, const void* x, bool x_bf16, const beam_expert_weights_t* wts,
+                          const int32_t* ids, const float* w, void* y, void* ws, const Layout& L,
+                          const DeviceInfo& d, bool hist_ready, cudaStream_t stream) {
+  beam_status_t st = run_dispatch(s, ids, ws, L, chunk_rows(s.T), hist_ready, stream);
+  if (st == BEAM_OK) st = run_gather(s, x, x_bf16, ws, L, d, stream);
+  if (st == BEAM_OK) st = run_gemm(0, s, wts, ws, L, d, stream);
+  if (st == BEAM_OK) st = run_gemm(1, s, wts, ws, L, d, stream);
+  if (st == BEAM_OK) st = run_combine(s, w, y, x_bf16, ws, L, stream);
+  return st;
+}
+
+// Validation shared by beam_moe_forward and beam_moe_forward_stage.
+beam_status_t check_forward(const beam_moe_shape_t* shape, const beam_moe_args_t& a, void* workspace,
+                            size_t workspace_bytes, Layout& L, DeviceInfo& d) {
+  beam_status_t st = check_shape(shape);
+  if (st != BEAM_OK) return st;
+  if (!a.x || !a.router_w || !a.topk_ids || !a.topk_w || !a.y) return BEAM_ERR_INVALID_ARG;
+  if (!aligned16(a.x) || !aligned16(a.router_w) || !aligned16(a.topk_ids) || !aligned16(a.topk_w) ||
+      !aligned16(a.y) || (a.router_bias && !aligned16(a.router_bias)))
+    return BEAM_ERR_INVALID_ARG;
+  if (a.xdtype != BEAM_F32 && a.xdtype != BEAM_BF16) return BEAM_ERR_UNSUPPORTED;
+  st = check_weights(a.weights);
+  if (st != BEAM_OK) return st;
+  st = check_workspace(shape, workspace, workspace_bytes, L);
+  if (st != BEAM_OK) return st;
+  if (!device_info(d)) return BEAM_ERR_CUDA;
+  if (d.cc_major < 10) return BEAM_ERR_UNSUPPORTED;
+  return BEAM_OK;
+}
+
+beam_status_t run_stage(const beam_moe_shape_t& s, const beam_moe_args_t& a, int stage, void* ws, const Layout& L,
+                        const DeviceInfo& d, cudaStream_t cs) {
+  const bool xb = a.xdtype == BEAM_BF16;
+  switch (stage) {
+    case BEAM_STAGE_ROUTE:
+      return run_route(s, a.x, xb, a.router_w, a.router_bias, a.topk_ids, a.topk_w, ws, L, d, cs);
+    case BEAM_STAGE_DISPATCH:
+      return run_dispatch(s, a.topk_ids, ws, L, chunk_rows(s.T), true, cs);
+    case BEAM_STAGE_GATHER:
+      return run_gather(s, a.x, xb, ws, L, d, cs);
+    case BEAM_STAGE_GATE_UP:
+      return run_gemm(0, s, a.weights, ws, L, d, cs);
+    case BEAM_STAGE_DOWN:
+      return run_gemm(1, s, a.weights, ws, L, d, cs);
+    case BEAM_STAGE_COMBINE:
+      return run_combine(s, a.topk_w, a.y, xb, ws, L, cs);
+  }
+  return BEAM_ERR_INVALID_ARG;
 }
 
 }  // namespace
@@ -347,25 +404,47 @@ beam_status_t beam_moe_forward(const beam_moe_shape_t* shape, const void* x, bea
                                const float* router_w, const float* router_bias, const beam_expert_weights_t* weights,
                                void* y, int32_t* topk_ids, float* topk_w, void* workspace, size_t workspace_bytes,
                                void* stream) {
-  beam_status_t st = check_shape(shape);
-  if (st != BEAM_OK) return st;
-  if (!x || !router_w || !topk_ids || !topk_w || !y) return BEAM_ERR_INVALID_ARG;
-  if (!aligned16(x) || !aligned16(router_w) || !aligned16(topk_ids) || !aligned16(topk_w) || !aligned16(y) ||
-      (router_bias && !aligned16(router_bias)))
-    return BEAM_ERR_INVALID_ARG;
-  if (xdtype != BEAM_F32 && xdtype != BEAM_BF16) return BEAM_ERR_UNSUPPORTED;
-  st = check_weights(weights);
-  if (st != BEAM_OK) return st;
+  const beam_moe_args_t a = {x, xdtype, router_w, router_bias, weights, y, topk_ids, topk_w};
   Layout L;
-  st = check_workspace(shape, workspace, workspace_bytes, L);
-  if (st != BEAM_OK) return st;
   DeviceInfo d;
-  if (!device_info(d)) return BEAM_ERR_CUDA;
-  if (d.cc_major < 10) return BEAM_ERR_UNSUPPORTED;
-  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  st = run_route(*shape, x, xdtype == BEAM_BF16, router_w, router_bias, topk_ids, topk_w, workspace, L, d, cs);
+  beam_status_t st = check_forward(shape, a, workspace, workspace_bytes, L, d);
   if (st != BEAM_OK) return st;
-  return run_experts(*shape, x, xdtype == BEAM_BF16, weights, topk_ids, topk_w, y, workspace, L, d, true, cs);
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  for (int stage = 0; stage < BEAM_STAGE_COUNT && st == BEAM_OK; ++stage)
+    st = run_stage(*shape, a, stage, workspace, L, d, cs);
+  return st;
+}
+
+beam_status_t beam_moe_forward_stage(const beam_moe_shape_t* shape, const beam_moe_args_t* args, beam_stage_t stage,
+                                     void* workspace, size_t workspace_bytes, void* stream) {
+  if (args == nullptr) return BEAM_ERR_INVALID_ARG;
+  if (static_cast<int>(stage) < 0 || static_cast<int>(stage) >= BEAM_STAGE_COUNT) return BEAM_ERR_INVALID_ARG;
+  Layout L;
+  DeviceInfo d;
+  const beam_status_t st = check_forward(shape, *args, workspace, workspace_bytes, L, d);
+  if (st != BEAM_OK) return st;
+  return run_stage(*shape, *args, stage, workspace, L, d, static_cast<cudaStream_t>(stream));
+}
+
+int32_t beam_moe_stage_kernel_count(const beam_moe_shape_t* shape, beam_stage_t stage) {
+  if (check_shape(shape) != BEAM_OK) return -1;
+  DeviceInfo d;
+  if (!device_info(d)) return -1;
+  switch (stage) {
+    case BEAM_STAGE_ROUTE: {
+      Layout L;
+      make_layout(*shape, L);
+      int sp = router_splits(shape->T, shape->H, d.sms);
+      if (sp > L.split_cap) sp = L.split_cap;
+      return sp > 1 ? 2 : 1;
+    }
+    case BEAM_STAGE_DISPATCH: return 2;
+    case BEAM_STAGE_GATHER:
+    case BEAM_STAGE_GATE_UP:
+    case BEAM_STAGE_DOWN:
+    case BEAM_STAGE_COMBINE: return 1;
+    default: return -1;
+  }
 }
 
 beam_status_t beam_moe_read_device_status(void* workspace, uint32_t* where, void* stream) {

@@ -144,6 +144,44 @@ beam_status_t beam_moe_forward(const beam_moe_shape_t* shape, const void* x, bea
                                float* topk_w, void* workspace, size_t workspace_bytes,
                                void* stream);
 
+/* The steps of beam_moe_forward, in order.  beam_moe_forward enqueues all of
+ * them; beam_moe_forward_stage enqueues one, so that a caller can put events
+ * between them (per-step timing) or run the steps on its own schedule. */
+typedef enum {
+  BEAM_STAGE_ROUTE = 0,    /* router GEMV + selection (+ per-tile histogram) */
+  BEAM_STAGE_DISPATCH = 1, /* counts, offsets, perm, pos from the histograms */
+  BEAM_STAGE_GATHER = 2,   /* token rows into route order (BF16) */
+  BEAM_STAGE_GATE_UP = 3,  /* grouped gate/up GEMM with the SwiGLU epilogue */
+  BEAM_STAGE_DOWN = 4,     /* grouped down GEMM */
+  BEAM_STAGE_COMBINE = 5,  /* weighted sum of each token's expert outputs */
+  BEAM_STAGE_COUNT = 6
+} beam_stage_t;
+
+/* All tensors of one forward call (the arguments of beam_moe_forward). */
+typedef struct {
+  const void* x;
+  beam_dtype_t xdtype;
+  const float* router_w;
+  const float* router_bias;
+  const beam_expert_weights_t* weights;
+  void* y;
+  int32_t* topk_ids;
+  float* topk_w;
+} beam_moe_args_t;
+
+/* Enqueue stage `stage` of the forward pass.  Each stage reads what the
+ * previous stages left in `workspace` (and in topk_ids / topk_w), so the
+ * stages of one forward must be issued in order, on one stream (or with the
+ * caller's own ordering).  Arguments are validated as beam_moe_forward does. */
+beam_status_t beam_moe_forward_stage(const beam_moe_shape_t* shape, const beam_moe_args_t* args,
+                                     beam_stage_t stage, void* workspace, size_t workspace_bytes,
+                                     void* stream);
+
+/* Number of kernels stage `stage` launches for `shape` on the current device
+ * (the router launches a second kernel when it splits the hidden dimension
+ * across CTAs); -1 on an unsupported shape or stage. */
+int32_t beam_moe_stage_kernel_count(const beam_moe_shape_t* shape, beam_stage_t stage);
+
 /* Synchronises `stream`, returns the device status word of `workspace`
  * (BEAM_OK when no kernel reported a problem) and clears it.  `where`
  * (nullable) receives the code of the wait that gave up. */

@@ -20,7 +20,7 @@ import torch
 __all__ = [
     "BeamError", "Shape", "shape", "workspace_size", "workspace_layout", "alloc_workspace",
     "beam_moe_route", "beam_moe_dispatch", "beam_moe_experts", "beam_moe_forward", "beam_moe_forward_stage",
-    "ForwardCall", "STAGES", "beam_moe_stage_kernel_count",
+    "ForwardCall", "STAGES", "beam_moe_stage_kernel_count", "beam_moe_route_noalloc",
     "beam_moe_read_device_status", "beam_moe_debug_timeout", "beam_status_string", "BeamMoE",
     "library_path", "load",
 ]
@@ -92,6 +92,8 @@ def load():
     lib.beam_moe_forward.argtypes = [sp, vp, i32, vp, vp, ctypes.POINTER(_ExpertWeights), vp, vp, vp, vp, sz, vp]
     lib.beam_moe_forward_stage.argtypes = [sp, ctypes.POINTER(_Args), i32, vp, sz, vp]
     lib.beam_moe_read_device_status.argtypes = [vp, ctypes.POINTER(u32), vp]
+    lib.beam_moe_route_noalloc.argtypes = [sp, vp, i32, vp, vp, vp, vp, vp]
+    lib.beam_moe_route_noalloc.restype = i32
     lib.beam_moe_stage_kernel_count.argtypes = [sp, i32]
     lib.beam_moe_stage_kernel_count.restype = ctypes.c_int32
     lib.beam_moe_debug_timeout.argtypes = [vp, sz, u32, vp]
@@ -195,6 +197,16 @@ def beam_moe_route(sh, x, router_w, router_bias, topk_ids, topk_w, workspace, st
     _check(load().beam_moe_route(ctypes.byref(sh), _ptr(x), _act_dtype(x), _ptr(router_w), _ptr(router_bias),
                                  _ptr(topk_ids), _ptr(topk_w), _ptr(workspace), workspace.numel(),
                                  _stream(stream)), "beam_moe_route")
+
+
+def beam_moe_route_noalloc(sh, x, router_w, router_bias, topk_ids, topk_w, stream=None):
+    """beam_moe_route without a workspace, for callers that cannot allocate
+    device memory: scratch lives in a 6 MiB library-owned device buffer
+    (T <= 65536).  Calls share that buffer, so calls that overlap on the GPU
+    race; the first call on a device should come before any stream capture."""
+    _check(load().beam_moe_route_noalloc(ctypes.byref(sh), _ptr(x), _act_dtype(x), _ptr(router_w),
+                                         _ptr(router_bias), _ptr(topk_ids), _ptr(topk_w), _stream(stream)),
+           "beam_moe_route_noalloc")
 
 
 def beam_moe_dispatch(sh, topk_ids, workspace, stream=None):

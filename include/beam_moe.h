@@ -194,6 +194,27 @@ beam_status_t beam_moe_read_device_status(void* workspace, uint32_t* where, void
 beam_status_t beam_moe_debug_timeout(void* workspace, size_t workspace_bytes, uint32_t timeout_us,
                                      void* stream);
 
+/* Routing without a workspace, for callers that cannot allocate device memory
+ * (a host framework that owns all device memory and hands a plugin only its
+ * inputs and outputs, or a serving loop that must never allocate, since an
+ * allocation can stall the device).  The Beam post has no counterpart: this
+ * is an integration convenience.  Same result as beam_moe_route (the hidden
+ * dimension may be split across fewer CTAs, so FP32 logits can differ in the
+ * last bits).  Arguments as beam_moe_route, without the workspace.
+ *   - Scratch: a library-owned static device buffer of 6 MiB (2 MiB of tile
+ *     histograms + 4 MiB of partial logits) on every GPU that loads the
+ *     library, held until the process exits.  No allocation in any call.
+ *   - Limit: T <= 65536, else BEAM_ERR_UNSUPPORTED.
+ *   - The first call on a device looks up the buffer's device address (once
+ *     per device, with that device current); make that first call before any
+ *     stream capture.
+ *   - All calls share the buffer and it keeps the last call's contents
+ *     (nothing in it needs to start at zero); calls that overlap on the GPU,
+ *     on any stream or thread, race and must be serialised by the caller. */
+beam_status_t beam_moe_route_noalloc(const beam_moe_shape_t* shape, const void* x, beam_dtype_t xdtype,
+                                     const float* router_w, const float* router_bias, int32_t* topk_ids,
+                                     float* topk_w, void* stream);
+
 /* Static description of a status code. */
 const char* beam_status_string(beam_status_t status);
 

@@ -69,17 +69,22 @@ class ClockSampler:
         self.period = period_s
         self.samples = []
         self.max_mhz = None
+        self.index = index
+        self.source = None
         self._stop = threading.Event()
         self._thread = None
+        self._proc = None
+        self._nvml = None
         try:
             import pynvml
 
             pynvml.nvmlInit()
-            self._nvml = pynvml
             self._h = pynvml.nvmlDeviceGetHandleByIndex(index)
             self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self._h, pynvml.NVML_CLOCK_SM)
-        except Exception:  # NVML unavailable: report no clocks
-            self._nvml = None
+            self._nvml = pynvml
+            self.source = "nvml"
+        except Exception as exc:  # fall back to nvidia-smi's sampling loop
+            print(f"bench: NVML unavailable ({exc!r}); sampling clocks with nvidia-smi", file=sys.stderr)
 
     def _run(self):
         nv = self._nvml
@@ -96,12 +101,37 @@ class ClockSampler:
         if self._nvml is not None:
             self._thread = threading.Thread(target=self._run, daemon=True)
             self._thread.start()
+        else:
+            import subprocess
+
+            try:
+                self._proc = subprocess.Popen(
+                    ["nvidia-smi", "-i", str(self.index),
+                     "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.active",
+                     "--format=csv,noheader,nounits", "-lms", "20"],
+                    stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                self.source = "nvidia-smi"
+                time.sleep(0.3)  # let the first sample land
+            except Exception as exc:
+                print(f"bench: no clock sampling ({exc!r})", file=sys.stderr)
         return self
 
     def __exit__(self, *exc):
         self._stop.set()
         if self._thread is not None:
             self._thread.join()
+        if self._proc is not None:
+            time.sleep(0.05)
+            self._proc.terminate()
+            out, _ = self._proc.communicate(timeout=10)
+            for line in out.splitlines():
+                parts = [q.strip() for q in line.split(",")]
+                try:
+                    mhz, mx, rs = float(parts[0]), float(parts[1]), int(parts[2], 16)
+                except (ValueError, IndexError):
+                    continue
+                self.max_mhz = mx
+                self.samples.append((mhz, rs))
 
     def summary(self):
         if not self.samples:
@@ -112,7 +142,7 @@ class ClockSampler:
             active |= int(r)
         names = [n for n, bit in self.REASONS.items() if active & bit and n != "gpu_idle"]
         return {"sm_mhz": float(statistics.median(mhz)), "sm_max_mhz": self.max_mhz, "reasons": names,
-                "samples": len(mhz)}
+                "samples": len(mhz), "source": self.source}
 
 
 # ---------------------------------------------------------------------------
@@ -363,6 +393,8 @@ def main():
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--small", action="store_true",
+                    help="profiling shape H=2048, I=1024 (3.2 GB of experts) instead of 5120/2560")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -381,7 +413,8 @@ def main():
 
     _build.build()
     pk = peaks()
-    wl = inputs.workload(args.workload)
+    small = dict(H=2048, I=1024) if args.small else {}
+    wl = inputs.workload(args.workload, **small)
     m, state = measure(wl, args.steps, args.warmup, dev, world, torch.cuda.current_device())
     total_ms = max_over_ranks(m["total_ms"], world)
     sn = step_numbers(wl, m, args.steps)
@@ -402,13 +435,13 @@ def main():
 
     prefill = None
     if not args.no_prefill:
-        pw = inputs.workload("prefill")
+        pw = inputs.workload("prefill", **small)
         pm, pstate = measure(pw, max(3, args.steps // 2), args.warmup, dev, world, torch.cuda.current_device())
         p_ms = max_over_ranks(pm["total_ms"], world)
         psn = step_numbers(pw, pm, max(3, args.steps // 2))
         phbm, ptc = roofline(pw, pm, pk)
         prefill = dict(value=pw.T * max(3, args.steps // 2) * world / (p_ms * 1e-3), unit="tokens/s",
-                       config={"workload": "prefill T=8192 H=5120 I=2560 E=256 bf16 experts", "T": pw.T},
+                       config={"workload": f"prefill T={pw.T} H={pw.H} I={pw.I} E=256 bf16 experts", "T": pw.T},
                        roofline=ptc, roofline_hbm=phbm, clocks=pm["clocks"], **psn)
         del pstate
         torch.cuda.empty_cache()

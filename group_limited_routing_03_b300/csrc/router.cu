@@ -6,14 +6,17 @@
 // 4 groups kept, the top-8 experts inside them, weights normalised and scaled.
 //
 // One CTA owns 32 tokens.  Phase 1 computes the FP32 logits of those tokens
-// against all 256 experts (thread e owns expert e, 32 accumulators, the
-// router weight streamed through shared memory in 32-wide k-chunks).  When the
-// hidden dimension is split across CTAs (small T) the partial logits go to the
-// workspace and a second kernel sums them in a fixed order.  Phase 2 is the
-// selection: one warp per token, lane l holding experts 8l..8l+7 (so the four
-// lanes 4j..4j+3 hold group j); group top-2 sums, group ranking and the
-// masked top-8 all run on warp shuffles.  The CTA also counts its routes per
-// expert for the dispatch step.
+// against all 256 experts: thread (warp w, lane l) owns experts
+// 128*(w%2) + l + 32*i (i = 0..3) and tokens 8*(w/2) .. +7, i.e. 32
+// accumulators; the router weight and the activations stream through shared
+// memory in 32-wide k-chunks, the next chunk prefetched into registers while
+// the current one is consumed.  When the hidden dimension is split across
+// CTAs (small T) the partial logits go to the workspace and a second kernel,
+// one CTA per token, sums them in split order.  Phase 2 is the selection: one
+// warp per token, lane l holding experts 8l..8l+7 (so the four lanes
+// 4j..4j+3 hold group j); group top-2 sums, group ranking and the masked
+// top-8 all run on warp shuffles.  The tile's routes are counted per expert
+// for the dispatch step.
 #include <cuda_bf16.h>
 
 #include <cmath>
@@ -23,15 +26,16 @@
 namespace beam {
 namespace {
 
-constexpr int kLogitLd = kExperts + 4;  // row stride of the logits tile (16-byte aligned rows)
-constexpr int kWLd = kExperts + 1;      // row stride of the transposed weight chunk
+constexpr int kLogitLd = kExperts + 4;       // row stride of the logits tile (16-byte aligned rows)
+constexpr int kWLd = kRouterKChunk + 1;      // row stride of the weight chunk [e][k] (conflict-free)
+constexpr int kXLd = kRouterTile + 4;        // row stride of the activation chunk [k][token]
 
 struct RouterSmem {
   union {
-    float w[kRouterKChunk * kWLd];       // weight chunk, [k][e]
+    float w[kExperts * kWLd];              // weight chunk, [e][k]
     float logits[kRouterTile * kLogitLd];  // [token][e]
   };
-  float x[kRouterKChunk * kRouterTile];  // activation chunk, [k][token]
+  float x[kRouterKChunk * kXLd];           // activation chunk, [k][token]
   int hist[kExperts];
 };
 
@@ -39,29 +43,54 @@ __device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
   return __uint_as_float(static_cast<uint32_t>(b) << 16);
 }
 
-// Loads activations [t0, t0+32) x [k0, k0+32) into s.x as [k][token] (f32).
+// Register staging of one k-chunk: 8 float4 of the router weight (rows
+// tid/8 + 32*j, columns 4*(tid%8)..+3) and 4 activations (token tid/8,
+// columns 4*(tid%8)..+3).
+struct ChunkRegs {
+  float4 w[8];
+  float x[4];
+};
+
 template <bool kBf16>
-__device__ __forceinline__ void load_x_chunk(const RouterParams& p, RouterSmem& s, int t0, int k0) {
+__device__ __forceinline__ void load_chunk(const RouterParams& p, int t0, int k0, ChunkRegs& r) {
   const int tid = threadIdx.x;
-  const int tok = tid >> 3;        // 0..31
-  const int kq = (tid & 7) * 4;    // 0..28
-  const int t = t0 + tok;
-  float v[4] = {0.f, 0.f, 0.f, 0.f};
+  const int c4 = 4 * (tid & 7);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int row = (tid >> 3) + 32 * j;
+    r.w[j] = __ldg(reinterpret_cast<const float4*>(p.wr + static_cast<size_t>(row) * p.H + k0 + c4));
+  }
+  const int t = t0 + (tid >> 3);
   if (t < p.T) {
-    const size_t base = static_cast<size_t>(t) * p.H + k0 + kq;
+    const size_t base = static_cast<size_t>(t) * p.H + k0 + c4;
     if (kBf16) {
-      const uint2 raw = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(p.x) + base);
-      v[0] = bf16_bits_to_float(raw.x & 0xFFFFu);
-      v[1] = bf16_bits_to_float(raw.x >> 16);
-      v[2] = bf16_bits_to_float(raw.y & 0xFFFFu);
-      v[3] = bf16_bits_to_float(raw.y >> 16);
+      const uint2 raw = __ldg(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(p.x) + base));
+      r.x[0] = bf16_bits_to_float(raw.x & 0xFFFFu);
+      r.x[1] = bf16_bits_to_float(raw.x >> 16);
+      r.x[2] = bf16_bits_to_float(raw.y & 0xFFFFu);
+      r.x[3] = bf16_bits_to_float(raw.y >> 16);
     } else {
-      const float4 f = *reinterpret_cast<const float4*>(static_cast<const float*>(p.x) + base);
-      v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
+      const float4 f = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(p.x) + base));
+      r.x[0] = f.x; r.x[1] = f.y; r.x[2] = f.z; r.x[3] = f.w;
     }
+  } else {
+    r.x[0] = r.x[1] = r.x[2] = r.x[3] = 0.0f;
+  }
+}
+
+__device__ __forceinline__ void store_chunk(RouterSmem& s, const ChunkRegs& r) {
+  const int tid = threadIdx.x;
+  const int c4 = 4 * (tid & 7);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    float* dst = &s.w[((tid >> 3) + 32 * j) * kWLd + c4];
+    dst[0] = r.w[j].x;
+    dst[1] = r.w[j].y;
+    dst[2] = r.w[j].z;
+    dst[3] = r.w[j].w;
   }
 #pragma unroll
-  for (int j = 0; j < 4; ++j) s.x[(kq + j) * kRouterTile + tok] = v[j];
+  for (int j = 0; j < 4; ++j) s.x[(c4 + j) * kXLd + (tid >> 3)] = r.x[j];
 }
 
 // Selection for one token, by one warp.  `lrow` = the token's 256 logits in
@@ -180,75 +209,95 @@ __device__ __forceinline__ void select_tile(const RouterParams& p, RouterSmem& s
 template <bool kBf16>
 __global__ void __launch_bounds__(256) router_gemm_kernel(RouterParams p) {
   __shared__ __align__(16) RouterSmem s;
-  const int e = threadIdx.x;  // expert owned by this thread
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ebase = 128 * (warp & 1) + lane;  // experts ebase + 32*i
+  const int tbase = 8 * (warp >> 1);          // tokens tbase .. tbase+7 of the tile
   const int tile = blockIdx.x, split = blockIdx.y;
   const int t0 = tile * kRouterTile;
   const int kc_begin = split * p.n_kchunks / p.splits;
   const int kc_end = (split + 1) * p.n_kchunks / p.splits;
   s.hist[threadIdx.x] = 0;
+  if (p.splits > 1 && split == 0) p.tile_hist[static_cast<size_t>(threadIdx.x) * p.n_tiles + tile] = 0;
 
-  float acc[kRouterTile];
+  float acc[4][8];
 #pragma unroll
-  for (int j = 0; j < kRouterTile; ++j) acc[j] = 0.0f;
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
 
+  ChunkRegs r;
+  if (kc_begin < kc_end) load_chunk<kBf16>(p, t0, kc_begin * kRouterKChunk, r);
   for (int kc = kc_begin; kc < kc_end; ++kc) {
-    const int k0 = kc * kRouterKChunk;
-    // Weight chunk: warp w loads rows 32w..32w+31, lanes along k (coalesced),
-    // stored transposed [k][e] (row stride 257 keeps the stores conflict-free).
-#pragma unroll 8
-    for (int i = 0; i < 32; ++i) {
-      const int row = warp * 32 + i;
-      s.w[lane * kWLd + row] = p.wr[static_cast<size_t>(row) * p.H + k0 + lane];
-    }
-    load_x_chunk<kBf16>(p, s, t0, k0);
+    store_chunk(s, r);
     __syncthreads();
-#pragma unroll 4
+    if (kc + 1 < kc_end) load_chunk<kBf16>(p, t0, (kc + 1) * kRouterKChunk, r);
+#pragma unroll 8
     for (int kk = 0; kk < kRouterKChunk; ++kk) {
-      const float wv = s.w[kk * kWLd + e];
-      const float4* xr = reinterpret_cast<const float4*>(&s.x[kk * kRouterTile]);
+      float wv[4];
 #pragma unroll
-      for (int q = 0; q < kRouterTile / 4; ++q) {
-        const float4 xv = xr[q];
-        acc[4 * q + 0] = fmaf(xv.x, wv, acc[4 * q + 0]);
-        acc[4 * q + 1] = fmaf(xv.y, wv, acc[4 * q + 1]);
-        acc[4 * q + 2] = fmaf(xv.z, wv, acc[4 * q + 2]);
-        acc[4 * q + 3] = fmaf(xv.w, wv, acc[4 * q + 3]);
-      }
+      for (int i = 0; i < 4; ++i) wv[i] = s.w[(ebase + 32 * i) * kWLd + kk];
+      const float4 xa = *reinterpret_cast<const float4*>(&s.x[kk * kXLd + tbase]);
+      const float4 xb = *reinterpret_cast<const float4*>(&s.x[kk * kXLd + tbase + 4]);
+      const float xv[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(xv[j], wv[i], acc[i][j]);
     }
     __syncthreads();
   }
 
   if (p.splits > 1) {
 #pragma unroll
-    for (int j = 0; j < kRouterTile; ++j) {
-      const int t = t0 + j;
-      if (t < p.T) p.part[(static_cast<size_t>(split) * p.T + t) * kExperts + e] = acc[j];
+    for (int j = 0; j < 8; ++j) {
+      const int t = t0 + tbase + j;
+      if (t < p.T) {
+        float* dst = p.part + (static_cast<size_t>(split) * p.T + t) * kExperts;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) dst[ebase + 32 * i] = acc[i][j];
+      }
     }
     return;
   }
 #pragma unroll
-  for (int j = 0; j < kRouterTile; ++j) s.logits[j * kLogitLd + e] = acc[j];
+  for (int j = 0; j < 8; ++j)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) s.logits[(tbase + j) * kLogitLd + ebase + 32 * i] = acc[i][j];
   __syncthreads();
   select_tile(p, s, tile);
 }
 
-// splits > 1: sum the partial logits in split order, then select.
+// splits > 1: one CTA per token sums the partial logits in split order, then
+// warp 0 selects; the tile histogram (zeroed by the GEMM kernel) is counted
+// with atomics.
 __global__ void __launch_bounds__(256) router_select_kernel(RouterParams p) {
-  __shared__ __align__(16) RouterSmem s;
+  __shared__ __align__(16) float lrow[kExperts];
   const int e = threadIdx.x;
-  const int tile = blockIdx.x;
-  const int t0 = tile * kRouterTile;
-  s.hist[threadIdx.x] = 0;
-  for (int j = 0; j < kRouterTile; ++j) {
-    const int t = t0 + j;
-    float v = 0.0f;
-    if (t < p.T)
-      for (int sp = 0; sp < p.splits; ++sp) v += p.part[(static_cast<size_t>(sp) * p.T + t) * kExperts + e];
-    s.logits[j * kLogitLd + e] = v;
+  const int t = blockIdx.x;
+  const float* src = p.part + static_cast<size_t>(t) * kExperts + e;
+  const size_t stride = static_cast<size_t>(p.T) * kExperts;
+  float v = 0.0f;
+  int sp = 0;
+  for (; sp + 8 <= p.splits; sp += 8) {
+    float q[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) q[u] = src[(sp + u) * stride];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) v += q[u];
   }
+  for (; sp < p.splits; ++sp) v += src[sp * stride];
+  lrow[e] = v;
   __syncthreads();
-  select_tile(p, s, tile);
+  if (threadIdx.x < 32) {
+    int id;
+    float wv;
+    select_token(lrow, p.bias, p.scale, threadIdx.x, id, wv);
+    if (threadIdx.x < kTopK) {
+      p.ids[static_cast<size_t>(t) * kTopK + threadIdx.x] = id;
+      p.w[static_cast<size_t>(t) * kTopK + threadIdx.x] = wv;
+      atomicAdd(&p.tile_hist[static_cast<size_t>(id) * p.n_tiles + t / kRouterTile], 1);
+    }
+  }
 }
 
 }  // namespace
@@ -276,7 +325,7 @@ cudaError_t launch_router(const RouterParams& p, bool x_bf16, cudaStream_t strea
     router_gemm_kernel<true><<<grid, 256, 0, stream>>>(p);
   else
     router_gemm_kernel<false><<<grid, 256, 0, stream>>>(p);
-  if (p.splits > 1) router_select_kernel<<<p.n_tiles, 256, 0, stream>>>(p);
+  if (p.splits > 1) router_select_kernel<<<p.T, 256, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -79,6 +79,21 @@ bool make_bf16_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t 
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D row-major byte matrix [rows, inner_bytes], boxes box_rows x box_inner
+// bytes, no swizzle (NVFP4 packed codes and block scales).
+bool make_u8_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
+                 uint32_t box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[2] = {inner, rows};
+  const cuuint64_t strides[1] = {inner};
+  const cuuint32_t box[2] = {box_inner, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // ------------------------------------------------------------------ layout
 struct Layout {
   size_t status, counts, offsets, chunk_prefix, tile_hist, part, perm, pos, xp, h, yr, total;
@@ -135,7 +150,7 @@ beam_status_t check_workspace(const beam_moe_shape_t* s, const void* ws, size_t 
   return BEAM_OK;
 }
 
-beam_status_t check_weights(const beam_expert_weights_t* w) {
+beam_status_t check_weights(const beam_moe_shape_t* s, const beam_expert_weights_t* w) {
   if (w == nullptr) return BEAM_ERR_INVALID_ARG;
   if (w->dtype == BEAM_BF16) {
     if (!w->gate || !w->up || !w->down) return BEAM_ERR_INVALID_ARG;
@@ -143,7 +158,18 @@ beam_status_t check_weights(const beam_expert_weights_t* w) {
     if (w->gate_sf || w->up_sf || w->down_sf || w->gate_gs || w->up_gs || w->down_gs) return BEAM_ERR_INVALID_ARG;
     return BEAM_OK;
   }
-  if (w->dtype == BEAM_NVFP4) return BEAM_ERR_UNSUPPORTED;
+  if (w->dtype == BEAM_NVFP4) {
+    if (!w->gate || !w->up || !w->down || !w->gate_sf || !w->up_sf || !w->down_sf || !w->gate_gs || !w->up_gs ||
+        !w->down_gs)
+      return BEAM_ERR_INVALID_ARG;
+    if (!aligned16(w->gate) || !aligned16(w->up) || !aligned16(w->down) || !aligned16(w->gate_sf) ||
+        !aligned16(w->up_sf) || !aligned16(w->down_sf) || !aligned16(w->gate_gs) || !aligned16(w->up_gs) ||
+        !aligned16(w->down_gs))
+      return BEAM_ERR_INVALID_ARG;
+    // scale rows of K/16 bytes must be whole 16-byte TMA strides
+    if (s->H % 256 != 0 || s->I % 256 != 0) return BEAM_ERR_UNSUPPORTED;
+    return BEAM_OK;
+  }
   return BEAM_ERR_UNSUPPORTED;
 }
 
@@ -218,16 +244,31 @@ beam_status_t run_gemm(int mode, const beam_moe_shape_t& s, const beam_expert_we
   __nv_bfloat16* h = at<__nv_bfloat16>(ws, L.h);
   __nv_bfloat16* yr = at<__nv_bfloat16>(ws, L.yr);
   const uint64_t E = kExperts, H = s.H, I = s.I;
-  CUtensorMap ma0, ma1, mb;
+  const bool fp4 = wts->dtype == BEAM_NVFP4;
+  GemmMaps maps;
+  std::memset(&maps, 0, sizeof(maps));
+  bool ok;
   if (mode == 0) {
-    if (!make_bf16_map(&ma0, wts->gate, H, E * I, kBlockM) || !make_bf16_map(&ma1, wts->up, H, E * I, kBlockM) ||
-        !make_bf16_map(&mb, xp, H, R_pad, kBoxRows))
-      return BEAM_ERR_CUDA;
+    ok = make_bf16_map(&maps.b, xp, H, R_pad, kBoxRows);
+    if (fp4)
+      ok = ok && make_u8_map(&maps.a0, wts->gate, H / 2, E * I, kBlockK / 2, kBlockM) &&
+           make_u8_map(&maps.a1, wts->up, H / 2, E * I, kBlockK / 2, kBlockM) &&
+           make_u8_map(&maps.s0, wts->gate_sf, H / 16, E * I, kScaleBoxCols, kBlockM) &&
+           make_u8_map(&maps.s1, wts->up_sf, H / 16, E * I, kScaleBoxCols, kBlockM);
+    else
+      ok = ok && make_bf16_map(&maps.a0, wts->gate, H, E * I, kBlockM) &&
+           make_bf16_map(&maps.a1, wts->up, H, E * I, kBlockM);
   } else {
-    if (!make_bf16_map(&ma0, wts->down, I, E * H, kBlockM) || !make_bf16_map(&mb, h, I, R_pad, kBoxRows))
-      return BEAM_ERR_CUDA;
-    ma1 = ma0;
+    ok = make_bf16_map(&maps.b, h, I, R_pad, kBoxRows);
+    if (fp4)
+      ok = ok && make_u8_map(&maps.a0, wts->down, I / 2, E * H, kBlockK / 2, kBlockM) &&
+           make_u8_map(&maps.s0, wts->down_sf, I / 16, E * H, kScaleBoxCols, kBlockM);
+    else
+      ok = ok && make_bf16_map(&maps.a0, wts->down, I, E * H, kBlockM);
+    maps.a1 = maps.a0;
+    maps.s1 = maps.s0;
   }
+  if (!ok) return BEAM_ERR_CUDA;
   GemmParams p;
   p.counts = at<int32_t>(ws, L.counts);
   p.offsets = at<int32_t>(ws, L.offsets);
@@ -236,8 +277,8 @@ beam_status_t run_gemm(int mode, const beam_moe_shape_t& s, const beam_expert_we
   p.a_rows_per_expert = mode == 0 ? s.I : s.H;
   p.k_blocks = (mode == 0 ? s.H : s.I) / kBlockK;
   p.nmax = nmax;
-  const size_t budget = static_cast<size_t>(d.smem_optin) - 1024 - 256;
-  const size_t sb = gemm_stage_bytes(mode, nmax);
+  const size_t budget = static_cast<size_t>(d.smem_optin) - 1024 - 512;
+  const size_t sb = gemm_stage_bytes(mode, fp4, nmax);
   int stages = static_cast<int>(budget / sb);
   if (stages > 8) stages = 8;
   if (stages < 2) return BEAM_ERR_UNSUPPORTED;
@@ -248,14 +289,17 @@ beam_status_t run_gemm(int mode, const beam_moe_shape_t& s, const beam_expert_we
   if (acc_stages < 1) acc_stages = 1;
   p.acc_stages = acc_stages;
   p.tmem_cols = pow2_at_least(static_cast<uint32_t>(acc_stages) * p.acc_cols);
+  // Weight k-blocks prefetched into L2 ahead of the shared-memory ring (off:
+  // measured slower on B300 than the ring alone).
+  p.prefetch = 0;
   p.out = mode == 0 ? h : yr;
   p.out_ld = mode == 0 ? s.I : s.H;
-  p.gs0 = nullptr;
-  p.gs1 = nullptr;
+  p.gs0 = fp4 ? (mode == 0 ? wts->gate_gs : wts->down_gs) : nullptr;
+  p.gs1 = fp4 && mode == 0 ? wts->up_gs : nullptr;
   p.status = at<uint32_t>(ws, L.status);
   p.timeout_ns = kDefaultTimeoutNs;
-  const size_t smem = 1024 + static_cast<size_t>(stages) * sb + (2 * stages + 2 * acc_stages + 1) * 8 + 16;
-  return cuda_status(launch_gemm(mode, ma0, ma1, mb, p, d.sms, smem, stream));
+  const size_t smem = gemm_smem_bytes(stages, acc_stages, sb);
+  return cuda_status(launch_gemm(mode, fp4, maps, p, d.sms, smem, stream));
 }
 
 beam_status_t run_combine(const beam_moe_shape_t& s, const float* w, void* y, bool y_bf16, void* ws, const Layout& L,
@@ -285,7 +329,7 @@ beam_status_t check_forward(const beam_moe_shape_t* shape, const beam_moe_args_t
       !aligned16(a.y) || (a.router_bias && !aligned16(a.router_bias)))
     return BEAM_ERR_INVALID_ARG;
   if (a.xdtype != BEAM_F32 && a.xdtype != BEAM_BF16) return BEAM_ERR_UNSUPPORTED;
-  st = check_weights(a.weights);
+  st = check_weights(shape, a.weights);
   if (st != BEAM_OK) return st;
   st = check_workspace(shape, workspace, workspace_bytes, L);
   if (st != BEAM_OK) return st;
@@ -388,7 +432,7 @@ beam_status_t beam_moe_experts(const beam_moe_shape_t* shape, const void* x, bea
   if (!x || !topk_ids || !topk_w || !y) return BEAM_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(topk_ids) || !aligned16(topk_w) || !aligned16(y)) return BEAM_ERR_INVALID_ARG;
   if (xdtype != BEAM_F32 && xdtype != BEAM_BF16) return BEAM_ERR_UNSUPPORTED;
-  st = check_weights(weights);
+  st = check_weights(shape, weights);
   if (st != BEAM_OK) return st;
   Layout L;
   st = check_workspace(shape, workspace, workspace_bytes, L);

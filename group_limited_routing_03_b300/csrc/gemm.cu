@@ -3,7 +3,9 @@
 //
 // Beam launch post, section "Mixture of Experts": every expert is a SwiGLU MLP
 // (hidden 5120, intermediate 2560); section "Residual Stream": the SwiGLU
-// product is computed in FP32.
+// product is computed in FP32.  The same post names NVFP4 as the Blackwell
+// checkpoint format (4-bit weights); here those weights are expanded to BF16
+// in shared memory and multiplied with BF16 activations (W4A16).
 //
 //   mode 0 (gate/up):  h[r, i]  = silu(x_r . Wg[e,i,:]) * (x_r . Wu[e,i,:])
 //   mode 1 (down):     yr[r, j] = h_r . Wd[e,j,:]
@@ -19,15 +21,21 @@
 // through L2.  The grid is persistent (one CTA per SM), units are dealt
 // round-robin.
 //
-// Warp roles (192 threads):
-//   warp 0      TMA producer: weight tile(s) 128x64 and ceil(n/32) boxes of
-//               32 activation rows x 64 per stage, 128-byte swizzle;
-//   warp 1      TMEM allocator and MMA issuer (one thread):
-//               tcgen05.mma kind::f16, M=128, N=round_up(n,16), K=16 steps;
-//   warps 2-5   epilogue: tcgen05.ld of the accumulators (warp w reads TMEM
-//               lanes 32*(w%4)..+31), SwiGLU in FP32 (mode 0), BF16 stores.
-// Shared-memory stages are recycled through full/empty mbarriers, TMEM
-// accumulator buffers through acc_full/acc_empty.  Every wait is bounded.
+// Warp roles:
+//   warp 0       TMA producer: weight tile(s) 128x64 and ceil(n/32) boxes of
+//                32 activation rows x 64 per stage, 128-byte swizzle (NVFP4:
+//                the packed 128x32-byte tile(s) and their E4M3 scales);
+//   warp 1       TMEM allocator and MMA issuer (one thread):
+//                tcgen05.mma kind::f16, M=128, N=round_up(n,16), K=16 steps;
+//   warps 2-9    epilogue: tcgen05.ld of the accumulators (warp w reads TMEM
+//                lanes 32*(w%4)..+31; warps 2-5 take the even 16-column
+//                chunks, warps 6-9 the odd ones), NVFP4 global scale, SwiGLU
+//                in FP32 (mode 0), BF16 stores;
+//   warps 10-17  (NVFP4 only) converters: packed E2M1 x E4M3 -> BF16 weight
+//                tile in the 128-byte-swizzled layout the MMA reads.
+// Shared-memory stages are recycled through full/empty mbarriers (plus
+// conv for NVFP4), TMEM accumulator buffers through acc_full/acc_empty.
+// Every wait is bounded.
 #include <cuda.h>
 #include <cuda_bf16.h>
 
@@ -37,9 +45,12 @@
 namespace beam {
 namespace {
 
-constexpr int kThreads = 192;
-constexpr uint32_t kATileBytes = kBlockM * kBlockK * 2;  // 16 KiB
-constexpr uint32_t kBoxBytes = kBoxRows * kBlockK * 2;   // 4 KiB
+constexpr int kEpilogueWarps = 8;
+constexpr int kConvertWarps = 8;
+constexpr int kThreadsBf16 = 32 * (2 + kEpilogueWarps);
+constexpr int kThreadsFp4 = 32 * (2 + kEpilogueWarps + kConvertWarps);
+constexpr uint32_t kATileBytes = kBlockM * kBlockK * 2;     // 16 KiB of BF16
+constexpr uint32_t kBoxBytes = kBoxRows * kBlockK * 2;      // 4 KiB
 
 struct Unit {
   int e, m, start, n;
@@ -59,50 +70,136 @@ __device__ __forceinline__ Unit unit_at(const GemmParams& p, int u) {
       hi = mid;
   }
   U.e = lo;
+  // The expert's routes are cut into nch = ceil(count / nmax) chunks of
+  // near-equal size (sizes differ by at most one), so the CTAs that run the
+  // chunks of one weight tile side by side progress in step and share the
+  // weight tile through L2.
   const int c = q - __ldg(&p.chunk_prefix[lo]);
-  U.start = __ldg(&p.offsets[lo]) + c * p.nmax;
-  const int left = __ldg(&p.counts[lo]) - c * p.nmax;
-  U.n = left < p.nmax ? left : p.nmax;
+  const int nch = __ldg(&p.chunk_prefix[lo + 1]) - __ldg(&p.chunk_prefix[lo]);
+  const int count = __ldg(&p.counts[lo]);
+  const int base = count / nch, rem = count - base * nch;
+  U.start = __ldg(&p.offsets[lo]) + c * base + (c < rem ? c : rem);
+  U.n = base + (c < rem ? 1 : 0);
   return U;
 }
 
-template <int kMode>
-__global__ void __launch_bounds__(kThreads, 1)
-    moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ CUtensorMap tm_a1,
-                    const __grid_constant__ CUtensorMap tm_b, const GemmParams p) {
+// ---------------------------------------------------------------------------
+// NVFP4 -> BF16 (exact): an E2M1 magnitude has at most 2 significant bits and
+// an E4M3 scale at most 4, so their product fits BF16's 8 bits, and every
+// such product (>= 2^-10, <= 2688) is a normal BF16 number.
+// ---------------------------------------------------------------------------
+// E4M3 (sign, 4 exponent bits with bias 7, 3 mantissa bits) to BF16 bits.
+__device__ __forceinline__ uint32_t e4m3_to_bf16_bits(uint32_t code) {
+  const uint32_t sign = (code & 0x80u) << 8;
+  const uint32_t ex = (code >> 3) & 0xFu;
+  const uint32_t man = code & 7u;
+  if (ex != 0) return sign | ((ex + 120u) << 7) | (man << 4);
+  if (man == 0) return sign;
+  // subnormal: man * 2^-9, renormalised
+  const float f = static_cast<float>(man) * 0.001953125f;
+  return sign | (__float_as_uint(f) >> 16);
+}
+
+// Eight E2M1 codes (one 32-bit word, element i in bits 4i..4i+3) times a
+// BF16 scale -> four BF16x2 words (element 2j in the low half of word j).
+// Magnitudes come from two byte-permute lookups (high and low byte of the
+// BF16 pattern of 0, .5, 1, 1.5, 2, 3, 4, 6), signs are moved to bits 15/31.
+__device__ __forceinline__ uint4 e2m1x8_to_bf16(uint32_t w, __nv_bfloat162 scale2) {
+  constexpr uint32_t kHi0 = 0x3F3F3F00u, kHi1 = 0x40404040u;  // high bytes of codes 0..7
+  constexpr uint32_t kLo0 = 0xC0800000u, kLo1 = 0xC0804000u;  // low bytes of codes 0..7
+  const uint32_t sel_a = w & 0x7777u;           // magnitudes of elements 0..3
+  const uint32_t sel_b = (w >> 16) & 0x7777u;   // magnitudes of elements 4..7
+  uint32_t ha, la, hb, lb;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(ha) : "r"(kHi0), "r"(kHi1), "r"(sel_a));
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(la) : "r"(kLo0), "r"(kLo1), "r"(sel_a));
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(hb) : "r"(kHi0), "r"(kHi1), "r"(sel_b));
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(lb) : "r"(kLo0), "r"(kLo1), "r"(sel_b));
+  uint32_t q[4];
+  asm("prmt.b32 %0, %1, %2, 0x5140;" : "=r"(q[0]) : "r"(la), "r"(ha));  // elements 0, 1
+  asm("prmt.b32 %0, %1, %2, 0x7362;" : "=r"(q[1]) : "r"(la), "r"(ha));  // elements 2, 3
+  asm("prmt.b32 %0, %1, %2, 0x5140;" : "=r"(q[2]) : "r"(lb), "r"(hb));  // elements 4, 5
+  asm("prmt.b32 %0, %1, %2, 0x7362;" : "=r"(q[3]) : "r"(lb), "r"(hb));  // elements 6, 7
+  // sign of element i is bit 4i+3 of w
+  q[0] |= ((w << 12) & 0x00008000u) | ((w << 24) & 0x80000000u);
+  q[1] |= ((w << 4) & 0x00008000u) | ((w << 16) & 0x80000000u);
+  q[2] |= ((w >> 4) & 0x00008000u) | ((w << 8) & 0x80000000u);
+  q[3] |= ((w >> 12) & 0x00008000u) | (w & 0x80000000u);
+  uint4 out;
+  uint32_t* o = reinterpret_cast<uint32_t*>(&out);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&q[j]);
+    v = __hmul2(v, scale2);  // exact: at most 6 significant bits
+    o[j] = *reinterpret_cast<uint32_t*>(&v);
+  }
+  return out;
+}
+
+// One converter thread: `nchunk` 16-byte output chunks (8 K elements each,
+// starting at chunk c0) of weight row `row`, from the packed tile (32 bytes
+// per row) and the scale tile (16 bytes per row; this k-block's 4 scales at
+// byte 4*(kb%4)), into the 128-byte-swizzled BF16 tile.
+__device__ __forceinline__ void convert_row(const uint8_t* packed, const uint8_t* scales, uint8_t* dst, int row,
+                                            int kb, int c0, int nchunk) {
+  const uint32_t sc4 = *reinterpret_cast<const uint32_t*>(scales + row * kScaleBoxCols + 4 * (kb & 3));
+  const uint32_t* src = reinterpret_cast<const uint32_t*>(packed + row * (kBlockK / 2));
+  uint8_t* drow = dst + row * 128;
+  for (int c = c0; c < c0 + nchunk; ++c) {
+    const uint32_t sbits = e4m3_to_bf16_bits((sc4 >> (8 * (c >> 1))) & 0xFFu);  // 16 elements per scale
+    const uint32_t s2bits = sbits | (sbits << 16);
+    const __nv_bfloat162 s2 = *reinterpret_cast<const __nv_bfloat162*>(&s2bits);
+    const uint4 v = e2m1x8_to_bf16(src[c], s2);
+    *reinterpret_cast<uint4*>(drow + ((c ^ (row & 7)) << 4)) = v;
+  }
+}
+
+template <int kMode, bool kFp4>
+__global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
+    moe_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
   constexpr int kNumA = kMode == 0 ? 2 : 1;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t b_tile_bytes = static_cast<uint32_t>(p.nmax) * kBlockK * 2;
-  const uint32_t stage_bytes = kNumA * kATileBytes + b_tile_bytes;
+  const uint32_t stage_bytes = static_cast<uint32_t>(gemm_stage_bytes(kMode, kFp4, p.nmax));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(p.stages) * stage_bytes);
   uint64_t* full = bars;
   uint64_t* empty = full + p.stages;
-  uint64_t* acc_full = empty + p.stages;
+  uint64_t* conv = empty + p.stages;  // NVFP4: BF16 weight tile ready
+  uint64_t* acc_full = conv + p.stages;
   uint64_t* acc_empty = acc_full + p.acc_stages;
   uint64_t* drain = acc_empty + p.acc_stages;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile uint32_t* abort_flag = tmem_slot + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // Stage layout: [A bf16 x kNumA][B][packed x kNumA][scales x kNumA]
   auto a_tile = [&](int s, int which) { return smem + static_cast<size_t>(s) * stage_bytes + which * kATileBytes; };
   auto b_tile = [&](int s) { return smem + static_cast<size_t>(s) * stage_bytes + kNumA * kATileBytes; };
+  auto p_tile = [&](int s, int which) { return b_tile(s) + b_tile_bytes + which * kPackedTileBytes; };
+  auto s_tile = [&](int s, int which) {
+    return b_tile(s) + b_tile_bytes + kNumA * kPackedTileBytes + which * kScaleTileBytes;
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
+      mbar_init(&conv[s], kConvertWarps);
     }
     for (int a = 0; a < p.acc_stages; ++a) {
       mbar_init(&acc_full[a], 1);
-      mbar_init(&acc_empty[a], 4);
+      mbar_init(&acc_empty[a], kEpilogueWarps);
     }
     mbar_init(drain, 1);
     *abort_flag = 0u;
     fence_mbar_init();
-    tma_prefetch_desc(&tm_a0);
-    if (kMode == 0) tma_prefetch_desc(&tm_a1);
-    tma_prefetch_desc(&tm_b);
+    tma_prefetch_desc(&maps.a0);
+    if (kMode == 0) tma_prefetch_desc(&maps.a1);
+    tma_prefetch_desc(&maps.b);
+    if (kFp4) {
+      tma_prefetch_desc(&maps.s0);
+      if (kMode == 0) tma_prefetch_desc(&maps.s1);
+    }
   }
   if (warp == 1) tmem_alloc(tmem_slot, p.tmem_cols);
   tc_fence_before();
@@ -115,28 +212,61 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      const uint64_t pol_w = l2_policy_evict_first();
       const uint64_t pol_x = l2_policy_evict_last();
       int stage = 0;
       uint32_t phase = 0;
       long long issued = 0;
       bool ok = true;
+      // Optional: weight k-blocks prefetched into L2 p.prefetch k-blocks
+      // ahead of the shared-memory ring, across unit boundaries.
+      int pf_u = blockIdx.x, pf_kb = 0, pf_row = 0;
+      if (pf_u < total_units && p.prefetch > 0) {
+        const Unit P = unit_at(p, pf_u);
+        pf_row = P.e * p.a_rows_per_expert + P.m * kBlockM;
+      }
+      auto prefetch_next = [&]() {
+        if (pf_u >= total_units || p.prefetch <= 0) return;
+        const int px = kFp4 ? pf_kb * (kBlockK / 2) : pf_kb * kBlockK;
+        tma_prefetch_l2_2d(&maps.a0, px, pf_row);
+        if (kMode == 0) tma_prefetch_l2_2d(&maps.a1, px, pf_row);
+        if (++pf_kb == p.k_blocks) {
+          pf_kb = 0;
+          pf_u += gridDim.x;
+          if (pf_u < total_units) {
+            const Unit P = unit_at(p, pf_u);
+            pf_row = P.e * p.a_rows_per_expert + P.m * kBlockM;
+          }
+        }
+      };
+      for (int i = 0; i < p.prefetch; ++i) prefetch_next();
       for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
         const Unit U = unit_at(p, u);
         const int a_row = U.e * p.a_rows_per_expert + U.m * kBlockM;
         const int nbox = (U.n + kBoxRows - 1) / kBoxRows;
-        const uint32_t bytes = kNumA * kATileBytes + static_cast<uint32_t>(nbox) * kBoxBytes;
+        const uint32_t a_bytes = kFp4 ? kNumA * (kPackedTileBytes + kScaleTileBytes) : kNumA * kATileBytes;
+        const uint32_t bytes = a_bytes + static_cast<uint32_t>(nbox) * kBoxBytes;
         for (int kb = 0; kb < p.k_blocks; ++kb) {
+          prefetch_next();
           if (!mbar_wait(&empty[stage], phase ^ 1u, p.timeout_ns, abort_flag, p.status, kWhereProducerEmpty)) {
             ok = false;
             break;
           }
           mbar_arrive_expect_tx(&full[stage], bytes);
           const int kx = kb * kBlockK;
-          tma_load_2d(a_tile(stage, 0), &tm_a0, &full[stage], kx, a_row, pol_w);
-          if (kMode == 0) tma_load_2d(a_tile(stage, 1), &tm_a1, &full[stage], kx, a_row, pol_w);
+          if (kFp4) {
+            const int sx = (kb >> 2) * static_cast<int>(kScaleBoxCols);
+            tma_load_2d_nohint(p_tile(stage, 0), &maps.a0, &full[stage], kx / 2, a_row);
+            tma_load_2d_nohint(s_tile(stage, 0), &maps.s0, &full[stage], sx, a_row);
+            if (kMode == 0) {
+              tma_load_2d_nohint(p_tile(stage, 1), &maps.a1, &full[stage], kx / 2, a_row);
+              tma_load_2d_nohint(s_tile(stage, 1), &maps.s1, &full[stage], sx, a_row);
+            }
+          } else {
+            tma_load_2d_nohint(a_tile(stage, 0), &maps.a0, &full[stage], kx, a_row);
+            if (kMode == 0) tma_load_2d_nohint(a_tile(stage, 1), &maps.a1, &full[stage], kx, a_row);
+          }
           for (int b = 0; b < nbox; ++b)
-            tma_load_2d(b_tile(stage) + b * kBoxBytes, &tm_b, &full[stage], kx, U.start + b * kBoxRows, pol_x);
+            tma_load_2d(b_tile(stage) + b * kBoxBytes, &maps.b, &full[stage], kx, U.start + b * kBoxRows, pol_x);
           ++issued;
           if (++stage == p.stages) {
             stage = 0;
@@ -168,7 +298,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t d0 = tmem_base + static_cast<uint32_t>(acc) * p.acc_cols;
         const uint32_t d1 = d0 + static_cast<uint32_t>(p.nmax);
         for (int kb = 0; kb < p.k_blocks; ++kb) {
-          if (!mbar_wait(&full[stage], phase, p.timeout_ns, abort_flag, p.status, kWhereMmaFull)) {
+          // BF16: the TMA bytes; NVFP4: the converters' BF16 tile (they waited
+          // for the TMA bytes of the same stage before writing it).
+          if (!mbar_wait(kFp4 ? &conv[stage] : &full[stage], phase, p.timeout_ns, abort_flag, p.status,
+                         kWhereMmaFull)) {
             ok = false;
             break;
           }
@@ -199,9 +332,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(drain);
       mbar_wait(drain, 0, p.timeout_ns, nullptr, p.status, kWhereDrain);
     }
-  } else {
+  } else if (warp < 2 + kEpilogueWarps) {
     // ------------------------------------------------------------ epilogue
-    const int quad = warp & 3;
+    const int quad = warp & 3;               // TMEM lanes this warp may read
+    const int half = (warp - 2) >> 2;        // which 16-column chunks (even / odd)
     const int row = quad * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -219,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float s1 = (kMode == 0 && p.gs1 != nullptr) ? __ldg(&p.gs1[U.e]) : 1.0f;
       const int ncols = (U.n + 15) & ~15;
       __nv_bfloat16* out = p.out + static_cast<size_t>(U.start) * p.out_ld + feat;
-      for (int c0 = 0; c0 < ncols; c0 += 16) {
+      for (int c0 = 16 * half; c0 < ncols; c0 += 32) {
         float g[16];
         tmem_ld16(tbase + static_cast<uint32_t>(c0), g);
         if (kMode == 0) {
@@ -231,7 +365,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (c0 + j < U.n) {
               const float a = g[j] * s0;
               const float b = up[j] * s1;
-              const float hval = a / (1.0f + expf(-a)) * b;  // SiLU(gate) * up, FP32
+              // SiLU(gate) * up in FP32 (fast exp / divide: the result is
+              // rounded to BF16 right after, far coarser than their error)
+              const float hval = __fdividef(a, 1.0f + __expf(-a)) * b;
               out[static_cast<size_t>(c0 + j) * p.out_ld] = __float2bfloat16_rn(hval);
             }
           }
@@ -250,6 +386,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         acc_phase ^= 1u;
       }
     }
+  } else if (kFp4) {
+    // ------------------------------------------------------------ converters
+    // mode 0: thread c converts row c%128 of matrix c/128 (gate / up), all 8
+    // chunks; mode 1: row c%128, chunks 4*(c/128)..+3.
+    const int c = threadIdx.x - 32 * (2 + kEpilogueWarps);
+    const int row = c & (kBlockM - 1);
+    const int which = kMode == 0 ? (c >> 7) : 0;
+    const int chunk0 = kMode == 0 ? 0 : 4 * (c >> 7);
+    const int nchunk = kMode == 0 ? 8 : 4;
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
+      for (int kb = 0; kb < p.k_blocks; ++kb) {
+        int good = 1;
+        if (lane == 0)
+          good = mbar_wait(&full[stage], phase, p.timeout_ns, abort_flag, p.status, kWhereConvert) ? 1 : 0;
+        good = __shfl_sync(0xFFFFFFFFu, good, 0);
+        if (!good) {
+          ok = false;
+          break;
+        }
+        convert_row(p_tile(stage, which), s_tile(stage, which), a_tile(stage, which), row, kb, chunk0, nchunk);
+        fence_proxy_async_smem();  // generic-proxy writes -> visible to the tensor core
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&conv[stage]);
+        if (++stage == p.stages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
   }
 
   tc_fence_before();
@@ -260,27 +428,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-}  // namespace
-
-size_t gemm_stage_bytes(int mode, int nmax) {
-  return static_cast<size_t>(mode == 0 ? 2 : 1) * kATileBytes + static_cast<size_t>(nmax) * kBlockK * 2;
+template <int kMode, bool kFp4>
+cudaError_t launch_one(const GemmMaps& maps, const GemmParams& p, int grid, size_t smem_bytes, cudaStream_t stream) {
+  const cudaError_t err = cudaFuncSetAttribute(moe_gemm_kernel<kMode, kFp4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>(smem_bytes));
+  if (err != cudaSuccess) return err;
+  moe_gemm_kernel<kMode, kFp4><<<grid, kFp4 ? kThreadsFp4 : kThreadsBf16, smem_bytes, stream>>>(maps, p);
+  return cudaGetLastError();
 }
 
-cudaError_t launch_gemm(int mode, const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b,
-                        const GemmParams& p, int grid, size_t smem_bytes, cudaStream_t stream) {
-  cudaError_t err;
-  if (mode == 0) {
-    err = cudaFuncSetAttribute(moe_gemm_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(smem_bytes));
-    if (err != cudaSuccess) return err;
-    moe_gemm_kernel<0><<<grid, kThreads, smem_bytes, stream>>>(a0, a1, b, p);
-  } else {
-    err = cudaFuncSetAttribute(moe_gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(smem_bytes));
-    if (err != cudaSuccess) return err;
-    moe_gemm_kernel<1><<<grid, kThreads, smem_bytes, stream>>>(a0, a1, b, p);
-  }
-  return cudaGetLastError();
+}  // namespace
+
+size_t gemm_smem_bytes(int stages, int acc_stages, size_t stage_bytes) {
+  return 1024 + static_cast<size_t>(stages) * stage_bytes + (3 * stages + 2 * acc_stages + 1) * 8 + 16;
+}
+
+cudaError_t launch_gemm(int mode, bool fp4, const GemmMaps& maps, const GemmParams& p, int grid, size_t smem_bytes,
+                        cudaStream_t stream) {
+  if (mode == 0)
+    return fp4 ? launch_one<0, true>(maps, p, grid, smem_bytes, stream)
+               : launch_one<0, false>(maps, p, grid, smem_bytes, stream);
+  return fp4 ? launch_one<1, true>(maps, p, grid, smem_bytes, stream)
+             : launch_one<1, false>(maps, p, grid, smem_bytes, stream);
 }
 
 }  // namespace beam

@@ -21,6 +21,9 @@ constexpr int kBlockM = 128;       // weight rows per MMA tile (TMEM lanes)
 constexpr int kBlockK = 64;        // K elements per pipeline stage (128 bytes of bf16)
 constexpr int kBoxRows = 32;       // token rows per TMA box of the activation operand
 constexpr int kMaxSmsForSizing = 256;  // bound on the SM count used to size the workspace
+constexpr uint32_t kPackedTileBytes = kBlockM * kBlockK / 2;  // NVFP4: 128 rows x 32 bytes
+constexpr uint32_t kScaleBoxCols = 16;                       // NVFP4: scale bytes per TMA box row (4 k-blocks)
+constexpr uint32_t kScaleTileBytes = kBlockM * kScaleBoxCols;  // NVFP4: 2 KiB
 
 // ---------------------------------------------------------------------------
 // Router
@@ -55,6 +58,7 @@ struct GemmParams {
   int acc_stages;               // TMEM accumulator buffers
   uint32_t acc_cols;            // TMEM columns per accumulator buffer
   uint32_t tmem_cols;           // TMEM columns allocated (power of two)
+  int prefetch;                 // weight k-blocks prefetched into L2 ahead of the ring
   __nv_bfloat16* out;           // h [R, I] or yr [R, H], perm order
   int out_ld;                   // I or H
   const float* gs0;             // NVFP4 global scales (gate or down) [E], else null
@@ -62,6 +66,21 @@ struct GemmParams {
   uint32_t* status;
   uint64_t timeout_ns;
 };
+
+// TMA descriptors of one grouped GEMM: weights a0 (gate or down) and a1 (up),
+// activations b, and for NVFP4 the block scales s0 / s1 of a0 / a1.
+struct GemmMaps {
+  CUtensorMap a0, a1, b, s0, s1;
+};
+
+// Bytes of one pipeline stage: BF16 weight tile(s), activation boxes, and for
+// NVFP4 the packed tile(s) and scale tile(s) the converters read.
+__host__ __device__ inline size_t gemm_stage_bytes(int mode, bool fp4, int nmax) {
+  const size_t num_a = mode == 0 ? 2 : 1;
+  size_t b = num_a * kBlockM * kBlockK * 2 + static_cast<size_t>(nmax) * kBlockK * 2;
+  if (fp4) b += num_a * (kPackedTileBytes + kScaleTileBytes);
+  return b;
+}
 
 // ---------------------------------------------------------------------------
 // Host launchers (each returns cudaGetLastError() of its launches)
@@ -77,9 +96,9 @@ cudaError_t launch_dispatch(const int32_t* ids, int R, int n_tiles, int32_t* til
                             int32_t* perm, int32_t* pos, cudaStream_t stream);
 cudaError_t launch_gather(const void* x, bool x_bf16, int H, const int32_t* perm, int R,
                           __nv_bfloat16* xp, int num_sms, cudaStream_t stream);
-cudaError_t launch_gemm(int mode, const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b,
-                        const GemmParams& p, int grid, size_t smem_bytes, cudaStream_t stream);
-size_t gemm_stage_bytes(int mode, int nmax);
+cudaError_t launch_gemm(int mode, bool fp4, const GemmMaps& maps, const GemmParams& p, int grid,
+                        size_t smem_bytes, cudaStream_t stream);
+size_t gemm_smem_bytes(int stages, int acc_stages, size_t stage_bytes);
 cudaError_t launch_combine(const __nv_bfloat16* yr, const int32_t* pos, const float* w, int T, int H,
                            void* y, bool y_bf16, cudaStream_t stream);
 cudaError_t launch_debug_timeout(uint32_t* status, uint64_t timeout_ns, cudaStream_t stream);

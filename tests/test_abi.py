@@ -113,6 +113,25 @@ def test_forward_weight_errors(lib):
     assert rc == moe.BEAM_ERR_INVALID_ARG
 
 
+def test_nvfp4_shape_and_pointer_rules(lib):
+    ew = moe._ExpertWeights()
+    ew.dtype = moe.BEAM_NVFP4
+    ew.gate, ew.up, ew.down = 0x1000, 0x2000, 0x3000
+    ew.gate_sf, ew.up_sf, ew.down_sf = 0x4000, 0x5000, 0x6000
+    ew.gate_gs, ew.up_gs, ew.down_gs = 0x7000, 0x8000, 0x9000
+    for H, I, want in ((384, 256, moe.BEAM_ERR_UNSUPPORTED), (256, 384, moe.BEAM_ERR_UNSUPPORTED)):
+        sh = _shape(T=16, H=H, I=I)
+        n = moe.workspace_size(sh, "nvfp4")
+        rc = lib.beam_moe_experts(ctypes.byref(sh), 0x10000, moe.BEAM_BF16, ctypes.byref(ew), 0x30000, 0x40000,
+                                  0x50000, 0x100000, n, None)
+        assert rc == want
+    sh = _shape(T=16, H=256, I=256)
+    ew.up_sf = None
+    rc = lib.beam_moe_experts(ctypes.byref(sh), 0x10000, moe.BEAM_BF16, ctypes.byref(ew), 0x30000, 0x40000,
+                              0x50000, 0x100000, moe.workspace_size(sh, "nvfp4"), None)
+    assert rc == moe.BEAM_ERR_INVALID_ARG
+
+
 def test_debug_timeout_argument_errors(lib):
     assert lib.beam_moe_debug_timeout(None, 4096, 100, None) == moe.BEAM_ERR_WORKSPACE
     assert lib.beam_moe_debug_timeout(0x100000, 4096, 0, None) == moe.BEAM_ERR_INVALID_ARG

@@ -71,6 +71,21 @@ def test_forward_small_all_tokens(T, H, I, x_dtype):
     assert err <= Y_TOL["bf16"], err
 
 
+@pytest.mark.parametrize("T,H,I", [(300, 512, 256), (40, 256, 512)])
+def test_forward_nvfp4_small_all_tokens(T, H, I):
+    """NVFP4 experts (E2M1 codes, E4M3 block scales, FP32 global scale),
+    dequantised in shared memory, BF16 activations."""
+    wl = inputs.workload("nvfp4", T=T, H=H, I=I, seed=31 + T)
+    dg, _ = _gpu_inputs(wl, cpu_gen=True)
+    y, ids, w, _ = _run_forward(wl, dg, dg)
+    ref = oracle_route(dg)
+    safe = compare_routing(ids.cpu().numpy(), w.cpu().numpy(), ref)
+    tok = np.nonzero(safe)[0]
+    y_ref = oracle_y(dg, tok, ref["ids"][tok], ref["weights"][tok])
+    err = rel_err(y.cpu().double().numpy()[tok], y_ref)
+    assert err <= Y_TOL["nvfp4"], err
+
+
 def test_zero_input_exact():
     wl = inputs.workload("tiny", T=40, x_dtype="bf16")
     dg, _ = _gpu_inputs(wl, cpu_gen=True)
@@ -122,6 +137,22 @@ def test_experts_given_routing(T, H, I, hot):
     assert rel_err(y.cpu().double().numpy(), y_ref) <= Y_TOL["bf16"]
 
 
+def test_experts_nvfp4_given_routing():
+    """NVFP4 experts on a seeded routing whose hot experts take every token
+    (several chunks per expert)."""
+    T, H, I = 520, 256, 256
+    wl = inputs.workload("nvfp4", T=T, H=H, I=I, seed=77)
+    dg, _ = _gpu_inputs(wl, cpu_gen=True)
+    ids, w = seeded_routing(T, seed=5, hot=(1, 100, 255))
+    sh = moe.shape(T, H, I)
+    ws = moe.alloc_workspace(sh, "nvfp4")
+    y = torch.empty((T, H), dtype=torch.bfloat16, device=DEV)
+    moe.beam_moe_experts(sh, dg["x"], dg, ids.to(DEV), w.to(DEV), y, ws)
+    assert moe.beam_moe_read_device_status(ws)[0] == 0
+    y_ref = oracle_y(dg, np.arange(T), ids.numpy(), w.numpy().astype(np.float64))
+    assert rel_err(y.cpu().double().numpy(), y_ref) <= Y_TOL["nvfp4"]
+
+
 def test_identical_experts_closed_form():
     """All experts share one weight set, so y = 2.5 * f(x) whatever the routing."""
     T, H, I = 200, 256, 256
@@ -160,7 +191,7 @@ def _sample_tokens(T, ids_ref, n, seed, hot_expert=None):
     return np.array(sorted(pick))
 
 
-@pytest.mark.parametrize("name,n_sample", [("decode", 8), ("prefill", 4), ("skew", 4)])
+@pytest.mark.parametrize("name,n_sample", [("decode", 8), ("prefill", 4), ("nvfp4", 4), ("skew", 4)])
 def test_full_size_workloads(name, n_sample):
     wl = inputs.workload(name)
     torch.cuda.empty_cache()

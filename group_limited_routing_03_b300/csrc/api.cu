@@ -269,16 +269,20 @@ beam_status_t run_gemm(int mode, const beam_moe_shape_t& s, const beam_expert_we
     maps.s1 = maps.s0;
   }
   if (!ok) return BEAM_ERR_CUDA;
+  // CTA pairs (one M=256 MMA per unit over two SMs) halve each SM's shared-
+  // memory operand traffic; used for BF16 weights when chunks reach 256 routes.
+  bool pair = !fp4 && nmax == 256 && s.H % 256 == 0 && s.I % 256 == 0 && d.sms >= 2;
+  const int rows_per_unit = pair ? 2 * kBlockM : kBlockM;
   GemmParams p;
   p.counts = at<int32_t>(ws, L.counts);
   p.offsets = at<int32_t>(ws, L.offsets);
   p.chunk_prefix = at<int32_t>(ws, L.chunk_prefix);
-  p.m_tiles = (mode == 0 ? s.I : s.H) / kBlockM;
+  p.m_tiles = (mode == 0 ? s.I : s.H) / rows_per_unit;
   p.a_rows_per_expert = mode == 0 ? s.I : s.H;
   p.k_blocks = (mode == 0 ? s.H : s.I) / kBlockK;
   p.nmax = nmax;
   const size_t budget = static_cast<size_t>(d.smem_optin) - 1024 - 512;
-  const size_t sb = gemm_stage_bytes(mode, fp4, nmax);
+  const size_t sb = gemm_stage_bytes(mode, fp4, pair ? nmax / 2 : nmax);
   int stages = static_cast<int>(budget / sb);
   if (stages > 8) stages = 8;
   if (stages < 2) return BEAM_ERR_UNSUPPORTED;
@@ -298,8 +302,29 @@ beam_status_t run_gemm(int mode, const beam_moe_shape_t& s, const beam_expert_we
   p.gs1 = fp4 && mode == 0 ? wts->up_gs : nullptr;
   p.status = at<uint32_t>(ws, L.status);
   p.timeout_ns = kDefaultTimeoutNs;
-  const size_t smem = gemm_smem_bytes(stages, acc_stages, sb);
-  return cuda_status(launch_gemm(mode, fp4, maps, p, d.sms, smem, stream));
+  size_t smem = gemm_smem_bytes(stages, acc_stages, sb);
+  int grid = d.sms;
+  if (pair) {
+    // persistent: as many pairs as can be resident at once (a TPC with a
+    // disabled SM cannot host one)
+    const int clusters = gemm_pair_max_clusters(mode, smem);
+    if (clusters > 0)
+      grid = 2 * (clusters < d.sms / 2 ? clusters : d.sms / 2);
+    else
+      pair = false;
+  }
+  if (!pair && nmax == 256 && !fp4) {
+    // fall back to one CTA per unit: recompute the per-CTA tiling
+    p.m_tiles = (mode == 0 ? s.I : s.H) / kBlockM;
+    const size_t sb1 = gemm_stage_bytes(mode, fp4, nmax);
+    int st1 = static_cast<int>(budget / sb1);
+    if (st1 > 8) st1 = 8;
+    if (st1 < 2) return BEAM_ERR_UNSUPPORTED;
+    p.stages = st1;
+    smem = gemm_smem_bytes(st1, acc_stages, sb1);
+    grid = d.sms;
+  }
+  return cuda_status(launch_gemm(mode, fp4, pair, maps, p, grid, smem, stream));
 }
 
 beam_status_t run_combine(const beam_moe_shape_t& s, const float* w, void* y, bool y_bf16, void* ws, const Layout& L,

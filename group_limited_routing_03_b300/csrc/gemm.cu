@@ -153,14 +153,22 @@ __device__ __forceinline__ void convert_row(const uint8_t* packed, const uint8_t
   }
 }
 
-template <int kMode, bool kFp4>
+// kPair: a cluster of two CTAs runs each unit as one M=256 pair MMA
+// (tcgen05 cta_group::2): CTA r holds weight rows 128r..128r+127 of the
+// 256-row tile and half of the token chunk (N/2 rows); each CTA's TMEM gets
+// its 128 rows x N accumulator.  The even CTA issues the MMAs; both CTAs'
+// TMA loads signal the even CTA's full barrier; commits are multicast to
+// both CTAs; both epilogues release the even CTA's acc_empty barrier.
+template <int kMode, bool kFp4, bool kPair>
 __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
     moe_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
   constexpr int kNumA = kMode == 0 ? 2 : 1;
+  constexpr int kRowsPerUnit = kPair ? 2 * kBlockM : kBlockM;
+  static_assert(!(kPair && kFp4), "pair MMA path is BF16 only");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const uint32_t b_tile_bytes = static_cast<uint32_t>(p.nmax) * kBlockK * 2;
-  const uint32_t stage_bytes = static_cast<uint32_t>(gemm_stage_bytes(kMode, kFp4, p.nmax));
+  const uint32_t b_tile_bytes = static_cast<uint32_t>(kPair ? p.nmax / 2 : p.nmax) * kBlockK * 2;
+  const uint32_t stage_bytes = static_cast<uint32_t>(gemm_stage_bytes(kMode, kFp4, kPair ? p.nmax / 2 : p.nmax));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(p.stages) * stage_bytes);
   uint64_t* full = bars;
   uint64_t* empty = full + p.stages;
@@ -172,6 +180,9 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
   volatile uint32_t* abort_flag = tmem_slot + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = kPair ? cluster_ctarank() : 0u;  // 0: the CTA that issues the MMAs
+  const int unit0 = kPair ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int unit_step = kPair ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
   // Stage layout: [A bf16 x kNumA][B][packed x kNumA][scales x kNumA]
   auto a_tile = [&](int s, int which) { return smem + static_cast<size_t>(s) * stage_bytes + which * kATileBytes; };
   auto b_tile = [&](int s) { return smem + static_cast<size_t>(s) * stage_bytes + kNumA * kATileBytes; };
@@ -188,7 +199,7 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
     }
     for (int a = 0; a < p.acc_stages; ++a) {
       mbar_init(&acc_full[a], 1);
-      mbar_init(&acc_empty[a], kEpilogueWarps);
+      mbar_init(&acc_empty[a], kPair ? 2 * kEpilogueWarps : kEpilogueWarps);
     }
     mbar_init(drain, 1);
     *abort_flag = 0u;
@@ -201,9 +212,17 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
       if (kMode == 0) tma_prefetch_desc(&maps.s1);
     }
   }
-  if (warp == 1) tmem_alloc(tmem_slot, p.tmem_cols);
+  if (warp == 1) {
+    if (kPair)
+      tmem_alloc_pair(tmem_slot, p.tmem_cols);
+    else
+      tmem_alloc(tmem_slot, p.tmem_cols);
+  }
   tc_fence_before();
-  __syncthreads();
+  if (kPair)
+    cluster_sync();  // both CTAs' barriers initialised before any cross-CTA arrive
+  else
+    __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -219,10 +238,10 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
       bool ok = true;
       // Optional: weight k-blocks prefetched into L2 p.prefetch k-blocks
       // ahead of the shared-memory ring, across unit boundaries.
-      int pf_u = blockIdx.x, pf_kb = 0, pf_row = 0;
+      int pf_u = unit0, pf_kb = 0, pf_row = 0;
       if (pf_u < total_units && p.prefetch > 0) {
         const Unit P = unit_at(p, pf_u);
-        pf_row = P.e * p.a_rows_per_expert + P.m * kBlockM;
+        pf_row = P.e * p.a_rows_per_expert + P.m * kRowsPerUnit + static_cast<int>(rank) * kBlockM;
       }
       auto prefetch_next = [&]() {
         if (pf_u >= total_units || p.prefetch <= 0) return;
@@ -231,18 +250,21 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
         if (kMode == 0) tma_prefetch_l2_2d(&maps.a1, px, pf_row);
         if (++pf_kb == p.k_blocks) {
           pf_kb = 0;
-          pf_u += gridDim.x;
+          pf_u += unit_step;
           if (pf_u < total_units) {
             const Unit P = unit_at(p, pf_u);
-            pf_row = P.e * p.a_rows_per_expert + P.m * kBlockM;
+            pf_row = P.e * p.a_rows_per_expert + P.m * kRowsPerUnit + static_cast<int>(rank) * kBlockM;
           }
         }
       };
       for (int i = 0; i < p.prefetch; ++i) prefetch_next();
-      for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
+      for (int u = unit0; u < total_units && ok; u += unit_step) {
         const Unit U = unit_at(p, u);
-        const int a_row = U.e * p.a_rows_per_expert + U.m * kBlockM;
-        const int nbox = (U.n + kBoxRows - 1) / kBoxRows;
+        const int a_row = U.e * p.a_rows_per_expert + U.m * kRowsPerUnit + static_cast<int>(rank) * kBlockM;
+        // pair: this CTA loads token rows [start + rank*N/2, +N/2), N = round16(n)
+        const int n_local = kPair ? ((U.n + 15) & ~15) / 2 : U.n;
+        const int b_row0 = U.start + static_cast<int>(rank) * n_local;
+        const int nbox = (n_local + kBoxRows - 1) / kBoxRows;
         const uint32_t a_bytes = kFp4 ? kNumA * (kPackedTileBytes + kScaleTileBytes) : kNumA * kATileBytes;
         const uint32_t bytes = a_bytes + static_cast<uint32_t>(nbox) * kBoxBytes;
         for (int kb = 0; kb < p.k_blocks; ++kb) {
@@ -251,8 +273,23 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full[stage], bytes);
           const int kx = kb * kBlockK;
+          if (kPair) {
+            // both CTAs' bytes land on the even CTA's full barrier
+            const uint32_t bar0 = mapa_shared(&full[stage], 0);
+            if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * bytes);
+            tma_load_2d_pair(a_tile(stage, 0), &maps.a0, bar0, kx, a_row);
+            if (kMode == 0) tma_load_2d_pair(a_tile(stage, 1), &maps.a1, bar0, kx, a_row);
+            for (int b = 0; b < nbox; ++b)
+              tma_load_2d_pair_hint(b_tile(stage) + b * kBoxBytes, &maps.b, bar0, kx, b_row0 + b * kBoxRows, pol_x);
+            ++issued;
+            if (++stage == p.stages) {
+              stage = 0;
+              phase ^= 1u;
+            }
+            continue;
+          }
+          mbar_arrive_expect_tx(&full[stage], bytes);
           if (kFp4) {
             const int sx = (kb >> 2) * static_cast<int>(kScaleBoxCols);
             tma_load_2d_nohint(p_tile(stage, 0), &maps.a0, &full[stage], kx / 2, a_row);
@@ -275,8 +312,9 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
         }
       }
       // Drain: the latest load issued on every slot has landed (immediate in
-      // the normal case, where the MMA warp consumed them all).
-      for (int s = 0; s < p.stages; ++s) {
+      // the normal case, where the MMA warp consumed them all).  Pair: the
+      // even CTA's barriers also count the other CTA's bytes.
+      for (int s = 0; s < p.stages && rank == 0; ++s) {
         if (issued <= s && issued < p.stages) continue;  // slot never used
         const uint32_t par = s < stage ? phase : (phase ^ 1u);
         mbar_wait(&full[s], par, p.timeout_ns, nullptr, p.status, kWhereDrain);
@@ -284,14 +322,14 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    if (lane == 0 && rank == 0) {
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
+      for (int u = unit0; u < total_units && ok; u += unit_step) {
         const Unit U = unit_at(p, u);
         const uint32_t n_mma = static_cast<uint32_t>((U.n + 15) & ~15);
-        const uint32_t idesc = idesc_bf16_f32(kBlockM, n_mma);
+        const uint32_t idesc = idesc_bf16_f32(kPair ? 2 * kBlockM : kBlockM, n_mma);
         if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1u, p.timeout_ns, abort_flag, p.status, kWhereMmaAccEmpty))
           break;
         tc_fence_after();
@@ -312,24 +350,38 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
 #pragma unroll
           for (int k = 0; k < kBlockK / 16; ++k) {
             const uint32_t accumulate = (kb | k) != 0 ? 1u : 0u;
-            mma_bf16(d0, da0 + 2u * k, db + 2u * k, idesc, accumulate);
-            if (kMode == 0) mma_bf16(d1, da1 + 2u * k, db + 2u * k, idesc, accumulate);
+            if (kPair) {
+              mma_bf16_pair(d0, da0 + 2u * k, db + 2u * k, idesc, accumulate);
+              if (kMode == 0) mma_bf16_pair(d1, da1 + 2u * k, db + 2u * k, idesc, accumulate);
+            } else {
+              mma_bf16(d0, da0 + 2u * k, db + 2u * k, idesc, accumulate);
+              if (kMode == 0) mma_bf16(d1, da1 + 2u * k, db + 2u * k, idesc, accumulate);
+            }
           }
-          mma_commit(&empty[stage]);
+          if (kPair)
+            mma_commit_pair_multicast(&empty[stage], 0x3);
+          else
+            mma_commit(&empty[stage]);
           if (++stage == p.stages) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        mma_commit(&acc_full[acc]);
+        if (kPair)
+          mma_commit_pair_multicast(&acc_full[acc], 0x3);
+        else
+          mma_commit(&acc_full[acc]);
         if (++acc == p.acc_stages) {
           acc = 0;
           acc_phase ^= 1u;
         }
       }
       // Every MMA issued by this thread has completed before TMEM is freed.
-      mma_commit(drain);
+      if (kPair)
+        mma_commit_pair_multicast(drain, 0x1);
+      else
+        mma_commit(drain);
       mbar_wait(drain, 0, p.timeout_ns, nullptr, p.status, kWhereDrain);
     }
   } else if (warp < 2 + kEpilogueWarps) {
@@ -339,7 +391,7 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
     const int row = quad * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
+    for (int u = unit0; u < total_units; u += unit_step) {
       const Unit U = unit_at(p, u);
       int ok = 1;
       if (lane == 0)
@@ -348,7 +400,7 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
       if (!ok) break;
       tc_fence_after();
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc) * p.acc_cols;
-      const int feat = U.m * kBlockM + row;
+      const int feat = U.m * kRowsPerUnit + static_cast<int>(rank) * kBlockM + row;
       const float s0 = p.gs0 != nullptr ? __ldg(&p.gs0[U.e]) : 1.0f;
       const float s1 = (kMode == 0 && p.gs1 != nullptr) ? __ldg(&p.gs1[U.e]) : 1.0f;
       const int ncols = (U.n + 15) & ~15;
@@ -380,7 +432,12 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[acc]);
+      if (lane == 0) {
+        if (kPair)
+          mbar_arrive_cluster(mapa_shared(&acc_empty[acc], 0));
+        else
+          mbar_arrive(&acc_empty[acc]);
+      }
       if (++acc == p.acc_stages) {
         acc = 0;
         acc_phase ^= 1u;
@@ -398,7 +455,7 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
+    for (int u = unit0; u < total_units && ok; u += unit_step) {
       for (int kb = 0; kb < p.k_blocks; ++kb) {
         int good = 1;
         if (lane == 0)
@@ -421,19 +478,42 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
   }
 
   tc_fence_before();
-  __syncthreads();
+  if (kPair)
+    cluster_sync();  // no CTA leaves while the other may still signal its barriers
+  else
+    __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, p.tmem_cols);
+    if (kPair)
+      tmem_dealloc_pair(tmem_base, p.tmem_cols);
+    else
+      tmem_dealloc(tmem_base, p.tmem_cols);
   }
 }
 
-template <int kMode, bool kFp4>
+template <int kMode, bool kFp4, bool kPair>
 cudaError_t launch_one(const GemmMaps& maps, const GemmParams& p, int grid, size_t smem_bytes, cudaStream_t stream) {
-  const cudaError_t err = cudaFuncSetAttribute(moe_gemm_kernel<kMode, kFp4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               static_cast<int>(smem_bytes));
+  auto kern = moe_gemm_kernel<kMode, kFp4, kPair>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_bytes));
   if (err != cudaSuccess) return err;
-  moe_gemm_kernel<kMode, kFp4><<<grid, kFp4 ? kThreadsFp4 : kThreadsBf16, smem_bytes, stream>>>(maps, p);
+  if (!kPair) {
+    kern<<<grid, kFp4 ? kThreadsFp4 : kThreadsBf16, smem_bytes, stream>>>(maps, p);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kThreadsBf16);
+  cfg.dynamicSmemBytes = smem_bytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  err = cudaLaunchKernelEx(&cfg, kern, maps, p);
+  if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
 
@@ -443,13 +523,43 @@ size_t gemm_smem_bytes(int stages, int acc_stages, size_t stage_bytes) {
   return 1024 + static_cast<size_t>(stages) * stage_bytes + (3 * stages + 2 * acc_stages + 1) * 8 + 16;
 }
 
-cudaError_t launch_gemm(int mode, bool fp4, const GemmMaps& maps, const GemmParams& p, int grid, size_t smem_bytes,
-                        cudaStream_t stream) {
+int gemm_pair_max_clusters(int mode, size_t smem_bytes) {
+  auto kern = mode == 0 ? moe_gemm_kernel<0, false, true> : moe_gemm_kernel<1, false, true>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_bytes)) !=
+      cudaSuccess)
+    return 0;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0) != cudaSuccess) return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2);
+  cfg.blockDim = dim3(kThreadsBf16);
+  cfg.dynamicSmemBytes = smem_bytes;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+cudaError_t launch_gemm(int mode, bool fp4, bool pair, const GemmMaps& maps, const GemmParams& p, int grid,
+                        size_t smem_bytes, cudaStream_t stream) {
+  if (pair) {
+    if (fp4) return cudaErrorInvalidValue;
+    return mode == 0 ? launch_one<0, false, true>(maps, p, grid, smem_bytes, stream)
+                     : launch_one<1, false, true>(maps, p, grid, smem_bytes, stream);
+  }
   if (mode == 0)
-    return fp4 ? launch_one<0, true>(maps, p, grid, smem_bytes, stream)
-               : launch_one<0, false>(maps, p, grid, smem_bytes, stream);
-  return fp4 ? launch_one<1, true>(maps, p, grid, smem_bytes, stream)
-             : launch_one<1, false>(maps, p, grid, smem_bytes, stream);
+    return fp4 ? launch_one<0, true, false>(maps, p, grid, smem_bytes, stream)
+               : launch_one<0, false, false>(maps, p, grid, smem_bytes, stream);
+  return fp4 ? launch_one<1, true, false>(maps, p, grid, smem_bytes, stream)
+             : launch_one<1, false, false>(maps, p, grid, smem_bytes, stream);
 }
 
 }  // namespace beam

@@ -50,7 +50,7 @@ struct GemmParams {
   const int32_t* counts;        // [E]
   const int32_t* offsets;       // [E+1]
   const int32_t* chunk_prefix;  // [E+1] exclusive scan of ceil(counts / nmax)
-  int m_tiles;                  // weight rows per expert / kBlockM
+  int m_tiles;                  // weight rows per expert / rows per unit (128, or 256 for CTA pairs)
   int a_rows_per_expert;        // I (gate/up) or H (down)
   int k_blocks;                 // K / kBlockK
   int nmax;                     // tokens per chunk (multiple of kBoxRows, <= 256)
@@ -96,9 +96,11 @@ cudaError_t launch_dispatch(const int32_t* ids, int R, int n_tiles, int32_t* til
                             int32_t* perm, int32_t* pos, cudaStream_t stream);
 cudaError_t launch_gather(const void* x, bool x_bf16, int H, const int32_t* perm, int R,
                           __nv_bfloat16* xp, int num_sms, cudaStream_t stream);
-cudaError_t launch_gemm(int mode, bool fp4, const GemmMaps& maps, const GemmParams& p, int grid,
+cudaError_t launch_gemm(int mode, bool fp4, bool pair, const GemmMaps& maps, const GemmParams& p, int grid,
                         size_t smem_bytes, cudaStream_t stream);
 size_t gemm_smem_bytes(int stages, int acc_stages, size_t stage_bytes);
+// Clusters of two CTAs of the pair kernel that can be resident at once (0: none).
+int gemm_pair_max_clusters(int mode, size_t smem_bytes);
 cudaError_t launch_combine(const __nv_bfloat16* yr, const int32_t* pos, const float* w, int T, int H,
                            void* y, bool y_bf16, cudaStream_t stream);
 cudaError_t launch_debug_timeout(uint32_t* status, uint64_t timeout_ns, cudaStream_t stream);

@@ -137,6 +137,24 @@ def test_experts_given_routing(T, H, I, hot):
     assert rel_err(y.cpu().double().numpy(), y_ref) <= Y_TOL["bf16"]
 
 
+@pytest.mark.parametrize("T,H,I,hot", [(600, 512, 512, None), (700, 512, 256, (4, 5, 6, 200)),
+                                       (256, 256, 768, None)])
+def test_experts_cta_pair_path(T, H, I, hot):
+    """Shapes that take the two-CTA (M=256 pair MMA) grouped GEMMs: BF16
+    weights, 256-route chunks, H and I multiples of 256."""
+    wl = inputs.workload("tiny", T=T, H=H, I=I, x_dtype="bf16", w_dtype="bf16", seed=3 + T)
+    dg, _ = _gpu_inputs(wl, cpu_gen=True)
+    ids, w = seeded_routing(T, seed=T + 2, hot=hot)
+    sh = moe.shape(T, H, I)
+    ws = moe.alloc_workspace(sh)
+    y = torch.empty((T, H), dtype=torch.bfloat16, device=DEV)
+    moe.beam_moe_experts(sh, dg["x"], dg, ids.to(DEV), w.to(DEV), y, ws)
+    code, where = moe.beam_moe_read_device_status(ws)
+    assert code == 0, (code, where)
+    y_ref = oracle_y(dg, np.arange(T), ids.numpy(), w.numpy().astype(np.float64))
+    assert rel_err(y.cpu().double().numpy(), y_ref) <= Y_TOL["bf16"]
+
+
 def test_experts_nvfp4_given_routing():
     """NVFP4 experts on a seeded routing whose hot experts take every token
     (several chunks per expert)."""

@@ -96,7 +96,7 @@ bool make_u8_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t ro
 
 // ------------------------------------------------------------------ layout
 struct Layout {
-  size_t status, counts, offsets, chunk_prefix, tile_hist, part, perm, pos, xp, h, yr, total;
+  size_t status, sched, counts, offsets, chunk_prefix, tile_hist, part, perm, pos, xp, h, yr, total;
   int n_tiles, split_cap;
 };
 
@@ -117,6 +117,7 @@ void make_layout(const beam_moe_shape_t& s, Layout& L) {
   L.n_tiles = static_cast<int>((T + kRouterTile - 1) / kRouterTile);
   L.split_cap = router_split_cap(s.T, s.H);
   L.status = take(16);
+  L.sched = take(16);
   L.counts = take(kExperts * 4);
   L.offsets = take((kExperts + 1) * 4);
   L.chunk_prefix = take((kExperts + 1) * 4);
@@ -293,9 +294,7 @@ beam_status_t run_gemm(int mode, const beam_moe_shape_t& s, const beam_expert_we
   if (acc_stages < 1) acc_stages = 1;
   p.acc_stages = acc_stages;
   p.tmem_cols = pow2_at_least(static_cast<uint32_t>(acc_stages) * p.acc_cols);
-  // Weight k-blocks prefetched into L2 ahead of the shared-memory ring (off:
-  // measured slower on B300 than the ring alone).
-  p.prefetch = 0;
+  p.sched = at<int>(ws, L.sched) + mode;
   p.out = mode == 0 ? h : yr;
   p.out_ld = mode == 0 ? s.I : s.H;
   p.gs0 = fp4 ? (mode == 0 ? wts->gate_gs : wts->down_gs) : nullptr;
@@ -324,6 +323,7 @@ beam_status_t run_gemm(int mode, const beam_moe_shape_t& s, const beam_expert_we
     smem = gemm_smem_bytes(st1, acc_stages, sb1);
     grid = d.sms;
   }
+  if (cudaMemsetAsync(p.sched, 0, sizeof(int), stream) != cudaSuccess) return BEAM_ERR_CUDA;
   return cuda_status(launch_gemm(mode, fp4, pair, maps, p, grid, smem, stream));
 }
 

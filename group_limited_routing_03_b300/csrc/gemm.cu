@@ -51,6 +51,7 @@ constexpr int kThreadsBf16 = 32 * (2 + kEpilogueWarps);
 constexpr int kThreadsFp4 = 32 * (2 + kEpilogueWarps + kConvertWarps);
 constexpr uint32_t kATileBytes = kBlockM * kBlockK * 2;     // 16 KiB of BF16
 constexpr uint32_t kBoxBytes = kBoxRows * kBlockK * 2;      // 4 KiB
+constexpr int kSchedRing = 8;                               // scheduled unit indices in flight
 
 struct Unit {
   int e, m, start, n;
@@ -165,6 +166,10 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
   constexpr int kNumA = kMode == 0 ? 2 : 1;
   constexpr int kRowsPerUnit = kPair ? 2 * kBlockM : kBlockM;
   static_assert(!(kPair && kFp4), "pair MMA path is BF16 only");
+  // Roles that read every scheduled unit index (they release ring slots).
+  constexpr uint32_t kRingConsumers =
+      kPair ? (1 + kEpilogueWarps) + (1 + kEpilogueWarps)  // even CTA: MMA + epilogue; odd: producer + epilogue
+            : 1 + kEpilogueWarps + (kFp4 ? kConvertWarps : 0);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t b_tile_bytes = static_cast<uint32_t>(kPair ? p.nmax / 2 : p.nmax) * kBlockK * 2;
@@ -176,13 +181,14 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
   uint64_t* acc_full = conv + p.stages;
   uint64_t* acc_empty = acc_full + p.acc_stages;
   uint64_t* drain = acc_empty + p.acc_stages;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* ufull = drain + 1;        // unit ring: index published
+  uint64_t* uempty = ufull + kSchedRing;  // unit ring: index read by every consumer
+  volatile int* ring = reinterpret_cast<volatile int*>(uempty + kSchedRing);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(const_cast<int*>(ring) + kSchedRing);
   volatile uint32_t* abort_flag = tmem_slot + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = kPair ? cluster_ctarank() : 0u;  // 0: the CTA that issues the MMAs
-  const int unit0 = kPair ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
-  const int unit_step = kPair ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
   // Stage layout: [A bf16 x kNumA][B][packed x kNumA][scales x kNumA]
   auto a_tile = [&](int s, int which) { return smem + static_cast<size_t>(s) * stage_bytes + which * kATileBytes; };
   auto b_tile = [&](int s) { return smem + static_cast<size_t>(s) * stage_bytes + kNumA * kATileBytes; };
@@ -202,6 +208,10 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
       mbar_init(&acc_empty[a], kPair ? 2 * kEpilogueWarps : kEpilogueWarps);
     }
     mbar_init(drain, 1);
+    for (int r = 0; r < kSchedRing; ++r) {
+      mbar_init(&ufull[r], 1);
+      mbar_init(&uempty[r], kRingConsumers);
+    }
     *abort_flag = 0u;
     fence_mbar_init();
     tma_prefetch_desc(&maps.a0);
@@ -226,39 +236,72 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  const int total_units = __ldg(&p.chunk_prefix[kExperts]) * p.m_tiles;
+  // --- dynamic unit schedule ------------------------------------------------
+  // The fetching thread (producer of the even CTA) takes unit indices from a
+  // global counter in order and publishes each one, or -1 at the end, into a
+  // ring read by every role of both CTAs, so units (and the sibling chunks of
+  // one expert, which share weight tiles through L2) start in index order.
+  int ring_slot = 0;
+  uint32_t ring_phase = 0;
+  auto ring_advance = [&]() {
+    if (++ring_slot == kSchedRing) {
+      ring_slot = 0;
+      ring_phase ^= 1u;
+    }
+  };
+  // One thread: the next unit index (-1: no more); false when a wait gave up.
+  auto ring_take = [&](int& u) -> bool {
+    if (!mbar_wait_cluster(&ufull[ring_slot], ring_phase, p.timeout_ns, abort_flag, p.status, kWhereSchedule))
+      return false;
+    u = ring[ring_slot];
+    if (kPair)
+      mbar_arrive_cluster(mapa_shared(&uempty[ring_slot], 0));
+    else
+      mbar_arrive(&uempty[ring_slot]);
+    ring_advance();
+    return true;
+  };
+  // Fetching thread only.
+  auto ring_publish = [&](int u) -> bool {
+    if (!mbar_wait(&uempty[ring_slot], ring_phase ^ 1u, p.timeout_ns, abort_flag, p.status, kWhereSchedule))
+      return false;
+    ring[ring_slot] = u;
+    if (kPair) {
+      st_shared_cluster_u32(mapa_shared(const_cast<int*>(&ring[ring_slot]), 1), static_cast<uint32_t>(u));
+      mbar_arrive_cluster(mapa_shared(&ufull[ring_slot], 1));
+    }
+    mbar_arrive(&ufull[ring_slot]);
+    ring_advance();
+    return true;
+  };
+  // Warp-wide version of ring_take for the epilogue / converter warps.
+  auto warp_take = [&](int& u) -> bool {
+    int good = 1, v = -1;
+    if (lane == 0) good = ring_take(v) ? 1 : 0;
+    good = __shfl_sync(0xFFFFFFFFu, good, 0);
+    u = __shfl_sync(0xFFFFFFFFu, v, 0);
+    return good != 0;
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       const uint64_t pol_x = l2_policy_evict_last();
+      const int total_units = __ldg(&p.chunk_prefix[kExperts]) * p.m_tiles;
       int stage = 0;
       uint32_t phase = 0;
       long long issued = 0;
       bool ok = true;
-      // Optional: weight k-blocks prefetched into L2 p.prefetch k-blocks
-      // ahead of the shared-memory ring, across unit boundaries.
-      int pf_u = unit0, pf_kb = 0, pf_row = 0;
-      if (pf_u < total_units && p.prefetch > 0) {
-        const Unit P = unit_at(p, pf_u);
-        pf_row = P.e * p.a_rows_per_expert + P.m * kRowsPerUnit + static_cast<int>(rank) * kBlockM;
-      }
-      auto prefetch_next = [&]() {
-        if (pf_u >= total_units || p.prefetch <= 0) return;
-        const int px = kFp4 ? pf_kb * (kBlockK / 2) : pf_kb * kBlockK;
-        tma_prefetch_l2_2d(&maps.a0, px, pf_row);
-        if (kMode == 0) tma_prefetch_l2_2d(&maps.a1, px, pf_row);
-        if (++pf_kb == p.k_blocks) {
-          pf_kb = 0;
-          pf_u += unit_step;
-          if (pf_u < total_units) {
-            const Unit P = unit_at(p, pf_u);
-            pf_row = P.e * p.a_rows_per_expert + P.m * kRowsPerUnit + static_cast<int>(rank) * kBlockM;
-          }
+      while (ok) {
+        int u;
+        if (rank == 0) {
+          u = atomicAdd(p.sched, 1);
+          if (u >= total_units) u = -1;
+          if (!ring_publish(u)) break;
+        } else if (!ring_take(u)) {
+          break;
         }
-      };
-      for (int i = 0; i < p.prefetch; ++i) prefetch_next();
-      for (int u = unit0; u < total_units && ok; u += unit_step) {
+        if (u < 0) break;
         const Unit U = unit_at(p, u);
         const int a_row = U.e * p.a_rows_per_expert + U.m * kRowsPerUnit + static_cast<int>(rank) * kBlockM;
         // pair: this CTA loads token rows [start + rank*N/2, +N/2), N = round16(n)
@@ -268,7 +311,6 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
         const uint32_t a_bytes = kFp4 ? kNumA * (kPackedTileBytes + kScaleTileBytes) : kNumA * kATileBytes;
         const uint32_t bytes = a_bytes + static_cast<uint32_t>(nbox) * kBoxBytes;
         for (int kb = 0; kb < p.k_blocks; ++kb) {
-          prefetch_next();
           if (!mbar_wait(&empty[stage], phase ^ 1u, p.timeout_ns, abort_flag, p.status, kWhereProducerEmpty)) {
             ok = false;
             break;
@@ -282,28 +324,23 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
             if (kMode == 0) tma_load_2d_pair(a_tile(stage, 1), &maps.a1, bar0, kx, a_row);
             for (int b = 0; b < nbox; ++b)
               tma_load_2d_pair_hint(b_tile(stage) + b * kBoxBytes, &maps.b, bar0, kx, b_row0 + b * kBoxRows, pol_x);
-            ++issued;
-            if (++stage == p.stages) {
-              stage = 0;
-              phase ^= 1u;
-            }
-            continue;
-          }
-          mbar_arrive_expect_tx(&full[stage], bytes);
-          if (kFp4) {
-            const int sx = (kb >> 2) * static_cast<int>(kScaleBoxCols);
-            tma_load_2d_nohint(p_tile(stage, 0), &maps.a0, &full[stage], kx / 2, a_row);
-            tma_load_2d_nohint(s_tile(stage, 0), &maps.s0, &full[stage], sx, a_row);
-            if (kMode == 0) {
-              tma_load_2d_nohint(p_tile(stage, 1), &maps.a1, &full[stage], kx / 2, a_row);
-              tma_load_2d_nohint(s_tile(stage, 1), &maps.s1, &full[stage], sx, a_row);
-            }
           } else {
-            tma_load_2d_nohint(a_tile(stage, 0), &maps.a0, &full[stage], kx, a_row);
-            if (kMode == 0) tma_load_2d_nohint(a_tile(stage, 1), &maps.a1, &full[stage], kx, a_row);
+            mbar_arrive_expect_tx(&full[stage], bytes);
+            if (kFp4) {
+              const int sx = (kb >> 2) * static_cast<int>(kScaleBoxCols);
+              tma_load_2d_nohint(p_tile(stage, 0), &maps.a0, &full[stage], kx / 2, a_row);
+              tma_load_2d_nohint(s_tile(stage, 0), &maps.s0, &full[stage], sx, a_row);
+              if (kMode == 0) {
+                tma_load_2d_nohint(p_tile(stage, 1), &maps.a1, &full[stage], kx / 2, a_row);
+                tma_load_2d_nohint(s_tile(stage, 1), &maps.s1, &full[stage], sx, a_row);
+              }
+            } else {
+              tma_load_2d_nohint(a_tile(stage, 0), &maps.a0, &full[stage], kx, a_row);
+              if (kMode == 0) tma_load_2d_nohint(a_tile(stage, 1), &maps.a1, &full[stage], kx, a_row);
+            }
+            for (int b = 0; b < nbox; ++b)
+              tma_load_2d(b_tile(stage) + b * kBoxBytes, &maps.b, &full[stage], kx, U.start + b * kBoxRows, pol_x);
           }
-          for (int b = 0; b < nbox; ++b)
-            tma_load_2d(b_tile(stage) + b * kBoxBytes, &maps.b, &full[stage], kx, U.start + b * kBoxRows, pol_x);
           ++issued;
           if (++stage == p.stages) {
             stage = 0;
@@ -326,7 +363,9 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
-      for (int u = unit0; u < total_units && ok; u += unit_step) {
+      while (ok) {
+        int u;
+        if (!ring_take(u) || u < 0) break;
         const Unit U = unit_at(p, u);
         const uint32_t n_mma = static_cast<uint32_t>((U.n + 15) & ~15);
         const uint32_t idesc = idesc_bf16_f32(kPair ? 2 * kBlockM : kBlockM, n_mma);
@@ -391,7 +430,9 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
     const int row = quad * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int u = unit0; u < total_units; u += unit_step) {
+    while (true) {
+      int u;
+      if (!warp_take(u) || u < 0) break;
       const Unit U = unit_at(p, u);
       int ok = 1;
       if (lane == 0)
@@ -455,7 +496,9 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    for (int u = unit0; u < total_units && ok; u += unit_step) {
+    while (ok) {
+      int u;
+      if (!warp_take(u) || u < 0) break;
       for (int kb = 0; kb < p.k_blocks; ++kb) {
         int good = 1;
         if (lane == 0)
@@ -520,7 +563,8 @@ cudaError_t launch_one(const GemmMaps& maps, const GemmParams& p, int grid, size
 }  // namespace
 
 size_t gemm_smem_bytes(int stages, int acc_stages, size_t stage_bytes) {
-  return 1024 + static_cast<size_t>(stages) * stage_bytes + (3 * stages + 2 * acc_stages + 1) * 8 + 16;
+  return 1024 + static_cast<size_t>(stages) * stage_bytes + (3 * stages + 2 * acc_stages + 1 + 2 * kSchedRing) * 8 +
+         kSchedRing * 4 + 16;
 }
 
 int gemm_pair_max_clusters(int mode, size_t smem_bytes) {

@@ -58,7 +58,7 @@ struct GemmParams {
   int acc_stages;               // TMEM accumulator buffers
   uint32_t acc_cols;            // TMEM columns per accumulator buffer
   uint32_t tmem_cols;           // TMEM columns allocated (power of two)
-  int prefetch;                 // weight k-blocks prefetched into L2 ahead of the ring
+  int* sched;                   // unit counter (zeroed before the launch)
   __nv_bfloat16* out;           // h [R, I] or yr [R, H], perm order
   int out_ld;                   // I or H
   const float* gs0;             // NVFP4 global scales (gate or down) [E], else null

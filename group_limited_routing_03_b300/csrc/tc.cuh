@@ -22,6 +22,7 @@ enum : uint32_t {
   kWhereEpiAccFull = 4,
   kWhereDrain = 5,
   kWhereConvert = 6,
+  kWhereSchedule = 7,
   kWhereDebug = 9,
 };
 
@@ -81,6 +82,36 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 15u) == 0) {
+      if (abort != nullptr && *abort != 0u) return false;
+      if (globaltimer_ns() - t0 > limit_ns) {
+        report_status(status, kStatusTimeout, where);
+        if (abort != nullptr) *abort = 1u;
+        return false;
+      }
+    }
+  }
+}
+
+// As mbar_wait, with acquire at cluster scope (for barriers another CTA of
+// the cluster arrives on after writing data this thread will read).
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, uint64_t limit_ns,
+                                                  volatile uint32_t* abort, uint32_t* status, uint32_t where) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
     if ((it & 15u) == 0) {
       if (abort != nullptr && *abort != 0u) return false;
       if (globaltimer_ns() - t0 > limit_ns) {
@@ -216,6 +247,10 @@ __device__ __forceinline__ uint32_t mapa_shared(const void* p, uint32_t rank) {
   uint32_t out;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(out) : "r"(smem_u32(p)), "r"(rank));
   return out;
+}
+// Store to shared memory of another CTA of the cluster.
+__device__ __forceinline__ void st_shared_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
 }
 // Arrive on an mbarrier of another CTA of the cluster (release, cluster scope).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {

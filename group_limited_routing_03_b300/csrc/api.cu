@@ -272,8 +272,9 @@ beam_status_t run_gemm(int mode, const beam_moe_shape_t& s, const beam_expert_we
   if (!ok) return BEAM_ERR_CUDA;
   // CTA pairs (one M=256 MMA per unit over two SMs) halve each SM's shared-
   // memory operand traffic; used for BF16 weights when chunks reach 256 routes.
-  bool pair = !fp4 && nmax == 256 && s.H % 256 == 0 && s.I % 256 == 0 && d.sms >= 2;
-  const int rows_per_unit = pair ? 2 * kBlockM : kBlockM;
+  bool pair = !fp4 && nmax == 256 && s.H % 512 == 0 && s.I % 256 == 0 && d.sms >= 2;
+  // pair units: gate/up 256 features (gate and up tiles), down 512 features
+  const int rows_per_unit = pair ? (mode == 0 ? 2 * kBlockM : 4 * kBlockM) : kBlockM;
   GemmParams p;
   p.counts = at<int32_t>(ws, L.counts);
   p.offsets = at<int32_t>(ws, L.offsets);
@@ -283,12 +284,12 @@ beam_status_t run_gemm(int mode, const beam_moe_shape_t& s, const beam_expert_we
   p.k_blocks = (mode == 0 ? s.H : s.I) / kBlockK;
   p.nmax = nmax;
   const size_t budget = static_cast<size_t>(d.smem_optin) - 1024 - 512;
-  const size_t sb = gemm_stage_bytes(mode, fp4, pair ? nmax / 2 : nmax);
+  const size_t sb = gemm_stage_bytes((mode == 0 || pair) ? 2 : 1, fp4, pair ? nmax / 2 : nmax);
   int stages = static_cast<int>(budget / sb);
   if (stages > 8) stages = 8;
   if (stages < 2) return BEAM_ERR_UNSUPPORTED;
   p.stages = stages;
-  p.acc_cols = static_cast<uint32_t>(mode == 0 ? 2 * nmax : nmax);
+  p.acc_cols = static_cast<uint32_t>((mode == 0 || pair) ? 2 * nmax : nmax);
   int acc_stages = static_cast<int>(512 / p.acc_cols);
   if (acc_stages > 4) acc_stages = 4;
   if (acc_stages < 1) acc_stages = 1;
@@ -315,7 +316,13 @@ beam_status_t run_gemm(int mode, const beam_moe_shape_t& s, const beam_expert_we
   if (!pair && nmax == 256 && !fp4) {
     // fall back to one CTA per unit: recompute the per-CTA tiling
     p.m_tiles = (mode == 0 ? s.I : s.H) / kBlockM;
-    const size_t sb1 = gemm_stage_bytes(mode, fp4, nmax);
+    const size_t sb1 = gemm_stage_bytes(mode == 0 ? 2 : 1, fp4, nmax);
+    p.acc_cols = static_cast<uint32_t>(mode == 0 ? 2 * nmax : nmax);
+    acc_stages = static_cast<int>(512 / p.acc_cols);
+    if (acc_stages > 4) acc_stages = 4;
+    if (acc_stages < 1) acc_stages = 1;
+    p.acc_stages = acc_stages;
+    p.tmem_cols = pow2_at_least(static_cast<uint32_t>(acc_stages) * p.acc_cols);
     int st1 = static_cast<int>(budget / sb1);
     if (st1 > 8) st1 = 8;
     if (st1 < 2) return BEAM_ERR_UNSUPPORTED;

@@ -163,8 +163,10 @@ __device__ __forceinline__ void convert_row(const uint8_t* packed, const uint8_t
 template <int kMode, bool kFp4, bool kPair>
 __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
     moe_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
-  constexpr int kNumA = kMode == 0 ? 2 : 1;
-  constexpr int kRowsPerUnit = kPair ? 2 * kBlockM : kBlockM;
+  // Weight tiles per stage: gate/up always two (gate, up); down two on CTA
+  // pairs (two 256-row halves of a 512-row unit sharing the token tile).
+  constexpr int kNumA = (kMode == 0 || kPair) ? 2 : 1;
+  constexpr int kRowsPerUnit = kPair ? (kMode == 0 ? 2 * kBlockM : 4 * kBlockM) : kBlockM;
   static_assert(!(kPair && kFp4), "pair MMA path is BF16 only");
   // Roles that read every scheduled unit index (they release ring slots).
   constexpr uint32_t kRingConsumers =
@@ -173,7 +175,7 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t b_tile_bytes = static_cast<uint32_t>(kPair ? p.nmax / 2 : p.nmax) * kBlockK * 2;
-  const uint32_t stage_bytes = static_cast<uint32_t>(gemm_stage_bytes(kMode, kFp4, kPair ? p.nmax / 2 : p.nmax));
+  const uint32_t stage_bytes = static_cast<uint32_t>(gemm_stage_bytes(kNumA, kFp4, kPair ? p.nmax / 2 : p.nmax));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(p.stages) * stage_bytes);
   uint64_t* full = bars;
   uint64_t* empty = full + p.stages;
@@ -321,7 +323,10 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
             const uint32_t bar0 = mapa_shared(&full[stage], 0);
             if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * bytes);
             tma_load_2d_pair(a_tile(stage, 0), &maps.a0, bar0, kx, a_row);
-            if (kMode == 0) tma_load_2d_pair(a_tile(stage, 1), &maps.a1, bar0, kx, a_row);
+            if (kMode == 0)
+              tma_load_2d_pair(a_tile(stage, 1), &maps.a1, bar0, kx, a_row);
+            else  // second 256-row half of the down unit
+              tma_load_2d_pair(a_tile(stage, 1), &maps.a0, bar0, kx, a_row + 2 * kBlockM);
             for (int b = 0; b < nbox; ++b)
               tma_load_2d_pair_hint(b_tile(stage) + b * kBoxBytes, &maps.b, bar0, kx, b_row0 + b * kBoxRows, pol_x);
           } else {
@@ -391,7 +396,7 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
             const uint32_t accumulate = (kb | k) != 0 ? 1u : 0u;
             if (kPair) {
               mma_bf16_pair(d0, da0 + 2u * k, db + 2u * k, idesc, accumulate);
-              if (kMode == 0) mma_bf16_pair(d1, da1 + 2u * k, db + 2u * k, idesc, accumulate);
+              mma_bf16_pair(d1, da1 + 2u * k, db + 2u * k, idesc, accumulate);
             } else {
               mma_bf16(d0, da0 + 2u * k, db + 2u * k, idesc, accumulate);
               if (kMode == 0) mma_bf16(d1, da1 + 2u * k, db + 2u * k, idesc, accumulate);
@@ -465,10 +470,17 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
             }
           }
         } else {
+          float g2[16];
+          if (kNumA == 2) tmem_ld16(tbase + static_cast<uint32_t>(p.nmax + c0), g2);
           tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < 16; ++j)
-            if (c0 + j < U.n) out[static_cast<size_t>(c0 + j) * p.out_ld] = __float2bfloat16_rn(g[j] * s0);
+          for (int j = 0; j < 16; ++j) {
+            if (c0 + j < U.n) {
+              out[static_cast<size_t>(c0 + j) * p.out_ld] = __float2bfloat16_rn(g[j] * s0);
+              // second half of a pair down unit: features + 256
+              if (kNumA == 2) out[static_cast<size_t>(c0 + j) * p.out_ld + 2 * kBlockM] = __float2bfloat16_rn(g2[j]);
+            }
+          }
         }
       }
       tc_fence_before();

@@ -75,9 +75,8 @@ struct GemmMaps {
 
 // Bytes of one pipeline stage: BF16 weight tile(s), activation boxes, and for
 // NVFP4 the packed tile(s) and scale tile(s) the converters read.
-__host__ __device__ inline size_t gemm_stage_bytes(int mode, bool fp4, int nmax) {
-  const size_t num_a = mode == 0 ? 2 : 1;
-  size_t b = num_a * kBlockM * kBlockK * 2 + static_cast<size_t>(nmax) * kBlockK * 2;
+__host__ __device__ inline size_t gemm_stage_bytes(int num_a, bool fp4, int nmax) {
+  size_t b = static_cast<size_t>(num_a) * kBlockM * kBlockK * 2 + static_cast<size_t>(nmax) * kBlockK * 2;
   if (fp4) b += num_a * (kPackedTileBytes + kScaleTileBytes);
   return b;
 }

@@ -138,10 +138,11 @@ def test_experts_given_routing(T, H, I, hot):
 
 
 @pytest.mark.parametrize("T,H,I,hot", [(600, 512, 512, None), (700, 512, 256, (4, 5, 6, 200)),
-                                       (256, 256, 768, None)])
+                                       (640, 1024, 256, (3, 250)), (256, 256, 768, None)])
 def test_experts_cta_pair_path(T, H, I, hot):
     """Shapes that take the two-CTA (M=256 pair MMA) grouped GEMMs: BF16
-    weights, 256-route chunks, H and I multiples of 256."""
+    weights, 256-route chunks, H a multiple of 512 and I of 256 (the last
+    shape checks the one-CTA fallback)."""
     wl = inputs.workload("tiny", T=T, H=H, I=I, x_dtype="bf16", w_dtype="bf16", seed=3 + T)
     dg, _ = _gpu_inputs(wl, cpu_gen=True)
     ids, w = seeded_routing(T, seed=T + 2, hot=hot)

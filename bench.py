@@ -195,7 +195,8 @@ def measure(wl, steps, warmup, dev, world, sampler_index):
         raise RuntimeError(f"device status {code} at {where} in the timed region")
     ids_h = ids.cpu()
     touched = int(torch.unique(ids_h).numel())
-    launches = sum(moe.beam_moe_stage_kernel_count(sh, i) for i in range(len(STAGES)))
+    xdt = moe.BEAM_BF16 if d["x"].dtype == torch.bfloat16 else moe.BEAM_F32
+    launches = sum(moe.beam_moe_stage_kernel_count(sh, i, xdt) for i in range(len(STAGES)))
     out = dict(total_ms=total_ms, stage_ms=stage_ms, touched=touched, launches_per_step=launches,
                clocks=clk.summary(), counts=torch.bincount(ids_h.reshape(-1).long(), minlength=256))
     return out, (d, sh, ws, y, ids, w, call)

@@ -94,7 +94,7 @@ def load():
     lib.beam_moe_read_device_status.argtypes = [vp, ctypes.POINTER(u32), vp]
     lib.beam_moe_route_noalloc.argtypes = [sp, vp, i32, vp, vp, vp, vp, vp]
     lib.beam_moe_route_noalloc.restype = i32
-    lib.beam_moe_stage_kernel_count.argtypes = [sp, i32]
+    lib.beam_moe_stage_kernel_count.argtypes = [sp, i32, i32]
     lib.beam_moe_stage_kernel_count.restype = ctypes.c_int32
     lib.beam_moe_debug_timeout.argtypes = [vp, sz, u32, vp]
     lib.beam_status_string.argtypes = [i32]
@@ -263,9 +263,9 @@ def beam_moe_forward_stage(sh, stage: int, x, router_w, router_bias, weights: di
     ForwardCall(sh, x, router_w, router_bias, weights, y, topk_ids, topk_w, workspace, stream).stage(stage)
 
 
-def beam_moe_stage_kernel_count(sh, stage: int) -> int:
+def beam_moe_stage_kernel_count(sh, stage: int, xdtype=BEAM_BF16) -> int:
     """Kernels the library launches for stage ``stage`` of a forward of ``sh``."""
-    n = int(load().beam_moe_stage_kernel_count(ctypes.byref(sh), int(stage)))
+    n = int(load().beam_moe_stage_kernel_count(ctypes.byref(sh), int(xdtype), int(stage)))
     if n < 0:
         raise BeamError(BEAM_ERR_UNSUPPORTED, "beam_moe_stage_kernel_count")
     return n

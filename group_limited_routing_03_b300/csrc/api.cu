@@ -96,7 +96,7 @@ bool make_u8_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t ro
 
 // ------------------------------------------------------------------ layout
 struct Layout {
-  size_t status, sched, counts, offsets, chunk_prefix, tile_hist, part, perm, pos, xp, h, yr, total;
+  size_t status, sched, counts, offsets, chunk_prefix, tile_hist, part, wsplit, perm, pos, xp, h, yr, total;
   int n_tiles, split_cap;
 };
 
@@ -123,6 +123,7 @@ void make_layout(const beam_moe_shape_t& s, Layout& L) {
   L.chunk_prefix = take((kExperts + 1) * 4);
   L.tile_hist = take(static_cast<size_t>(kExperts) * L.n_tiles * 4);
   L.part = take(L.split_cap > 1 ? static_cast<size_t>(L.split_cap) * T * kExperts * 4 : 0);
+  L.wsplit = take(s.T >= kRouterTcMinTokens ? 3 * static_cast<size_t>(kExperts) * H * 2 : 0);
   L.perm = take(R * 4);
   L.pos = take(R * 4);
   L.xp = take(R_pad * H * 2);
@@ -182,6 +183,13 @@ T* at(void* ws, size_t off) {
 beam_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? BEAM_OK : BEAM_ERR_CUDA; }
 
 // ------------------------------------------------------------------ stages
+// Large batches of BF16 tokens route on the tensor cores (three-term BF16
+// split of the FP32 router weight); small batches and FP32 x on CUDA cores.
+bool use_router_tc(const beam_moe_shape_t& s, bool x_bf16, const DeviceInfo& d) {
+  return x_bf16 && s.T >= kRouterTcMinTokens && d.cc_major >= 10 &&
+         router_tc_smem_bytes() <= static_cast<size_t>(d.smem_optin);
+}
+
 beam_status_t run_route(const beam_moe_shape_t& s, const void* x, bool x_bf16, const float* wr, const float* bias,
                         int32_t* ids, float* w, void* ws, const Layout& L, const DeviceInfo& d,
                         cudaStream_t stream) {
@@ -200,6 +208,15 @@ beam_status_t run_route(const beam_moe_shape_t& s, const void* x, bool x_bf16, c
   p.ids = ids;
   p.w = w;
   p.tile_hist = at<int32_t>(ws, L.tile_hist);
+  if (use_router_tc(s, x_bf16, d)) {
+    CUtensorMap tm_x, tm_w;
+    __nv_bfloat16* wsplit = at<__nv_bfloat16>(ws, L.wsplit);
+    if (!make_bf16_map(&tm_x, x, static_cast<uint64_t>(s.H), static_cast<uint64_t>(s.T), 128) ||
+        !make_bf16_map(&tm_w, wsplit, static_cast<uint64_t>(s.H), 3ull * kExperts, kExperts))
+      return BEAM_ERR_CUDA;
+    return cuda_status(
+        launch_router_tc(tm_x, tm_w, p, wsplit, at<uint32_t>(ws, L.status), kDefaultTimeoutNs, d.sms, stream));
+  }
   return cuda_status(launch_router(p, x_bf16, stream));
 }
 
@@ -502,12 +519,13 @@ beam_status_t beam_moe_forward_stage(const beam_moe_shape_t* shape, const beam_m
   return run_stage(*shape, *args, stage, workspace, L, d, static_cast<cudaStream_t>(stream));
 }
 
-int32_t beam_moe_stage_kernel_count(const beam_moe_shape_t* shape, beam_stage_t stage) {
+int32_t beam_moe_stage_kernel_count(const beam_moe_shape_t* shape, beam_dtype_t xdtype, beam_stage_t stage) {
   if (check_shape(shape) != BEAM_OK) return -1;
   DeviceInfo d;
   if (!device_info(d)) return -1;
   switch (stage) {
     case BEAM_STAGE_ROUTE: {
+      if (use_router_tc(*shape, xdtype == BEAM_BF16, d)) return 2;  // weight split + logits/selection
       Layout L;
       make_layout(*shape, L);
       int sp = router_splits(shape->T, shape->H, d.sms);

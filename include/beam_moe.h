@@ -177,10 +177,11 @@ beam_status_t beam_moe_forward_stage(const beam_moe_shape_t* shape, const beam_m
                                      beam_stage_t stage, void* workspace, size_t workspace_bytes,
                                      void* stream);
 
-/* Number of kernels stage `stage` launches for `shape` on the current device
- * (the router launches a second kernel when it splits the hidden dimension
- * across CTAs); -1 on an unsupported shape or stage. */
-int32_t beam_moe_stage_kernel_count(const beam_moe_shape_t* shape, beam_stage_t stage);
+/* Number of kernels stage `stage` launches for `shape` and activations of
+ * type `xdtype` on the current device (the router launches a second kernel
+ * when it splits the hidden dimension across CTAs, or to split the router
+ * weight for its tensor-core path); -1 on an unsupported shape or stage. */
+int32_t beam_moe_stage_kernel_count(const beam_moe_shape_t* shape, beam_dtype_t xdtype, beam_stage_t stage);
 
 /* Synchronises `stream`, returns the device status word of `workspace`
  * (BEAM_OK when no kernel reported a problem) and clears it.  `where`

@@ -86,6 +86,28 @@ def test_forward_nvfp4_small_all_tokens(T, H, I):
     assert err <= Y_TOL["nvfp4"], err
 
 
+@pytest.mark.parametrize("name,T,H", [("prefill", 600, 1024), ("skew", 1536, 5120), ("prefill", 513, 256)])
+def test_route_tensor_core_path(name, T, H):
+    """T >= 512 BF16 tokens route on the tensor cores (three-term BF16 split
+    of the FP32 router weight, FP32 accumulation); same parity rules."""
+    wl = inputs.workload(name, T=T, H=H, seed=40 + T)
+    d = inputs.generate(wl, DEV, experts=False)
+    sh = moe.shape(T, H, 128)
+    ws = moe.alloc_workspace(sh)
+    ids = torch.empty((T, 8), dtype=torch.int32, device=DEV)
+    w = torch.empty((T, 8), dtype=torch.float32, device=DEV)
+    moe.beam_moe_route(sh, d["x"], d["router_w"], d.get("bias"), ids, w, ws)
+    assert moe.beam_moe_read_device_status(ws)[0] == 0
+    ref = oracle_route(d)
+    bias = None if d.get("bias") is None else d["bias"].cpu().numpy()
+    compare_routing(ids.cpu().numpy(), w.cpu().numpy(), ref, bias=bias)
+    # dispatch histograms written by the router agree with the ids
+    moe.beam_moe_dispatch(sh, ids, ws)
+    lay = moe.workspace_layout(sh)
+    counts = ws[lay["counts"]:lay["counts"] + 1024].view(torch.int32).cpu().numpy()
+    np.testing.assert_array_equal(counts, np.bincount(ids.cpu().numpy().reshape(-1), minlength=256))
+
+
 def test_zero_input_exact():
     wl = inputs.workload("tiny", T=40, x_dtype="bf16")
     dg, _ = _gpu_inputs(wl, cpu_gen=True)

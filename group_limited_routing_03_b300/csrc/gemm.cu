@@ -451,34 +451,38 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
       const float s1 = (kMode == 0 && p.gs1 != nullptr) ? __ldg(&p.gs1[U.e]) : 1.0f;
       const int ncols = (U.n + 15) & ~15;
       __nv_bfloat16* out = p.out + static_cast<size_t>(U.start) * p.out_ld + feat;
-      for (int c0 = 16 * half; c0 < ncols; c0 += 32) {
-        float g[16];
-        tmem_ld16(tbase + static_cast<uint32_t>(c0), g);
-        if (kMode == 0) {
-          float up[16];
-          tmem_ld16(tbase + static_cast<uint32_t>(p.nmax + c0), up);
-          tmem_ld_wait();
+      // 1) TMEM -> packed BF16 results in registers (this warp's 16-column
+      //    chunks), 2) release the accumulator so the next unit's MMAs start,
+      //    3) global stores.
+      constexpr int kMaxChunks = 8;                                 // 256 columns / (2 x 16)
+      constexpr int kOut = (kMode == 1 && kNumA == 2) ? 2 : 1;      // pair down: two 256-row halves
+      uint32_t hp[kOut][kMaxChunks][8];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            if (c0 + j < U.n) {
-              const float a = g[j] * s0;
-              const float b = up[j] * s1;
-              // SiLU(gate) * up in FP32 (fast exp / divide: the result is
-              // rounded to BF16 right after, far coarser than their error)
-              const float hval = __fdividef(a, 1.0f + __expf(-a)) * b;
-              out[static_cast<size_t>(c0 + j) * p.out_ld] = __float2bfloat16_rn(hval);
-            }
-          }
-        } else {
-          float g2[16];
+      for (int ci = 0; ci < kMaxChunks; ++ci) {
+        const int c0 = 16 * half + 32 * ci;
+        if (c0 < ncols) {
+          float g[16], g2[16];
+          tmem_ld16(tbase + static_cast<uint32_t>(c0), g);
           if (kNumA == 2) tmem_ld16(tbase + static_cast<uint32_t>(p.nmax + c0), g2);
           tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            if (c0 + j < U.n) {
-              out[static_cast<size_t>(c0 + j) * p.out_ld] = __float2bfloat16_rn(g[j] * s0);
-              // second half of a pair down unit: features + 256
-              if (kNumA == 2) out[static_cast<size_t>(c0 + j) * p.out_ld + 2 * kBlockM] = __float2bfloat16_rn(g2[j]);
+          for (int j = 0; j < 8; ++j) {
+            float v0, v1;
+            if (kMode == 0) {
+              // SiLU(gate) * up in FP32 (fast exp / divide: the result is
+              // rounded to BF16 right after, far coarser than their error)
+              const float a0 = g[2 * j] * s0, a1 = g[2 * j + 1] * s0;
+              v0 = __fdividef(a0, 1.0f + __expf(-a0)) * (g2[2 * j] * s1);
+              v1 = __fdividef(a1, 1.0f + __expf(-a1)) * (g2[2 * j + 1] * s1);
+            } else {
+              v0 = g[2 * j] * s0;
+              v1 = g[2 * j + 1] * s0;
+            }
+            __nv_bfloat162 q = __floats2bfloat162_rn(v0, v1);
+            hp[0][ci][j] = *reinterpret_cast<uint32_t*>(&q);
+            if (kOut == 2) {
+              __nv_bfloat162 q2 = __floats2bfloat162_rn(g2[2 * j], g2[2 * j + 1]);
+              hp[kOut - 1][ci][j] = *reinterpret_cast<uint32_t*>(&q2);
             }
           }
         }
@@ -490,6 +494,25 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
           mbar_arrive_cluster(mapa_shared(&acc_empty[acc], 0));
         else
           mbar_arrive(&acc_empty[acc]);
+      }
+#pragma unroll
+      for (int ci = 0; ci < kMaxChunks; ++ci) {
+        const int c0 = 16 * half + 32 * ci;
+        if (c0 < ncols) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            if (c0 + j < U.n) {
+              const uint32_t w0 = hp[0][ci][j >> 1];
+              const uint16_t b0 = static_cast<uint16_t>((j & 1) ? (w0 >> 16) : (w0 & 0xFFFFu));
+              *reinterpret_cast<uint16_t*>(out + static_cast<size_t>(c0 + j) * p.out_ld) = b0;
+              if (kOut == 2) {
+                const uint32_t w1 = hp[kOut - 1][ci][j >> 1];
+                const uint16_t b1 = static_cast<uint16_t>((j & 1) ? (w1 >> 16) : (w1 & 0xFFFFu));
+                *reinterpret_cast<uint16_t*>(out + static_cast<size_t>(c0 + j) * p.out_ld + 2 * kBlockM) = b1;
+              }
+            }
+          }
+        }
       }
       if (++acc == p.acc_stages) {
         acc = 0;

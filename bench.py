@@ -375,13 +375,20 @@ def barrier(world):
 
 
 def max_over_ranks(v, world):
+    """The slowest replica's time: the whole job finishes when it does."""
     if world == 1:
         return v
     import torch.distributed as dist
 
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_throughput(tokens_per_replica_step, steps, world, max_ms):
+    """Whole-job tokens/s: every replica processes its own batch each step."""
+    return tokens_per_replica_step * steps * world / (max_ms * 1e-3)
 
 
 def main():
@@ -419,7 +426,7 @@ def main():
     m, state = measure(wl, args.steps, args.warmup, dev, world, torch.cuda.current_device())
     total_ms = max_over_ranks(m["total_ms"], world)
     sn = step_numbers(wl, m, args.steps)
-    value = wl.T * args.steps * world / (total_ms * 1e-3)
+    value = job_throughput(wl.T, args.steps, world, total_ms)
     hbm, tc = roofline(wl, m, pk)
 
     e2e = None

@@ -234,9 +234,12 @@ beam_status_t run_dispatch(const beam_moe_shape_t& s, const int32_t* ids, void* 
   return cuda_status(e);
 }
 
-int chunk_rows(int T) {
+// Routes per GEMM unit: all of an expert's routes up to a cap (BF16 256, the
+// widest MMA; NVFP4 160, so that TMEM also holds three BF16 weight tiles).
+int chunk_rows(int T, bool fp4) {
+  const int cap = fp4 ? kChunkRowsFp4 : kChunkRowsBf16;
   int n = ((T + kBoxRows - 1) / kBoxRows) * kBoxRows;
-  return n > 256 ? 256 : n;
+  return n > cap ? cap : n;
 }
 
 uint32_t pow2_at_least(uint32_t v) {
@@ -257,12 +260,12 @@ beam_status_t run_gemm(int mode, const beam_moe_shape_t& s, const beam_expert_we
                        const Layout& L, const DeviceInfo& d, cudaStream_t stream) {
   const int R = s.T * kTopK;
   const uint64_t R_pad = static_cast<uint64_t>((R + kBoxRows - 1) / kBoxRows * kBoxRows);
-  const int nmax = chunk_rows(s.T);
+  const bool fp4 = wts->dtype == BEAM_NVFP4;
+  const int nmax = chunk_rows(s.T, fp4);
   __nv_bfloat16* xp = at<__nv_bfloat16>(ws, L.xp);
   __nv_bfloat16* h = at<__nv_bfloat16>(ws, L.h);
   __nv_bfloat16* yr = at<__nv_bfloat16>(ws, L.yr);
   const uint64_t E = kExperts, H = s.H, I = s.I;
-  const bool fp4 = wts->dtype == BEAM_NVFP4;
   GemmMaps maps;
   std::memset(&maps, 0, sizeof(maps));
   bool ok;
@@ -280,7 +283,7 @@ beam_status_t run_gemm(int mode, const beam_moe_shape_t& s, const beam_expert_we
     ok = make_bf16_map(&maps.b, h, I, R_pad, kBoxRows);
     if (fp4)
       ok = ok && make_u8_map(&maps.a0, wts->down, I / 2, E * H, kBlockK / 2, kBlockM) &&
-           make_u8_map(&maps.s0, wts->down_sf, I / 16, E * H, kScaleBoxCols, kBlockM);
+           make_u8_map(&maps.s0, wts->down_sf, I / 16, E * H, kScaleBoxCols, kBlockM);  // a1 / s1 = a0 / s0
     else
       ok = ok && make_bf16_map(&maps.a0, wts->down, I, E * H, kBlockM);
     maps.a1 = maps.a0;
@@ -291,7 +294,8 @@ beam_status_t run_gemm(int mode, const beam_moe_shape_t& s, const beam_expert_we
   // memory operand traffic; used for BF16 weights when chunks reach 256 routes.
   bool pair = !fp4 && nmax == 256 && s.H % 512 == 0 && s.I % 256 == 0 && d.sms >= 2;
   // pair units: gate/up 256 features (gate and up tiles), down 512 features
-  const int rows_per_unit = pair ? (mode == 0 ? 2 * kBlockM : 4 * kBlockM) : kBlockM;
+  // NVFP4 down units: 256 features (two weight tiles, two accumulators)
+  const int rows_per_unit = pair ? (mode == 0 ? 2 * kBlockM : 4 * kBlockM) : (fp4 && mode == 1 ? 2 * kBlockM : kBlockM);
   GemmParams p;
   p.counts = at<int32_t>(ws, L.counts);
   p.offsets = at<int32_t>(ws, L.offsets);
@@ -301,17 +305,35 @@ beam_status_t run_gemm(int mode, const beam_moe_shape_t& s, const beam_expert_we
   p.k_blocks = (mode == 0 ? s.H : s.I) / kBlockK;
   p.nmax = nmax;
   const size_t budget = static_cast<size_t>(d.smem_optin) - 1024 - 512;
-  const size_t sb = gemm_stage_bytes((mode == 0 || pair) ? 2 : 1, fp4, pair ? nmax / 2 : nmax);
+  const int num_a = (mode == 0 || pair || fp4) ? 2 : 1;  // weight tiles per stage
+  const size_t sb = gemm_stage_bytes(num_a, fp4, pair ? nmax / 2 : nmax);
   int stages = static_cast<int>(budget / sb);
   if (stages > 8) stages = 8;
   if (stages < 2) return BEAM_ERR_UNSUPPORTED;
   p.stages = stages;
-  p.acc_cols = static_cast<uint32_t>((mode == 0 || pair) ? 2 * nmax : nmax);
+  p.acc_cols = static_cast<uint32_t>(num_a * nmax);
   int acc_stages = static_cast<int>(512 / p.acc_cols);
   if (acc_stages > 4) acc_stages = 4;
   if (acc_stages < 1) acc_stages = 1;
   p.acc_stages = acc_stages;
   p.tmem_cols = pow2_at_least(static_cast<uint32_t>(acc_stages) * p.acc_cols);
+  p.a_stages = 0;
+  p.a_col0 = 0;
+  if (fp4) {
+    // TMEM (512 columns): the accumulator buffer(s), then a ring of BF16
+    // weight tiles (32 columns per 128x64 tile) with room for at least three
+    const uint32_t a_cols = static_cast<uint32_t>(num_a * (kBlockK / 2));
+    acc_stages = static_cast<int>((512 - 3 * a_cols) / p.acc_cols);
+    if (acc_stages > 2) acc_stages = 2;
+    if (acc_stages < 1) return BEAM_ERR_UNSUPPORTED;
+    p.acc_stages = acc_stages;
+    p.a_col0 = static_cast<uint32_t>(acc_stages) * p.acc_cols;
+    p.a_stages = static_cast<int>((512 - p.a_col0) / a_cols);
+    if (p.a_stages > kMaxAStages) p.a_stages = kMaxAStages;
+    if (p.a_stages > p.stages) p.a_stages = p.stages;  // a tile is freed through the smem ring's empty barriers
+    if (p.a_stages < 2) return BEAM_ERR_UNSUPPORTED;   // the converter groups alternate
+    p.tmem_cols = 512;
+  }
   p.sched = at<int>(ws, L.sched) + mode;
   p.out = mode == 0 ? h : yr;
   p.out_ld = mode == 0 ? s.I : s.H;
@@ -360,7 +382,7 @@ beam_status_t run_combine(const beam_moe_shape_t& s, const float* w, void* y, bo
 beam_status_t run_experts(const beam_moe_shape_t& s, const void* x, bool x_bf16, const beam_expert_weights_t* wts,
                           const int32_t* ids, const float* w, void* y, void* ws, const Layout& L,
                           const DeviceInfo& d, bool hist_ready, cudaStream_t stream) {
-  beam_status_t st = run_dispatch(s, ids, ws, L, chunk_rows(s.T), hist_ready, stream);
+  beam_status_t st = run_dispatch(s, ids, ws, L, chunk_rows(s.T, wts->dtype == BEAM_NVFP4), hist_ready, stream);
   if (st == BEAM_OK) st = run_gather(s, x, x_bf16, ws, L, d, stream);
   if (st == BEAM_OK) st = run_gemm(0, s, wts, ws, L, d, stream);
   if (st == BEAM_OK) st = run_gemm(1, s, wts, ws, L, d, stream);
@@ -394,7 +416,7 @@ beam_status_t run_stage(const beam_moe_shape_t& s, const beam_moe_args_t& a, int
     case BEAM_STAGE_ROUTE:
       return run_route(s, a.x, xb, a.router_w, a.router_bias, a.topk_ids, a.topk_w, ws, L, d, cs);
     case BEAM_STAGE_DISPATCH:
-      return run_dispatch(s, a.topk_ids, ws, L, chunk_rows(s.T), true, cs);
+      return run_dispatch(s, a.topk_ids, ws, L, chunk_rows(s.T, a.weights->dtype == BEAM_NVFP4), true, cs);
     case BEAM_STAGE_GATHER:
       return run_gather(s, a.x, xb, ws, L, d, cs);
     case BEAM_STAGE_GATE_UP:
@@ -470,7 +492,7 @@ beam_status_t beam_moe_dispatch(const beam_moe_shape_t* shape, const int32_t* to
   if (st != BEAM_OK) return st;
   DeviceInfo d;
   if (!device_info(d)) return BEAM_ERR_CUDA;
-  return run_dispatch(*shape, topk_ids, workspace, L, chunk_rows(shape->T), false, static_cast<cudaStream_t>(stream));
+  return run_dispatch(*shape, topk_ids, workspace, L, chunk_rows(shape->T, false), false, static_cast<cudaStream_t>(stream));
 }
 
 beam_status_t beam_moe_experts(const beam_moe_shape_t* shape, const void* x, beam_dtype_t xdtype,

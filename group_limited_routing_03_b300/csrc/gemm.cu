@@ -32,10 +32,19 @@
 //                chunks, warps 6-9 the odd ones), NVFP4 global scale, SwiGLU
 //                in FP32 (mode 0), BF16 stores;
 //   warps 10-17  (NVFP4 only) converters: packed E2M1 x E4M3 -> BF16 weight
-//                tile in the 128-byte-swizzled layout the MMA reads.
-// Shared-memory stages are recycled through full/empty mbarriers (plus
-// conv for NVFP4), TMEM accumulator buffers through acc_full/acc_empty.
-// Every wait is bounded.
+//                tile, written straight into TMEM (tcgen05.st; the thread of
+//                TMEM lane m expands weight row m), where the MMA reads its A
+//                operand.  Shared memory then carries only the packed bytes
+//                and the activations, and its bandwidth stays with the MMA's
+//                B operand.
+// Shared-memory stages are recycled through full/empty mbarriers, TMEM
+// accumulator buffers through acc_full/acc_empty.  NVFP4: the converters wait
+// for the TMA bytes of a stage before expanding its weights, and the MMA
+// thread waits only for the converters (afull), whose arrival follows their
+// observation of the TMA completion; a TMEM weight tile is reused once the
+// empty barrier of the k-block that last read it has completed.  One wait and
+// one commit per k-block keep the single MMA-issuing thread ahead of the
+// tensor pipe.  Every wait is bounded.
 #include <cuda.h>
 #include <cuda_bf16.h>
 
@@ -89,68 +98,44 @@ __device__ __forceinline__ Unit unit_at(const GemmParams& p, int u) {
 // an E4M3 scale at most 4, so their product fits BF16's 8 bits, and every
 // such product (>= 2^-10, <= 2688) is a normal BF16 number.
 // ---------------------------------------------------------------------------
-// E4M3 (sign, 4 exponent bits with bias 7, 3 mantissa bits) to BF16 bits.
-__device__ __forceinline__ uint32_t e4m3_to_bf16_bits(uint32_t code) {
-  const uint32_t sign = (code & 0x80u) << 8;
-  const uint32_t ex = (code >> 3) & 0xFu;
-  const uint32_t man = code & 7u;
-  if (ex != 0) return sign | ((ex + 120u) << 7) | (man << 4);
-  if (man == 0) return sign;
-  // subnormal: man * 2^-9, renormalised
-  const float f = static_cast<float>(man) * 0.001953125f;
-  return sign | (__float_as_uint(f) >> 16);
+// E4M3 code (low 8 bits) -> BF16 bits in both halves.  The 7 magnitude bits
+// placed at FP32 bits 20..26 read as the E4M3 value times 2^-120 (E4M3
+// subnormals become FP32 subnormals), and the product with 2^120 is exact.
+__device__ __forceinline__ uint32_t e4m3_to_bf16x2(uint32_t code) {
+  const float f = __fmul_rn(__uint_as_float((code & 0x7Fu) << 20), 0x1p120f);
+  const uint32_t b = (__float_as_uint(f) >> 16) | ((code & 0x80u) << 8);
+  return b | (b << 16);
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+  return r;
 }
 
 // Eight E2M1 codes (one 32-bit word, element i in bits 4i..4i+3) times a
-// BF16 scale -> four BF16x2 words (element 2j in the low half of word j).
-// Magnitudes come from two byte-permute lookups (high and low byte of the
-// BF16 pattern of 0, .5, 1, 1.5, 2, 3, 4, 6), signs are moved to bits 15/31.
-__device__ __forceinline__ uint4 e2m1x8_to_bf16(uint32_t w, __nv_bfloat162 scale2) {
+// BF16 scale pair -> four BF16x2 words (element 2j in the low half of word
+// j).  Magnitudes come from byte-permute lookups into the high and low bytes
+// of the BF16 patterns of 0, .5, 1, 1.5, 2, 3, 4, 6; the signs are moved to
+// bit 7 of the high bytes by one more permute per four elements; a final
+// permute interleaves low and high bytes.  No branches.
+__device__ __forceinline__ void e2m1x8_to_bf16(uint32_t w, uint32_t scale2, uint32_t* o) {
   constexpr uint32_t kHi0 = 0x3F3F3F00u, kHi1 = 0x40404040u;  // high bytes of codes 0..7
   constexpr uint32_t kLo0 = 0xC0800000u, kLo1 = 0xC0804000u;  // low bytes of codes 0..7
-  const uint32_t sel_a = w & 0x7777u;           // magnitudes of elements 0..3
-  const uint32_t sel_b = (w >> 16) & 0x7777u;   // magnitudes of elements 4..7
-  uint32_t ha, la, hb, lb;
-  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(ha) : "r"(kHi0), "r"(kHi1), "r"(sel_a));
-  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(la) : "r"(kLo0), "r"(kLo1), "r"(sel_a));
-  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(hb) : "r"(kHi0), "r"(kHi1), "r"(sel_b));
-  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(lb) : "r"(kLo0), "r"(kLo1), "r"(sel_b));
-  uint32_t q[4];
-  asm("prmt.b32 %0, %1, %2, 0x5140;" : "=r"(q[0]) : "r"(la), "r"(ha));  // elements 0, 1
-  asm("prmt.b32 %0, %1, %2, 0x7362;" : "=r"(q[1]) : "r"(la), "r"(ha));  // elements 2, 3
-  asm("prmt.b32 %0, %1, %2, 0x5140;" : "=r"(q[2]) : "r"(lb), "r"(hb));  // elements 4, 5
-  asm("prmt.b32 %0, %1, %2, 0x7362;" : "=r"(q[3]) : "r"(lb), "r"(hb));  // elements 6, 7
-  // sign of element i is bit 4i+3 of w
-  q[0] |= ((w << 12) & 0x00008000u) | ((w << 24) & 0x80000000u);
-  q[1] |= ((w << 4) & 0x00008000u) | ((w << 16) & 0x80000000u);
-  q[2] |= ((w >> 4) & 0x00008000u) | ((w << 8) & 0x80000000u);
-  q[3] |= ((w >> 12) & 0x00008000u) | (w & 0x80000000u);
-  uint4 out;
-  uint32_t* o = reinterpret_cast<uint32_t*>(&out);
+  const uint32_t m = w & 0x77777777u;      // magnitude codes (a selector uses its low 16 bits)
+  const uint32_t mb = __umulhi(m, 0x10000u);  // m >> 16, on the multiply pipe
+  const uint32_t w4 = w * 16u;                // w << 4, on the multiply pipe
+  // bit 7 of byte i = sign of element i: (w4.b0, w.b0, w4.b1, w.b1), then bytes 2, 3
+  const uint32_t ha = prmt(kHi0, kHi1, m) | (prmt(w, w4, 0x1504u) & 0x80808080u);
+  const uint32_t hb = prmt(kHi0, kHi1, mb) | (prmt(w, w4, 0x3726u) & 0x80808080u);
+  const uint32_t la = prmt(kLo0, kLo1, m), lb = prmt(kLo0, kLo1, mb);
+  uint32_t q[4] = {prmt(la, ha, 0x5140u), prmt(la, ha, 0x7362u), prmt(lb, hb, 0x5140u), prmt(lb, hb, 0x7362u)};
+  const __nv_bfloat162 s2 = *reinterpret_cast<const __nv_bfloat162*>(&scale2);
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&q[j]);
-    v = __hmul2(v, scale2);  // exact: at most 6 significant bits
+    v = __hmul2(v, s2);  // exact: at most 6 significant bits
     o[j] = *reinterpret_cast<uint32_t*>(&v);
-  }
-  return out;
-}
-
-// One converter thread: `nchunk` 16-byte output chunks (8 K elements each,
-// starting at chunk c0) of weight row `row`, from the packed tile (32 bytes
-// per row) and the scale tile (16 bytes per row; this k-block's 4 scales at
-// byte 4*(kb%4)), into the 128-byte-swizzled BF16 tile.
-__device__ __forceinline__ void convert_row(const uint8_t* packed, const uint8_t* scales, uint8_t* dst, int row,
-                                            int kb, int c0, int nchunk) {
-  const uint32_t sc4 = *reinterpret_cast<const uint32_t*>(scales + row * kScaleBoxCols + 4 * (kb & 3));
-  const uint32_t* src = reinterpret_cast<const uint32_t*>(packed + row * (kBlockK / 2));
-  uint8_t* drow = dst + row * 128;
-  for (int c = c0; c < c0 + nchunk; ++c) {
-    const uint32_t sbits = e4m3_to_bf16_bits((sc4 >> (8 * (c >> 1))) & 0xFFu);  // 16 elements per scale
-    const uint32_t s2bits = sbits | (sbits << 16);
-    const __nv_bfloat162 s2 = *reinterpret_cast<const __nv_bfloat162*>(&s2bits);
-    const uint4 v = e2m1x8_to_bf16(src[c], s2);
-    *reinterpret_cast<uint4*>(drow + ((c ^ (row & 7)) << 4)) = v;
   }
 }
 
@@ -164,9 +149,13 @@ template <int kMode, bool kFp4, bool kPair>
 __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
     moe_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
   // Weight tiles per stage: gate/up always two (gate, up); down two on CTA
-  // pairs (two 256-row halves of a 512-row unit sharing the token tile).
-  constexpr int kNumA = (kMode == 0 || kPair) ? 2 : 1;
-  constexpr int kRowsPerUnit = kPair ? (kMode == 0 ? 2 * kBlockM : 4 * kBlockM) : kBlockM;
+  // pairs (two 256-row halves of a 512-row unit sharing the token tile) and
+  // for NVFP4 (two 128-row halves of a 256-row unit), so that every k-block
+  // carries two accumulators' worth of MMAs.
+  constexpr int kNumA = (kMode == 0 || kPair || kFp4) ? 2 : 1;
+  constexpr int kRowsPerUnit = kPair ? (kMode == 0 ? 2 * kBlockM : 4 * kBlockM) : (kNumA == 2 && kMode == 1 ? 2 * kBlockM : kBlockM);
+  // down with two tiles: feature offset of the second tile's rows
+  constexpr int kHalfRows = kPair ? 2 * kBlockM : kBlockM;
   static_assert(!(kPair && kFp4), "pair MMA path is BF16 only");
   // Roles that read every scheduled unit index (they release ring slots).
   constexpr uint32_t kRingConsumers =
@@ -179,8 +168,8 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(p.stages) * stage_bytes);
   uint64_t* full = bars;
   uint64_t* empty = full + p.stages;
-  uint64_t* conv = empty + p.stages;  // NVFP4: BF16 weight tile ready
-  uint64_t* acc_full = conv + p.stages;
+  uint64_t* afull = empty + p.stages;        // NVFP4: BF16 weight tile written to TMEM
+  uint64_t* acc_full = afull + kMaxAStages;
   uint64_t* acc_empty = acc_full + p.acc_stages;
   uint64_t* drain = acc_empty + p.acc_stages;
   uint64_t* ufull = drain + 1;        // unit ring: index published
@@ -191,9 +180,11 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = kPair ? cluster_ctarank() : 0u;  // 0: the CTA that issues the MMAs
-  // Stage layout: [A bf16 x kNumA][B][packed x kNumA][scales x kNumA]
+  // Stage layout: BF16 weights [A x kNumA][B]; NVFP4 [B][packed x kNumA][scales x kNumA]
   auto a_tile = [&](int s, int which) { return smem + static_cast<size_t>(s) * stage_bytes + which * kATileBytes; };
-  auto b_tile = [&](int s) { return smem + static_cast<size_t>(s) * stage_bytes + kNumA * kATileBytes; };
+  auto b_tile = [&](int s) {
+    return smem + static_cast<size_t>(s) * stage_bytes + (kFp4 ? 0u : kNumA * kATileBytes);
+  };
   auto p_tile = [&](int s, int which) { return b_tile(s) + b_tile_bytes + which * kPackedTileBytes; };
   auto s_tile = [&](int s, int which) {
     return b_tile(s) + b_tile_bytes + kNumA * kPackedTileBytes + which * kScaleTileBytes;
@@ -203,8 +194,8 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
     for (int s = 0; s < p.stages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
-      mbar_init(&conv[s], kConvertWarps);
     }
+    for (int a = 0; a < kMaxAStages; ++a) mbar_init(&afull[a], kConvertWarps / 2);  // one converter group per k-block
     for (int a = 0; a < p.acc_stages; ++a) {
       mbar_init(&acc_full[a], 1);
       mbar_init(&acc_empty[a], kPair ? 2 * kEpilogueWarps : kEpilogueWarps);
@@ -333,12 +324,12 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
             mbar_arrive_expect_tx(&full[stage], bytes);
             if (kFp4) {
               const int sx = (kb >> 2) * static_cast<int>(kScaleBoxCols);
+              // gate/up: gate and up tiles of the same rows; down: rows a_row and a_row + 128
+              const int a_row1 = kMode == 0 ? a_row : a_row + kHalfRows;
               tma_load_2d_nohint(p_tile(stage, 0), &maps.a0, &full[stage], kx / 2, a_row);
               tma_load_2d_nohint(s_tile(stage, 0), &maps.s0, &full[stage], sx, a_row);
-              if (kMode == 0) {
-                tma_load_2d_nohint(p_tile(stage, 1), &maps.a1, &full[stage], kx / 2, a_row);
-                tma_load_2d_nohint(s_tile(stage, 1), &maps.s1, &full[stage], sx, a_row);
-              }
+              tma_load_2d_nohint(p_tile(stage, 1), &maps.a1, &full[stage], kx / 2, a_row1);
+              tma_load_2d_nohint(s_tile(stage, 1), &maps.s1, &full[stage], sx, a_row1);
             } else {
               tma_load_2d_nohint(a_tile(stage, 0), &maps.a0, &full[stage], kx, a_row);
               if (kMode == 0) tma_load_2d_nohint(a_tile(stage, 1), &maps.a1, &full[stage], kx, a_row);
@@ -365,8 +356,8 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && rank == 0) {
-      int stage = 0, acc = 0;
-      uint32_t phase = 0, acc_phase = 0;
+      int stage = 0, acc = 0, astage = 0;
+      uint32_t phase = 0, acc_phase = 0, aphase = 0;
       bool ok = true;
       while (ok) {
         int u;
@@ -380,35 +371,47 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
         const uint32_t d0 = tmem_base + static_cast<uint32_t>(acc) * p.acc_cols;
         const uint32_t d1 = d0 + static_cast<uint32_t>(p.nmax);
         for (int kb = 0; kb < p.k_blocks; ++kb) {
-          // BF16: the TMA bytes; NVFP4: the converters' BF16 tile (they waited
-          // for the TMA bytes of the same stage before writing it).
-          if (!mbar_wait(kFp4 ? &conv[stage] : &full[stage], phase, p.timeout_ns, abort_flag, p.status,
-                         kWhereMmaFull)) {
+          // BF16: the TMA bytes of the stage.  NVFP4: the converters' BF16
+          // tile in TMEM; they arrive after observing the stage's TMA bytes.
+          if (!mbar_wait(kFp4 ? &afull[astage] : &full[stage], kFp4 ? aphase : phase, p.timeout_ns, abort_flag,
+                         p.status, kWhereMmaFull)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint64_t da0 = sdesc_k_sw128(smem_u32(a_tile(stage, 0)));
-          const uint64_t da1 = sdesc_k_sw128(smem_u32(a_tile(stage, kNumA - 1)));
           const uint64_t db = sdesc_k_sw128(smem_u32(b_tile(stage)));
+          if (kFp4) {
+            const uint32_t ta = tmem_base + p.a_col0 + static_cast<uint32_t>(astage * kNumA * (kBlockK / 2));
 #pragma unroll
-          for (int k = 0; k < kBlockK / 16; ++k) {
-            const uint32_t accumulate = (kb | k) != 0 ? 1u : 0u;
-            if (kPair) {
-              mma_bf16_pair(d0, da0 + 2u * k, db + 2u * k, idesc, accumulate);
-              mma_bf16_pair(d1, da1 + 2u * k, db + 2u * k, idesc, accumulate);
-            } else {
-              mma_bf16(d0, da0 + 2u * k, db + 2u * k, idesc, accumulate);
-              if (kMode == 0) mma_bf16(d1, da1 + 2u * k, db + 2u * k, idesc, accumulate);
+            for (int k = 0; k < kBlockK / 16; ++k) {
+              const uint32_t accumulate = (kb | k) != 0 ? 1u : 0u;
+              mma_bf16_ts(d0, ta + 8u * k, db + 2u * k, idesc, accumulate);
+              mma_bf16_ts(d1, ta + kBlockK / 2 + 8u * k, db + 2u * k, idesc, accumulate);
+            }
+          } else {
+            const uint64_t da0 = sdesc_k_sw128(smem_u32(a_tile(stage, 0)));
+            const uint64_t da1 = sdesc_k_sw128(smem_u32(a_tile(stage, kNumA - 1)));
+#pragma unroll
+            for (int k = 0; k < kBlockK / 16; ++k) {
+              const uint32_t accumulate = (kb | k) != 0 ? 1u : 0u;
+              if (kPair) {
+                mma_bf16_pair(d0, da0 + 2u * k, db + 2u * k, idesc, accumulate);
+                mma_bf16_pair(d1, da1 + 2u * k, db + 2u * k, idesc, accumulate);
+              } else {
+                mma_bf16(d0, da0 + 2u * k, db + 2u * k, idesc, accumulate);
+                if (kMode == 0) mma_bf16(d1, da1 + 2u * k, db + 2u * k, idesc, accumulate);
+              }
             }
           }
           if (kPair)
             mma_commit_pair_multicast(&empty[stage], 0x3);
           else
             mma_commit(&empty[stage]);
-          if (++stage == p.stages) {
-            stage = 0;
-            phase ^= 1u;
+          stage = stage + 1 == p.stages ? 0 : stage + 1;
+          phase ^= stage == 0 ? 1u : 0u;
+          if (kFp4) {
+            astage = astage + 1 == p.a_stages ? 0 : astage + 1;
+            aphase ^= astage == 0 ? 1u : 0u;
           }
         }
         if (!ok) break;
@@ -454,8 +457,8 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
       // 1) TMEM -> packed BF16 results in registers (this warp's 16-column
       //    chunks), 2) release the accumulator so the next unit's MMAs start,
       //    3) global stores.
-      constexpr int kMaxChunks = 8;                                 // 256 columns / (2 x 16)
-      constexpr int kOut = (kMode == 1 && kNumA == 2) ? 2 : 1;      // pair down: two 256-row halves
+      constexpr int kMaxChunks = (kFp4 ? kChunkRowsFp4 : kChunkRowsBf16) / 32;  // columns / (2 x 16)
+      constexpr int kOut = (kMode == 1 && kNumA == 2) ? 2 : 1;      // down with two weight tiles
       uint32_t hp[kOut][kMaxChunks][8];
 #pragma unroll
       for (int ci = 0; ci < kMaxChunks; ++ci) {
@@ -481,7 +484,7 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
             __nv_bfloat162 q = __floats2bfloat162_rn(v0, v1);
             hp[0][ci][j] = *reinterpret_cast<uint32_t*>(&q);
             if (kOut == 2) {
-              __nv_bfloat162 q2 = __floats2bfloat162_rn(g2[2 * j], g2[2 * j + 1]);
+              __nv_bfloat162 q2 = __floats2bfloat162_rn(g2[2 * j] * s0, g2[2 * j + 1] * s0);
               hp[kOut - 1][ci][j] = *reinterpret_cast<uint32_t*>(&q2);
             }
           }
@@ -508,7 +511,7 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
               if (kOut == 2) {
                 const uint32_t w1 = hp[kOut - 1][ci][j >> 1];
                 const uint16_t b1 = static_cast<uint16_t>((j & 1) ? (w1 >> 16) : (w1 & 0xFFFFu));
-                *reinterpret_cast<uint16_t*>(out + static_cast<size_t>(c0 + j) * p.out_ld + 2 * kBlockM) = b1;
+                *reinterpret_cast<uint16_t*>(out + static_cast<size_t>(c0 + j) * p.out_ld + kHalfRows) = b1;
               }
             }
           }
@@ -521,36 +524,83 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
     }
   } else if (kFp4) {
     // ------------------------------------------------------------ converters
-    // mode 0: thread c converts row c%128 of matrix c/128 (gate / up), all 8
-    // chunks; mode 1: row c%128, chunks 4*(c/128)..+3.
-    const int c = threadIdx.x - 32 * (2 + kEpilogueWarps);
-    const int row = c & (kBlockM - 1);
-    const int which = kMode == 0 ? (c >> 7) : 0;
-    const int chunk0 = kMode == 0 ? 0 : 4 * (c >> 7);
-    const int nchunk = kMode == 0 ? 8 : 4;
-    int stage = 0;
+    // Warp w may write TMEM lanes 32*(w%4)..+31, so its lane i expands weight
+    // row 32*(w%4)+i.  Warps 10-13 take the even k-blocks (counted over all
+    // units), warps 14-17 the odd ones, so two k-blocks are expanded at once;
+    // a thread expands its row of every weight matrix of the unit (gate and
+    // up, or down): 64 K elements = 32 TMEM columns each.
+    const int cw = warp - (2 + kEpilogueWarps);
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const int group = cw >> 2;
+    const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+    // This group's k-blocks i = group, group+2, ...: smem stage / phase of i,
+    // TMEM tile of i, and smem stage / phase of i - a_stages (the k-block that
+    // last read that tile; its empty barrier completing frees the tile).  The
+    // host keeps 2 <= a_stages <= stages.
+    int stage = group, astage = group;
     uint32_t phase = 0;
+    int rstage = group - p.a_stages + p.stages;
+    uint32_t rphase = 1;
+    int i = group;
+    uint32_t parity = 0;                // k-blocks seen so far, modulo 2
     bool ok = true;
     while (ok) {
       int u;
       if (!warp_take(u) || u < 0) break;
       for (int kb = 0; kb < p.k_blocks; ++kb) {
+        const bool mine = parity == static_cast<uint32_t>(group);
+        parity ^= 1u;
+        if (!mine) continue;
         int good = 1;
         if (lane == 0)
-          good = mbar_wait(&full[stage], phase, p.timeout_ns, abort_flag, p.status, kWhereConvert) ? 1 : 0;
+          good = (mbar_wait(&full[stage], phase, p.timeout_ns, abort_flag, p.status, kWhereConvert) &&
+                  (i < p.a_stages ||
+                   mbar_wait(&empty[rstage], rphase, p.timeout_ns, abort_flag, p.status, kWhereConvert)))
+                     ? 1
+                     : 0;
         good = __shfl_sync(0xFFFFFFFFu, good, 0);
         if (!good) {
           ok = false;
           break;
         }
-        convert_row(p_tile(stage, which), s_tile(stage, which), a_tile(stage, which), row, kb, chunk0, nchunk);
-        fence_proxy_async_smem();  // generic-proxy writes -> visible to the tensor core
+        tc_fence_after();
+        const uint32_t ta0 = tmem_base + lane_addr + p.a_col0 + static_cast<uint32_t>(astage * kNumA * (kBlockK / 2));
+#pragma unroll
+        for (int mat = 0; mat < kNumA; ++mat) {
+          // packed row: 32 bytes (64 elements); scale row: this k-block's 4
+          // E4M3 codes at byte 4*(kb%4), one per 16 elements
+          const uint4* src = reinterpret_cast<const uint4*>(p_tile(stage, mat) + row * (kBlockK / 2));
+          const uint4 v0 = src[0], v1 = src[1];
+          const uint32_t wv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+          const uint32_t sc4 =
+              *reinterpret_cast<const uint32_t*>(s_tile(stage, mat) + row * kScaleBoxCols + 4 * (kb & 3));
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint32_t out[16];
+#pragma unroll
+            for (int g = 0; g < 2; ++g) {  // 16 elements per scale
+              const uint32_t s2 = e4m3_to_bf16x2((sc4 >> (8 * (2 * h + g))) & 0xFFu);
+              e2m1x8_to_bf16(wv[4 * h + 2 * g], s2, out + 8 * g);
+              e2m1x8_to_bf16(wv[4 * h + 2 * g + 1], s2, out + 8 * g + 4);
+            }
+            tmem_st16(ta0 + static_cast<uint32_t>(mat * (kBlockK / 2) + 16 * h), out);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&conv[stage]);
-        if (++stage == p.stages) {
-          stage = 0;
+        if (lane == 0) mbar_arrive(&afull[astage]);
+        if ((stage += 2) >= p.stages) {
+          stage -= p.stages;
           phase ^= 1u;
         }
+        if ((astage += 2) >= p.a_stages) astage -= p.a_stages;
+        if ((rstage += 2) >= p.stages) {
+          rstage -= p.stages;
+          rphase ^= 1u;
+        }
+        i += 2;
       }
     }
   }
@@ -598,8 +648,8 @@ cudaError_t launch_one(const GemmMaps& maps, const GemmParams& p, int grid, size
 }  // namespace
 
 size_t gemm_smem_bytes(int stages, int acc_stages, size_t stage_bytes) {
-  return 1024 + static_cast<size_t>(stages) * stage_bytes + (3 * stages + 2 * acc_stages + 1 + 2 * kSchedRing) * 8 +
-         kSchedRing * 4 + 16;
+  return 1024 + static_cast<size_t>(stages) * stage_bytes +
+         (2 * stages + 2 * kMaxAStages + 2 * acc_stages + 1 + 2 * kSchedRing) * 8 + kSchedRing * 4 + 16;
 }
 
 int gemm_pair_max_clusters(int mode, size_t smem_bytes) {

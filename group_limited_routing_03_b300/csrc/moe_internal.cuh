@@ -24,6 +24,9 @@ constexpr int kMaxSmsForSizing = 256;  // bound on the SM count used to size the
 constexpr uint32_t kPackedTileBytes = kBlockM * kBlockK / 2;  // NVFP4: 128 rows x 32 bytes
 constexpr uint32_t kScaleBoxCols = 16;                       // NVFP4: scale bytes per TMA box row (4 k-blocks)
 constexpr uint32_t kScaleTileBytes = kBlockM * kScaleBoxCols;  // NVFP4: 2 KiB
+constexpr int kMaxAStages = 8;     // NVFP4: BF16 weight tiles in TMEM in flight (at most)
+constexpr int kChunkRowsBf16 = 256;  // routes per GEMM unit (BF16 weights)
+constexpr int kChunkRowsFp4 = 160;   // NVFP4: TMEM holds the accumulators and the weight tiles
 
 // ---------------------------------------------------------------------------
 // Router
@@ -58,6 +61,8 @@ struct GemmParams {
   int acc_stages;               // TMEM accumulator buffers
   uint32_t acc_cols;            // TMEM columns per accumulator buffer
   uint32_t tmem_cols;           // TMEM columns allocated (power of two)
+  int a_stages;                 // NVFP4: BF16 weight tiles in TMEM (ring depth)
+  uint32_t a_col0;              // NVFP4: first TMEM column of that ring
   int* sched;                   // unit counter (zeroed before the launch)
   __nv_bfloat16* out;           // h [R, I] or yr [R, H], perm order
   int out_ld;                   // I or H
@@ -73,12 +78,13 @@ struct GemmMaps {
   CUtensorMap a0, a1, b, s0, s1;
 };
 
-// Bytes of one pipeline stage: BF16 weight tile(s), activation boxes, and for
-// NVFP4 the packed tile(s) and scale tile(s) the converters read.
+// Bytes of one pipeline stage: the activation boxes plus, for BF16 weights,
+// the weight tile(s), or for NVFP4 the packed tile(s) and scale tile(s) that
+// the converters expand into TMEM.
 __host__ __device__ inline size_t gemm_stage_bytes(int num_a, bool fp4, int nmax) {
-  size_t b = static_cast<size_t>(num_a) * kBlockM * kBlockK * 2 + static_cast<size_t>(nmax) * kBlockK * 2;
-  if (fp4) b += num_a * (kPackedTileBytes + kScaleTileBytes);
-  return b;
+  const size_t b = static_cast<size_t>(nmax) * kBlockK * 2;
+  if (fp4) return b + static_cast<size_t>(num_a) * (kPackedTileBytes + kScaleTileBytes);
+  return b + static_cast<size_t>(num_a) * kBlockM * kBlockK * 2;
 }
 
 // ---------------------------------------------------------------------------

@@ -71,6 +71,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// As mbar_try_wait, letting the hardware suspend the thread for up to
+// `hint_ns` nanoseconds (it resumes as soon as the phase completes), so that a
+// waiting warp does not keep taking issue slots from the warps sharing its
+// scheduler.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+constexpr uint32_t kWaitSleepNs = 20000;
+
 // Wait until the phase with parity `parity` of `bar` has completed.  Gives up
 // after `limit_ns` nanoseconds, or as soon as *abort becomes non-zero (another
 // role of the CTA gave up); on giving up records (kStatusTimeout, where) in
@@ -81,8 +98,8 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 15u) == 0) {
+    if (mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) return true;
+    if ((it & 3u) == 0) {
       if (abort != nullptr && *abort != 0u) return false;
       if (globaltimer_ns() - t0 > limit_ns) {
         report_status(status, kStatusTimeout, where);

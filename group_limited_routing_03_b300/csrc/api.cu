@@ -369,6 +369,11 @@ beam_status_t run_gemm(int mode, const beam_moe_shape_t& s, const beam_expert_we
     smem = gemm_smem_bytes(st1, acc_stages, sb1);
     grid = d.sms;
   }
+  // activations in one box per k-block: the B tile's full height
+  p.b_big_rows = pair ? nmax / 2 : nmax;
+  if (!make_bf16_map(&maps.bb, mode == 0 ? static_cast<const void*>(xp) : static_cast<const void*>(h),
+                     mode == 0 ? H : I, R_pad, static_cast<uint32_t>(p.b_big_rows)))
+    return BEAM_ERR_CUDA;
   if (cudaMemsetAsync(p.sched, 0, sizeof(int), stream) != cudaSuccess) return BEAM_ERR_CUDA;
   return cuda_status(launch_gemm(mode, fp4, pair, maps, p, grid, smem, stream));
 }

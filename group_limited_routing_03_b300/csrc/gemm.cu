@@ -210,6 +210,7 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
     tma_prefetch_desc(&maps.a0);
     if (kMode == 0) tma_prefetch_desc(&maps.a1);
     tma_prefetch_desc(&maps.b);
+    tma_prefetch_desc(&maps.bb);
     if (kFp4) {
       tma_prefetch_desc(&maps.s0);
       if (kMode == 0) tma_prefetch_desc(&maps.s1);
@@ -300,9 +301,16 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
         // pair: this CTA loads token rows [start + rank*N/2, +N/2), N = round16(n)
         const int n_local = kPair ? ((U.n + 15) & ~15) / 2 : U.n;
         const int b_row0 = U.start + static_cast<int>(rank) * n_local;
-        const int nbox = (n_local + kBoxRows - 1) / kBoxRows;
+        // activations: one box of the tile's full height when the chunk fills
+        // more than half of it (rows past the chunk are loaded and not read),
+        // else ceil(n / 32) boxes of 32 rows
+        const bool big = 2 * n_local > p.b_big_rows;
+        const int nbox = big ? 1 : (n_local + kBoxRows - 1) / kBoxRows;
         const uint32_t a_bytes = kFp4 ? kNumA * (kPackedTileBytes + kScaleTileBytes) : kNumA * kATileBytes;
-        const uint32_t bytes = a_bytes + static_cast<uint32_t>(nbox) * kBoxBytes;
+        const uint32_t bytes =
+            a_bytes + (big ? static_cast<uint32_t>(p.b_big_rows) * (kBlockK * 2) : static_cast<uint32_t>(nbox) * kBoxBytes);
+        const CUtensorMap* bmap = big ? &maps.bb : &maps.b;
+        const int box_rows = big ? 0 : kBoxRows;  // row step between boxes
         for (int kb = 0; kb < p.k_blocks; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, p.timeout_ns, abort_flag, p.status, kWhereProducerEmpty)) {
             ok = false;
@@ -319,7 +327,7 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
             else  // second 256-row half of the down unit
               tma_load_2d_pair(a_tile(stage, 1), &maps.a0, bar0, kx, a_row + 2 * kBlockM);
             for (int b = 0; b < nbox; ++b)
-              tma_load_2d_pair_hint(b_tile(stage) + b * kBoxBytes, &maps.b, bar0, kx, b_row0 + b * kBoxRows, pol_x);
+              tma_load_2d_pair_hint(b_tile(stage) + b * kBoxBytes, bmap, bar0, kx, b_row0 + b * box_rows, pol_x);
           } else {
             mbar_arrive_expect_tx(&full[stage], bytes);
             if (kFp4) {
@@ -335,7 +343,7 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
               if (kMode == 0) tma_load_2d_nohint(a_tile(stage, 1), &maps.a1, &full[stage], kx, a_row);
             }
             for (int b = 0; b < nbox; ++b)
-              tma_load_2d(b_tile(stage) + b * kBoxBytes, &maps.b, &full[stage], kx, U.start + b * kBoxRows, pol_x);
+              tma_load_2d(b_tile(stage) + b * kBoxBytes, bmap, &full[stage], kx, U.start + b * box_rows, pol_x);
           }
           ++issued;
           if (++stage == p.stages) {

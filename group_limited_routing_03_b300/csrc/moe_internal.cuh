@@ -61,6 +61,7 @@ struct GemmParams {
   int acc_stages;               // TMEM accumulator buffers
   uint32_t acc_cols;            // TMEM columns per accumulator buffer
   uint32_t tmem_cols;           // TMEM columns allocated (power of two)
+  int b_big_rows;               // rows of the bb box (the B tile's capacity: nmax, or nmax / 2 for CTA pairs)
   int a_stages;                 // NVFP4: BF16 weight tiles in TMEM (ring depth)
   uint32_t a_col0;              // NVFP4: first TMEM column of that ring
   int* sched;                   // unit counter (zeroed before the launch)
@@ -73,9 +74,10 @@ struct GemmParams {
 };
 
 // TMA descriptors of one grouped GEMM: weights a0 (gate or down) and a1 (up),
-// activations b, and for NVFP4 the block scales s0 / s1 of a0 / a1.
+// activations b (boxes of kBoxRows rows) and bb (one box of a whole chunk,
+// b_big_rows rows), and for NVFP4 the block scales s0 / s1 of a0 / a1.
 struct GemmMaps {
-  CUtensorMap a0, a1, b, s0, s1;
+  CUtensorMap a0, a1, b, bb, s0, s1;
 };
 
 // Bytes of one pipeline stage: the activation boxes plus, for BF16 weights,

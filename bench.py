@@ -262,7 +262,10 @@ def roofline(wl, m, pk):
     """Dominant kernel: the gate/up GEMM (2/3 of the weight bytes and FLOPs)."""
     R = wl.T * 8
     ms = m["stage_ms"][STAGES.index("gate_up")]
-    wbytes = m["touched"] * 2 * wl.I * wl.H * 2
+    # gate + up weights of the touched experts: BF16 2 bytes per element,
+    # NVFP4 half a byte plus one E4M3 scale per 16 elements
+    per_elem = 0.5 + 1.0 / 16 if wl.w_dtype == "nvfp4" else 2.0
+    wbytes = int(m["touched"] * 2 * wl.I * wl.H * per_elem)
     act_bytes = R * wl.H * 2 + R * wl.I * 2
     flops = 2.0 * R * 2 * wl.I * wl.H
     gbs = (wbytes + act_bytes) / (ms * 1e-3) / 1e9

@@ -214,6 +214,7 @@ beam_status_t run_route(const beam_moe_shape_t& s, const void* x, bool x_bf16, c
     if (!make_bf16_map(&tm_x, x, static_cast<uint64_t>(s.H), static_cast<uint64_t>(s.T), 128) ||
         !make_bf16_map(&tm_w, wsplit, static_cast<uint64_t>(s.H), 3ull * kExperts, kExperts))
       return BEAM_ERR_CUDA;
+    p.splits = router_tc_splits(s.T, s.H, d.sms, L.split_cap);
     return cuda_status(
         launch_router_tc(tm_x, tm_w, p, wsplit, at<uint32_t>(ws, L.status), kDefaultTimeoutNs, d.sms, stream));
   }
@@ -552,9 +553,10 @@ int32_t beam_moe_stage_kernel_count(const beam_moe_shape_t* shape, beam_dtype_t 
   if (!device_info(d)) return -1;
   switch (stage) {
     case BEAM_STAGE_ROUTE: {
-      if (use_router_tc(*shape, xdtype == BEAM_BF16, d)) return 2;  // weight split + logits/selection
       Layout L;
       make_layout(*shape, L);
+      if (use_router_tc(*shape, xdtype == BEAM_BF16, d))  // weight split + logits (+ selection of split K)
+        return router_tc_splits(shape->T, shape->H, d.sms, L.split_cap) > 1 ? 3 : 2;
       int sp = router_splits(shape->T, shape->H, d.sms);
       if (sp > L.split_cap) sp = L.split_cap;
       return sp > 1 ? 2 : 1;

@@ -96,11 +96,17 @@ int router_splits(int T, int H, int num_sms);
 int router_split_cap(int T, int H);
 
 cudaError_t launch_router(const RouterParams& p, bool x_bf16, cudaStream_t stream);
+// Sum p.splits partial logits per token (in split order), select, count the
+// tile histogram with atomics (zeroed by the logits kernel).
+cudaError_t launch_router_select(const RouterParams& p, cudaStream_t stream);
 // Tensor-core router (router_tc.cu) for BF16 x and large T: splits the FP32
 // router weight into three BF16 terms (wsplit [3, E, H]) and runs the logits
 // on tcgen05; tm_x = x [T, H] boxes 64x128, tm_w = wsplit [3E, H] boxes 64x256.
 constexpr int kRouterTcMinTokens = 512;
 size_t router_tc_smem_bytes();
+// K ranges of the tensor-core router: about one CTA per SM, at most split_cap
+// (the partial-logit rows the workspace holds).
+int router_tc_splits(int T, int H, int num_sms, int split_cap);
 cudaError_t launch_router_tc(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const RouterParams& p,
                              __nv_bfloat16* wsplit, uint32_t* status, uint64_t timeout_ns, int num_sms,
                              cudaStream_t stream);

@@ -237,4 +237,9 @@ cudaError_t launch_router(const RouterParams& p, bool x_bf16, cudaStream_t strea
   return cudaGetLastError();
 }
 
+cudaError_t launch_router_select(const RouterParams& p, cudaStream_t stream) {
+  router_select_kernel<<<p.T, 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
 }  // namespace beam

@@ -17,9 +17,13 @@
 // measured ~1e-4 logit error on B300, far above FP32 FMA's; short partials
 // keep every tensor-core rounding relative to a small partial sum.)
 // One CTA owns 128 tokens x 256 experts (tcgen05.mma M=128, N=256, BF16,
-// FP32 accumulation); 8 epilogue warps hold the logits (lane = token, half
-// the experts each), write them to shared memory, and all warps then run the
-// same warp-per-token group-limited selection as the CUDA-core router.
+// FP32 accumulation) over a range of the K' reduction: with one range it holds
+// whole logits, which 8 epilogue warps (lane = token, half the experts each)
+// write to shared memory for the same warp-per-token group-limited selection
+// as the CUDA-core router; with p.splits ranges (blockIdx.y) it writes FP32
+// partial logits, which router_select_kernel sums in range order.  Every k-block
+// moves 48 KiB through shared memory (TMA in, MMA out), so the router is bound
+// by shared-memory bandwidth per SM; splitting K spreads it over more SMs.
 #include <cuda.h>
 #include <cuda_bf16.h>
 
@@ -83,7 +87,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t0 = blockIdx.x * kTok;
   const int kb_per = p.H / kBlockK;
-  const int total_kb = 3 * kb_per;
+  const int split = blockIdx.y;
+  // this CTA's k-blocks [kb_lo, kb_hi) of the 3 x kb_per (term-major) sequence
+  const int kb_lo = static_cast<int>(static_cast<long long>(3 * kb_per) * split / p.splits);
+  const int kb_hi = static_cast<int>(static_cast<long long>(3 * kb_per) * (split + 1) / p.splits);
+  const int total_kb = kb_hi - kb_lo;
 
   for (int i = threadIdx.x; i < kDispatchTiles * kExperts; i += kThreads) (&tail.hist[0][0])[i] = 0;
   if (threadIdx.x == 0) {
@@ -115,10 +123,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int kb = 0; kb < total_kb; ++kb) {
         if (!mbar_wait(&tail.empty[stage], phase ^ 1u, timeout_ns, abort_flag, status, kWhereProducerEmpty)) break;
         mbar_arrive_expect_tx(&tail.full[stage], kStage);
-        const int kx = (kb % kb_per) * kBlockK;
+        const int g = kb_lo + kb;  // position in the 3 x kb_per sequence
+        const int kx = (g % kb_per) * kBlockK;
         uint8_t* st = smem + stage * kStage;
         tma_load_2d_nohint(st, &tm_x, &tail.full[stage], kx, t0);
-        tma_load_2d_nohint(st + kATile, &tm_w, &tail.full[stage], kx, (kb / kb_per) * kExperts);
+        tma_load_2d_nohint(st + kATile, &tm_w, &tail.full[stage], kx, (g / kb_per) * kExperts);
         ++issued;
         if (++stage == kStages) {
           stage = 0;
@@ -211,16 +220,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         buf_phase ^= 1u;
       }
     }
-    if (ok) {
-      // wait for every stage's TMA bytes to have been consumed before the
-      // stage memory is reused for the logits (the MMA issued them all)
+    if (ok && p.splits > 1) {
+      // partial logits of this K range -> part[split][t][:]
+      const int t = t0 + quad * 32 + lane;
+      if (t < p.T) {
+        float* row = p.part + (static_cast<size_t>(split) * p.T + t) * kExperts + half * (kExperts / 2);
+#pragma unroll
+        for (int j = 0; j < kExperts / 2; j += 4)
+          *reinterpret_cast<float4*>(row + j) = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
+      }
+    } else if (ok) {
+      // every stage's TMA bytes were consumed by the MMAs before the last
+      // partial sum completed, so the stage memory can hold the logits
       float* row = logits + (quad * 32 + lane) * kLd + half * (kExperts / 2);
 #pragma unroll
       for (int j = 0; j < kExperts / 2; j += 4) *reinterpret_cast<float4*>(row + j) = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
     }
   }
   __syncthreads();
-  if (tail.abort_flag == 0u) {
+  if (p.splits > 1) {
+    // router_select_kernel counts the tile histogram with atomics: the first
+    // K range zeroes this CTA's dispatch tiles
+    if (split == 0) {
+      for (int i = threadIdx.x; i < kDispatchTiles * kExperts; i += kThreads) {
+        const int sub = i / kExperts, e = i % kExperts;
+        const int dt = blockIdx.x * kDispatchTiles + sub;
+        if (dt < p.n_tiles) p.tile_hist[static_cast<size_t>(e) * p.n_tiles + dt] = 0;
+      }
+    }
+  } else if (tail.abort_flag == 0u) {
     // warp-per-token selection, all 6 warps
     for (int j = warp; j < kTok; j += kThreads / 32) {
       const int t = t0 + j;
@@ -236,10 +264,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < kDispatchTiles * kExperts; i += kThreads) {
-    const int sub = i / kExperts, e = i % kExperts;
-    const int dt = blockIdx.x * kDispatchTiles + sub;
-    if (dt < p.n_tiles) p.tile_hist[static_cast<size_t>(e) * p.n_tiles + dt] = tail.hist[sub][e];
+  if (p.splits == 1) {
+    for (int i = threadIdx.x; i < kDispatchTiles * kExperts; i += kThreads) {
+      const int sub = i / kExperts, e = i % kExperts;
+      const int dt = blockIdx.x * kDispatchTiles + sub;
+      if (dt < p.n_tiles) p.tile_hist[static_cast<size_t>(e) * p.n_tiles + dt] = tail.hist[sub][e];
+    }
   }
   if (warp == 1) {
     tc_fence_after();
@@ -251,6 +281,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 size_t router_tc_smem_bytes() { return 1024 + kStages * kStage + sizeof(TcSmemTail); }
 
+int router_tc_splits(int T, int H, int num_sms, int split_cap) {
+  const int tiles = (T + kTok - 1) / kTok;
+  int s = num_sms / tiles;  // about one CTA per SM
+  if (s > split_cap) s = split_cap;
+  const int kbs = 3 * (H / kBlockK);
+  if (s > kbs / kPartial) s = kbs / kPartial;  // at least one whole partial sum per range
+  return s < 1 ? 1 : s;
+}
+
 cudaError_t launch_router_tc(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const RouterParams& p,
                              __nv_bfloat16* wsplit, uint32_t* status, uint64_t timeout_ns, int num_sms,
                              cudaStream_t stream) {
@@ -261,8 +300,13 @@ cudaError_t launch_router_tc(const CUtensorMap& tm_x, const CUtensorMap& tm_w, c
   const size_t smem = router_tc_smem_bytes();
   cudaError_t err = cudaFuncSetAttribute(router_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (err != cudaSuccess) return err;
-  const int grid = (p.T + kTok - 1) / kTok;
+  const dim3 grid((p.T + kTok - 1) / kTok, p.splits);
   router_tc_kernel<<<grid, kThreads, smem, stream>>>(tm_x, tm_w, p, status, timeout_ns);
+  if (p.splits > 1) {
+    err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    return launch_router_select(p, stream);
+  }
   return cudaGetLastError();
 }
 

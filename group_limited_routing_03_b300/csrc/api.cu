@@ -251,8 +251,7 @@ uint32_t pow2_at_least(uint32_t v) {
 
 beam_status_t run_gather(const beam_moe_shape_t& s, const void* x, bool x_bf16, void* ws, const Layout& L,
                          const DeviceInfo& d, cudaStream_t stream) {
-  const int R = s.T * kTopK;
-  return cuda_status(launch_gather(x, x_bf16, s.H, at<int32_t>(ws, L.perm), R, at<__nv_bfloat16>(ws, L.xp), d.sms,
+  return cuda_status(launch_gather(x, x_bf16, s.H, at<int32_t>(ws, L.pos), s.T, at<__nv_bfloat16>(ws, L.xp), d.sms,
                                    stream));
 }
 

@@ -10,7 +10,10 @@
 //     offsets[e] + (routes of e in earlier tiles) + (rank inside the tile),
 // which keeps the routes of an expert in ascending r: a deterministic
 // permutation with no global atomics.  gather_kernel then copies the token
-// rows into that order (BF16) as the B operand of the gate/up GEMM.
+// rows into that order (BF16) as the B operand of the gate/up GEMM, reading
+// each token row once and writing it to its 8 route positions (reading per
+// route would fetch x from DRAM several times, as the 8x larger output
+// streams through L2 and evicts it).
 #include <cuda_bf16.h>
 
 #include "moe_internal.cuh"
@@ -132,17 +135,17 @@ __global__ void __launch_bounds__(256) scatter_kernel(const int32_t* ids, int R,
   }
 }
 
-// xp[p, :] = bf16(x[perm[p] / 8, :]); 8 elements (16 output bytes) per step.
+// xp[pos[t*8+k], :] = bf16(x[t, :]) for k = 0..7 (routes with pos < 0, whose
+// expert id was out of range, are skipped); 8 elements (16 bytes) per step.
 template <bool kBf16>
-__global__ void __launch_bounds__(256) gather_kernel(const void* x, int H, const int32_t* perm, int R,
+__global__ void __launch_bounds__(256) gather_kernel(const void* x, int H, const int32_t* pos, int T,
                                                      __nv_bfloat16* xp) {
   const int vecs_per_row = H / 8;
-  const size_t n = static_cast<size_t>(R) * vecs_per_row;
+  const size_t n = static_cast<size_t>(T) * vecs_per_row;
   for (size_t v = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; v < n;
        v += static_cast<size_t>(gridDim.x) * blockDim.x) {
-    const int p = static_cast<int>(v / vecs_per_row);
+    const int t = static_cast<int>(v / vecs_per_row);
     const int c = static_cast<int>(v % vecs_per_row);
-    const int t = perm[p] / kTopK;
     uint4 out;
     if (kBf16) {
       out = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(x) + static_cast<size_t>(t) * H + c * 8);
@@ -156,7 +159,12 @@ __global__ void __launch_bounds__(256) gather_kernel(const void* x, int H, const
       out.z = *reinterpret_cast<uint32_t*>(&q2);
       out.w = *reinterpret_cast<uint32_t*>(&q3);
     }
-    *reinterpret_cast<uint4*>(xp + static_cast<size_t>(p) * H + c * 8) = out;
+    const int4 p0 = *reinterpret_cast<const int4*>(pos + static_cast<size_t>(t) * kTopK);
+    const int4 p1 = *reinterpret_cast<const int4*>(pos + static_cast<size_t>(t) * kTopK + 4);
+    const int dst[kTopK] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+#pragma unroll
+    for (int k = 0; k < kTopK; ++k)
+      if (dst[k] >= 0) *reinterpret_cast<uint4*>(xp + static_cast<size_t>(dst[k]) * H + c * 8) = out;
   }
 }
 
@@ -177,17 +185,17 @@ cudaError_t launch_dispatch(const int32_t* ids, int R, int n_tiles, int32_t* til
   return cudaGetLastError();
 }
 
-cudaError_t launch_gather(const void* x, bool x_bf16, int H, const int32_t* perm, int R, __nv_bfloat16* xp,
+cudaError_t launch_gather(const void* x, bool x_bf16, int H, const int32_t* pos, int T, __nv_bfloat16* xp,
                           int num_sms, cudaStream_t stream) {
-  const size_t n = static_cast<size_t>(R) * (H / 8);
+  const size_t n = static_cast<size_t>(T) * (H / 8);
   size_t blocks = (n + 255) / 256;
   const size_t cap = static_cast<size_t>(num_sms) * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   if (x_bf16)
-    gather_kernel<true><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(x, H, perm, R, xp);
+    gather_kernel<true><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(x, H, pos, T, xp);
   else
-    gather_kernel<false><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(x, H, perm, R, xp);
+    gather_kernel<false><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(x, H, pos, T, xp);
   return cudaGetLastError();
 }
 

@@ -115,7 +115,7 @@ cudaError_t launch_tile_hist(const int32_t* ids, int R, int n_tiles, int32_t* ti
 cudaError_t launch_dispatch(const int32_t* ids, int R, int n_tiles, int32_t* tile_hist,
                             int32_t* counts, int32_t* offsets, int32_t* chunk_prefix, int nmax,
                             int32_t* perm, int32_t* pos, cudaStream_t stream);
-cudaError_t launch_gather(const void* x, bool x_bf16, int H, const int32_t* perm, int R,
+cudaError_t launch_gather(const void* x, bool x_bf16, int H, const int32_t* pos, int T,
                           __nv_bfloat16* xp, int num_sms, cudaStream_t stream);
 cudaError_t launch_gemm(int mode, bool fp4, bool pair, const GemmMaps& maps, const GemmParams& p, int grid,
                         size_t smem_bytes, cudaStream_t stream);

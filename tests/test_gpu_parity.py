@@ -254,3 +254,50 @@ def test_full_size_workloads(name, n_sample):
     del dg, y, ws
     gc.collect()
     torch.cuda.empty_cache()
+
+
+def test_maximum_token_count():
+    """T = 2^20, the largest token count the library takes (8M routes), at
+    H = I = 128: the dispatch (per-expert counts, stable positions, their
+    inverse) checked against the GPU's own ids in full, routing and y of
+    sampled tokens against the oracle."""
+    T = 1 << 20
+    wl = inputs.workload("prefill", T=T, H=128, I=128, seed=91)
+    torch.cuda.empty_cache()
+    dg = inputs.generate(wl, DEV)
+    y, ids, w, ws = _run_forward(wl, dg, dg)
+    sh = moe.shape(wl.T, wl.H, wl.I)
+    lay = moe.workspace_layout(sh)
+    R = T * 8
+
+    def ws_i32(off, n):
+        return ws[off:off + 4 * n].view(torch.int32).cpu().numpy()
+
+    ids_h = ids.cpu().numpy()
+    counts = ws_i32(lay["counts"], 256)
+    np.testing.assert_array_equal(counts, np.bincount(ids_h.reshape(-1), minlength=256))
+    offsets = ws_i32(lay["offsets"], 257)
+    assert offsets[0] == 0 and offsets[-1] == R and (np.diff(offsets) == counts).all()
+    perm = ws_i32(lay["perm"], R)
+    pos = ws_i32(lay["pos"], R)
+    np.testing.assert_array_equal(perm[pos], np.arange(R))
+    # routes of each expert in ascending route index
+    e_of_p = ids_h.reshape(-1)[perm]
+    assert (np.diff(e_of_p) >= 0).all()
+    same = np.diff(e_of_p) == 0
+    assert (np.diff(perm)[same] > 0).all()
+    del perm, pos, e_of_p, same
+    # routing and outputs of sampled tokens
+    rng = np.random.default_rng(91)
+    tok = np.unique(np.concatenate([[0, T - 1], rng.integers(0, T, 2000)]))
+    x_h = host_act(dg["x"])
+    bias = None if dg.get("bias") is None else dg["bias"].cpu().numpy()
+    ref = oracle.route(x_h[tok], dg["router_w"].cpu().numpy(), bias, want_scores=True)
+    safe = compare_routing(ids_h[tok], w.cpu().numpy()[tok], ref, bias=bias)
+    few = tok[safe][:24]
+    y_ref = oracle_y(dg, few, ref["ids"][safe][:24], ref["weights"][safe][:24])
+    err = rel_err(y.cpu()[few].double().numpy(), y_ref)
+    assert err <= Y_TOL["bf16"], err
+    del dg, y, ws
+    gc.collect()
+    torch.cuda.empty_cache()

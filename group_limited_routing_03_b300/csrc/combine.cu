@@ -3,8 +3,10 @@
 // Beam launch post, section "Mixture of Experts": the expert outputs are
 // combined with the normalised router weights (already scaled by 2.5 by the
 // router); there is no shared expert.  y[t, :] = sum_k w[t,k] * yr[pos[t*8+k], :],
-// FP32 accumulation in k order 0..7, one CTA per token, 8 elements per thread
-// step (16-byte loads of the BF16 expert outputs).
+// FP32 accumulation in k order 0..7.  CTA (t, j) covers the 8-element groups
+// c = 128 j + threadIdx.x + 128 gridDim.y i of token t (16-byte loads of the
+// BF16 expert outputs); for few tokens (decode) gridDim.y splits each row so
+// the work still spreads over many SMs, for many tokens one CTA per token.
 #include <cuda_bf16.h>
 
 #include "moe_internal.cuh"
@@ -19,12 +21,13 @@ __global__ void __launch_bounds__(128) combine_kernel(const __nv_bfloat16* yr, c
   __shared__ int ps[kTopK];
   __shared__ float ws[kTopK];
   const int t = blockIdx.x;
+
   if (threadIdx.x < kTopK) {
     ps[threadIdx.x] = pos[static_cast<size_t>(t) * kTopK + threadIdx.x];
     ws[threadIdx.x] = w[static_cast<size_t>(t) * kTopK + threadIdx.x];
   }
   __syncthreads();
-  for (int c = threadIdx.x; c < H / 8; c += blockDim.x) {
+  for (int c = blockIdx.y * blockDim.x + threadIdx.x; c < H / 8; c += gridDim.y * blockDim.x) {
     float acc[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
@@ -76,10 +79,11 @@ __global__ void debug_timeout_kernel(uint32_t* status, uint64_t timeout_ns) {
 
 cudaError_t launch_combine(const __nv_bfloat16* yr, const int32_t* pos, const float* w, int T, int H, void* y,
                            bool y_bf16, cudaStream_t stream) {
+  const dim3 grid(T, T >= 1024 ? 1 : (H / 8 + 127) / 128);
   if (y_bf16)
-    combine_kernel<true><<<T, 128, 0, stream>>>(yr, pos, w, H, y);
+    combine_kernel<true><<<grid, 128, 0, stream>>>(yr, pos, w, H, y);
   else
-    combine_kernel<false><<<T, 128, 0, stream>>>(yr, pos, w, H, y);
+    combine_kernel<false><<<grid, 128, 0, stream>>>(yr, pos, w, H, y);
   return cudaGetLastError();
 }
 

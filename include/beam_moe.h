@@ -178,9 +178,10 @@ beam_status_t beam_moe_forward_stage(const beam_moe_shape_t* shape, const beam_m
                                      void* stream);
 
 /* Number of kernels stage `stage` launches for `shape` and activations of
- * type `xdtype` on the current device (the router launches a second kernel
- * when it splits the hidden dimension across CTAs, or to split the router
- * weight for its tensor-core path); -1 on an unsupported shape or stage. */
+ * type `xdtype` on the current device: the router adds a selection kernel
+ * when it splits its reduction across CTAs, and its tensor-core path (BF16
+ * x, T >= 512) a kernel that splits the router weight into BF16 terms; the
+ * dispatch is two kernels; -1 on an unsupported shape or stage. */
 int32_t beam_moe_stage_kernel_count(const beam_moe_shape_t* shape, beam_dtype_t xdtype, beam_stage_t stage);
 
 /* Synchronises `stream`, returns the device status word of `workspace`

@@ -14,17 +14,20 @@
 // rows are the MMA's M side (128 rows per tile = the 128 TMEM lanes) and the
 // routed tokens are its N side ("swap AB"): an expert sees 1..3 tokens at
 // decode and ~256 at prefill, and N can be any multiple of 16 up to 256,
-// while M is fixed at 128.  A work unit is (expert, token chunk of <= nmax
-// routes, 128-row weight tile); units are enumerated in the order
-// (expert, chunk, row tile) so that CTAs running side by side share the
-// activation chunk (and, for several chunks of one expert, the weight tile)
-// through L2.  The grid is persistent (one CTA per SM), units are dealt
-// round-robin.
+// while M is 128 per CTA.  A work unit is (expert, token chunk of <= nmax
+// routes, weight row tile): 128 rows, or on CTA pairs 256 (gate/up) / 512
+// (down) rows, and 256 rows for NVFP4 down; each k-block issues its MMAs into
+// two accumulators (gate and up, or two row halves).  Units are numbered in
+// the order (expert, chunk, row tile) and taken from a global counter in that
+// order by a persistent grid (one CTA, or CTA pair, per SM), so CTAs running
+// side by side share the token chunk (and, for several chunks of one expert,
+// the weight tiles) through L2.
 //
 // Warp roles:
-//   warp 0       TMA producer: weight tile(s) 128x64 and ceil(n/32) boxes of
-//                32 activation rows x 64 per stage, 128-byte swizzle (NVFP4:
-//                the packed 128x32-byte tile(s) and their E4M3 scales);
+//   warp 0       TMA producer: weight tile(s) 128x64 and the chunk's token
+//                rows x 64 (one box of the tile's height, or 32-row boxes for
+//                a small chunk) per stage, 128-byte swizzle (NVFP4: the
+//                packed 128x32-byte tiles and their E4M3 scales);
 //   warp 1       TMEM allocator and MMA issuer (one thread):
 //                tcgen05.mma kind::f16, M=128, N=round_up(n,16), K=16 steps;
 //   warps 2-9    epilogue: tcgen05.ld of the accumulators (warp w reads TMEM
@@ -42,9 +45,9 @@
 // for the TMA bytes of a stage before expanding its weights, and the MMA
 // thread waits only for the converters (afull), whose arrival follows their
 // observation of the TMA completion; a TMEM weight tile is reused once the
-// empty barrier of the k-block that last read it has completed.  One wait and
-// one commit per k-block keep the single MMA-issuing thread ahead of the
-// tensor pipe.  Every wait is bounded.
+// empty barrier of the k-block that last read it has completed, so the single
+// MMA-issuing thread waits once and commits once per k-block.  Every wait is
+// bounded; waits after the first poll let the thread sleep (see mbar_wait).
 #include <cuda.h>
 #include <cuda_bf16.h>
 

@@ -175,37 +175,82 @@ __global__ void __launch_bounds__(256) router_gemm_kernel(RouterParams p) {
   select_tile(p, s, tile);
 }
 
-// splits > 1: one CTA per token sums the partial logits in split order, then
-// warp 0 selects; the tile histogram (zeroed by the GEMM kernel) is counted
-// with atomics.
-__global__ void __launch_bounds__(256) router_select_kernel(RouterParams p) {
+// splits > 1: the partial logits of each token are summed (FP32, a fixed
+// order), then one warp selects; the tile histogram (zeroed by the logits
+// kernel) is counted with atomics.
+__device__ __forceinline__ void select_and_count(const RouterParams& p, const float* lrow, int t, int lane) {
+  int id;
+  float wv;
+  select_token(lrow, p.bias, p.scale, lane, id, wv);
+  if (lane < kTopK) {
+    p.ids[static_cast<size_t>(t) * kTopK + lane] = id;
+    p.w[static_cast<size_t>(t) * kTopK + lane] = wv;
+    atomicAdd(&p.tile_hist[static_cast<size_t>(id) * p.n_tiles + t / kRouterTile], 1);
+  }
+}
+
+// Many tokens: one warp per token, 8 tokens per CTA; lane l sums experts
+// 8l..8l+7 over the splits in order.
+constexpr int kSelTokens = 8;
+__global__ void __launch_bounds__(32 * kSelTokens) router_select_tokens_kernel(RouterParams p) {
+  __shared__ __align__(16) float lrow[kSelTokens][kExperts];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kSelTokens + warp;
+  if (t >= p.T) return;
+  const size_t stride = static_cast<size_t>(p.T) * kExperts;
+  const float4* src = reinterpret_cast<const float4*>(p.part + static_cast<size_t>(t) * kExperts + 8 * lane);
+  float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+  for (int sp = 0; sp < p.splits; ++sp) {
+    const float4 u = src[sp * stride / 4], v = src[sp * stride / 4 + 1];
+    a.x += u.x; a.y += u.y; a.z += u.z; a.w += u.w;
+    b.x += v.x; b.y += v.y; b.z += v.z; b.w += v.w;
+  }
+  float* row = lrow[warp];
+  *reinterpret_cast<float4*>(row + 8 * lane) = a;
+  *reinterpret_cast<float4*>(row + 8 * lane + 4) = b;
+  __syncwarp();
+  select_and_count(p, row, t, lane);
+}
+
+// Few tokens, many splits: one CTA per token, 4 x 256 threads; thread group g
+// sums splits g, g+4, g+8, ... for one expert, then the 4 sums are added in
+// group order.
+constexpr int kSelGroups = 4;
+__global__ void __launch_bounds__(kSelGroups * kExperts) router_select_wide_kernel(RouterParams p) {
+  __shared__ __align__(16) float part[kSelGroups][kExperts];
   __shared__ __align__(16) float lrow[kExperts];
-  const int e = threadIdx.x;
+  const int e = threadIdx.x % kExperts, g = threadIdx.x / kExperts;
   const int t = blockIdx.x;
   const float* src = p.part + static_cast<size_t>(t) * kExperts + e;
   const size_t stride = static_cast<size_t>(p.T) * kExperts;
   float v = 0.0f;
-  int sp = 0;
-  for (; sp + 8 <= p.splits; sp += 8) {
-    float q[8];
+  int sp = g;
+  for (; sp + 4 * kSelGroups <= p.splits; sp += 4 * kSelGroups) {
+    float q[4];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) q[u] = src[(sp + u) * stride];
+    for (int u = 0; u < 4; ++u) q[u] = src[static_cast<size_t>(sp + u * kSelGroups) * stride];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) v += q[u];
+    for (int u = 0; u < 4; ++u) v += q[u];
   }
-  for (; sp < p.splits; ++sp) v += src[sp * stride];
-  lrow[e] = v;
+  for (; sp < p.splits; sp += kSelGroups) v += src[static_cast<size_t>(sp) * stride];
+  part[g][e] = v;
   __syncthreads();
-  if (threadIdx.x < 32) {
-    int id;
-    float wv;
-    select_token(lrow, p.bias, p.scale, threadIdx.x, id, wv);
-    if (threadIdx.x < kTopK) {
-      p.ids[static_cast<size_t>(t) * kTopK + threadIdx.x] = id;
-      p.w[static_cast<size_t>(t) * kTopK + threadIdx.x] = wv;
-      atomicAdd(&p.tile_hist[static_cast<size_t>(id) * p.n_tiles + t / kRouterTile], 1);
-    }
+  if (g == 0) {
+    float s = part[0][e];
+#pragma unroll
+    for (int k = 1; k < kSelGroups; ++k) s += part[k][e];
+    lrow[e] = s;
   }
+  __syncthreads();
+  if (threadIdx.x < 32) select_and_count(p, lrow, t, threadIdx.x);
+}
+
+cudaError_t launch_select(const RouterParams& p, cudaStream_t stream) {
+  if (p.T >= 1024)
+    router_select_tokens_kernel<<<(p.T + kSelTokens - 1) / kSelTokens, 32 * kSelTokens, 0, stream>>>(p);
+  else
+    router_select_wide_kernel<<<p.T, kSelGroups * kExperts, 0, stream>>>(p);
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -233,13 +278,14 @@ cudaError_t launch_router(const RouterParams& p, bool x_bf16, cudaStream_t strea
     router_gemm_kernel<true><<<grid, 256, 0, stream>>>(p);
   else
     router_gemm_kernel<false><<<grid, 256, 0, stream>>>(p);
-  if (p.splits > 1) router_select_kernel<<<p.T, 256, 0, stream>>>(p);
+  if (p.splits > 1) {
+    const cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    return launch_select(p, stream);
+  }
   return cudaGetLastError();
 }
 
-cudaError_t launch_router_select(const RouterParams& p, cudaStream_t stream) {
-  router_select_kernel<<<p.T, 256, 0, stream>>>(p);
-  return cudaGetLastError();
-}
+cudaError_t launch_router_select(const RouterParams& p, cudaStream_t stream) { return launch_select(p, stream); }
 
 }  // namespace beam

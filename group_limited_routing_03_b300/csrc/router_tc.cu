@@ -21,7 +21,7 @@
 // whole logits, which 8 epilogue warps (lane = token, half the experts each)
 // write to shared memory for the same warp-per-token group-limited selection
 // as the CUDA-core router; with p.splits ranges (blockIdx.y) it writes FP32
-// partial logits, which router_select_kernel sums in range order.  Every k-block
+// partial logits, which the select kernel (router.cu) sums.  Every k-block
 // moves 48 KiB through shared memory (TMA in, MMA out), so the router is bound
 // by shared-memory bandwidth per SM; splitting K spreads it over more SMs.
 #include <cuda.h>
@@ -239,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
   if (p.splits > 1) {
-    // router_select_kernel counts the tile histogram with atomics: the first
+    // the select kernel counts the tile histogram with atomics: the first
     // K range zeroes this CTA's dispatch tiles
     if (split == 0) {
       for (int i = threadIdx.x; i < kDispatchTiles * kExperts; i += kThreads) {

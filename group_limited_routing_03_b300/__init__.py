@@ -20,7 +20,8 @@ import torch
 __all__ = [
     "BeamError", "Shape", "shape", "workspace_size", "workspace_layout", "alloc_workspace",
     "beam_moe_route", "beam_moe_dispatch", "beam_moe_experts", "beam_moe_forward", "beam_moe_forward_stage",
-    "ForwardCall", "STAGES", "beam_moe_stage_kernel_count", "beam_moe_route_noalloc",
+    "ForwardCall", "STAGES", "beam_moe_stage_kernel_count", "beam_moe_route_noalloc", "pack_weights",
+    "BEAM_LAYOUT_ROWS", "BEAM_LAYOUT_TILED",
     "beam_moe_read_device_status", "beam_moe_debug_timeout", "beam_status_string", "BeamMoE",
     "library_path", "load",
 ]
@@ -49,7 +50,10 @@ class _ExpertWeights(ctypes.Structure):
     _fields_ = [("dtype", ctypes.c_int), ("gate", ctypes.c_void_p), ("up", ctypes.c_void_p),
                 ("down", ctypes.c_void_p), ("gate_sf", ctypes.c_void_p), ("up_sf", ctypes.c_void_p),
                 ("down_sf", ctypes.c_void_p), ("gate_gs", ctypes.c_void_p), ("up_gs", ctypes.c_void_p),
-                ("down_gs", ctypes.c_void_p)]
+                ("down_gs", ctypes.c_void_p), ("layout", ctypes.c_int)]
+
+
+BEAM_LAYOUT_ROWS, BEAM_LAYOUT_TILED = 0, 1
 
 
 class _Args(ctypes.Structure):
@@ -97,6 +101,7 @@ def load():
     lib.beam_moe_stage_kernel_count.argtypes = [sp, i32, i32]
     lib.beam_moe_stage_kernel_count.restype = ctypes.c_int32
     lib.beam_moe_debug_timeout.argtypes = [vp, sz, u32, vp]
+    lib.beam_moe_pack_weights.argtypes = [sp, ctypes.POINTER(_ExpertWeights), ctypes.POINTER(_ExpertWeights), vp]
     lib.beam_status_string.argtypes = [i32]
     lib.beam_status_string.restype = ctypes.c_char_p
     for n in ("beam_moe_workspace_layout", "beam_moe_route", "beam_moe_dispatch", "beam_moe_experts",
@@ -151,6 +156,7 @@ def _weights(w: dict) -> _ExpertWeights:
     for name in ("gate", "up", "down", "gate_sf", "up_sf", "down_sf", "gate_gs", "up_gs", "down_gs"):
         t = w.get(name)
         setattr(ew, name, None if t is None else _ptr(t).value)
+    ew.layout = {"rows": BEAM_LAYOUT_ROWS, "tiled": BEAM_LAYOUT_TILED}[w.get("layout", "rows")]
     return ew
 
 
@@ -261,6 +267,22 @@ class ForwardCall:
 def beam_moe_forward_stage(sh, stage: int, x, router_w, router_bias, weights: dict, y, topk_ids, topk_w,
                            workspace, stream=None):
     ForwardCall(sh, x, router_w, router_bias, weights, y, topk_ids, topk_w, workspace, stream).stage(stage)
+
+
+def pack_weights(sh, weights: dict, stream=None) -> dict:
+    """The expert weights regrouped into the library's tiled layout
+    (beam_moe_pack_weights): new device arrays of the same shapes and dtypes
+    for gate / up / down (and the NVFP4 block scales); the global scales are
+    shared with ``weights``."""
+    out = {k: v for k, v in weights.items()}
+    for name in ("gate", "up", "down", "gate_sf", "up_sf", "down_sf"):
+        if weights.get(name) is not None:
+            out[name] = torch.empty_like(weights[name])
+    src, dst = _weights(weights), _weights(out)
+    _check(load().beam_moe_pack_weights(ctypes.byref(sh), ctypes.byref(src), ctypes.byref(dst), _stream(stream)),
+           "beam_moe_pack_weights")
+    out["layout"] = "tiled"
+    return out
 
 
 def beam_moe_stage_kernel_count(sh, stage: int, xdtype=BEAM_BF16) -> int:

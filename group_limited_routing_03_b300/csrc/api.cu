@@ -154,6 +154,7 @@ beam_status_t check_workspace(const beam_moe_shape_t* s, const void* ws, size_t 
 
 beam_status_t check_weights(const beam_moe_shape_t* s, const beam_expert_weights_t* w) {
   if (w == nullptr) return BEAM_ERR_INVALID_ARG;
+  if (w->layout != BEAM_LAYOUT_ROWS && w->layout != BEAM_LAYOUT_TILED) return BEAM_ERR_INVALID_ARG;
   if (w->dtype == BEAM_BF16) {
     if (!w->gate || !w->up || !w->down) return BEAM_ERR_INVALID_ARG;
     if (!aligned16(w->gate) || !aligned16(w->up) || !aligned16(w->down)) return BEAM_ERR_INVALID_ARG;
@@ -269,33 +270,62 @@ beam_status_t run_gemm(int mode, const beam_moe_shape_t& s, const beam_expert_we
   GemmMaps maps;
   std::memset(&maps, 0, sizeof(maps));
   bool ok;
+  // Weight maps of an [E * N, K] matrix (N rows per expert): row-major, or
+  // the tiled layout seen as a column of 128-row tiles whose rows are one
+  // box wide (64 BF16 / 32 code bytes / 16 scale bytes), each box one tile.
+  const bool tiled = wts->layout == BEAM_LAYOUT_TILED;
+  auto wmap_bf16 = [&](CUtensorMap* m, const void* base, uint64_t N, uint64_t K) {
+    return tiled ? make_bf16_map(m, base, kBlockK, E * N * (K / kBlockK), kBlockM)
+                 : make_bf16_map(m, base, K, E * N, kBlockM);
+  };
+  auto wmap_codes = [&](CUtensorMap* m, const void* base, uint64_t N, uint64_t K) {
+    return tiled ? make_u8_map(m, base, kBlockK / 2, E * N * (K / kBlockK), kBlockK / 2, kBlockM)
+                 : make_u8_map(m, base, K / 2, E * N, kBlockK / 2, kBlockM);
+  };
+  auto wmap_scales = [&](CUtensorMap* m, const void* base, uint64_t N, uint64_t K) {
+    return tiled ? make_u8_map(m, base, kScaleBoxCols, E * N * (K / (16 * kScaleBoxCols)), kScaleBoxCols, kBlockM)
+                 : make_u8_map(m, base, K / 16, E * N, kScaleBoxCols, kBlockM);
+  };
   if (mode == 0) {
     ok = make_bf16_map(&maps.b, xp, H, R_pad, kBoxRows);
     if (fp4)
-      ok = ok && make_u8_map(&maps.a0, wts->gate, H / 2, E * I, kBlockK / 2, kBlockM) &&
-           make_u8_map(&maps.a1, wts->up, H / 2, E * I, kBlockK / 2, kBlockM) &&
-           make_u8_map(&maps.s0, wts->gate_sf, H / 16, E * I, kScaleBoxCols, kBlockM) &&
-           make_u8_map(&maps.s1, wts->up_sf, H / 16, E * I, kScaleBoxCols, kBlockM);
+      ok = ok && wmap_codes(&maps.a0, wts->gate, I, H) && wmap_codes(&maps.a1, wts->up, I, H) &&
+           wmap_scales(&maps.s0, wts->gate_sf, I, H) && wmap_scales(&maps.s1, wts->up_sf, I, H);
     else
-      ok = ok && make_bf16_map(&maps.a0, wts->gate, H, E * I, kBlockM) &&
-           make_bf16_map(&maps.a1, wts->up, H, E * I, kBlockM);
+      ok = ok && wmap_bf16(&maps.a0, wts->gate, I, H) && wmap_bf16(&maps.a1, wts->up, I, H);
   } else {
     ok = make_bf16_map(&maps.b, h, I, R_pad, kBoxRows);
     if (fp4)
-      ok = ok && make_u8_map(&maps.a0, wts->down, I / 2, E * H, kBlockK / 2, kBlockM) &&
-           make_u8_map(&maps.s0, wts->down_sf, I / 16, E * H, kScaleBoxCols, kBlockM);  // a1 / s1 = a0 / s0
+      ok = ok && wmap_codes(&maps.a0, wts->down, H, I) && wmap_scales(&maps.s0, wts->down_sf, H, I);  // a1 / s1 = a0 / s0
     else
-      ok = ok && make_bf16_map(&maps.a0, wts->down, I, E * H, kBlockM);
+      ok = ok && wmap_bf16(&maps.a0, wts->down, H, I);
     maps.a1 = maps.a0;
     maps.s1 = maps.s0;
   }
   if (!ok) return BEAM_ERR_CUDA;
   // CTA pairs (one M=256 MMA per unit over two SMs) halve each SM's shared-
   // memory operand traffic; used for BF16 weights when chunks reach 256 routes.
+  // Decided first, so the tiling below is derived once for the kernel that
+  // runs: a pair tile's stage is fixed (two weight tiles, 128 token rows per
+  // CTA, one 2 x 256-column accumulator), and if no pair fits on the device
+  // the GEMM runs one CTA per unit.
+  const size_t budget = static_cast<size_t>(d.smem_optin) - 1024 - 512;
   bool pair = !fp4 && nmax == 256 && s.H % 512 == 0 && s.I % 256 == 0 && d.sms >= 2;
-  // pair units: gate/up 256 features (gate and up tiles), down 512 features
-  // NVFP4 down units: 256 features (two weight tiles, two accumulators)
-  const int rows_per_unit = pair ? (mode == 0 ? 2 * kBlockM : 4 * kBlockM) : (fp4 && mode == 1 ? 2 * kBlockM : kBlockM);
+  int clusters = 0;
+  if (pair) {
+    const size_t sbp = gemm_stage_bytes(2, false, nmax / 2);
+    int stp = static_cast<int>(budget / sbp);
+    if (stp > kMaxStages) stp = kMaxStages;
+    clusters = stp >= 2 ? gemm_pair_max_clusters(mode, gemm_smem_bytes(stp, 1, sbp)) : 0;
+    if (clusters <= 0) pair = false;
+  }
+  // pair units: gate/up 256 features (gate and up tiles), down 512 features.
+  // Down on one CTA per unit: 256 features (two weight tiles, two
+  // accumulators: two MMA chains per k-block) for NVFP4, and for BF16 when H
+  // allows ("wide"); else 128.
+  const bool wide = mode == 1 && !pair && !fp4 && s.H % 256 == 0;
+  const int rows_per_unit =
+      pair ? (mode == 0 ? 2 * kBlockM : 4 * kBlockM) : ((fp4 || wide) && mode == 1 ? 2 * kBlockM : kBlockM);
   GemmParams p;
   p.counts = at<int32_t>(ws, L.counts);
   p.offsets = at<int32_t>(ws, L.offsets);
@@ -303,12 +333,12 @@ beam_status_t run_gemm(int mode, const beam_moe_shape_t& s, const beam_expert_we
   p.m_tiles = (mode == 0 ? s.I : s.H) / rows_per_unit;
   p.a_rows_per_expert = mode == 0 ? s.I : s.H;
   p.k_blocks = (mode == 0 ? s.H : s.I) / kBlockK;
+  p.a_tiled = tiled ? 1 : 0;
   p.nmax = nmax;
-  const size_t budget = static_cast<size_t>(d.smem_optin) - 1024 - 512;
-  const int num_a = (mode == 0 || pair || fp4) ? 2 : 1;  // weight tiles per stage
+  const int num_a = (mode == 0 || pair || fp4 || wide) ? 2 : 1;  // weight tiles per stage
   const size_t sb = gemm_stage_bytes(num_a, fp4, pair ? nmax / 2 : nmax);
   int stages = static_cast<int>(budget / sb);
-  if (stages > 8) stages = 8;
+  if (stages > kMaxStages) stages = kMaxStages;
   if (stages < 2) return BEAM_ERR_UNSUPPORTED;
   p.stages = stages;
   p.acc_cols = static_cast<uint32_t>(num_a * nmax);
@@ -341,41 +371,17 @@ beam_status_t run_gemm(int mode, const beam_moe_shape_t& s, const beam_expert_we
   p.gs1 = fp4 && mode == 0 ? wts->up_gs : nullptr;
   p.status = at<uint32_t>(ws, L.status);
   p.timeout_ns = kDefaultTimeoutNs;
-  size_t smem = gemm_smem_bytes(stages, acc_stages, sb);
-  int grid = d.sms;
-  if (pair) {
-    // persistent: as many pairs as can be resident at once (a TPC with a
-    // disabled SM cannot host one)
-    const int clusters = gemm_pair_max_clusters(mode, smem);
-    if (clusters > 0)
-      grid = 2 * (clusters < d.sms / 2 ? clusters : d.sms / 2);
-    else
-      pair = false;
-  }
-  if (!pair && nmax == 256 && !fp4) {
-    // fall back to one CTA per unit: recompute the per-CTA tiling
-    p.m_tiles = (mode == 0 ? s.I : s.H) / kBlockM;
-    const size_t sb1 = gemm_stage_bytes(mode == 0 ? 2 : 1, fp4, nmax);
-    p.acc_cols = static_cast<uint32_t>(mode == 0 ? 2 * nmax : nmax);
-    acc_stages = static_cast<int>(512 / p.acc_cols);
-    if (acc_stages > 4) acc_stages = 4;
-    if (acc_stages < 1) acc_stages = 1;
-    p.acc_stages = acc_stages;
-    p.tmem_cols = pow2_at_least(static_cast<uint32_t>(acc_stages) * p.acc_cols);
-    int st1 = static_cast<int>(budget / sb1);
-    if (st1 > 8) st1 = 8;
-    if (st1 < 2) return BEAM_ERR_UNSUPPORTED;
-    p.stages = st1;
-    smem = gemm_smem_bytes(st1, acc_stages, sb1);
-    grid = d.sms;
-  }
+  const size_t smem = gemm_smem_bytes(stages, acc_stages, sb);
+  // persistent: one CTA per SM, or as many pairs as can be resident at once
+  // (a TPC with a disabled SM cannot host one)
+  const int grid = pair ? 2 * (clusters < d.sms / 2 ? clusters : d.sms / 2) : d.sms;
   // activations in one box per k-block: the B tile's full height
   p.b_big_rows = pair ? nmax / 2 : nmax;
   if (!make_bf16_map(&maps.bb, mode == 0 ? static_cast<const void*>(xp) : static_cast<const void*>(h),
                      mode == 0 ? H : I, R_pad, static_cast<uint32_t>(p.b_big_rows)))
     return BEAM_ERR_CUDA;
   if (cudaMemsetAsync(p.sched, 0, sizeof(int), stream) != cudaSuccess) return BEAM_ERR_CUDA;
-  return cuda_status(launch_gemm(mode, fp4, pair, maps, p, grid, smem, stream));
+  return cuda_status(launch_gemm(mode, fp4, pair, wide, maps, p, grid, smem, stream));
 }
 
 beam_status_t run_combine(const beam_moe_shape_t& s, const float* w, void* y, bool y_bf16, void* ws, const Layout& L,
@@ -578,6 +584,57 @@ beam_status_t beam_moe_read_device_status(void* workspace, uint32_t* where, void
   if (cudaMemset(workspace, 0, sizeof(word)) != cudaSuccess) return BEAM_ERR_CUDA;
   if (where != nullptr) *where = word[1];
   return static_cast<beam_status_t>(word[0]);
+}
+
+beam_status_t beam_moe_pack_weights(const beam_moe_shape_t* shape, const beam_expert_weights_t* src,
+                                    beam_expert_weights_t* dst, void* stream) {
+  beam_status_t st = check_shape(shape);
+  if (st != BEAM_OK) return st;
+  if (src == nullptr || dst == nullptr || src->layout != BEAM_LAYOUT_ROWS || dst->dtype != src->dtype)
+    return BEAM_ERR_INVALID_ARG;
+  beam_expert_weights_t probe = *dst;
+  probe.layout = BEAM_LAYOUT_TILED;
+  st = check_weights(shape, src);
+  if (st == BEAM_OK) st = check_weights(shape, &probe);
+  if (st != BEAM_OK) return st;
+  const size_t E = kExperts, H = shape->H, I = shape->I;
+  const bool fp4 = src->dtype == BEAM_NVFP4;
+  // (array, rows, row bytes, tile row bytes) for gate, up, down [, their scales]
+  struct Job {
+    const void* s;
+    const void* d;
+    size_t rows, row_bytes;
+    uint32_t tile_row_bytes;
+  };
+  Job jobs[6];
+  int n = 0;
+  const uint32_t wb = fp4 ? kBlockK / 2 : kBlockK * 2;  // bytes of 64 K elements
+  auto row_bytes = [&](size_t K) { return fp4 ? K / 2 : K * 2; };
+  jobs[n++] = {src->gate, dst->gate, E * I, row_bytes(H), wb};
+  jobs[n++] = {src->up, dst->up, E * I, row_bytes(H), wb};
+  jobs[n++] = {src->down, dst->down, E * H, row_bytes(I), wb};
+  if (fp4) {
+    jobs[n++] = {src->gate_sf, dst->gate_sf, E * I, H / 16, kScaleBoxCols};
+    jobs[n++] = {src->up_sf, dst->up_sf, E * I, H / 16, kScaleBoxCols};
+    jobs[n++] = {src->down_sf, dst->down_sf, E * H, I / 16, kScaleBoxCols};
+  }
+  for (int j = 0; j < n; ++j) {
+    if (jobs[j].row_bytes % jobs[j].tile_row_bytes != 0 || jobs[j].rows % kBlockM != 0) return BEAM_ERR_UNSUPPORTED;
+    // the arrays must not overlap
+    const uintptr_t a = reinterpret_cast<uintptr_t>(jobs[j].s), b = reinterpret_cast<uintptr_t>(jobs[j].d);
+    const size_t len = jobs[j].rows * jobs[j].row_bytes;
+    if (a < b + len && b < a + len) return BEAM_ERR_INVALID_ARG;
+  }
+  DeviceInfo d;
+  if (!device_info(d)) return BEAM_ERR_CUDA;
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  for (int j = 0; j < n; ++j) {
+    const cudaError_t e = launch_pack_tiles(jobs[j].s, const_cast<void*>(jobs[j].d), jobs[j].rows, jobs[j].row_bytes,
+                                            jobs[j].tile_row_bytes, d.sms, cs);
+    if (e != cudaSuccess) return BEAM_ERR_CUDA;
+  }
+  dst->layout = BEAM_LAYOUT_TILED;
+  return BEAM_OK;
 }
 
 beam_status_t beam_moe_debug_timeout(void* workspace, size_t workspace_bytes, uint32_t timeout_us, void* stream) {

@@ -148,14 +148,16 @@ __device__ __forceinline__ void e2m1x8_to_bf16(uint32_t w, uint32_t scale2, uint
 // its 128 rows x N accumulator.  The even CTA issues the MMAs; both CTAs'
 // TMA loads signal the even CTA's full barrier; commits are multicast to
 // both CTAs; both epilogues release the even CTA's acc_empty barrier.
-template <int kMode, bool kFp4, bool kPair>
+// kWide (down, one CTA per unit, BF16): 256-row units of two 128-row tiles,
+// two accumulators, so each k-block carries eight MMAs in two chains.
+template <int kMode, bool kFp4, bool kPair, bool kWide = false>
 __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
     moe_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
   // Weight tiles per stage: gate/up always two (gate, up); down two on CTA
   // pairs (two 256-row halves of a 512-row unit sharing the token tile) and
   // for NVFP4 (two 128-row halves of a 256-row unit), so that every k-block
   // carries two accumulators' worth of MMAs.
-  constexpr int kNumA = (kMode == 0 || kPair || kFp4) ? 2 : 1;
+  constexpr int kNumA = (kMode == 0 || kPair || kFp4 || kWide) ? 2 : 1;
   constexpr int kRowsPerUnit = kPair ? (kMode == 0 ? 2 * kBlockM : 4 * kBlockM) : (kNumA == 2 && kMode == 1 ? 2 * kBlockM : kBlockM);
   // down with two tiles: feature offset of the second tile's rows
   constexpr int kHalfRows = kPair ? 2 * kBlockM : kBlockM;
@@ -280,6 +282,14 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
     return good != 0;
   };
 
+  // TMA coordinates of the weight box of rows [row, row + 128) and k-block kb
+  // (x_rows: its column in the row-major layout); tiled layout: box (i, kb)
+  // of the 128-row block i is tile i * k_blocks + kb, 128 rows of the tiled
+  // view.  Scale boxes cover four k-blocks.
+  auto a_y = [&](int row, int kb) { return p.a_tiled ? ((row >> 7) * p.k_blocks + kb) << 7 : row; };
+  auto a_x = [&](int x_rows) { return p.a_tiled ? 0 : x_rows; };
+  auto s_y = [&](int row, int kb) { return p.a_tiled ? ((row >> 7) * (p.k_blocks >> 2) + (kb >> 2)) << 7 : row; };
+
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -324,26 +334,29 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
             // both CTAs' bytes land on the even CTA's full barrier
             const uint32_t bar0 = mapa_shared(&full[stage], 0);
             if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * bytes);
-            tma_load_2d_pair(a_tile(stage, 0), &maps.a0, bar0, kx, a_row);
+            tma_load_2d_pair(a_tile(stage, 0), &maps.a0, bar0, a_x(kx), a_y(a_row, kb));
             if (kMode == 0)
-              tma_load_2d_pair(a_tile(stage, 1), &maps.a1, bar0, kx, a_row);
+              tma_load_2d_pair(a_tile(stage, 1), &maps.a1, bar0, a_x(kx), a_y(a_row, kb));
             else  // second 256-row half of the down unit
-              tma_load_2d_pair(a_tile(stage, 1), &maps.a0, bar0, kx, a_row + 2 * kBlockM);
+              tma_load_2d_pair(a_tile(stage, 1), &maps.a0, bar0, a_x(kx), a_y(a_row + 2 * kBlockM, kb));
             for (int b = 0; b < nbox; ++b)
               tma_load_2d_pair_hint(b_tile(stage) + b * kBoxBytes, bmap, bar0, kx, b_row0 + b * box_rows, pol_x);
           } else {
             mbar_arrive_expect_tx(&full[stage], bytes);
             if (kFp4) {
-              const int sx = (kb >> 2) * static_cast<int>(kScaleBoxCols);
+              const int sx = a_x((kb >> 2) * static_cast<int>(kScaleBoxCols));
               // gate/up: gate and up tiles of the same rows; down: rows a_row and a_row + 128
               const int a_row1 = kMode == 0 ? a_row : a_row + kHalfRows;
-              tma_load_2d_nohint(p_tile(stage, 0), &maps.a0, &full[stage], kx / 2, a_row);
-              tma_load_2d_nohint(s_tile(stage, 0), &maps.s0, &full[stage], sx, a_row);
-              tma_load_2d_nohint(p_tile(stage, 1), &maps.a1, &full[stage], kx / 2, a_row1);
-              tma_load_2d_nohint(s_tile(stage, 1), &maps.s1, &full[stage], sx, a_row1);
+              tma_load_2d_nohint(p_tile(stage, 0), &maps.a0, &full[stage], a_x(kx / 2), a_y(a_row, kb));
+              tma_load_2d_nohint(s_tile(stage, 0), &maps.s0, &full[stage], sx, s_y(a_row, kb));
+              tma_load_2d_nohint(p_tile(stage, 1), &maps.a1, &full[stage], a_x(kx / 2), a_y(a_row1, kb));
+              tma_load_2d_nohint(s_tile(stage, 1), &maps.s1, &full[stage], sx, s_y(a_row1, kb));
             } else {
-              tma_load_2d_nohint(a_tile(stage, 0), &maps.a0, &full[stage], kx, a_row);
-              if (kMode == 0) tma_load_2d_nohint(a_tile(stage, 1), &maps.a1, &full[stage], kx, a_row);
+              tma_load_2d_nohint(a_tile(stage, 0), &maps.a0, &full[stage], a_x(kx), a_y(a_row, kb));
+              // gate/up: the up tile of the same rows; wide down: rows a_row + 128 (a1 = a0)
+              if (kNumA == 2)
+                tma_load_2d_nohint(a_tile(stage, 1), &maps.a1, &full[stage], a_x(kx),
+                                   a_y(kMode == 0 ? a_row : a_row + kHalfRows, kb));
             }
             for (int b = 0; b < nbox; ++b)
               tma_load_2d(b_tile(stage) + b * kBoxBytes, bmap, &full[stage], kx, U.start + b * box_rows, pol_x);
@@ -410,7 +423,7 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
                 mma_bf16_pair(d1, da1 + 2u * k, db + 2u * k, idesc, accumulate);
               } else {
                 mma_bf16(d0, da0 + 2u * k, db + 2u * k, idesc, accumulate);
-                if (kMode == 0) mma_bf16(d1, da1 + 2u * k, db + 2u * k, idesc, accumulate);
+                if (kNumA == 2) mma_bf16(d1, da1 + 2u * k, db + 2u * k, idesc, accumulate);
               }
             }
           }
@@ -630,9 +643,9 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
   }
 }
 
-template <int kMode, bool kFp4, bool kPair>
+template <int kMode, bool kFp4, bool kPair, bool kWide = false>
 cudaError_t launch_one(const GemmMaps& maps, const GemmParams& p, int grid, size_t smem_bytes, cudaStream_t stream) {
-  auto kern = moe_gemm_kernel<kMode, kFp4, kPair>;
+  auto kern = moe_gemm_kernel<kMode, kFp4, kPair, kWide>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_bytes));
   if (err != cudaSuccess) return err;
   if (!kPair) {
@@ -688,7 +701,7 @@ int gemm_pair_max_clusters(int mode, size_t smem_bytes) {
   return n;
 }
 
-cudaError_t launch_gemm(int mode, bool fp4, bool pair, const GemmMaps& maps, const GemmParams& p, int grid,
+cudaError_t launch_gemm(int mode, bool fp4, bool pair, bool wide, const GemmMaps& maps, const GemmParams& p, int grid,
                         size_t smem_bytes, cudaStream_t stream) {
   if (pair) {
     if (fp4) return cudaErrorInvalidValue;
@@ -698,8 +711,9 @@ cudaError_t launch_gemm(int mode, bool fp4, bool pair, const GemmMaps& maps, con
   if (mode == 0)
     return fp4 ? launch_one<0, true, false>(maps, p, grid, smem_bytes, stream)
                : launch_one<0, false, false>(maps, p, grid, smem_bytes, stream);
-  return fp4 ? launch_one<1, true, false>(maps, p, grid, smem_bytes, stream)
-             : launch_one<1, false, false>(maps, p, grid, smem_bytes, stream);
+  if (fp4) return launch_one<1, true, false>(maps, p, grid, smem_bytes, stream);
+  return wide ? launch_one<1, false, false, true>(maps, p, grid, smem_bytes, stream)
+              : launch_one<1, false, false>(maps, p, grid, smem_bytes, stream);
 }
 
 }  // namespace beam

@@ -25,6 +25,7 @@ constexpr uint32_t kPackedTileBytes = kBlockM * kBlockK / 2;  // NVFP4: 128 rows
 constexpr uint32_t kScaleBoxCols = 16;                       // NVFP4: scale bytes per TMA box row (4 k-blocks)
 constexpr uint32_t kScaleTileBytes = kBlockM * kScaleBoxCols;  // NVFP4: 2 KiB
 constexpr int kMaxAStages = 8;     // NVFP4: BF16 weight tiles in TMEM in flight (at most)
+constexpr int kMaxStages = 8;      // shared-memory ring depth
 constexpr int kChunkRowsBf16 = 256;  // routes per GEMM unit (BF16 weights)
 constexpr int kChunkRowsFp4 = 160;   // NVFP4: TMEM holds the accumulators and the weight tiles
 
@@ -62,6 +63,7 @@ struct GemmParams {
   uint32_t acc_cols;            // TMEM columns per accumulator buffer
   uint32_t tmem_cols;           // TMEM columns allocated (power of two)
   int b_big_rows;               // rows of the bb box (the B tile's capacity: nmax, or nmax / 2 for CTA pairs)
+  int a_tiled;                  // weights (codes, scales) in BEAM_LAYOUT_TILED: every box is one contiguous tile
   int a_stages;                 // NVFP4: BF16 weight tiles in TMEM (ring depth)
   uint32_t a_col0;              // NVFP4: first TMEM column of that ring
   int* sched;                   // unit counter (zeroed before the launch)
@@ -117,7 +119,8 @@ cudaError_t launch_dispatch(const int32_t* ids, int R, int n_tiles, int32_t* til
                             int32_t* perm, int32_t* pos, cudaStream_t stream);
 cudaError_t launch_gather(const void* x, bool x_bf16, int H, const int32_t* pos, int T,
                           __nv_bfloat16* xp, int num_sms, cudaStream_t stream);
-cudaError_t launch_gemm(int mode, bool fp4, bool pair, const GemmMaps& maps, const GemmParams& p, int grid,
+// wide: BF16 down on one CTA per unit with 256-row units (two tiles per k-block)
+cudaError_t launch_gemm(int mode, bool fp4, bool pair, bool wide, const GemmMaps& maps, const GemmParams& p, int grid,
                         size_t smem_bytes, cudaStream_t stream);
 size_t gemm_smem_bytes(int stages, int acc_stages, size_t stage_bytes);
 // Clusters of two CTAs of the pair kernel that can be resident at once (0: none).
@@ -125,5 +128,10 @@ int gemm_pair_max_clusters(int mode, size_t smem_bytes);
 cudaError_t launch_combine(const __nv_bfloat16* yr, const int32_t* pos, const float* w, int T, int H,
                            void* y, bool y_bf16, cudaStream_t stream);
 cudaError_t launch_debug_timeout(uint32_t* status, uint64_t timeout_ns, cudaStream_t stream);
+// Regroup `rows` x `row_bytes` (row-major) into contiguous tiles of 128 rows
+// x `tile_row_bytes` (pack.cu); rows % 128 == 0, row_bytes % tile_row_bytes
+// == 0, tile_row_bytes % 16 == 0.
+cudaError_t launch_pack_tiles(const void* src, void* dst, size_t rows, size_t row_bytes, uint32_t tile_row_bytes,
+                              int num_sms, cudaStream_t stream);
 
 }  // namespace beam

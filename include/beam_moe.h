@@ -62,6 +62,19 @@ typedef struct {
   float routed_scale;
 } beam_moe_shape_t;
 
+/* Storage order of the expert weight arrays (codes and block scales for
+ * NVFP4; the global scales are always [E]).
+ *   BEAM_LAYOUT_ROWS : row-major as described at beam_expert_weights_t.
+ *   BEAM_LAYOUT_TILED: the same bytes regrouped so that every tile the GEMMs
+ *     load is contiguous: the matrix of R = E*N rows (N = I for gate / up, H
+ *     for down) and B bytes per row is cut into tiles of 128 rows x b bytes,
+ *     b = 128 for BF16 (64 elements), 32 for E2M1 codes (64 elements), 16 for
+ *     E4M3 scales (256 elements); tile (i, j) (rows 128i.., bytes bj..) is
+ *     stored at byte (i * B/b + j) * 128 * b, its rows b bytes apart.  Made by
+ *     beam_moe_pack_weights; streams ~3% faster from HBM (each tile is one
+ *     contiguous block instead of 128 pieces). */
+typedef enum { BEAM_LAYOUT_ROWS = 0, BEAM_LAYOUT_TILED = 1 } beam_weight_layout_t;
+
 /* Expert weights, all experts stacked, linear-layer orientation [out, in]:
  *   BF16 : gate [E, I, H], up [E, I, H], down [E, H, I]  (bf16 elements)
  *   NVFP4: gate/up [E, I, H/2], down [E, H, I/2] bytes, two E2M1 codes per
@@ -69,6 +82,7 @@ typedef struct {
  *          [E, I, H/16] / [E, H, I/16], one per 16 consecutive K elements;
  *          *_gs = FP32 global scale per expert and matrix [E].
  *          Element value = e2m1 * e4m3 * global.
+ * (in `layout` order; BEAM_LAYOUT_ROWS when the field is zero-initialised).
  * Pointers the dtype does not use must be NULL. */
 typedef struct {
   beam_dtype_t dtype; /* BEAM_BF16 or BEAM_NVFP4 */
@@ -81,6 +95,7 @@ typedef struct {
   const float* gate_gs;
   const float* up_gs;
   const float* down_gs;
+  beam_weight_layout_t layout;
 } beam_expert_weights_t;
 
 /* Where the intermediates of the last call live inside the workspace (byte
@@ -183,6 +198,18 @@ beam_status_t beam_moe_forward_stage(const beam_moe_shape_t* shape, const beam_m
  * x, T >= 512) a kernel that splits the router weight into BF16 terms; the
  * dispatch is two kernels; -1 on an unsupported shape or stage. */
 int32_t beam_moe_stage_kernel_count(const beam_moe_shape_t* shape, beam_dtype_t xdtype, beam_stage_t stage);
+
+/* Regroup row-major expert weights into BEAM_LAYOUT_TILED (a one-time step
+ * when loading a model; not part of the Beam post's method, which fixes the
+ * arithmetic, not the storage).  `src`: layout BEAM_LAYOUT_ROWS; `dst`: the
+ * same dtype, caller-allocated arrays of the same sizes (gate, up, down and,
+ * for NVFP4, the three scale arrays; dst's global-scale pointers are used as
+ * given and may alias src's); dst->layout is set to BEAM_LAYOUT_TILED.  The
+ * arrays must not overlap.  Async on `stream`.  Errors as for the forward
+ * call's weights; BEAM_ERR_UNSUPPORTED unless N and K are multiples of 128 / 64
+ * elements (BF16) or 128 / 256 (NVFP4). */
+beam_status_t beam_moe_pack_weights(const beam_moe_shape_t* shape, const beam_expert_weights_t* src,
+                                    beam_expert_weights_t* dst, void* stream);
 
 /* Synchronises `stream`, returns the device status word of `workspace`
  * (BEAM_OK when no kernel reported a problem) and clears it.  `where`

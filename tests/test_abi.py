@@ -149,3 +149,40 @@ def test_missing_library_fails_loudly(tmp_path, monkeypatch):
     monkeypatch.setattr(moe, "_lib", None)
     with pytest.raises(ImportError):
         moe.load()
+
+
+def test_pack_weights_argument_errors(lib):
+    sh = _shape(T=16, H=256, I=256)
+    src = moe._ExpertWeights()
+    src.dtype = moe.BEAM_BF16
+    src.gate, src.up, src.down = 0x100000, 0x2000000, 0x4000000
+    dst = moe._ExpertWeights()
+    dst.dtype = moe.BEAM_BF16
+    dst.gate, dst.up, dst.down = 0x10000000, 0x12000000, 0x14000000
+
+    def call(s, d):
+        return lib.beam_moe_pack_weights(ctypes.byref(sh), ctypes.byref(s), ctypes.byref(d), None)
+
+    src.layout = moe.BEAM_LAYOUT_TILED  # the source must be row-major
+    assert call(src, dst) == moe.BEAM_ERR_INVALID_ARG
+    src.layout = moe.BEAM_LAYOUT_ROWS
+    dst.dtype = moe.BEAM_NVFP4  # dtypes must agree
+    assert call(src, dst) == moe.BEAM_ERR_INVALID_ARG
+    dst.dtype = moe.BEAM_BF16
+    dst.up = 0x100000 + 4096  # overlaps src.gate (256 x 256 x 256 x 2 bytes)
+    assert call(src, dst) == moe.BEAM_ERR_INVALID_ARG
+    src.layout = 7  # not a layout
+    dst.up = 0x12000000
+    assert call(src, dst) == moe.BEAM_ERR_INVALID_ARG
+
+
+def test_forward_rejects_unknown_layout(lib):
+    sh = _shape()
+    ew = moe._ExpertWeights()
+    ew.dtype = moe.BEAM_BF16
+    ew.gate, ew.up, ew.down = 0x1000, 0x2000, 0x3000
+    ew.layout = 2
+    n = moe.workspace_size(sh)
+    rc = lib.beam_moe_forward(ctypes.byref(sh), 0x10000, moe.BEAM_BF16, 0x20000, None, ctypes.byref(ew), 0x50000,
+                              0x30000, 0x40000, 0x100000, n, None)
+    assert rc == moe.BEAM_ERR_INVALID_ARG

@@ -310,14 +310,19 @@ def beam_moe_debug_timeout(workspace, timeout_us: int, stream=None):
 # --------------------------------------------------------------------------
 class BeamMoE:
     """One MoE layer: router weight/bias, expert weights and a workspace sized
-    for up to ``max_tokens`` tokens, all caller-owned torch device tensors."""
+    for up to ``max_tokens`` tokens, all caller-owned torch device tensors.
+    ``pack=True`` regroups row-major expert weights once into the tiled
+    layout (a copy; the given arrays are not modified)."""
 
-    def __init__(self, router_w, router_bias, weights: dict, max_tokens: int, routed_scale=2.5):
-        self.router_w, self.router_bias, self.weights = router_w, router_bias, weights
+    def __init__(self, router_w, router_bias, weights: dict, max_tokens: int, routed_scale=2.5, pack=False):
+        self.router_w, self.router_bias = router_w, router_bias
         self.E, self.H = router_w.shape
         self.I = weights["gate"].shape[1]
         self.routed_scale = routed_scale
         self.max_tokens = max_tokens
+        if pack and weights.get("layout", "rows") == "rows":
+            weights = pack_weights(self.shape(max_tokens), weights)
+        self.weights = weights
         self.workspace = alloc_workspace(self.shape(max_tokens), _wdtype(weights), router_w.device)
 
     def shape(self, T):

@@ -60,7 +60,12 @@ namespace {
 constexpr int kEpilogueWarps = 8;
 constexpr int kConvertWarps = 8;
 constexpr int kThreadsBf16 = 32 * (2 + kEpilogueWarps);
-constexpr int kThreadsFp4 = 32 * (2 + kEpilogueWarps + kConvertWarps);
+// NVFP4: a second MMA-issuing warp (after the converters): one thread issues
+// the first tile's MMAs (gate, or the first row half), the other the
+// second's, each its own accumulator chain, so MMA issue is not bound by one
+// thread's instruction rate at N ~ 144.
+constexpr int kMma2Warp = 2 + kEpilogueWarps + kConvertWarps;
+constexpr int kThreadsFp4 = 32 * (kMma2Warp + 1);
 constexpr uint32_t kATileBytes = kBlockM * kBlockK * 2;     // 16 KiB of BF16
 constexpr uint32_t kBoxBytes = kBoxRows * kBlockK * 2;      // 4 KiB
 constexpr int kSchedRing = 8;                               // scheduled unit indices in flight
@@ -165,7 +170,8 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
   // Roles that read every scheduled unit index (they release ring slots).
   constexpr uint32_t kRingConsumers =
       kPair ? (1 + kEpilogueWarps) + (1 + kEpilogueWarps)  // even CTA: MMA + epilogue; odd: producer + epilogue
-            : 1 + kEpilogueWarps + (kFp4 ? kConvertWarps : 0);
+            : 1 + kEpilogueWarps + (kFp4 ? kConvertWarps + 1 : 0);
+  constexpr uint32_t kIssuers = kFp4 ? 2 : 1;  // MMA-issuing threads: commits per k-block / unit
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t b_tile_bytes = static_cast<uint32_t>(kPair ? p.nmax / 2 : p.nmax) * kBlockK * 2;
@@ -198,14 +204,14 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], kIssuers);
     }
     for (int a = 0; a < kMaxAStages; ++a) mbar_init(&afull[a], kConvertWarps / 2);  // one converter group per k-block
     for (int a = 0; a < p.acc_stages; ++a) {
-      mbar_init(&acc_full[a], 1);
+      mbar_init(&acc_full[a], kIssuers);
       mbar_init(&acc_empty[a], kPair ? 2 * kEpilogueWarps : kEpilogueWarps);
     }
-    mbar_init(drain, 1);
+    mbar_init(drain, kIssuers);
     for (int r = 0; r < kSchedRing; ++r) {
       mbar_init(&ufull[r], 1);
       mbar_init(&uempty[r], kRingConsumers);
@@ -377,8 +383,9 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
         mbar_wait(&full[s], par, p.timeout_ns, nullptr, p.status, kWhereDrain);
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 || (kFp4 && warp == kMma2Warp)) {
     // ------------------------------------------------------------ MMA issuer
+    const int issuer = warp == 1 ? 0 : 1;  // NVFP4: which tile's MMAs this thread issues
     if (lane == 0 && rank == 0) {
       int stage = 0, acc = 0, astage = 0;
       uint32_t phase = 0, acc_phase = 0, aphase = 0;
@@ -409,8 +416,8 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
 #pragma unroll
             for (int k = 0; k < kBlockK / 16; ++k) {
               const uint32_t accumulate = (kb | k) != 0 ? 1u : 0u;
-              mma_bf16_ts(d0, ta + 8u * k, db + 2u * k, idesc, accumulate);
-              mma_bf16_ts(d1, ta + kBlockK / 2 + 8u * k, db + 2u * k, idesc, accumulate);
+              mma_bf16_ts(issuer == 0 ? d0 : d1, ta + static_cast<uint32_t>(issuer * (kBlockK / 2)) + 8u * k,
+                          db + 2u * k, idesc, accumulate);
             }
           } else {
             const uint64_t da0 = sdesc_k_sw128(smem_u32(a_tile(stage, 0)));
@@ -546,7 +553,7 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
         acc_phase ^= 1u;
       }
     }
-  } else if (kFp4) {
+  } else if (kFp4 && warp < kMma2Warp) {
     // ------------------------------------------------------------ converters
     // Warp w may write TMEM lanes 32*(w%4)..+31, so its lane i expands weight
     // row 32*(w%4)+i.  Warps 10-13 take the even k-blocks (counted over all

@@ -142,6 +142,7 @@ __global__ void __launch_bounds__(256) gather_kernel(const void* x, int H, const
                                                      __nv_bfloat16* xp) {
   const int vecs_per_row = H / 8;
   const size_t n = static_cast<size_t>(T) * vecs_per_row;
+#pragma unroll 2
   for (size_t v = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; v < n;
        v += static_cast<size_t>(gridDim.x) * blockDim.x) {
     const int t = static_cast<int>(v / vecs_per_row);
@@ -189,7 +190,7 @@ cudaError_t launch_gather(const void* x, bool x_bf16, int H, const int32_t* pos,
                           int num_sms, cudaStream_t stream) {
   const size_t n = static_cast<size_t>(T) * (H / 8);
   size_t blocks = (n + 255) / 256;
-  const size_t cap = static_cast<size_t>(num_sms) * 8;
+  const size_t cap = static_cast<size_t>(num_sms) * 16;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   if (x_bf16)

@@ -213,35 +213,54 @@ def measure(wl, steps, warmup, dev, world, sampler_index):
 
 
 def measure_e2e(wl, state, steps, warmup, dev):
-    """Same step through the public call with host buffers: pinned x copied in,
-    y / ids / weights copied out, every step, inside the timed region."""
+    """Same step through the public call with host buffers: every step copies
+    its x in from pinned host memory and its y / ids / weights out, inside the
+    timed region.  As a serving loop would, the copies run on two copy streams
+    with double-buffered device and host buffers, so step i+1's input copy and
+    step i-1's output copy overlap step i's compute."""
+    import group_limited_routing_03_b300 as moe
+
     d, sh, ws, y, ids, w, call = state
-    x_dev = d["x"]
-    x_host = x_dev.cpu().pin_memory()
-    y_host = torch.empty(y.shape, dtype=y.dtype).pin_memory()
-    ids_host = torch.empty(ids.shape, dtype=ids.dtype).pin_memory()
-    w_host = torch.empty(w.shape, dtype=w.dtype).pin_memory()
-    stream = torch.cuda.current_stream()
+    comp = torch.cuda.current_stream()
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    x_host = [d["x"].cpu().pin_memory() for _ in range(2)]
+    x_dev = [torch.empty_like(d["x"]) for _ in range(2)]
+    outs = [(torch.empty_like(y), torch.empty_like(ids), torch.empty_like(w)) for _ in range(2)]
+    outs_host = [tuple(torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in o) for o in outs]
+    calls = [moe.ForwardCall(sh, x_dev[b], d["router_w"], d.get("bias"), call.weights, *outs[b], ws) for b in range(2)]
+    ev = {k: [torch.cuda.Event() for _ in range(2)] for k in ("h2d", "comp", "d2h")}
 
-    def step():
-        x_dev.copy_(x_host, non_blocking=True)
-        call.run()
-        y_host.copy_(y, non_blocking=True)
-        ids_host.copy_(ids, non_blocking=True)
-        w_host.copy_(w, non_blocking=True)
+    def step(i):
+        b = i % 2
+        with torch.cuda.stream(s_in):
+            if i >= 2:
+                s_in.wait_event(ev["comp"][b])  # the slot's previous step no longer reads x
+            x_dev[b].copy_(x_host[b], non_blocking=True)
+            ev["h2d"][b].record(s_in)
+        comp.wait_event(ev["h2d"][b])
+        if i >= 2:
+            comp.wait_event(ev["d2h"][b])  # the slot's previous outputs have been read out
+        calls[b].run()
+        ev["comp"][b].record(comp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev["comp"][b])
+            for dst, src in zip(outs_host[b], outs[b]):
+                dst.copy_(src, non_blocking=True)
+            ev["d2h"][b].record(s_out)
 
-    for _ in range(warmup):
-        step()
+    for i in range(warmup):
+        step(i)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(steps):
-        step()
-    e1.record(stream)
+    e0.record(comp)
+    for i in range(steps):
+        step(i)
+    comp.wait_event(ev["d2h"][(steps - 1) % 2])  # the last step's results are on the host
+    e1.record(comp)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1)
-    h2d = x_host.numel() * x_host.element_size()
-    d2h = sum(t.numel() * t.element_size() for t in (y_host, ids_host, w_host))
+    h2d = x_host[0].numel() * x_host[0].element_size()
+    d2h = sum(t.numel() * t.element_size() for t in outs_host[0])
     return ms, h2d, d2h
 
 

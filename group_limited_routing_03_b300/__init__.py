@@ -248,6 +248,7 @@ class ForwardCall:
                            None if router_bias is None else _ptr(router_bias).value, ctypes.pointer(self._ew),
                            _ptr(y).value, _ptr(topk_ids).value, _ptr(topk_w).value)
         self._keep = (x, router_w, router_bias, weights, y, topk_ids, topk_w, workspace)
+        self.weights = weights
         self._ws = _ptr(workspace)
         self._ws_bytes = workspace.numel()
         self._stream = _stream(stream)

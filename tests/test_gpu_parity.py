@@ -71,7 +71,7 @@ def test_forward_small_all_tokens(T, H, I, x_dtype):
     assert err <= Y_TOL["bf16"], err
 
 
-@pytest.mark.parametrize("T,H,I", [(300, 512, 256), (40, 256, 512)])
+@pytest.mark.parametrize("T,H,I", [(300, 512, 256), (40, 256, 512), (1, 256, 256), (257, 256, 256)])
 def test_forward_nvfp4_small_all_tokens(T, H, I):
     """NVFP4 experts (E2M1 codes, E4M3 block scales, FP32 global scale),
     dequantised in shared memory, BF16 activations."""

@@ -12,7 +12,9 @@ written from the Beam launch post:
   experts inside them, normalised weights times 2.5, no shared expert,
   SwiGLU experts (intermediate 2560, hidden 5120);
 * the same post, section "Residual Stream" -- router and SwiGLU product in
-  FP32 (the oracle uses double, the exact definition);
+  FP32 (the oracle uses double, the exact definition); the stream update
+  sqrt((k-1)/k) * stream + output / sqrt(k) at step k, sublayer outputs
+  normalised (RMSNorm) after the sublayer;
 * the Chinese translation "Reflection 发布 501B 开放模型 Beam ..."
   (sihot.dev), section 混合专家, says the same.
 
@@ -26,6 +28,12 @@ Parity status of each function (what pins it is in ``tests/test_oracle_*``):
 * ``expert_ffn``   pinned: numpy matmul on decoded weights, closed forms.
 * ``combine``      pinned: identical-expert closed form, zero input.
 * ``dispatch``     pinned: numpy stable argsort / bincount.
+* ``residual_update`` pinned: the post's own statements -- the two weights'
+                   squares sum to one (unit-RMS stream and normalised output on
+                   disjoint supports keep unit RMS at every step), and after
+                   the steps 2..105 the embedding and every normalised output
+                   carry the same weight 1/sqrt(105); closed forms of RMSNorm
+                   (constant rows, with and without eps).
 * decoders         pinned: torch float8_e4m3fn conversion (all 256 codes),
                    the OCP E2M1 value table.
 """
@@ -71,6 +79,8 @@ def _load():
         lib.oracle_expert_ffn.restype = i32
         lib.oracle_combine.argtypes = [i64, i32, i64, vp, vp, vp]
         lib.oracle_combine.restype = i32
+        lib.oracle_residual_update.argtypes = [i64, i64, vp, vp, vp, dbl, i32, vp]
+        lib.oracle_residual_update.restype = i32
         lib.oracle_dispatch.argtypes = [i64, i32, vp, vp, vp, vp, vp]
         lib.oracle_dispatch.restype = i32
         for name in ("oracle_decode_bf16", "oracle_decode_e4m3", "oracle_decode_e2m1"):
@@ -185,6 +195,25 @@ def combine(weights, o):
     if rc != 0:
         raise ValueError(f"oracle_combine failed ({rc})")
     return y
+
+
+def residual_update(y, stream, w, eps, k):
+    """The stream after the MoE sublayer at step k (section "Residual Stream"):
+    sqrt((k-1)/k) * stream + RMSNorm(y) * w / sqrt(k), in double.  y f64[n,H];
+    stream f64[n,H], f32, or uint16 BF16 bits; w f64/f32[H]."""
+    lib = _load()
+    y = np.ascontiguousarray(y, dtype=np.float64)
+    n, H = y.shape
+    stream = np.asarray(stream)
+    if stream.dtype == np.uint16:  # BF16 bits: the upper half of an FP32 pattern (exact)
+        stream = (stream.astype(np.uint32) << 16).view(np.float32)
+    stream = np.ascontiguousarray(stream, dtype=np.float64).reshape(n, H)
+    w = np.ascontiguousarray(w, dtype=np.float64).reshape(H)
+    out = np.zeros((n, H), np.float64)
+    rc = lib.oracle_residual_update(n, H, _ptr(y), _ptr(stream), _ptr(w), ctypes.c_double(eps), int(k), _ptr(out))
+    if rc != 0:
+        raise ValueError(f"oracle_residual_update failed ({rc})")
+    return out
 
 
 def dispatch(ids, n_experts=256):

@@ -377,6 +377,31 @@ int oracle_combine(int64_t n, int K, int64_t H, const double* weights, const dou
 }
 
 /*
+ * oracle_residual_update: the step that follows the MoE sublayer in the
+ * residual stream (Beam launch post, section "Residual Stream"): the input
+ * embedding is step 1; at step k >= 2 the stream is kept with weight
+ * sqrt((k-1)/k) and the sublayer output is added with weight 1/sqrt(k), the
+ * two weights' squares summing to one.  Every sublayer's output is
+ * normalised after the sublayer (the post names RMSNorm as its norm); here,
+ * in double:
+ *   yn[t, j]  = y[t, j] / sqrt(mean_j' y[t, j']^2 + eps) * w[j]
+ *   out[t, j] = sqrt((k-1)/k) * stream[t, j] + yn[t, j] / sqrt(k)
+ */
+int oracle_residual_update(int64_t n, int64_t H, const double* y, const double* stream, const double* w, double eps,
+                           int k, double* out) {
+  if (n < 0 || H <= 0 || k < 2 || !(eps >= 0.0)) return -1;
+  const double keep = sqrt((double)(k - 1) / (double)k), add = 1.0 / sqrt((double)k);
+  for (int64_t t = 0; t < n; ++t) {
+    double ss = 0.0;
+    for (int64_t j = 0; j < H; ++j) ss += y[t * H + j] * y[t * H + j];
+    const double inv = 1.0 / sqrt(ss / (double)H + eps);
+    for (int64_t j = 0; j < H; ++j)
+      out[t * H + j] = keep * stream[t * H + j] + y[t * H + j] * inv * w[j] * add;
+  }
+  return 0;
+}
+
+/*
  * oracle_dispatch: per-expert route lists implied by "each token runs only
  * its 8 experts".  Route r = t*K + k goes to expert ids[r].
  *   counts  [E]    routes per expert

@@ -346,3 +346,64 @@ def test_workload_shapes_match_published_figures():
     moe_layers = g["decoder_layers"] - g["dense_mlp_layers"]
     share = moe_layers * wl.E * per_expert / g["total_params"] * 100
     assert abs(share - g["expert_share_of_params_percent"]) < 0.1
+
+
+# ---------------------------------------------------------------------------
+# residual stream update after the MoE sublayer (section "Residual Stream")
+# ---------------------------------------------------------------------------
+def test_residual_equal_weights_after_all_additions():
+    """The post: the embedding is step 1, each of the 104 additions (steps
+    2..105) adds a sublayer output with weight 1/sqrt(k) and keeps the stream
+    with sqrt((k-1)/k), so in the final state the embedding and every output
+    carry the same weight.  With already-normalised outputs (unit RMS, w = 1,
+    eps = 0) the oracle's normalisation is the identity and the final state
+    must be (e + sum_k y_k) / sqrt(105)."""
+    rng = np.random.default_rng(7)
+    H = 64
+    e = rng.standard_normal((3, H))
+    ys = rng.standard_normal((104, 3, H))
+    ys /= np.sqrt((ys ** 2).mean(axis=2, keepdims=True))  # unit RMS rows
+    w = np.ones(H)
+    s = e.copy()
+    for k in range(2, 106):
+        s = oracle.residual_update(ys[k - 2], s, w, 0.0, k)
+    np.testing.assert_allclose(s, (e + ys.sum(axis=0)) / np.sqrt(105.0), rtol=0, atol=1e-12)
+
+
+def test_residual_weights_squares_sum_to_one():
+    """A unit-RMS stream and a normalised output on disjoint supports: the
+    new stream keeps unit RMS at every step k (the squares of the two
+    weights sum to one)."""
+    H = 128
+    stream = np.zeros((1, H))
+    stream[0, : H // 2] = np.sqrt(2.0) * np.where(np.arange(H // 2) % 2 == 0, 1.0, -1.0)  # RMS 1 over H
+    y = np.zeros((1, H))
+    y[0, H // 2:] = np.linspace(-3.0, 5.0, H // 2)
+    w = np.ones(H)
+    for k in (2, 3, 10, 57, 105):
+        out = oracle.residual_update(y, stream, w, 0.0, k)
+        assert abs(np.sqrt((out ** 2).mean()) - 1.0) < 1e-12, k
+
+
+def test_residual_rmsnorm_closed_forms():
+    """Constant rows: RMSNorm(c) = c / sqrt(c^2 + eps); with a zero stream and
+    the learned scale w the output is w * c / sqrt(c^2 + eps) / sqrt(k); the
+    stream alone is scaled by sqrt((k-1)/k)."""
+    H = 32
+    w = np.linspace(0.5, 2.0, H)
+    for c, eps, k in ((3.0, 0.0, 2), (-0.25, 1e-6, 5), (1e-3, 1e-6, 105)):
+        y = np.full((1, H), c)
+        out = oracle.residual_update(y, np.zeros((1, H)), w, eps, k)
+        np.testing.assert_allclose(out[0], w * c / np.sqrt(c * c + eps) / np.sqrt(k), rtol=1e-13)
+        st = np.arange(H, dtype=np.float64)[None] - 7.0
+        out = oracle.residual_update(np.zeros((1, H)), st, w, max(eps, 1e-6), k)  # y = 0 adds nothing
+        np.testing.assert_allclose(out, st * np.sqrt((k - 1) / k), rtol=1e-15)
+
+
+def test_residual_bf16_stream_bits():
+    """A stream given as BF16 bits is read as its exact values."""
+    bits = np.array([[0x3F80, 0xC000, 0x4049, 0x0000]], dtype=np.uint16)  # 1, -2, 3.140625, 0
+    vals = np.array([[1.0, -2.0, 3.140625, 0.0]])
+    y = np.zeros((1, 4))
+    out = oracle.residual_update(y, bits, np.ones(4), 1e-6, 4)
+    np.testing.assert_allclose(out, vals * np.sqrt(3 / 4), rtol=1e-15)

@@ -149,6 +149,7 @@ class ClockSampler:
 # our arm
 # ---------------------------------------------------------------------------
 WEIGHTS_LAYOUT = "tiled"  # set from --weights-layout
+RESIDUAL_STEP = 105  # step of the stream at the last sublayer of a 52-layer stack
 
 
 def make_layer(wl, dev, layout=None):
@@ -172,12 +173,22 @@ def make_layer(wl, dev, layout=None):
     return d, sh, ws, y, ids, w, call
 
 
-def measure(wl, steps, warmup, dev, world, sampler_index):
+def measure(wl, steps, warmup, dev, world, sampler_index, state=None, residual_step=None):
     """Device-timed steps through the per-stage C-ABI calls, events between
-    the stages on the launching stream.  Returns a dict of timings."""
+    the stages on the launching stream.  Returns a dict of timings.  With
+    ``residual_step`` k the combine stage also applies the post-norm residual
+    update at step k, in place on a seeded stream (no y written), reusing the
+    layer of ``state``."""
     import group_limited_routing_03_b300 as moe
+    from group_limited_routing_03_b300 import inputs
 
-    d, sh, ws, y, ids, w, call = make_layer(wl, dev)
+    if state is None:
+        state = make_layer(wl, dev)
+    d, sh, ws, y, ids, w, call = state
+    if residual_step is not None:
+        resid, g = inputs.residual_inputs(wl, dev)
+        call = moe.ForwardCall(sh, d["x"], d["router_w"], d.get("bias"), call.weights, None, ids, w, ws,
+                               residual=(resid, resid, g, inputs.RESIDUAL_EPS, residual_step))
     stream = torch.cuda.current_stream()
     for _ in range(warmup):
         for i in range(len(STAGES)):
@@ -209,7 +220,26 @@ def measure(wl, steps, warmup, dev, world, sampler_index):
     launches = sum(moe.beam_moe_stage_kernel_count(sh, i, xdt) for i in range(len(STAGES)))
     out = dict(total_ms=total_ms, stage_ms=stage_ms, touched=touched, launches_per_step=launches,
                clocks=clk.summary(), counts=torch.bincount(ids_h.reshape(-1).long(), minlength=256))
-    return out, (d, sh, ws, y, ids, w, call)
+    return out, state
+
+
+def residual_numbers(wl, m_plain, m_res, steps, pk, k):
+    """The post-norm residual update fused into the combine: its stage time
+    against the plain combine's in the same step, and its own HBM roofline.
+    Algorithmic bytes per launch: the 8 expert-output rows of every token
+    (BF16), the stream read and written (x's dtype), the norm scale, and the
+    routing weights and positions."""
+    c = STAGES.index("combine")
+    ms = m_res["stage_ms"][c]
+    xb = 2 if wl.x_dtype == "bf16" else 4
+    alg = wl.T * 8 * wl.H * 2 + 2 * wl.T * wl.H * xb + wl.H * 4 + wl.T * 8 * 8
+    gbs = alg / (ms * 1e-3) / 1e9
+    return dict(step_k=k, in_place=True, combine_ms=round(m_plain["stage_ms"][c], 4), combine_residual_ms=round(ms, 4),
+                ms_per_step=round(m_res["total_ms"] / steps, 4),
+                roofline=dict(bound="hbm", achieved=round(gbs, 1), peak=pk["hbm"], unit="GB/s",
+                              frac=round(gbs / pk["hbm"], 4), algorithmic_bytes=alg, launch_ms=round(ms, 4),
+                              kernel="combine_residual_kernel", peak_source=pk["source"]),
+                clocks=m_res["clocks"])
 
 
 def measure_e2e(wl, state, steps, warmup, dev):
@@ -433,6 +463,8 @@ def main():
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-residual", action="store_true",
+                    help="skip the extra steps with the post-norm residual update fused into the combine")
     ap.add_argument("--small", action="store_true",
                     help="profiling shape H=2048, I=1024 (3.2 GB of experts) instead of 5120/2560")
     ap.add_argument("--weights-layout", choices=("tiled", "rows"), default="tiled",
@@ -474,6 +506,11 @@ def main():
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = oracle_sample(wl, state[0])
+    residual = None
+    if not args.no_residual:
+        rm, _ = measure(wl, args.steps, args.warmup, dev, world, torch.cuda.current_device(), state=state,
+                        residual_step=RESIDUAL_STEP)
+        residual = residual_numbers(wl, m, rm, args.steps, pk, RESIDUAL_STEP)
     del state
     torch.cuda.empty_cache()
 
@@ -484,9 +521,14 @@ def main():
         p_ms = max_over_ranks(pm["total_ms"], world)
         psn = step_numbers(pw, pm, max(3, args.steps // 2))
         phbm, ptc = roofline(pw, pm, pk)
+        presidual = None
+        if not args.no_residual:
+            rm, _ = measure(pw, max(3, args.steps // 2), args.warmup, dev, world, torch.cuda.current_device(),
+                            state=pstate, residual_step=RESIDUAL_STEP)
+            presidual = residual_numbers(pw, pm, rm, max(3, args.steps // 2), pk, RESIDUAL_STEP)
         prefill = dict(value=pw.T * max(3, args.steps // 2) * world / (p_ms * 1e-3), unit="tokens/s",
                        config={"workload": f"prefill T={pw.T} H={pw.H} I={pw.I} E=256 bf16 experts", "T": pw.T},
-                       roofline=ptc, roofline_hbm=phbm, clocks=pm["clocks"], **psn)
+                       roofline=ptc, roofline_hbm=phbm, clocks=pm["clocks"], residual_epilogue=presidual, **psn)
         del pstate
         torch.cuda.empty_cache()
 
@@ -503,7 +545,7 @@ def main():
                          f"({m['touched']} x {weight_bytes_per_expert(wl) / 1e6:.1f} MB), far larger than L2"},
         "roofline": hbm, "roofline_tensor": tc, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": m["launches_per_step"] * args.steps, "clocks": m["clocks"],
-        "step": sn, "prefill": prefill,
+        "step": sn, "residual_epilogue": residual, "prefill": prefill,
     }
     print(json.dumps(line), flush=True)
 

@@ -56,10 +56,16 @@ class _ExpertWeights(ctypes.Structure):
 BEAM_LAYOUT_ROWS, BEAM_LAYOUT_TILED = 0, 1
 
 
+class _Residual(ctypes.Structure):
+    _fields_ = [("stream", ctypes.c_void_p), ("out", ctypes.c_void_p), ("norm_weight", ctypes.c_void_p),
+                ("eps", ctypes.c_float), ("step", ctypes.c_int32)]
+
+
 class _Args(ctypes.Structure):
     _fields_ = [("x", ctypes.c_void_p), ("xdtype", ctypes.c_int), ("router_w", ctypes.c_void_p),
                 ("router_bias", ctypes.c_void_p), ("weights", ctypes.POINTER(_ExpertWeights)),
-                ("y", ctypes.c_void_p), ("topk_ids", ctypes.c_void_p), ("topk_w", ctypes.c_void_p)]
+                ("y", ctypes.c_void_p), ("topk_ids", ctypes.c_void_p), ("topk_w", ctypes.c_void_p),
+                ("residual", ctypes.POINTER(_Residual))]
 
 
 STAGES = ("route", "dispatch", "gather", "gate_up", "down", "combine")
@@ -95,6 +101,7 @@ def load():
     lib.beam_moe_experts.argtypes = [sp, vp, i32, ctypes.POINTER(_ExpertWeights), vp, vp, vp, vp, sz, vp]
     lib.beam_moe_forward.argtypes = [sp, vp, i32, vp, vp, ctypes.POINTER(_ExpertWeights), vp, vp, vp, vp, sz, vp]
     lib.beam_moe_forward_stage.argtypes = [sp, ctypes.POINTER(_Args), i32, vp, sz, vp]
+    lib.beam_moe_forward_residual.argtypes = [sp, ctypes.POINTER(_Args), vp, sz, vp]
     lib.beam_moe_read_device_status.argtypes = [vp, ctypes.POINTER(u32), vp]
     lib.beam_moe_route_noalloc.argtypes = [sp, vp, i32, vp, vp, vp, vp, vp]
     lib.beam_moe_route_noalloc.restype = i32
@@ -105,7 +112,8 @@ def load():
     lib.beam_status_string.argtypes = [i32]
     lib.beam_status_string.restype = ctypes.c_char_p
     for n in ("beam_moe_workspace_layout", "beam_moe_route", "beam_moe_dispatch", "beam_moe_experts",
-              "beam_moe_forward", "beam_moe_forward_stage", "beam_moe_read_device_status",
+              "beam_moe_forward", "beam_moe_forward_stage", "beam_moe_forward_residual",
+              "beam_moe_read_device_status",
               "beam_moe_debug_timeout"):
         getattr(lib, n).restype = i32
     _lib = lib
@@ -234,20 +242,33 @@ def beam_moe_forward(sh, x, router_w, router_bias, weights: dict, y, topk_ids, t
                                    workspace.numel(), _stream(stream)), "beam_moe_forward")
 
 
+def _residual(x, resid, out, norm_weight, eps, step) -> _Residual:
+    if resid.dtype != x.dtype or out.dtype != x.dtype or resid.shape != x.shape or out.shape != x.shape:
+        raise ValueError("residual stream and out must have x's shape and dtype")
+    if norm_weight.dtype != torch.float32 or norm_weight.shape != (x.shape[1],):
+        raise ValueError("norm_weight must be float32 of shape [H]")
+    return _Residual(_ptr(resid).value, _ptr(out).value, _ptr(norm_weight).value, float(eps), int(step))
+
+
 class ForwardCall:
     """The marshalled arguments of one forward call, reusable across calls.
 
     ``stage(i)`` enqueues step i of the forward (``STAGES[i]``) through
     beam_moe_forward_stage; ``run()`` enqueues all of them through
-    beam_moe_forward.  The tensors must stay alive while the object is used."""
+    beam_moe_forward (beam_moe_forward_residual when ``residual`` =
+    (stream, out, norm_weight, eps, step) is given; ``y`` may then be None).
+    The tensors must stay alive while the object is used."""
 
-    def __init__(self, sh, x, router_w, router_bias, weights: dict, y, topk_ids, topk_w, workspace, stream=None):
+    def __init__(self, sh, x, router_w, router_bias, weights: dict, y, topk_ids, topk_w, workspace, stream=None,
+                 residual=None):
         self.sh = sh
         self._ew = _weights(weights)
+        self._res = None if residual is None else _residual(x, *residual)
         self._args = _Args(_ptr(x).value, _act_dtype(x), _ptr(router_w).value,
                            None if router_bias is None else _ptr(router_bias).value, ctypes.pointer(self._ew),
-                           _ptr(y).value, _ptr(topk_ids).value, _ptr(topk_w).value)
-        self._keep = (x, router_w, router_bias, weights, y, topk_ids, topk_w, workspace)
+                           None if y is None else _ptr(y).value, _ptr(topk_ids).value, _ptr(topk_w).value,
+                           None if self._res is None else ctypes.pointer(self._res))
+        self._keep = (x, router_w, router_bias, weights, y, topk_ids, topk_w, workspace, residual)
         self.weights = weights
         self._ws = _ptr(workspace)
         self._ws_bytes = workspace.numel()
@@ -260,6 +281,10 @@ class ForwardCall:
 
     def run(self):
         a = self._args
+        if self._res is not None:
+            _check(self._lib.beam_moe_forward_residual(ctypes.byref(self.sh), ctypes.byref(a), self._ws,
+                                                       self._ws_bytes, self._stream), "beam_moe_forward_residual")
+            return
         _check(self._lib.beam_moe_forward(ctypes.byref(self.sh), a.x, a.xdtype, a.router_w, a.router_bias,
                                           a.weights, a.y, a.topk_ids, a.topk_w, self._ws, self._ws_bytes,
                                           self._stream), "beam_moe_forward")
@@ -268,6 +293,16 @@ class ForwardCall:
 def beam_moe_forward_stage(sh, stage: int, x, router_w, router_bias, weights: dict, y, topk_ids, topk_w,
                            workspace, stream=None):
     ForwardCall(sh, x, router_w, router_bias, weights, y, topk_ids, topk_w, workspace, stream).stage(stage)
+
+
+def beam_moe_forward_residual(sh, x, router_w, router_bias, weights: dict, resid, out, norm_weight, eps, step,
+                              topk_ids, topk_w, workspace, y=None, stream=None):
+    """The block followed by the post-norm residual update at step ``step``:
+    out = sqrt((k-1)/k) resid + RMSNorm(y) * norm_weight / sqrt(k).  ``out``
+    may be ``resid`` (in place); ``y`` (optional) also receives the block's
+    output."""
+    ForwardCall(sh, x, router_w, router_bias, weights, y, topk_ids, topk_w, workspace, stream,
+                residual=(resid, out, norm_weight, eps, step)).run()
 
 
 def pack_weights(sh, weights: dict, stream=None) -> dict:
@@ -340,3 +375,18 @@ class BeamMoE:
         beam_moe_forward(self.shape(T), x, self.router_w, self.router_bias, self.weights, y, topk_ids, topk_w,
                          self.workspace, stream)
         return y, topk_ids, topk_w
+
+    def residual(self, x, resid, norm_weight, eps, step, out=None, y=None, topk_ids=None, topk_w=None,
+                 stream=None):
+        """The layer followed by the residual update at step ``step``; returns
+        (new stream, topk_ids, topk_w).  ``out=resid`` updates in place."""
+        T = x.shape[0]
+        if T > self.max_tokens:
+            raise ValueError(f"{T} tokens > workspace capacity {self.max_tokens}")
+        dev = x.device
+        out = torch.empty_like(x) if out is None else out
+        topk_ids = torch.empty((T, 8), dtype=torch.int32, device=dev) if topk_ids is None else topk_ids
+        topk_w = torch.empty((T, 8), dtype=torch.float32, device=dev) if topk_w is None else topk_w
+        beam_moe_forward_residual(self.shape(T), x, self.router_w, self.router_bias, self.weights, resid, out,
+                                  norm_weight, eps, step, topk_ids, topk_w, self.workspace, y=y, stream=stream)
+        return out, topk_ids, topk_w

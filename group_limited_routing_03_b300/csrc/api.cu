@@ -401,16 +401,52 @@ beam_status_t run_experts(const beam_moe_shape_t& s, const void* x, bool x_bf16,
   return st;
 }
 
-// Validation shared by beam_moe_forward and beam_moe_forward_stage.
+// The residual-update arguments: pointers set and aligned, out either the
+// stream itself or disjoint from it, y (when written) disjoint from both,
+// step >= 2, eps finite and >= 0.
+beam_status_t check_residual(const beam_moe_shape_t* s, const beam_residual_t& r, beam_dtype_t xdtype,
+                             const void* y) {
+  if (!r.stream || !r.out || !r.norm_weight) return BEAM_ERR_INVALID_ARG;
+  if (!aligned16(r.stream) || !aligned16(r.out) || !aligned16(r.norm_weight)) return BEAM_ERR_INVALID_ARG;
+  if (r.step < 2 || !std::isfinite(r.eps) || r.eps < 0.0f) return BEAM_ERR_INVALID_ARG;
+  const size_t len = static_cast<size_t>(s->T) * s->H * (xdtype == BEAM_BF16 ? 2 : 4);
+  auto overlap = [len](const void* p, const void* q) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p), b = reinterpret_cast<uintptr_t>(q);
+    return a < b + len && b < a + len;
+  };
+  if (r.out != r.stream && overlap(r.out, r.stream)) return BEAM_ERR_INVALID_ARG;
+  if (y && (overlap(y, r.out) || overlap(y, r.stream))) return BEAM_ERR_INVALID_ARG;
+  return BEAM_OK;
+}
+
+beam_status_t run_combine_residual(const beam_moe_shape_t& s, const float* w, const beam_residual_t& res, void* y,
+                                   bool bf16, void* ws, const Layout& L, cudaStream_t stream) {
+  ResidualParams r;
+  r.stream = res.stream;
+  r.out = res.out;
+  r.norm_w = res.norm_weight;
+  r.eps = res.eps;
+  r.keep = static_cast<float>(std::sqrt(static_cast<double>(res.step - 1) / res.step));
+  r.add = static_cast<float>(1.0 / std::sqrt(static_cast<double>(res.step)));
+  return cuda_status(launch_combine_residual(at<__nv_bfloat16>(ws, L.yr), at<int32_t>(ws, L.pos), w, s.T, s.H, r, y,
+                                             bf16, stream));
+}
+
+// Validation shared by beam_moe_forward, beam_moe_forward_stage and
+// beam_moe_forward_residual.
 beam_status_t check_forward(const beam_moe_shape_t* shape, const beam_moe_args_t& a, void* workspace,
                             size_t workspace_bytes, Layout& L, DeviceInfo& d) {
   beam_status_t st = check_shape(shape);
   if (st != BEAM_OK) return st;
-  if (!a.x || !a.router_w || !a.topk_ids || !a.topk_w || !a.y) return BEAM_ERR_INVALID_ARG;
+  if (!a.x || !a.router_w || !a.topk_ids || !a.topk_w || (!a.y && !a.residual)) return BEAM_ERR_INVALID_ARG;
   if (!aligned16(a.x) || !aligned16(a.router_w) || !aligned16(a.topk_ids) || !aligned16(a.topk_w) ||
-      !aligned16(a.y) || (a.router_bias && !aligned16(a.router_bias)))
+      (a.y && !aligned16(a.y)) || (a.router_bias && !aligned16(a.router_bias)))
     return BEAM_ERR_INVALID_ARG;
   if (a.xdtype != BEAM_F32 && a.xdtype != BEAM_BF16) return BEAM_ERR_UNSUPPORTED;
+  if (a.residual) {
+    st = check_residual(shape, *a.residual, a.xdtype, a.y);
+    if (st != BEAM_OK) return st;
+  }
   st = check_weights(shape, a.weights);
   if (st != BEAM_OK) return st;
   st = check_workspace(shape, workspace, workspace_bytes, L);
@@ -435,6 +471,7 @@ beam_status_t run_stage(const beam_moe_shape_t& s, const beam_moe_args_t& a, int
     case BEAM_STAGE_DOWN:
       return run_gemm(1, s, a.weights, ws, L, d, cs);
     case BEAM_STAGE_COMBINE:
+      if (a.residual) return run_combine_residual(s, a.topk_w, *a.residual, a.y, xb, ws, L, cs);
       return run_combine(s, a.topk_w, a.y, xb, ws, L, cs);
   }
   return BEAM_ERR_INVALID_ARG;
@@ -538,6 +575,19 @@ beam_status_t beam_moe_forward(const beam_moe_shape_t* shape, const void* x, bea
   const cudaStream_t cs = static_cast<cudaStream_t>(stream);
   for (int stage = 0; stage < BEAM_STAGE_COUNT && st == BEAM_OK; ++stage)
     st = run_stage(*shape, a, stage, workspace, L, d, cs);
+  return st;
+}
+
+beam_status_t beam_moe_forward_residual(const beam_moe_shape_t* shape, const beam_moe_args_t* args, void* workspace,
+                                        size_t workspace_bytes, void* stream) {
+  if (args == nullptr || args->residual == nullptr) return BEAM_ERR_INVALID_ARG;
+  Layout L;
+  DeviceInfo d;
+  beam_status_t st = check_forward(shape, *args, workspace, workspace_bytes, L, d);
+  if (st != BEAM_OK) return st;
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  for (int stage = 0; stage < BEAM_STAGE_COUNT && st == BEAM_OK; ++stage)
+    st = run_stage(*shape, *args, stage, workspace, L, d, cs);
   return st;
 }
 

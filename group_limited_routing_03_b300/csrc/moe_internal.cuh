@@ -127,6 +127,19 @@ size_t gemm_smem_bytes(int stages, int acc_stages, size_t stage_bytes);
 int gemm_pair_max_clusters(int mode, size_t smem_bytes);
 cudaError_t launch_combine(const __nv_bfloat16* yr, const int32_t* pos, const float* w, int T, int H,
                            void* y, bool y_bf16, cudaStream_t stream);
+// Post-norm residual update fused into the combine (see combine.cu).
+struct ResidualParams {
+  const void* stream;   // [T, H] residual stream, the activations' dtype
+  void* out;            // [T, H] new stream; may equal `stream`
+  const float* norm_w;  // [H] RMSNorm scale
+  float eps, keep, add;
+};
+cudaError_t launch_combine_residual(const __nv_bfloat16* yr, const int32_t* pos, const float* w, int T, int H,
+                                    const ResidualParams& r, void* y_out, bool bf16, cudaStream_t stream);
+// Row split (CTAs per token, one cluster) and dynamic shared memory of the
+// fused kernel.
+int residual_cluster_y(int T, int H);
+size_t residual_smem_bytes(int T, int H);
 cudaError_t launch_debug_timeout(uint32_t* status, uint64_t timeout_ns, cudaStream_t stream);
 // Regroup `rows` x `row_bytes` (row-major) into contiguous tiles of 128 rows
 // x `tile_row_bytes` (pack.cu); rows % 128 == 0, row_bytes % tile_row_bytes

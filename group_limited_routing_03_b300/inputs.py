@@ -177,6 +177,24 @@ def generate(wl: Workload, device="cpu", *, experts=True):
     return out
 
 
+RESIDUAL_EPS = 1e-6  # RMSNorm eps of the post-norm (a common value; the post gives none)
+
+
+def residual_inputs(wl: Workload, device="cpu", *, seed_offset=1000):
+    """The residual stream entering the update and the post-norm's scale.
+
+    stream [T,H] ~ N(0, 1) in x's dtype (the update keeps the stream at unit
+    scale, so a unit-RMS stream is its steady state); norm_weight [H] f32
+    ~ 1 + N(0, 0.1^2) (a learned scale near one).  Seed: the workload's seed
+    plus ``seed_offset``, so the block's own inputs are unchanged."""
+    gen = torch.Generator(device=device)
+    gen.manual_seed(wl.seed + seed_offset)
+    s = _randn((wl.T, wl.H), gen, device)
+    stream = s if wl.x_dtype == "f32" else s.to(torch.bfloat16)
+    g = _randn((wl.H,), gen, device, std=0.1).add_(1.0)
+    return stream, g
+
+
 def bf16_bits(t: torch.Tensor):
     """Host numpy uint16 view of a bf16 tensor's bit patterns."""
     return t.detach().to("cpu").contiguous().view(torch.int16).numpy().view("uint16")

@@ -168,11 +168,40 @@ typedef enum {
   BEAM_STAGE_GATHER = 2,   /* token rows into route order (BF16) */
   BEAM_STAGE_GATE_UP = 3,  /* grouped gate/up GEMM with the SwiGLU epilogue */
   BEAM_STAGE_DOWN = 4,     /* grouped down GEMM */
-  BEAM_STAGE_COMBINE = 5,  /* weighted sum of each token's expert outputs */
+  BEAM_STAGE_COMBINE = 5,  /* weighted sum of each token's expert outputs
+                              (+ the residual update when args->residual) */
   BEAM_STAGE_COUNT = 6
 } beam_stage_t;
 
-/* All tensors of one forward call (the arguments of beam_moe_forward). */
+/* Post-norm residual update after the block, fused into its combine step.
+ * Source: the Beam post, section "Residual Stream": the stream starts from the
+ * embedding (step 1); at step k >= 2 the stream is kept with weight
+ * sqrt((k-1)/k) and the sublayer's output, normalised after the sublayer,
+ * added with weight 1/sqrt(k) (the two weights' squares sum to one, so the
+ * embedding and every sublayer output end with equal weight); norms in FP32.
+ * The post does not say which norm follows a sublayer; it is read as RMSNorm
+ * (the norm the post names, in section "Attention", for queries and keys)
+ * with a learned scale g and an eps inside the root:
+ *   out[t,:] = sqrt((k-1)/k) * stream[t,:]
+ *            + (1/sqrt(k)) * g * y[t,:] / sqrt(mean_j y[t,j]^2 + eps)
+ * where y is the block's output (kept in FP32 inside the kernel, not rounded
+ * to the activations' dtype first).  All arithmetic FP32; out rounded to the
+ * stream's dtype (round to nearest even).  A row with y = 0 and eps = 0
+ * gives NaN, as the formula does. */
+typedef struct {
+  const void* stream;       /* [T, H] stream before the update, x's dtype */
+  void* out;                /* [T, H] stream after it, x's dtype; may be `stream`
+                               itself (in place), else must not overlap it */
+  const float* norm_weight; /* [H] the post-norm's scale g, FP32 */
+  float eps;                /* finite, >= 0 */
+  int32_t step;             /* k >= 2 (the embedding is step 1) */
+} beam_residual_t;
+
+/* All tensors of one forward call (the arguments of beam_moe_forward).
+ * `residual` (nullable, last so that older initialisers stay valid): when set,
+ * the combine step applies the residual update above and `y` becomes
+ * optional (NULL: the block's output is not written; else it is written too,
+ * in x's dtype, and must not overlap the stream or out). */
 typedef struct {
   const void* x;
   beam_dtype_t xdtype;
@@ -182,7 +211,16 @@ typedef struct {
   void* y;
   int32_t* topk_ids;
   float* topk_w;
+  const beam_residual_t* residual;
 } beam_moe_args_t;
+
+/* The whole block followed by the residual update: beam_moe_forward with
+ * args->residual (required) applied in the combine kernel.  The routing
+ * outputs are written as by beam_moe_forward.  BEAM_ERR_INVALID_ARG for a
+ * null or misaligned residual pointer, step < 2, eps negative or not finite,
+ * or overlapping stream / out / y. */
+beam_status_t beam_moe_forward_residual(const beam_moe_shape_t* shape, const beam_moe_args_t* args,
+                                        void* workspace, size_t workspace_bytes, void* stream);
 
 /* Enqueue stage `stage` of the forward pass.  Each stage reads what the
  * previous stages left in `workspace` (and in topk_ids / topk_w), so the

@@ -14,7 +14,8 @@ written from the Beam launch post:
 * the same post, section "Residual Stream" -- router and SwiGLU product in
   FP32 (the oracle uses double, the exact definition); the stream update
   sqrt((k-1)/k) * stream + output / sqrt(k) at step k, sublayer outputs
-  normalised (RMSNorm) after the sublayer;
+  normalised after the sublayer (read as RMSNorm, the norm the post names in
+  section "Attention");
 * the Chinese translation "Reflection 发布 501B 开放模型 Beam ..."
   (sihot.dev), section 混合专家, says the same.
 

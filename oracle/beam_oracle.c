@@ -382,7 +382,9 @@ int oracle_combine(int64_t n, int K, int64_t H, const double* weights, const dou
  * embedding is step 1; at step k >= 2 the stream is kept with weight
  * sqrt((k-1)/k) and the sublayer output is added with weight 1/sqrt(k), the
  * two weights' squares summing to one.  Every sublayer's output is
- * normalised after the sublayer (the post names RMSNorm as its norm); here,
+ * normalised after the sublayer.  The post does not say which norm; it is
+ * read as RMSNorm (the norm the post names elsewhere, in section "Attention",
+ * for queries and keys) with a learned scale w and eps inside the root; here,
  * in double:
  *   yn[t, j]  = y[t, j] / sqrt(mean_j' y[t, j']^2 + eps) * w[j]
  *   out[t, j] = sqrt((k-1)/k) * stream[t, j] + yn[t, j] / sqrt(k)

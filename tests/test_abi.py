@@ -186,3 +186,34 @@ def test_forward_rejects_unknown_layout(lib):
     rc = lib.beam_moe_forward(ctypes.byref(sh), 0x10000, moe.BEAM_BF16, 0x20000, None, ctypes.byref(ew), 0x50000,
                               0x30000, 0x40000, 0x100000, n, None)
     assert rc == moe.BEAM_ERR_INVALID_ARG
+
+
+def test_forward_residual_argument_errors(lib):
+    sh = _shape(T=64, H=256, I=256)
+    ew = moe._ExpertWeights()
+    ew.dtype = moe.BEAM_BF16
+    ew.gate, ew.up, ew.down = 0x1000, 0x2000, 0x3000
+    n = moe.workspace_size(sh)
+    row_bytes = 64 * 256 * 2  # the stream, BF16
+
+    def call(stream, out, g, eps, step, y=None):
+        r = moe._Residual(stream, out, g, eps, step)
+        a = moe._Args(0x10000, moe.BEAM_BF16, 0x20000, None, ctypes.pointer(ew), y, 0x30000, 0x40000,
+                      ctypes.pointer(r))
+        return lib.beam_moe_forward_residual(ctypes.byref(sh), ctypes.byref(a), 0x100000, n, None)
+
+    S, O, G = 0x1000000, 0x2000000, 0x3000000
+    assert call(S, O, G, 1e-6, 1) == moe.BEAM_ERR_INVALID_ARG  # step < 2
+    assert call(S, O, G, -1.0, 2) == moe.BEAM_ERR_INVALID_ARG  # eps < 0
+    assert call(S, O, G, float("inf"), 2) == moe.BEAM_ERR_INVALID_ARG
+    assert call(S, O, None, 1e-6, 2) == moe.BEAM_ERR_INVALID_ARG  # no norm weight
+    assert call(S, O + 8, G, 1e-6, 2) == moe.BEAM_ERR_INVALID_ARG  # misaligned out
+    assert call(S, S + 16, G, 1e-6, 2) == moe.BEAM_ERR_INVALID_ARG  # out overlaps the stream
+    assert call(S, O, G, 1e-6, 2, y=O + row_bytes - 16) == moe.BEAM_ERR_INVALID_ARG  # y overlaps out
+    # no residual at all: the entry point needs one
+    a = moe._Args(0x10000, moe.BEAM_BF16, 0x20000, None, ctypes.pointer(ew), None, 0x30000, 0x40000, None)
+    assert lib.beam_moe_forward_residual(ctypes.byref(sh), ctypes.byref(a), 0x100000, n, None) == \
+        moe.BEAM_ERR_INVALID_ARG
+    # without a residual, the plain stages still need y
+    assert lib.beam_moe_forward_stage(ctypes.byref(sh), ctypes.byref(a), 0, 0x100000, n, None) == \
+        moe.BEAM_ERR_INVALID_ARG

@@ -16,6 +16,10 @@ written from the Beam launch post:
   sqrt((k-1)/k) * stream + output / sqrt(k) at step k, sublayer outputs
   normalised after the sublayer (read as RMSNorm, the norm the post names in
   section "Attention");
+* the same post, section "Mixture of Experts", names an FP8 checkpoint
+  beside BF16 and NVFP4 without its layout: read as E4M3 weights with an FP32
+  scale per output row and activations quantised per row to E4M3 at run time
+  (scale = row amax / 448) -- ``expert_ffn_fp8``;
 * the Chinese translation "Reflection 发布 501B 开放模型 Beam ..."
   (sihot.dev), section 混合专家, says the same.
 
@@ -37,6 +41,14 @@ Parity status of each function (what pins it is in ``tests/test_oracle_*``):
                    (constant rows, with and without eps).
 * decoders         pinned: torch float8_e4m3fn conversion (all 256 codes),
                    the OCP E2M1 value table.
+* ``encode_e4m3``  pinned: torch's float -> float8_e4m3fn cast (nearest, ties
+                   to even) on every code value, every midpoint and random
+                   values; saturation closed form.
+* ``quantize_e4m3_rows`` pinned: closed forms (the row maximum encodes to
+                   +-448, zero rows, power-of-two rows reconstruct exactly)
+                   and torch's cast of a / (amax / 448).
+* ``expert_ffn_fp8`` pinned: numpy matmuls on values decoded and quantised by
+                   torch (float8_e4m3fn), independent of the oracle's encoder.
 """
 from __future__ import annotations
 
@@ -78,6 +90,12 @@ def _load():
         lib.oracle_expert_ffn.argtypes = [i64, i64, i64, vp, i32, i32, vp, vp, vp, vp, vp, vp, dbl,
                                           dbl, dbl, vp, vp, i32]
         lib.oracle_expert_ffn.restype = i32
+        lib.oracle_expert_ffn_fp8.argtypes = [i64, i64, i64, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, i32]
+        lib.oracle_expert_ffn_fp8.restype = i32
+        lib.oracle_encode_e4m3.argtypes = [ctypes.c_float]
+        lib.oracle_encode_e4m3.restype = ctypes.c_uint8
+        lib.oracle_quantize_e4m3_row.argtypes = [vp, i64, vp, vp]
+        lib.oracle_quantize_e4m3_row.restype = None
         lib.oracle_combine.argtypes = [i64, i32, i64, vp, vp, vp]
         lib.oracle_combine.restype = i32
         lib.oracle_residual_update.argtypes = [i64, i64, vp, vp, vp, dbl, i32, vp]
@@ -215,6 +233,47 @@ def residual_update(y, stream, w, eps, k):
     if rc != 0:
         raise ValueError(f"oracle_residual_update failed ({rc})")
     return out
+
+
+def encode_e4m3(v) -> int:
+    """E4M3 code of one float32 value (nearest, ties to even, saturating)."""
+    return int(_load().oracle_encode_e4m3(float(np.float32(v))))
+
+
+def quantize_e4m3_rows(a):
+    """Per-row E4M3 quantisation of float32 rows a [n, K]: (codes uint8 [n, K],
+    scales float32 [n]) with scale = amax / 448 (1 for a zero row)."""
+    lib = _load()
+    a = np.ascontiguousarray(a, dtype=np.float32)
+    n, K = a.shape
+    codes = np.zeros((n, K), np.uint8)
+    scales = np.zeros(n, np.float32)
+    for r in range(n):
+        row = a[r]
+        lib.oracle_quantize_e4m3_row(_ptr(row), K, _ptr(codes[r]), scales[r:r + 1].ctypes.data_as(ctypes.c_void_p))
+    return codes, scales
+
+
+def expert_ffn_fp8(x, wg, wu, wd, rg, ru, rd, *, want_h=False, threads=None):
+    """One expert with FP8 weights (E4M3 codes [I,H] / [H,I] uint8, FP32 row
+    scales [I] / [H]) on the rows of x (float32 or BF16 bits); activations
+    quantised per row to E4M3 before each GEMM.  Returns f64[n, H] (and the
+    unquantised h f64[n, I])."""
+    lib = _load()
+    x, xd = _act(x)
+    n, H = x.shape
+    I = wg.shape[0]
+    assert wg.shape == (I, H) and wu.shape == (I, H) and wd.shape == (H, I)
+    wg, wu, wd = (np.ascontiguousarray(m, dtype=np.uint8) for m in (wg, wu, wd))
+    rg, ru, rd = (np.ascontiguousarray(v, dtype=np.float32) for v in (rg, ru, rd))
+    assert rg.shape == (I,) and ru.shape == (I,) and rd.shape == (H,)
+    out = np.zeros((n, H), np.float64)
+    h = np.zeros((n, I), np.float64) if want_h else None
+    rc = lib.oracle_expert_ffn_fp8(H, I, n, _ptr(x), xd, _ptr(wg), _ptr(wu), _ptr(wd), _ptr(rg), _ptr(ru),
+                                   _ptr(rd), _ptr(out), _ptr(h), threads or default_threads())
+    if rc != 0:
+        raise ValueError(f"oracle_expert_ffn_fp8 failed ({rc})")
+    return (out, h) if want_h else out
 
 
 def dispatch(ids, n_experts=256):

@@ -53,6 +53,7 @@
 #define ORACLE_F32 0
 #define ORACLE_BF16 1
 #define ORACLE_NVFP4 2
+#define ORACLE_FP8 3
 
 /* ------------------------------------------------------------------ */
 /* Exact decoders (each format written out from its bit layout).      */
@@ -81,6 +82,53 @@ double oracle_decode_e4m3(uint8_t code) {
   return sign ? -v : v;
 }
 
+/* Float -> E4M3 (layout above): round to nearest, ties to even; magnitudes
+ * of 448 (the largest finite value) and above give +-448 (saturation, as the
+ * FP8 formats have no infinity).  Written from the layout: the binade of |v|
+ * fixes the quantum 2^(e-3) (2^-9 below 2^-6, the subnormal range), |v| is
+ * rounded to a whole number of quanta, and a carry into 16 quanta moves to
+ * the next binade. */
+uint8_t oracle_encode_e4m3(float v) {
+  const uint8_t sign = signbit(v) ? 0x80 : 0x00;
+  const double a = fabs((double)v);
+  if (isnan(v)) return 0x7F;
+  if (a >= 448.0) return sign | 0x7E;
+  if (a == 0.0) return sign;
+  int e2;
+  frexp(a, &e2); /* a = f * 2^e2, f in [0.5, 1): binade 2^(e2-1) */
+  int e = e2 - 1;
+  if (e < -6) e = -6;
+  double m = nearbyint(ldexp(a, 3 - e)); /* quanta of 2^(e-3); default mode: ties to even */
+  if (m >= 16.0) {
+    e += 1;
+    m = 8.0;
+  }
+  if (m < 8.0) return sign | (uint8_t)m; /* subnormal (only reachable for e = -6): exponent field 0 */
+  return sign | (uint8_t)(((e + 7) << 3) | ((int)m - 8));
+}
+
+/* Per-row dynamic quantisation of a GEMM input row to E4M3, the reading used
+ * for FP8 expert weights: the row's scale is s = amax / 448 (amax = the
+ * largest magnitude in the row; FP32 division; s = 1 when that is 0), each
+ * element is encoded as E4M3(a / s) with the division in FP32, and stands for
+ * e4m3 * s.  Both decisions are taken in FP32 so that the product path, which
+ * makes them in FP32 too, picks the same codes from the same inputs. */
+void oracle_quantize_e4m3_row(const float* a, int64_t K, uint8_t* codes, float* scale) {
+  float amax = 0.0f;
+  for (int64_t j = 0; j < K; ++j) {
+    const float m = fabsf(a[j]);
+    if (m > amax) amax = m;
+  }
+  volatile float s = amax / 448.0f; /* one FP32 rounding */
+  float sf = s;
+  if (sf == 0.0f) sf = 1.0f;
+  for (int64_t j = 0; j < K; ++j) {
+    volatile float q = a[j] / sf;
+    codes[j] = oracle_encode_e4m3(q);
+  }
+  *scale = sf;
+}
+
 /* E2M1 (OCP 4-bit float): 1 sign, 2 exponent bits (bias 1), 1 mantissa bit,
  * no infinities or NaN. */
 double oracle_decode_e2m1(uint8_t nibble) {
@@ -97,16 +145,19 @@ double oracle_decode_e2m1(uint8_t nibble) {
 
 /* One element [row, k] of a weight matrix with `cols` columns (K). */
 typedef struct {
-  int dtype;            /* ORACLE_F32 / ORACLE_BF16 / ORACLE_NVFP4 */
-  const void* data;     /* f32 [rows, cols] | bf16 [rows, cols] | u8 [rows, cols/2] */
+  int dtype;            /* ORACLE_F32 / ORACLE_BF16 / ORACLE_NVFP4 / ORACLE_FP8 */
+  const void* data;     /* f32 [rows, cols] | bf16 [rows, cols] | u8 [rows, cols/2] | u8 [rows, cols] */
   const uint8_t* scale; /* NVFP4 only: E4M3 [rows, cols/16] */
   double global_scale;  /* NVFP4 only */
   int64_t cols;
+  const float* row_scale; /* FP8 only: FP32 scale per row [rows] */
 } oracle_matrix_t;
 
 static double mat_elem(const oracle_matrix_t* m, int64_t row, int64_t k) {
   if (m->dtype == ORACLE_F32) return (double)((const float*)m->data)[row * m->cols + k];
   if (m->dtype == ORACLE_BF16) return oracle_decode_bf16(((const uint16_t*)m->data)[row * m->cols + k]);
+  if (m->dtype == ORACLE_FP8)
+    return oracle_decode_e4m3(((const uint8_t*)m->data)[row * m->cols + k]) * (double)m->row_scale[row];
   /* NVFP4: byte k/2 of the row holds elements k (low nibble, k even) and k+1. */
   {
     uint8_t byte = ((const uint8_t*)m->data)[row * (m->cols / 2) + k / 2];
@@ -299,6 +350,7 @@ typedef struct {
   oracle_matrix_t wg, wu, wd;
   double* h; /* [n, I] */
   double* out; /* [n, H] */
+  const double* xq; /* FP8 only: quantised x values [n, H] (NULL: read x) */
 } ffn_args_t;
 
 /* h[r, i] = silu(a) * u with a = x_r . Wg[i,:], u = x_r . Wu[i,:]. */
@@ -308,7 +360,7 @@ static void ffn_hidden(void* p, int64_t lo, int64_t hi) {
     int64_t r = q / a->I, i = q % a->I;
     double ga = 0.0, ua = 0.0;
     for (int64_t hh = 0; hh < a->H; ++hh) {
-      double xv = act_elem(a->x, a->x_dtype, r * a->H + hh);
+      double xv = a->xq ? a->xq[r * a->H + hh] : act_elem(a->x, a->x_dtype, r * a->H + hh);
       ga += xv * mat_elem(&a->wg, i, hh);
       ua += xv * mat_elem(&a->wu, i, hh);
     }
@@ -349,9 +401,11 @@ int oracle_expert_ffn(int64_t H, int64_t I, int64_t n, const void* x, int x_dtyp
   a.n = n;
   a.x = x;
   a.x_dtype = x_dtype;
-  a.wg = (oracle_matrix_t){w_dtype, wg, sg, gg, H};
-  a.wu = (oracle_matrix_t){w_dtype, wu, su, gu, H};
-  a.wd = (oracle_matrix_t){w_dtype, wd, sd, gd, I};
+  a.xq = NULL;
+  if (w_dtype == ORACLE_FP8) return -1; /* oracle_expert_ffn_fp8 */
+  a.wg = (oracle_matrix_t){w_dtype, wg, sg, gg, H, NULL};
+  a.wu = (oracle_matrix_t){w_dtype, wu, su, gu, H, NULL};
+  a.wd = (oracle_matrix_t){w_dtype, wd, sd, gd, I, NULL};
   a.out = out;
   a.h = h_out ? h_out : (double*)malloc(sizeof(double) * (size_t)(n * I > 0 ? n * I : 1));
   if (!a.h) return -2;
@@ -359,6 +413,75 @@ int oracle_expert_ffn(int64_t H, int64_t I, int64_t n, const void* x, int x_dtyp
   parallel_for(n * H, nthreads, ffn_down, &a);
   if (!h_out) free(a.h);
   return 0;
+}
+
+/*
+ * oracle_expert_ffn_fp8: one expert with FP8 weights applied to n rows.  The
+ * launch post names an FP8 checkpoint beside BF16 and NVFP4 (section
+ * "Mixture of Experts") without giving its layout; it is read as E4M3
+ * weights with one FP32 scale per output row (weight = e4m3 * row_scale) and
+ * FP8 activations quantised per row at run time (oracle_quantize_e4m3_row):
+ * the rows of x before gate/up, the rows of h before down.
+ *   x          [n, H]  FP32 or BF16 bits (x_dtype), quantised from its own values
+ *   wg, wu     [I, H]  E4M3 codes; rg, ru [I] row scales
+ *   wd         [H, I]  E4M3 codes; rd [H] row scales
+ *   out        [n, H]  out;  h_out [n, I] out (nullable): h before quantisation
+ * h = silu(xq . wg) * (xq . wu) in double; each h row is rounded to FP32 and
+ * quantised; out = hq . wd.  Sums run in index order, in double.
+ */
+int oracle_expert_ffn_fp8(int64_t H, int64_t I, int64_t n, const void* x, int x_dtype, const uint8_t* wg,
+                          const uint8_t* wu, const uint8_t* wd, const float* rg, const float* ru, const float* rd,
+                          double* out, double* h_out, int nthreads) {
+  if (H <= 0 || I <= 0 || n < 0 || !rg || !ru || !rd) return -1;
+  const int64_t nn = n > 0 ? n : 1;
+  float* rowf = (float*)malloc(sizeof(float) * (size_t)(H > I ? H : I));
+  uint8_t* codes = (uint8_t*)malloc((size_t)(H > I ? H : I));
+  double* xq = (double*)malloc(sizeof(double) * (size_t)(nn * H));
+  double* hq = (double*)malloc(sizeof(double) * (size_t)(nn * I));
+  double* h = h_out ? h_out : (double*)malloc(sizeof(double) * (size_t)(nn * I));
+  int rc = 0;
+  if (!rowf || !codes || !xq || !hq || !h) {
+    rc = -2;
+    goto done;
+  }
+  /* x rows -> E4M3 codes and scales -> the values the GEMM multiplies */
+  for (int64_t r = 0; r < n; ++r) {
+    float sc;
+    for (int64_t j = 0; j < H; ++j) rowf[j] = (float)act_elem(x, x_dtype, r * H + j);
+    oracle_quantize_e4m3_row(rowf, H, codes, &sc);
+    for (int64_t j = 0; j < H; ++j) xq[r * H + j] = oracle_decode_e4m3(codes[j]) * (double)sc;
+  }
+  {
+    ffn_args_t a;
+    a.H = H;
+    a.I = I;
+    a.n = n;
+    a.x = NULL;
+    a.x_dtype = -1;
+    a.wg = (oracle_matrix_t){ORACLE_FP8, wg, NULL, 1.0, H, rg};
+    a.wu = (oracle_matrix_t){ORACLE_FP8, wu, NULL, 1.0, H, ru};
+    a.wd = (oracle_matrix_t){ORACLE_FP8, wd, NULL, 1.0, I, rd};
+    a.h = h;
+    a.out = out;
+    a.xq = xq;
+    parallel_for(n * I, nthreads, ffn_hidden, &a);
+    /* h rows -> FP32 -> E4M3 codes and scales */
+    for (int64_t r = 0; r < n; ++r) {
+      float sc;
+      for (int64_t i = 0; i < I; ++i) rowf[i] = (float)h[r * I + i];
+      oracle_quantize_e4m3_row(rowf, I, codes, &sc);
+      for (int64_t i = 0; i < I; ++i) hq[r * I + i] = oracle_decode_e4m3(codes[i]) * (double)sc;
+    }
+    a.h = hq;
+    parallel_for(n * H, nthreads, ffn_down, &a);
+  }
+done:
+  free(rowf);
+  free(codes);
+  free(xq);
+  free(hq);
+  if (!h_out) free(h);
+  return rc;
 }
 
 /*

@@ -407,3 +407,106 @@ def test_residual_bf16_stream_bits():
     y = np.zeros((1, 4))
     out = oracle.residual_update(y, bits, np.ones(4), 1e-6, 4)
     np.testing.assert_allclose(out, vals * np.sqrt(3 / 4), rtol=1e-15)
+
+
+# ---------------------------------------------------------------------------
+# FP8 (E4M3) weights and per-row activation quantisation
+# ---------------------------------------------------------------------------
+def _torch_e4m3(v):
+    """torch's float32 -> float8_e4m3fn cast (nearest, ties to even) as codes."""
+    return torch.as_tensor(np.asarray(v, np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def _e4m3_values():
+    codes = np.arange(256, dtype=np.uint8)
+    vals = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float32).numpy()
+    return codes, vals
+
+
+def test_encode_e4m3_matches_torch_cast():
+    codes, vals = _e4m3_values()
+    finite = ~np.isnan(vals)
+    # every code's own value encodes back to it (both zeros keep their sign)
+    for c, v in zip(codes[finite], vals[finite]):
+        assert oracle.encode_e4m3(v) == c, (c, v)
+    # midpoints between neighbouring positive values: ties to the even code
+    pos = np.unique(vals[finite & (vals >= 0)])
+    mids = ((pos[:-1].astype(np.float64) + pos[1:]) / 2).astype(np.float32)
+    want = _torch_e4m3(np.concatenate([mids, -mids]))
+    got = np.array([oracle.encode_e4m3(v) for v in np.concatenate([mids, -mids])], np.uint8)
+    np.testing.assert_array_equal(got, want)
+    # random values across the whole range, including the subnormals
+    rng = np.random.default_rng(3)
+    r = (rng.standard_normal(4000) * np.exp2(rng.integers(-12, 9, 4000))).astype(np.float32)
+    r = np.clip(r, -448, 448)
+    np.testing.assert_array_equal(np.array([oracle.encode_e4m3(v) for v in r], np.uint8), _torch_e4m3(r))
+
+
+def test_encode_e4m3_saturates():
+    for v, c in ((448.0, 0x7E), (460.0, 0x7E), (1e30, 0x7E), (-500.0, 0xFE), (-448.0, 0xFE)):
+        assert oracle.encode_e4m3(v) == c
+    assert oracle.encode_e4m3(2.0 ** -10) == 0x00  # half the smallest subnormal: tie to even 0
+    assert oracle.encode_e4m3(3 * 2.0 ** -10) == 0x02  # 1.5 quanta: tie to even 2
+
+
+def test_quantize_rows_closed_forms():
+    rng = np.random.default_rng(9)
+    a = rng.standard_normal((6, 96)).astype(np.float32)
+    a[2] = 0.0
+    codes, scales = oracle.quantize_e4m3_rows(a)
+    # scale = amax / 448 in FP32; a zero row gets scale 1 and zero codes
+    amax = np.abs(a).max(1)
+    for r in range(6):
+        want = np.float32(1.0) if amax[r] == 0 else np.float32(amax[r]) / np.float32(448.0)
+        assert scales[r] == want
+    assert (codes[2] == 0).all()
+    # the row maximum always encodes to +-448
+    j = np.abs(a).argmax(1)
+    for r in (0, 1, 3, 4, 5):
+        assert codes[r, j[r]] in (0x7E, 0xFE)
+    # the other codes are torch's cast of a / s
+    np.testing.assert_array_equal(codes, _torch_e4m3(a / scales[:, None]))
+    # a row of E4M3 values times a power of two with maximum 448 * 2^-3
+    _, vals = _e4m3_values()
+    grid = vals[~np.isnan(vals)]
+    row = (rng.choice(grid[np.abs(grid) <= 448], 64) * 0.125).astype(np.float32)
+    row[5] = 56.0
+    c2, s2 = oracle.quantize_e4m3_rows(row[None])
+    assert s2[0] == np.float32(0.125)
+    dec = torch.from_numpy(c2[0]).view(torch.float8_e4m3fn).to(torch.float64).numpy() * s2[0]
+    np.testing.assert_array_equal(dec, row.astype(np.float64))
+
+
+def test_expert_ffn_fp8_matches_numpy_with_torch_quantisation():
+    """The FP8 expert: weights = e4m3 * row scale; x and h quantised per row
+    (torch's cast of a / (amax / 448)); numpy matmuls in double."""
+    rng = np.random.default_rng(12)
+    n, H, I = 5, 64, 48
+    x = rng.standard_normal((n, H)).astype(np.float32)
+    wcodes = [_torch_e4m3(np.clip(rng.standard_normal(s) * 60, -448, 448)) for s in ((I, H), (I, H), (H, I))]
+    rs = [(rng.random(m) * 0.01 + 0.001).astype(np.float32) for m in (I, I, H)]
+
+    def dec(c):
+        return torch.from_numpy(c).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+    def quant(a32):
+        amax = np.abs(a32).max(1)
+        s = np.where(amax == 0, np.float32(1), amax / np.float32(448)).astype(np.float32)
+        return dec(_torch_e4m3(a32 / s[:, None])) * s[:, None].astype(np.float64)
+
+    wg, wu, wd = (dec(c) * r[:, None].astype(np.float64) for c, r in zip(wcodes, rs))
+    xq = quant(x)
+    ga, ua = xq @ wg.T, xq @ wu.T
+    h = ga / (1 + np.exp(-ga)) * ua
+    ref = quant(h.astype(np.float32)) @ wd.T
+    got, h_got = oracle.expert_ffn_fp8(x, *wcodes, *rs, want_h=True)
+    np.testing.assert_allclose(h_got, h, rtol=1e-12, atol=1e-12 * np.abs(h).max())
+    np.testing.assert_allclose(got, ref, rtol=1e-10, atol=1e-12 * np.abs(ref).max())
+    # BF16 x takes the same path from its exact values
+    xb = torch.from_numpy(x).to(torch.bfloat16)
+    bits = xb.view(torch.int16).numpy().view(np.uint16)
+    got_b = oracle.expert_ffn_fp8(bits, *wcodes, *rs)
+    xq_b = quant(xb.to(torch.float32).numpy())
+    gb, ub = xq_b @ wg.T, xq_b @ wu.T
+    ref_b = quant((gb / (1 + np.exp(-gb)) * ub).astype(np.float32)) @ wd.T
+    np.testing.assert_allclose(got_b, ref_b, rtol=1e-10, atol=1e-12 * np.abs(ref_b).max())

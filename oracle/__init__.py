@@ -48,7 +48,10 @@ Parity status of each function (what pins it is in ``tests/test_oracle_*``):
                    +-448, zero rows, power-of-two rows reconstruct exactly)
                    and torch's cast of a / (amax / 448).
 * ``expert_ffn_fp8`` pinned: numpy matmuls on values decoded and quantised by
-                   torch (float8_e4m3fn), independent of the oracle's encoder.
+                   torch (float8_e4m3fn), independent of the oracle's encoder,
+                   with h rounded to BF16 by torch.
+* ``round_bf16``   pinned: torch's float32 -> bfloat16 cast on float inputs
+                   (every tie of a random sample), closed forms on doubles.
 """
 from __future__ import annotations
 
@@ -92,6 +95,8 @@ def _load():
         lib.oracle_expert_ffn.restype = i32
         lib.oracle_expert_ffn_fp8.argtypes = [i64, i64, i64, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, i32]
         lib.oracle_expert_ffn_fp8.restype = i32
+        lib.oracle_round_bf16.argtypes = [dbl]
+        lib.oracle_round_bf16.restype = ctypes.c_float
         lib.oracle_encode_e4m3.argtypes = [ctypes.c_float]
         lib.oracle_encode_e4m3.restype = ctypes.c_uint8
         lib.oracle_quantize_e4m3_row.argtypes = [vp, i64, vp, vp]
@@ -233,6 +238,11 @@ def residual_update(y, stream, w, eps, k):
     if rc != 0:
         raise ValueError(f"oracle_residual_update failed ({rc})")
     return out
+
+
+def round_bf16(v: float) -> float:
+    """The BF16 value nearest to the double v (ties to even)."""
+    return float(_load().oracle_round_bf16(float(v)))
 
 
 def encode_e4m3(v) -> int:

@@ -143,6 +143,24 @@ double oracle_decode_e2m1(uint8_t nibble) {
   return sign ? -v : v;
 }
 
+/* double -> the nearest BF16 value (ties to even), as a float, rounded from
+ * the double's own value (no intermediate FP32 rounding): |v| is written in
+ * quanta of 2^(e-7) (8 significant bits in its binade 2^e) and rounded to a
+ * whole number of them. */
+float oracle_round_bf16(double v) {
+  if (v != v) return (float)v;
+  if (v == 0.0) return (float)v;
+  int e2;
+  const double a = fabs(v);
+  frexp(a, &e2); /* a in [2^(e2-1), 2^e2) */
+  int e = e2 - 1;
+  if (e < -126) e = -126; /* BF16 subnormals share FP32's exponent range */
+  const double q = nearbyint(ldexp(a, 7 - e)); /* quanta of 2^(e-7): 8 significant bits */
+  double r = ldexp(q, e - 7);
+  if (r > 0x1.FEp127) r = INFINITY; /* beyond the largest finite BF16 */
+  return (float)(v < 0 ? -r : r);
+}
+
 /* One element [row, k] of a weight matrix with `cols` columns (K). */
 typedef struct {
   int dtype;            /* ORACLE_F32 / ORACLE_BF16 / ORACLE_NVFP4 / ORACLE_FP8 */
@@ -421,12 +439,15 @@ int oracle_expert_ffn(int64_t H, int64_t I, int64_t n, const void* x, int x_dtyp
  * "Mixture of Experts") without giving its layout; it is read as E4M3
  * weights with one FP32 scale per output row (weight = e4m3 * row_scale) and
  * FP8 activations quantised per row at run time (oracle_quantize_e4m3_row):
- * the rows of x before gate/up, the rows of h before down.
+ * the rows of x before gate/up, the rows of h before down.  The quantised
+ * inputs are the block's activations in their storage type: x as given
+ * (FP32 or BF16), h as a BF16 tensor, i.e. rounded to BF16 (nearest even)
+ * before its row is quantised.
  *   x          [n, H]  FP32 or BF16 bits (x_dtype), quantised from its own values
  *   wg, wu     [I, H]  E4M3 codes; rg, ru [I] row scales
  *   wd         [H, I]  E4M3 codes; rd [H] row scales
- *   out        [n, H]  out;  h_out [n, I] out (nullable): h before quantisation
- * h = silu(xq . wg) * (xq . wu) in double; each h row is rounded to FP32 and
+ *   out        [n, H]  out;  h_out [n, I] out (nullable): h before rounding
+ * h = silu(xq . wg) * (xq . wu) in double; each h row is rounded to BF16 and
  * quantised; out = hq . wd.  Sums run in index order, in double.
  */
 int oracle_expert_ffn_fp8(int64_t H, int64_t I, int64_t n, const void* x, int x_dtype, const uint8_t* wg,
@@ -465,10 +486,10 @@ int oracle_expert_ffn_fp8(int64_t H, int64_t I, int64_t n, const void* x, int x_
     a.out = out;
     a.xq = xq;
     parallel_for(n * I, nthreads, ffn_hidden, &a);
-    /* h rows -> FP32 -> E4M3 codes and scales */
+    /* h rows -> BF16 -> E4M3 codes and scales */
     for (int64_t r = 0; r < n; ++r) {
       float sc;
-      for (int64_t i = 0; i < I; ++i) rowf[i] = (float)h[r * I + i];
+      for (int64_t i = 0; i < I; ++i) rowf[i] = oracle_round_bf16(h[r * I + i]);
       oracle_quantize_e4m3_row(rowf, I, codes, &sc);
       for (int64_t i = 0; i < I; ++i) hq[r * I + i] = oracle_decode_e4m3(codes[i]) * (double)sc;
     }

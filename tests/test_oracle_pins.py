@@ -495,10 +495,13 @@ def test_expert_ffn_fp8_matches_numpy_with_torch_quantisation():
         return dec(_torch_e4m3(a32 / s[:, None])) * s[:, None].astype(np.float64)
 
     wg, wu, wd = (dec(c) * r[:, None].astype(np.float64) for c, r in zip(wcodes, rs))
+    def bf16(a):  # h leaves the gate/up GEMM as a BF16 tensor
+        return torch.from_numpy(a.astype(np.float32)).to(torch.bfloat16).to(torch.float32).numpy()
+
     xq = quant(x)
     ga, ua = xq @ wg.T, xq @ wu.T
     h = ga / (1 + np.exp(-ga)) * ua
-    ref = quant(h.astype(np.float32)) @ wd.T
+    ref = quant(bf16(h)) @ wd.T
     got, h_got = oracle.expert_ffn_fp8(x, *wcodes, *rs, want_h=True)
     np.testing.assert_allclose(h_got, h, rtol=1e-12, atol=1e-12 * np.abs(h).max())
     np.testing.assert_allclose(got, ref, rtol=1e-10, atol=1e-12 * np.abs(ref).max())
@@ -508,5 +511,23 @@ def test_expert_ffn_fp8_matches_numpy_with_torch_quantisation():
     got_b = oracle.expert_ffn_fp8(bits, *wcodes, *rs)
     xq_b = quant(xb.to(torch.float32).numpy())
     gb, ub = xq_b @ wg.T, xq_b @ wu.T
-    ref_b = quant((gb / (1 + np.exp(-gb)) * ub).astype(np.float32)) @ wd.T
+    ref_b = quant(bf16(gb / (1 + np.exp(-gb)) * ub)) @ wd.T
     np.testing.assert_allclose(got_b, ref_b, rtol=1e-10, atol=1e-12 * np.abs(ref_b).max())
+
+
+def test_round_bf16():
+    """Nearest BF16 value, ties to even: torch's float32 -> bfloat16 cast on
+    float inputs (random values and exact midpoints); on doubles, values a hair
+    above or below a midpoint go up or down (no rounding through FP32)."""
+    rng = np.random.default_rng(21)
+    f = (rng.standard_normal(3000) * np.exp2(rng.integers(-30, 30, 3000))).astype(np.float32)
+    # exact midpoints between neighbouring BF16 values: low 16 bits 0x8000
+    mids = ((f.view(np.uint32) & 0xFFFF0000) | 0x8000).view(np.float32)
+    for v in np.concatenate([f, mids]):
+        want = torch.tensor([v]).to(torch.bfloat16).to(torch.float32).item()
+        assert oracle.round_bf16(float(v)) == want, v
+    m = 1.0 + 2.0 ** -8  # midpoint between 1 and 1 + 2^-7: tie to even (1.0)
+    assert oracle.round_bf16(m) == 1.0
+    assert oracle.round_bf16(m + 2.0 ** -40) == 1.0 + 2.0 ** -7  # above the midpoint (FP32 would round it to m)
+    assert oracle.round_bf16(-(m + 2.0 ** -40)) == -(1.0 + 2.0 ** -7)
+    assert oracle.round_bf16(1.0 + 3 * 2.0 ** -8) == 1.0 + 2 * 2.0 ** -7  # tie between odd and even: to even

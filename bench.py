@@ -165,7 +165,7 @@ def make_layer(wl, dev, layout=None):
     if (layout or WEIGHTS_LAYOUT) == "tiled":
         weights = moe.pack_weights(sh, d)
         torch.cuda.synchronize()
-    ws = moe.alloc_workspace(sh, "nvfp4" if wl.w_dtype == "nvfp4" else "bf16", dev)
+    ws = moe.alloc_workspace(sh, wl.w_dtype if wl.w_dtype in ("nvfp4", "fp8") else "bf16", dev)
     y = torch.empty((wl.T, wl.H), dtype=d["x"].dtype, device=dev)
     ids = torch.empty((wl.T, 8), dtype=torch.int32, device=dev)
     w = torch.empty((wl.T, 8), dtype=torch.float32, device=dev)
@@ -217,7 +217,7 @@ def measure(wl, steps, warmup, dev, world, sampler_index, state=None, residual_s
     ids_h = ids.cpu()
     touched = int(torch.unique(ids_h).numel())
     xdt = moe.BEAM_BF16 if d["x"].dtype == torch.bfloat16 else moe.BEAM_F32
-    launches = sum(moe.beam_moe_stage_kernel_count(sh, i, xdt) for i in range(len(STAGES)))
+    launches = sum(moe.beam_moe_stage_kernel_count(sh, i, xdt, call.weights) for i in range(len(STAGES)))
     out = dict(total_ms=total_ms, stage_ms=stage_ms, touched=touched, launches_per_step=launches,
                clocks=clk.summary(), counts=torch.bincount(ids_h.reshape(-1).long(), minlength=256))
     return out, state
@@ -297,6 +297,8 @@ def measure_e2e(wl, state, steps, warmup, dev):
 def weight_bytes_per_expert(wl):
     if wl.w_dtype == "nvfp4":
         return 3 * wl.H * wl.I // 2 + 3 * wl.H * wl.I // 16 + 12
+    if wl.w_dtype == "fp8":  # E4M3 codes + FP32 row scales
+        return 3 * wl.H * wl.I + 4 * (2 * wl.I + wl.H)
     return 3 * wl.H * wl.I * 2
 
 
@@ -322,19 +324,23 @@ def roofline(wl, m, pk):
     R = wl.T * 8
     ms = m["stage_ms"][STAGES.index("gate_up")]
     # gate + up weights of the touched experts: BF16 2 bytes per element,
-    # NVFP4 half a byte plus one E4M3 scale per 16 elements
-    per_elem = 0.5 + 1.0 / 16 if wl.w_dtype == "nvfp4" else 2.0
-    wbytes = int(m["touched"] * 2 * wl.I * wl.H * per_elem)
-    act_bytes = R * wl.H * 2 + R * wl.I * 2
+    # NVFP4 half a byte plus one E4M3 scale per 16 elements, FP8 one byte
+    # (+ an FP32 scale per row); activations: the route rows in (BF16, or
+    # E4M3 codes for FP8) and h out (BF16)
+    per_elem = {"nvfp4": 0.5 + 1.0 / 16, "fp8": 1.0}.get(wl.w_dtype, 2.0)
+    wbytes = int(m["touched"] * 2 * wl.I * wl.H * per_elem) + (m["touched"] * 2 * wl.I * 4 if wl.w_dtype == "fp8" else 0)
+    act_bytes = R * wl.H * (1 if wl.w_dtype == "fp8" else 2) + R * wl.I * 2
     flops = 2.0 * R * 2 * wl.I * wl.H
     gbs = (wbytes + act_bytes) / (ms * 1e-3) / 1e9
     tfs = flops / (ms * 1e-3) / 1e12
     hbm = dict(bound="hbm", achieved=round(gbs, 1), peak=pk["hbm"], unit="GB/s", frac=round(gbs / pk["hbm"], 4),
                traffic=traffic_record("moe_gemm_gate_up", wl.name), kernel="moe_gemm_kernel<0> (gate/up + SwiGLU)",
                algorithmic_bytes=wbytes + act_bytes, launch_ms=round(ms, 4), peak_source=pk["source"])
-    tc = dict(bound="tensor", achieved=round(tfs, 1), peak=pk["bf16"], unit="TFLOP/s", frac=round(tfs / pk["bf16"], 4),
+    # FP8 MMAs: the measured BF16 peak times the nominal FP8 / BF16 ratio (2)
+    tpk = pk["bf16"] * (2.0 if wl.w_dtype == "fp8" else 1.0)
+    tc = dict(bound="tensor", achieved=round(tfs, 1), peak=round(tpk, 1), unit="TFLOP/s", frac=round(tfs / tpk, 4),
               traffic=hbm["traffic"], kernel=hbm["kernel"], algorithmic_flops=flops, launch_ms=round(ms, 4),
-              peak_source=pk["source"])
+              peak_source=pk["source"] + (" bf16 x 2 (nominal fp8 / bf16 ratio)" if wl.w_dtype == "fp8" else ""))
     return hbm, tc
 
 
@@ -463,6 +469,8 @@ def main():
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-fp8", action="store_true",
+                    help="skip the FP8-weight layers (decode T=64 and prefill T=8192)")
     ap.add_argument("--no-residual", action="store_true",
                     help="skip the extra steps with the post-norm residual update fused into the combine")
     ap.add_argument("--small", action="store_true",
@@ -532,6 +540,22 @@ def main():
         del pstate
         torch.cuda.empty_cache()
 
+    fp8 = None
+    if not args.no_fp8 and not args.small:
+        fp8 = {}
+        for name, steps in (("fp8_decode", args.steps), ("fp8", max(3, args.steps // 2))):
+            fw = inputs.workload(name)
+            fm, fstate = measure(fw, steps, args.warmup, dev, world, torch.cuda.current_device())
+            f_ms = max_over_ranks(fm["total_ms"], world)
+            fhbm, ftc = roofline(fw, fm, pk)
+            fp8[name] = dict(value=fw.T * steps * world / (f_ms * 1e-3), unit="tokens/s",
+                             config={"workload": f"{name} T={fw.T} H={fw.H} I={fw.I} E=256 fp8 experts "
+                                                 "(E4M3 + row scales), E4M3 activations per row", "T": fw.T},
+                             roofline_hbm=fhbm, roofline=ftc, clocks=fm["clocks"],
+                             gpu_launches=fm["launches_per_step"] * steps, **step_numbers(fw, fm, steps))
+            del fstate
+            torch.cuda.empty_cache()
+
     if rank != 0:
         return
     line = {
@@ -545,7 +569,7 @@ def main():
                          f"({m['touched']} x {weight_bytes_per_expert(wl) / 1e6:.1f} MB), far larger than L2"},
         "roofline": hbm, "roofline_tensor": tc, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": m["launches_per_step"] * args.steps, "clocks": m["clocks"],
-        "step": sn, "residual_epilogue": residual, "prefill": prefill,
+        "step": sn, "residual_epilogue": residual, "prefill": prefill, "fp8": fp8,
     }
     print(json.dumps(line), flush=True)
 

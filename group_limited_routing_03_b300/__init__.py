@@ -31,7 +31,7 @@ _LIB_PATH = os.path.join(_PKG, "libbeam_moe.so")
 
 BEAM_OK, BEAM_ERR_INVALID_ARG, BEAM_ERR_UNSUPPORTED, BEAM_ERR_WORKSPACE = 0, 1, 2, 3
 BEAM_ERR_CUDA, BEAM_ERR_TIMEOUT, BEAM_ERR_DEVICE_CHECK = 4, 5, 6
-BEAM_F32, BEAM_BF16, BEAM_NVFP4 = 0, 1, 2
+BEAM_F32, BEAM_BF16, BEAM_NVFP4, BEAM_FP8 = 0, 1, 2, 3
 
 
 class BeamError(RuntimeError):
@@ -50,7 +50,8 @@ class _ExpertWeights(ctypes.Structure):
     _fields_ = [("dtype", ctypes.c_int), ("gate", ctypes.c_void_p), ("up", ctypes.c_void_p),
                 ("down", ctypes.c_void_p), ("gate_sf", ctypes.c_void_p), ("up_sf", ctypes.c_void_p),
                 ("down_sf", ctypes.c_void_p), ("gate_gs", ctypes.c_void_p), ("up_gs", ctypes.c_void_p),
-                ("down_gs", ctypes.c_void_p), ("layout", ctypes.c_int)]
+                ("down_gs", ctypes.c_void_p), ("layout", ctypes.c_int), ("gate_rs", ctypes.c_void_p),
+                ("up_rs", ctypes.c_void_p), ("down_rs", ctypes.c_void_p)]
 
 
 BEAM_LAYOUT_ROWS, BEAM_LAYOUT_TILED = 0, 1
@@ -73,7 +74,7 @@ STAGES = ("route", "dispatch", "gather", "gate_up", "down", "combine")
 
 class _WsLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in ("status", "counts", "offsets", "perm", "pos", "xp", "h", "yr",
-                                               "total")]
+                                               "total", "xq", "hq", "xs", "hs")]
 
 
 _lib = None
@@ -105,7 +106,7 @@ def load():
     lib.beam_moe_read_device_status.argtypes = [vp, ctypes.POINTER(u32), vp]
     lib.beam_moe_route_noalloc.argtypes = [sp, vp, i32, vp, vp, vp, vp, vp]
     lib.beam_moe_route_noalloc.restype = i32
-    lib.beam_moe_stage_kernel_count.argtypes = [sp, i32, i32]
+    lib.beam_moe_stage_kernel_count.argtypes = [sp, i32, i32, i32]
     lib.beam_moe_stage_kernel_count.restype = ctypes.c_int32
     lib.beam_moe_debug_timeout.argtypes = [vp, sz, u32, vp]
     lib.beam_moe_pack_weights.argtypes = [sp, ctypes.POINTER(_ExpertWeights), ctypes.POINTER(_ExpertWeights), vp]
@@ -159,9 +160,13 @@ def _weights(w: dict) -> _ExpertWeights:
         ew.dtype = BEAM_BF16
     elif w["gate"].dtype == torch.uint8:
         ew.dtype = BEAM_NVFP4
+    elif w["gate"].dtype == torch.float8_e4m3fn:
+        ew.dtype = BEAM_FP8
     else:
-        raise TypeError(f"expert weights must be bfloat16 or packed NVFP4 (uint8), got {w['gate'].dtype}")
-    for name in ("gate", "up", "down", "gate_sf", "up_sf", "down_sf", "gate_gs", "up_gs", "down_gs"):
+        raise TypeError(f"expert weights must be bfloat16, packed NVFP4 (uint8) or float8_e4m3fn, "
+                        f"got {w['gate'].dtype}")
+    for name in ("gate", "up", "down", "gate_sf", "up_sf", "down_sf", "gate_gs", "up_gs", "down_gs", "gate_rs",
+                 "up_rs", "down_rs"):
         t = w.get(name)
         setattr(ew, name, None if t is None else _ptr(t).value)
     ew.layout = {"rows": BEAM_LAYOUT_ROWS, "tiled": BEAM_LAYOUT_TILED}[w.get("layout", "rows")]
@@ -177,7 +182,9 @@ def _wdtype(w) -> int:
     if isinstance(w, int):
         return w
     if isinstance(w, str):
-        return {"bf16": BEAM_BF16, "nvfp4": BEAM_NVFP4}[w]
+        return {"bf16": BEAM_BF16, "nvfp4": BEAM_NVFP4, "fp8": BEAM_FP8}[w]
+    if w["gate"].dtype == torch.float8_e4m3fn:
+        return BEAM_FP8
     return BEAM_NVFP4 if w["gate"].dtype == torch.uint8 else BEAM_BF16
 
 
@@ -321,9 +328,9 @@ def pack_weights(sh, weights: dict, stream=None) -> dict:
     return out
 
 
-def beam_moe_stage_kernel_count(sh, stage: int, xdtype=BEAM_BF16) -> int:
+def beam_moe_stage_kernel_count(sh, stage: int, xdtype=BEAM_BF16, wdtype=BEAM_BF16) -> int:
     """Kernels the library launches for stage ``stage`` of a forward of ``sh``."""
-    n = int(load().beam_moe_stage_kernel_count(ctypes.byref(sh), int(xdtype), int(stage)))
+    n = int(load().beam_moe_stage_kernel_count(ctypes.byref(sh), int(xdtype), _wdtype(wdtype), int(stage)))
     if n < 0:
         raise BeamError(BEAM_ERR_UNSUPPORTED, "beam_moe_stage_kernel_count")
     return n

@@ -94,9 +94,28 @@ bool make_u8_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t ro
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D row-major byte matrix [rows, inner], boxes box_rows x 128 bytes with the
+// 128-byte swizzle the MMA descriptors expect (FP8 operand tiles).
+bool make_u8_sw128_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[2] = {inner, rows};
+  const cuuint64_t strides[1] = {inner};
+  const cuuint32_t box[2] = {128, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // ------------------------------------------------------------------ layout
+// FP8 weights: the E4M3 codes of x (xq, R_pad x H bytes) and of h (hq, R_pad x
+// I bytes, I <= H) share the xp region, which the BF16 rows do not use then;
+// xs / hs hold their row scales (R_pad + 32 floats: the GEMM epilogue reads
+// the scales of whole 16-column groups).
 struct Layout {
-  size_t status, sched, counts, offsets, chunk_prefix, tile_hist, part, wsplit, perm, pos, xp, h, yr, total;
+  size_t status, sched, counts, offsets, chunk_prefix, tile_hist, part, wsplit, perm, pos, xp, h, yr, xs, hs, total;
+  size_t xq, hq;
   int n_tiles, split_cap;
 };
 
@@ -129,6 +148,10 @@ void make_layout(const beam_moe_shape_t& s, Layout& L) {
   L.xp = take(R_pad * H * 2);
   L.h = take(R_pad * I * 2);
   L.yr = take(R_pad * H * 2);
+  L.xs = take((R_pad + 32) * 4);
+  L.hs = take((R_pad + 32) * 4);
+  L.xq = L.xp;
+  L.hq = L.xp + align256(R_pad * H);
   L.total = off;
 }
 
@@ -155,6 +178,17 @@ beam_status_t check_workspace(const beam_moe_shape_t* s, const void* ws, size_t 
 beam_status_t check_weights(const beam_moe_shape_t* s, const beam_expert_weights_t* w) {
   if (w == nullptr) return BEAM_ERR_INVALID_ARG;
   if (w->layout != BEAM_LAYOUT_ROWS && w->layout != BEAM_LAYOUT_TILED) return BEAM_ERR_INVALID_ARG;
+  if (w->dtype == BEAM_FP8) {
+    if (!w->gate || !w->up || !w->down || !w->gate_rs || !w->up_rs || !w->down_rs) return BEAM_ERR_INVALID_ARG;
+    if (!aligned16(w->gate) || !aligned16(w->up) || !aligned16(w->down) || !aligned16(w->gate_rs) ||
+        !aligned16(w->up_rs) || !aligned16(w->down_rs))
+      return BEAM_ERR_INVALID_ARG;
+    if (w->gate_sf || w->up_sf || w->down_sf || w->gate_gs || w->up_gs || w->down_gs) return BEAM_ERR_INVALID_ARG;
+    // h's codes share the x-code buffer (I <= H); the k-block is 128 elements
+    if (s->I > s->H) return BEAM_ERR_UNSUPPORTED;
+    return BEAM_OK;
+  }
+  if (w->gate_rs || w->up_rs || w->down_rs) return BEAM_ERR_INVALID_ARG;
   if (w->dtype == BEAM_BF16) {
     if (!w->gate || !w->up || !w->down) return BEAM_ERR_INVALID_ARG;
     if (!aligned16(w->gate) || !aligned16(w->up) || !aligned16(w->down)) return BEAM_ERR_INVALID_ARG;
@@ -250,8 +284,11 @@ uint32_t pow2_at_least(uint32_t v) {
   return p;
 }
 
-beam_status_t run_gather(const beam_moe_shape_t& s, const void* x, bool x_bf16, void* ws, const Layout& L,
+beam_status_t run_gather(const beam_moe_shape_t& s, const void* x, bool x_bf16, bool fp8, void* ws, const Layout& L,
                          const DeviceInfo& d, cudaStream_t stream) {
+  if (fp8)
+    return cuda_status(launch_gather_q8(x, x_bf16, s.H, at<int32_t>(ws, L.pos), s.T, at<uint8_t>(ws, L.xq),
+                                        at<float>(ws, L.xs), stream));
   return cuda_status(launch_gather(x, x_bf16, s.H, at<int32_t>(ws, L.pos), s.T, at<__nv_bfloat16>(ws, L.xp), d.sms,
                                    stream));
 }
@@ -262,7 +299,14 @@ beam_status_t run_gemm(int mode, const beam_moe_shape_t& s, const beam_expert_we
   const int R = s.T * kTopK;
   const uint64_t R_pad = static_cast<uint64_t>((R + kBoxRows - 1) / kBoxRows * kBoxRows);
   const bool fp4 = wts->dtype == BEAM_NVFP4;
+  const bool fp8 = wts->dtype == BEAM_FP8;
   const int nmax = chunk_rows(s.T, fp4);
+  // FP8: h's row quantisation comes first (its scales need whole rows of h)
+  if (fp8 && mode == 1) {
+    const cudaError_t e = launch_quantize_rows(at<__nv_bfloat16>(ws, L.h), s.T * kTopK, s.I, at<uint8_t>(ws, L.hq),
+                                               at<float>(ws, L.hs), stream);
+    if (e != cudaSuccess) return BEAM_ERR_CUDA;
+  }
   __nv_bfloat16* xp = at<__nv_bfloat16>(ws, L.xp);
   __nv_bfloat16* h = at<__nv_bfloat16>(ws, L.h);
   __nv_bfloat16* yr = at<__nv_bfloat16>(ws, L.yr);
@@ -286,7 +330,20 @@ beam_status_t run_gemm(int mode, const beam_moe_shape_t& s, const beam_expert_we
     return tiled ? make_u8_map(m, base, kScaleBoxCols, E * N * (K / (16 * kScaleBoxCols)), kScaleBoxCols, kBlockM)
                  : make_u8_map(m, base, K / 16, E * N, kScaleBoxCols, kBlockM);
   };
-  if (mode == 0) {
+  // FP8: E4M3 weight tiles of 128 rows x 128 bytes (128 K elements)
+  auto wmap_f8 = [&](CUtensorMap* m, const void* base, uint64_t N, uint64_t K) {
+    return tiled ? make_u8_sw128_map(m, base, 128, E * N * (K / 128), kBlockM) : make_u8_sw128_map(m, base, K, E * N, kBlockM);
+  };
+  uint8_t* xq = at<uint8_t>(ws, L.xq);
+  uint8_t* hq = at<uint8_t>(ws, L.hq);
+  if (fp8) {
+    if (mode == 0)
+      ok = make_u8_sw128_map(&maps.b, xq, H, R_pad, kBoxRows) && wmap_f8(&maps.a0, wts->gate, I, H) &&
+           wmap_f8(&maps.a1, wts->up, I, H);
+    else
+      ok = make_u8_sw128_map(&maps.b, hq, I, R_pad, kBoxRows) && wmap_f8(&maps.a0, wts->down, H, I);
+    if (mode == 1) maps.a1 = maps.a0;
+  } else if (mode == 0) {
     ok = make_bf16_map(&maps.b, xp, H, R_pad, kBoxRows);
     if (fp4)
       ok = ok && wmap_codes(&maps.a0, wts->gate, I, H) && wmap_codes(&maps.a1, wts->up, I, H) &&
@@ -332,7 +389,7 @@ beam_status_t run_gemm(int mode, const beam_moe_shape_t& s, const beam_expert_we
   p.chunk_prefix = at<int32_t>(ws, L.chunk_prefix);
   p.m_tiles = (mode == 0 ? s.I : s.H) / rows_per_unit;
   p.a_rows_per_expert = mode == 0 ? s.I : s.H;
-  p.k_blocks = (mode == 0 ? s.H : s.I) / kBlockK;
+  p.k_blocks = (mode == 0 ? s.H : s.I) / (fp8 ? 2 * kBlockK : kBlockK);
   p.a_tiled = tiled ? 1 : 0;
   p.nmax = nmax;
   const int num_a = (mode == 0 || pair || fp4 || wide) ? 2 : 1;  // weight tiles per stage
@@ -369,6 +426,9 @@ beam_status_t run_gemm(int mode, const beam_moe_shape_t& s, const beam_expert_we
   p.out_ld = mode == 0 ? s.I : s.H;
   p.gs0 = fp4 ? (mode == 0 ? wts->gate_gs : wts->down_gs) : nullptr;
   p.gs1 = fp4 && mode == 0 ? wts->up_gs : nullptr;
+  p.rs0 = fp8 ? (mode == 0 ? wts->gate_rs : wts->down_rs) : nullptr;
+  p.rs1 = fp8 && mode == 0 ? wts->up_rs : nullptr;
+  p.bscale = fp8 ? at<float>(ws, mode == 0 ? L.xs : L.hs) : nullptr;
   p.status = at<uint32_t>(ws, L.status);
   p.timeout_ns = kDefaultTimeoutNs;
   const size_t smem = gemm_smem_bytes(stages, acc_stages, sb);
@@ -377,11 +437,15 @@ beam_status_t run_gemm(int mode, const beam_moe_shape_t& s, const beam_expert_we
   const int grid = pair ? 2 * (clusters < d.sms / 2 ? clusters : d.sms / 2) : d.sms;
   // activations in one box per k-block: the B tile's full height
   p.b_big_rows = pair ? nmax / 2 : nmax;
-  if (!make_bf16_map(&maps.bb, mode == 0 ? static_cast<const void*>(xp) : static_cast<const void*>(h),
-                     mode == 0 ? H : I, R_pad, static_cast<uint32_t>(p.b_big_rows)))
+  if (fp8) {
+    if (!make_u8_sw128_map(&maps.bb, mode == 0 ? xq : hq, mode == 0 ? H : I, R_pad, static_cast<uint32_t>(p.b_big_rows)))
+      return BEAM_ERR_CUDA;
+  } else if (!make_bf16_map(&maps.bb, mode == 0 ? static_cast<const void*>(xp) : static_cast<const void*>(h),
+                            mode == 0 ? H : I, R_pad, static_cast<uint32_t>(p.b_big_rows))) {
     return BEAM_ERR_CUDA;
+  }
   if (cudaMemsetAsync(p.sched, 0, sizeof(int), stream) != cudaSuccess) return BEAM_ERR_CUDA;
-  return cuda_status(launch_gemm(mode, fp4, pair, wide, maps, p, grid, smem, stream));
+  return cuda_status(launch_gemm(mode, fp4, pair, wide, fp8, maps, p, grid, smem, stream));
 }
 
 beam_status_t run_combine(const beam_moe_shape_t& s, const float* w, void* y, bool y_bf16, void* ws, const Layout& L,
@@ -394,7 +458,7 @@ beam_status_t run_experts(const beam_moe_shape_t& s, const void* x, bool x_bf16,
                           const int32_t* ids, const float* w, void* y, void* ws, const Layout& L,
                           const DeviceInfo& d, bool hist_ready, cudaStream_t stream) {
   beam_status_t st = run_dispatch(s, ids, ws, L, chunk_rows(s.T, wts->dtype == BEAM_NVFP4), hist_ready, stream);
-  if (st == BEAM_OK) st = run_gather(s, x, x_bf16, ws, L, d, stream);
+  if (st == BEAM_OK) st = run_gather(s, x, x_bf16, wts->dtype == BEAM_FP8, ws, L, d, stream);
   if (st == BEAM_OK) st = run_gemm(0, s, wts, ws, L, d, stream);
   if (st == BEAM_OK) st = run_gemm(1, s, wts, ws, L, d, stream);
   if (st == BEAM_OK) st = run_combine(s, w, y, x_bf16, ws, L, stream);
@@ -465,7 +529,7 @@ beam_status_t run_stage(const beam_moe_shape_t& s, const beam_moe_args_t& a, int
     case BEAM_STAGE_DISPATCH:
       return run_dispatch(s, a.topk_ids, ws, L, chunk_rows(s.T, a.weights->dtype == BEAM_NVFP4), true, cs);
     case BEAM_STAGE_GATHER:
-      return run_gather(s, a.x, xb, ws, L, d, cs);
+      return run_gather(s, a.x, xb, a.weights->dtype == BEAM_FP8, ws, L, d, cs);
     case BEAM_STAGE_GATE_UP:
       return run_gemm(0, s, a.weights, ws, L, d, cs);
     case BEAM_STAGE_DOWN:
@@ -486,7 +550,7 @@ extern "C" {
 
 size_t beam_moe_workspace_size(const beam_moe_shape_t* shape, beam_dtype_t wdtype) {
   if (check_shape(shape) != BEAM_OK) return 0;
-  if (wdtype != BEAM_BF16 && wdtype != BEAM_NVFP4) return 0;
+  if (wdtype != BEAM_BF16 && wdtype != BEAM_NVFP4 && wdtype != BEAM_FP8) return 0;
   Layout L;
   make_layout(*shape, L);
   return L.total;
@@ -496,9 +560,13 @@ beam_status_t beam_moe_workspace_layout(const beam_moe_shape_t* shape, beam_dtyp
   const beam_status_t st = check_shape(shape);
   if (st != BEAM_OK) return st;
   if (out == nullptr) return BEAM_ERR_INVALID_ARG;
-  if (wdtype != BEAM_BF16 && wdtype != BEAM_NVFP4) return BEAM_ERR_UNSUPPORTED;
+  if (wdtype != BEAM_BF16 && wdtype != BEAM_NVFP4 && wdtype != BEAM_FP8) return BEAM_ERR_UNSUPPORTED;
   Layout L;
   make_layout(*shape, L);
+  out->xq = L.xq;
+  out->hq = L.hq;
+  out->xs = L.xs;
+  out->hs = L.hs;
   out->status = L.status;
   out->counts = L.counts;
   out->offsets = L.offsets;
@@ -602,8 +670,11 @@ beam_status_t beam_moe_forward_stage(const beam_moe_shape_t* shape, const beam_m
   return run_stage(*shape, *args, stage, workspace, L, d, static_cast<cudaStream_t>(stream));
 }
 
-int32_t beam_moe_stage_kernel_count(const beam_moe_shape_t* shape, beam_dtype_t xdtype, beam_stage_t stage) {
+int32_t beam_moe_stage_kernel_count(const beam_moe_shape_t* shape, beam_dtype_t xdtype, beam_dtype_t wdtype,
+                                    beam_stage_t stage) {
   if (check_shape(shape) != BEAM_OK) return -1;
+  if (xdtype != BEAM_F32 && xdtype != BEAM_BF16) return -1;
+  if (wdtype != BEAM_BF16 && wdtype != BEAM_NVFP4 && wdtype != BEAM_FP8) return -1;
   DeviceInfo d;
   if (!device_info(d)) return -1;
   switch (stage) {
@@ -617,9 +688,9 @@ int32_t beam_moe_stage_kernel_count(const beam_moe_shape_t* shape, beam_dtype_t 
       return sp > 1 ? 2 : 1;
     }
     case BEAM_STAGE_DISPATCH: return 2;
+    case BEAM_STAGE_DOWN: return wdtype == BEAM_FP8 ? 2 : 1;  // FP8: h quantised first
     case BEAM_STAGE_GATHER:
     case BEAM_STAGE_GATE_UP:
-    case BEAM_STAGE_DOWN:
     case BEAM_STAGE_COMBINE: return 1;
     default: return -1;
   }
@@ -648,7 +719,10 @@ beam_status_t beam_moe_pack_weights(const beam_moe_shape_t* shape, const beam_ex
   if (st == BEAM_OK) st = check_weights(shape, &probe);
   if (st != BEAM_OK) return st;
   const size_t E = kExperts, H = shape->H, I = shape->I;
-  const bool fp4 = src->dtype == BEAM_NVFP4;
+  const bool fp4 = src->dtype == BEAM_NVFP4, fp8 = src->dtype == BEAM_FP8;
+  // FP8 row scales keep their order: the same arrays serve both layouts
+  if (fp8 && (dst->gate_rs != src->gate_rs || dst->up_rs != src->up_rs || dst->down_rs != src->down_rs))
+    return BEAM_ERR_INVALID_ARG;
   // (array, rows, row bytes, tile row bytes) for gate, up, down [, their scales]
   struct Job {
     const void* s;
@@ -658,8 +732,8 @@ beam_status_t beam_moe_pack_weights(const beam_moe_shape_t* shape, const beam_ex
   };
   Job jobs[6];
   int n = 0;
-  const uint32_t wb = fp4 ? kBlockK / 2 : kBlockK * 2;  // bytes of 64 K elements
-  auto row_bytes = [&](size_t K) { return fp4 ? K / 2 : K * 2; };
+  const uint32_t wb = fp4 ? kBlockK / 2 : kBlockK * 2;  // tile row: 64 K elements (BF16, E2M1), 128 (E4M3)
+  auto row_bytes = [&](size_t K) { return fp4 ? K / 2 : (fp8 ? K : K * 2); };
   jobs[n++] = {src->gate, dst->gate, E * I, row_bytes(H), wb};
   jobs[n++] = {src->up, dst->up, E * I, row_bytes(H), wb};
   jobs[n++] = {src->down, dst->down, E * H, row_bytes(I), wb};

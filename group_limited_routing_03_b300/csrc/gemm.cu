@@ -155,7 +155,10 @@ __device__ __forceinline__ void e2m1x8_to_bf16(uint32_t w, uint32_t scale2, uint
 // both CTAs; both epilogues release the even CTA's acc_empty barrier.
 // kWide (down, one CTA per unit, BF16): 256-row units of two 128-row tiles,
 // two accumulators, so each k-block carries eight MMAs in two chains.
-template <int kMode, bool kFp4, bool kPair, bool kWide = false>
+// kFp8: E4M3 weights and E4M3 activations (kind::f8f6f4): the same tiles of
+// 128-byte rows, now 128 K elements per k-block; the epilogue multiplies each
+// accumulator element by its weight row's scale and its token row's scale.
+template <int kMode, bool kFp4, bool kPair, bool kWide = false, bool kFp8 = false>
 __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
     moe_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
   // Weight tiles per stage: gate/up always two (gate, up); down two on CTA
@@ -166,7 +169,9 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
   constexpr int kRowsPerUnit = kPair ? (kMode == 0 ? 2 * kBlockM : 4 * kBlockM) : (kNumA == 2 && kMode == 1 ? 2 * kBlockM : kBlockM);
   // down with two tiles: feature offset of the second tile's rows
   constexpr int kHalfRows = kPair ? 2 * kBlockM : kBlockM;
-  static_assert(!(kPair && kFp4), "pair MMA path is BF16 only");
+  static_assert(!(kPair && kFp4), "pair MMA path is BF16 / FP8 only");
+  static_assert(!(kFp4 && kFp8), "one weight format");
+  constexpr int kKElems = kFp8 ? 2 * kBlockK : kBlockK;  // K elements per k-block (128-byte rows)
   // Roles that read every scheduled unit index (they release ring slots).
   constexpr uint32_t kRingConsumers =
       kPair ? (1 + kEpilogueWarps) + (1 + kEpilogueWarps)  // even CTA: MMA + epilogue; odd: producer + epilogue
@@ -335,7 +340,7 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
             ok = false;
             break;
           }
-          const int kx = kb * kBlockK;
+          const int kx = kb * kKElems;
           if (kPair) {
             // both CTAs' bytes land on the even CTA's full barrier
             const uint32_t bar0 = mapa_shared(&full[stage], 0);
@@ -395,7 +400,8 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
         if (!ring_take(u) || u < 0) break;
         const Unit U = unit_at(p, u);
         const uint32_t n_mma = static_cast<uint32_t>((U.n + 15) & ~15);
-        const uint32_t idesc = idesc_bf16_f32(kPair ? 2 * kBlockM : kBlockM, n_mma);
+        const uint32_t idesc = kFp8 ? idesc_e4m3_f32(kPair ? 2 * kBlockM : kBlockM, n_mma)
+                                    : idesc_bf16_f32(kPair ? 2 * kBlockM : kBlockM, n_mma);
         if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1u, p.timeout_ns, abort_flag, p.status, kWhereMmaAccEmpty))
           break;
         tc_fence_after();
@@ -425,9 +431,15 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
 #pragma unroll
             for (int k = 0; k < kBlockK / 16; ++k) {
               const uint32_t accumulate = (kb | k) != 0 ? 1u : 0u;
-              if (kPair) {
+              if (kPair && kFp8) {
+                mma_f8_pair(d0, da0 + 2u * k, db + 2u * k, idesc, accumulate);
+                mma_f8_pair(d1, da1 + 2u * k, db + 2u * k, idesc, accumulate);
+              } else if (kPair) {
                 mma_bf16_pair(d0, da0 + 2u * k, db + 2u * k, idesc, accumulate);
                 mma_bf16_pair(d1, da1 + 2u * k, db + 2u * k, idesc, accumulate);
+              } else if (kFp8) {
+                mma_f8(d0, da0 + 2u * k, db + 2u * k, idesc, accumulate);
+                if (kNumA == 2) mma_f8(d1, da1 + 2u * k, db + 2u * k, idesc, accumulate);
               } else {
                 mma_bf16(d0, da0 + 2u * k, db + 2u * k, idesc, accumulate);
                 if (kNumA == 2) mma_bf16(d1, da1 + 2u * k, db + 2u * k, idesc, accumulate);
@@ -481,15 +493,24 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
       tc_fence_after();
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc) * p.acc_cols;
       const int feat = U.m * kRowsPerUnit + static_cast<int>(rank) * kBlockM + row;
-      const float s0 = p.gs0 != nullptr ? __ldg(&p.gs0[U.e]) : 1.0f;
-      const float s1 = (kMode == 0 && p.gs1 != nullptr) ? __ldg(&p.gs1[U.e]) : 1.0f;
+      constexpr int kOut = (kMode == 1 && kNumA == 2) ? 2 : 1;      // down with two weight tiles
+      // Row scales: NVFP4 the global scale of each matrix; FP8 this thread's
+      // weight row (s0: gate or down, s1: up, or the down unit's second tile)
+      float s0, s1;
+      if (kFp8) {
+        const size_t rrow = static_cast<size_t>(U.e) * p.a_rows_per_expert + feat;
+        s0 = __ldg(&p.rs0[rrow]);
+        s1 = kMode == 0 ? __ldg(&p.rs1[rrow]) : (kOut == 2 ? __ldg(&p.rs0[rrow + kHalfRows]) : 1.0f);
+      } else {
+        s0 = p.gs0 != nullptr ? __ldg(&p.gs0[U.e]) : 1.0f;
+        s1 = (kMode == 0 && p.gs1 != nullptr) ? __ldg(&p.gs1[U.e]) : 1.0f;
+      }
       const int ncols = (U.n + 15) & ~15;
       __nv_bfloat16* out = p.out + static_cast<size_t>(U.start) * p.out_ld + feat;
       // 1) TMEM -> packed BF16 results in registers (this warp's 16-column
       //    chunks), 2) release the accumulator so the next unit's MMAs start,
       //    3) global stores.
       constexpr int kMaxChunks = (kFp4 ? kChunkRowsFp4 : kChunkRowsBf16) / 32;  // columns / (2 x 16)
-      constexpr int kOut = (kMode == 1 && kNumA == 2) ? 2 : 1;      // down with two weight tiles
       uint32_t hp[kOut][kMaxChunks][8];
 #pragma unroll
       for (int ci = 0; ci < kMaxChunks; ++ci) {
@@ -499,6 +520,16 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
           tmem_ld16(tbase + static_cast<uint32_t>(c0), g);
           if (kNumA == 2) tmem_ld16(tbase + static_cast<uint32_t>(p.nmax + c0), g2);
           tmem_ld_wait();
+          if (kFp8) {
+            // token row scales of these 16 columns (the scale array is padded
+            // past the last route, so columns beyond the chunk read in bounds)
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const float cs = __ldg(&p.bscale[U.start + c0 + j]);
+              g[j] *= cs;
+              if (kNumA == 2) g2[j] *= cs;
+            }
+          }
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             float v0, v1;
@@ -515,7 +546,8 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
             __nv_bfloat162 q = __floats2bfloat162_rn(v0, v1);
             hp[0][ci][j] = *reinterpret_cast<uint32_t*>(&q);
             if (kOut == 2) {
-              __nv_bfloat162 q2 = __floats2bfloat162_rn(g2[2 * j] * s0, g2[2 * j + 1] * s0);
+              const float sb = kFp8 ? s1 : s0;  // the second tile's row scale
+              __nv_bfloat162 q2 = __floats2bfloat162_rn(g2[2 * j] * sb, g2[2 * j + 1] * sb);
               hp[kOut - 1][ci][j] = *reinterpret_cast<uint32_t*>(&q2);
             }
           }
@@ -650,9 +682,9 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
   }
 }
 
-template <int kMode, bool kFp4, bool kPair, bool kWide = false>
+template <int kMode, bool kFp4, bool kPair, bool kWide = false, bool kFp8 = false>
 cudaError_t launch_one(const GemmMaps& maps, const GemmParams& p, int grid, size_t smem_bytes, cudaStream_t stream) {
-  auto kern = moe_gemm_kernel<kMode, kFp4, kPair, kWide>;
+  auto kern = moe_gemm_kernel<kMode, kFp4, kPair, kWide, kFp8>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_bytes));
   if (err != cudaSuccess) return err;
   if (!kPair) {
@@ -708,8 +740,17 @@ int gemm_pair_max_clusters(int mode, size_t smem_bytes) {
   return n;
 }
 
-cudaError_t launch_gemm(int mode, bool fp4, bool pair, bool wide, const GemmMaps& maps, const GemmParams& p, int grid,
-                        size_t smem_bytes, cudaStream_t stream) {
+cudaError_t launch_gemm(int mode, bool fp4, bool pair, bool wide, bool fp8, const GemmMaps& maps, const GemmParams& p,
+                        int grid, size_t smem_bytes, cudaStream_t stream) {
+  if (fp8) {
+    if (fp4) return cudaErrorInvalidValue;
+    if (pair)
+      return mode == 0 ? launch_one<0, false, true, false, true>(maps, p, grid, smem_bytes, stream)
+                       : launch_one<1, false, true, false, true>(maps, p, grid, smem_bytes, stream);
+    if (mode == 0) return launch_one<0, false, false, false, true>(maps, p, grid, smem_bytes, stream);
+    return wide ? launch_one<1, false, false, true, true>(maps, p, grid, smem_bytes, stream)
+                : launch_one<1, false, false, false, true>(maps, p, grid, smem_bytes, stream);
+  }
   if (pair) {
     if (fp4) return cudaErrorInvalidValue;
     return mode == 0 ? launch_one<0, false, true>(maps, p, grid, smem_bytes, stream)

@@ -71,6 +71,9 @@ struct GemmParams {
   int out_ld;                   // I or H
   const float* gs0;             // NVFP4 global scales (gate or down) [E], else null
   const float* gs1;             // NVFP4 global scale (up) [E], else null
+  const float* rs0;             // FP8 row scales (gate or down) [E * rows], else null
+  const float* rs1;             // FP8 row scales (up) [E * I], else null
+  const float* bscale;          // FP8 token-row scales [R_pad + 32] (x or h rows, perm order), else null
   uint32_t* status;
   uint64_t timeout_ns;
 };
@@ -119,9 +122,18 @@ cudaError_t launch_dispatch(const int32_t* ids, int R, int n_tiles, int32_t* til
                             int32_t* perm, int32_t* pos, cudaStream_t stream);
 cudaError_t launch_gather(const void* x, bool x_bf16, int H, const int32_t* pos, int T,
                           __nv_bfloat16* xp, int num_sms, cudaStream_t stream);
-// wide: BF16 down on one CTA per unit with 256-row units (two tiles per k-block)
-cudaError_t launch_gemm(int mode, bool fp4, bool pair, bool wide, const GemmMaps& maps, const GemmParams& p, int grid,
-                        size_t smem_bytes, cudaStream_t stream);
+// FP8 weights: token rows (x in BF16 or FP32) to E4M3 codes in route order,
+// one FP32 scale per row (amax / 448, 1 for a zero row); every token's codes
+// are written to its 8 route rows (xq [R_pad, H], xs [R_pad]).
+cudaError_t launch_gather_q8(const void* x, bool x_bf16, int H, const int32_t* pos, int T, uint8_t* xq, float* xs,
+                             cudaStream_t stream);
+// FP8 weights: rows of h (BF16 [R, I]) to E4M3 codes hq [R_pad, I] and row
+// scales hs [R_pad], the same rule.
+cudaError_t launch_quantize_rows(const __nv_bfloat16* h, int R, int I, uint8_t* hq, float* hs, cudaStream_t stream);
+// wide: BF16 / FP8 down on one CTA per unit with 256-row units (two tiles per
+// k-block); fp8: E4M3 weights and activations (kind::f8f6f4)
+cudaError_t launch_gemm(int mode, bool fp4, bool pair, bool wide, bool fp8, const GemmMaps& maps, const GemmParams& p,
+                        int grid, size_t smem_bytes, cudaStream_t stream);
 size_t gemm_smem_bytes(int stages, int acc_stages, size_t stage_bytes);
 // Clusters of two CTAs of the pair kernel that can be resident at once (0: none).
 int gemm_pair_max_clusters(int mode, size_t smem_bytes);

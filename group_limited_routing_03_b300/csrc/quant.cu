@@ -1,0 +1,134 @@
+// quant.cu -- run-time E4M3 quantisation of the grouped GEMMs' inputs for FP8
+// expert weights.
+//
+// The Beam launch post (section "Mixture of Experts") lists an FP8 checkpoint
+// beside BF16 and NVFP4 without its layout.  The library reads it as E4M3
+// weights with an FP32 scale per output row and runs the GEMMs on E4M3 x E4M3
+// tensor cores, so the activations are quantised per row at run time:
+//   scale = amax(row) / 448 (FP32 division; 1 when that is 0),
+//   code  = E4M3(a / scale) (FP32 division, round to nearest even, saturating
+//           at +-448, the largest finite E4M3 value).
+// Both kernels give one warp a row: pass 1 finds the row's largest magnitude
+// (a warp max), pass 2 re-reads the row (from L1) and converts 16 elements
+// per lane and step into one 16-byte store.
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+
+#include "moe_internal.cuh"
+
+namespace beam {
+namespace {
+
+constexpr int kWarpsPerCta = 8;
+
+// 16 consecutive elements of a row, as FP32.
+template <bool kBf16>
+__device__ __forceinline__ void load16(const void* row, int g, float* v) {
+  if (kBf16) {
+    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(row) + 16 * g);
+    const uint4 r0 = src[0], r1 = src[1];
+    const __nv_bfloat162* a = reinterpret_cast<const __nv_bfloat162*>(&r0);
+    const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&r1);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 fa = __bfloat1622float2(a[i]), fb = __bfloat1622float2(b[i]);
+      v[2 * i] = fa.x, v[2 * i + 1] = fa.y, v[8 + 2 * i] = fb.x, v[8 + 2 * i + 1] = fb.y;
+    }
+  } else {
+    const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(row) + 16 * g);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float4 f = src[i];
+      v[4 * i] = f.x, v[4 * i + 1] = f.y, v[4 * i + 2] = f.z, v[4 * i + 3] = f.w;
+    }
+  }
+}
+
+template <bool kBf16>
+__device__ __forceinline__ float row_scale(const void* row, int groups, int lane) {
+  float amax = 0.0f;
+  for (int g = lane; g < groups; g += 32) {
+    float v[16];
+    load16<kBf16>(row, g, v);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  const float s = __fdiv_rn(amax, 448.0f);
+  return s == 0.0f ? 1.0f : s;
+}
+
+// 16 elements / scale -> 16 E4M3 codes (element i in byte i).
+template <bool kBf16>
+__device__ __forceinline__ uint4 codes16(const void* row, int g, float s) {
+  float v[16];
+  load16<kBf16>(row, g, v);
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __nv_fp8x2_storage_t lo =
+        __nv_cvt_float2_to_fp8x2(make_float2(__fdiv_rn(v[4 * i], s), __fdiv_rn(v[4 * i + 1], s)), __NV_SATFINITE,
+                                 __NV_E4M3);
+    const __nv_fp8x2_storage_t hi =
+        __nv_cvt_float2_to_fp8x2(make_float2(__fdiv_rn(v[4 * i + 2], s), __fdiv_rn(v[4 * i + 3], s)),
+                                 __NV_SATFINITE, __NV_E4M3);
+    w[i] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// One warp per token: its codes go to the token's 8 route rows.
+template <bool kBf16>
+__global__ void __launch_bounds__(32 * kWarpsPerCta) gather_q8_kernel(const void* x, int H, const int32_t* pos,
+                                                                      int T, uint8_t* xq, float* xs) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
+  if (t >= T) return;
+  const void* row = kBf16 ? static_cast<const void*>(static_cast<const __nv_bfloat16*>(x) + static_cast<size_t>(t) * H)
+                          : static_cast<const void*>(static_cast<const float*>(x) + static_cast<size_t>(t) * H);
+  const int groups = H / 16;
+  const float s = row_scale<kBf16>(row, groups, lane);
+  int p[kTopK];
+#pragma unroll
+  for (int k = 0; k < kTopK; ++k) p[k] = __ldg(&pos[static_cast<size_t>(t) * kTopK + k]);
+  if (lane < kTopK) xs[p[lane]] = s;
+  for (int g = lane; g < groups; g += 32) {
+    const uint4 c = codes16<kBf16>(row, g, s);
+#pragma unroll
+    for (int k = 0; k < kTopK; ++k) *reinterpret_cast<uint4*>(xq + static_cast<size_t>(p[k]) * H + 16 * g) = c;
+  }
+}
+
+__global__ void __launch_bounds__(32 * kWarpsPerCta) quantize_rows_kernel(const __nv_bfloat16* h, int R, int I,
+                                                                          uint8_t* hq, float* hs) {
+  const int lane = threadIdx.x & 31;
+  const int r = blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
+  if (r >= R) return;
+  const void* row = h + static_cast<size_t>(r) * I;
+  const int groups = I / 16;
+  const float s = row_scale<true>(row, groups, lane);
+  if (lane == 0) hs[r] = s;
+  for (int g = lane; g < groups; g += 32)
+    *reinterpret_cast<uint4*>(hq + static_cast<size_t>(r) * I + 16 * g) = codes16<true>(row, g, s);
+}
+
+}  // namespace
+
+cudaError_t launch_gather_q8(const void* x, bool x_bf16, int H, const int32_t* pos, int T, uint8_t* xq, float* xs,
+                             cudaStream_t stream) {
+  const int grid = (T + kWarpsPerCta - 1) / kWarpsPerCta;
+  if (x_bf16)
+    gather_q8_kernel<true><<<grid, 32 * kWarpsPerCta, 0, stream>>>(x, H, pos, T, xq, xs);
+  else
+    gather_q8_kernel<false><<<grid, 32 * kWarpsPerCta, 0, stream>>>(x, H, pos, T, xq, xs);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_rows(const __nv_bfloat16* h, int R, int I, uint8_t* hq, float* hs, cudaStream_t stream) {
+  const int grid = (R + kWarpsPerCta - 1) / kWarpsPerCta;
+  quantize_rows_kernel<<<grid, 32 * kWarpsPerCta, 0, stream>>>(h, R, I, hq, hs);
+  return cudaGetLastError();
+}
+
+}  // namespace beam

@@ -203,6 +203,17 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// The same with E4M3 operands (kind::f8f6f4): a K step is 32 elements, the
+// same 32 bytes of a 128-byte swizzled row as a BF16 K=16 step.
+__device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 // D[tmem] (+)= A[tmem] x B[smem]^T: the A tile sits in tensor memory, row m
 // in lane m, two BF16 K elements per 32-bit column (the even one in the low
 // half), so one K=16 step spans 8 columns.
@@ -327,6 +338,15 @@ __device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t a_desc, 
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+__device__ __forceinline__ void mma_f8_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 // Arrive once on the mbarrier at the same offset in every CTA of `cta_mask`
 // when the pair MMAs issued so far have completed.
 __device__ __forceinline__ void mma_commit_pair_multicast(uint64_t* bar, uint16_t cta_mask) {
@@ -361,6 +381,12 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N) {
   return (1u << 4)                 // D format: F32
          | (1u << 7)               // A format: BF16
          | (1u << 10)              // B format: BF16
+         | ((N >> 3) << 17)        // N >> 3
+         | ((M >> 4) << 24);       // M >> 4
+}
+// kind::f8f6f4, A and B E4M3 (format code 0), FP32 accumulator.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(uint32_t M, uint32_t N) {
+  return (1u << 4)                 // D format: F32
          | ((N >> 3) << 17)        // N >> 3
          | ((M >> 4) << 24);       // M >> 4
 }

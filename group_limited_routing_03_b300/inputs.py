@@ -18,11 +18,13 @@ decode     64      5120   2560   BF16 x, BF16 experts (~20 GB), FP32 router
 prefill    8192    5120   2560   same as decode, no router bias
 nvfp4      4096    5120   2560   BF16 x, NVFP4 experts, FP32 router
 skew       32768   5120   2560   BF16, Zipf(1.1) router bias scaled to [0, 3]
+fp8        8192    5120   2560   BF16 x, FP8 experts (E4M3 + row scales, ~10 GB)
+fp8_decode 64      5120   2560   same as fp8
 =========  ======  =====  =====  ============================================
 
 Distributions: x ~ N(0, 1) (a post-RMSNorm hidden state); router weight
 ~ N(0, variance 1/H), so logits are ~N(0, 1); expert weights ~ N(0, std 0.02).
-Seeds: tiny 0, decode 1, prefill 2, nvfp4 3, skew 4.  Draw order: x, router
+Seeds: tiny 0, decode 1, prefill 2, nvfp4 3, skew 4, fp8 5, fp8_decode 6.  Draw order: x, router
 weight, bias, gate (expert by expert), up, down.
 """
 from __future__ import annotations
@@ -46,7 +48,7 @@ class Workload:
     H: int
     I: int
     x_dtype: str  # "f32" | "bf16"
-    w_dtype: str  # "f32" | "bf16" | "nvfp4"
+    w_dtype: str  # "f32" | "bf16" | "nvfp4" | "fp8"
     seed: int
     bias: str  # "none" | "zipf"
     E: int = N_EXPERTS
@@ -62,6 +64,8 @@ WORKLOADS = {
     "prefill": Workload("prefill", 8192, 5120, 2560, "bf16", "bf16", 2, "none"),
     "nvfp4": Workload("nvfp4", 4096, 5120, 2560, "bf16", "nvfp4", 3, "none"),
     "skew": Workload("skew", 32768, 5120, 2560, "bf16", "bf16", 4, "zipf"),
+    "fp8": Workload("fp8", 8192, 5120, 2560, "bf16", "fp8", 5, "none"),
+    "fp8_decode": Workload("fp8_decode", 64, 5120, 2560, "bf16", "fp8", 6, "none"),
 }
 
 
@@ -121,6 +125,18 @@ def quantize_nvfp4(w: torch.Tensor):
     return packed.contiguous(), sc8.view(torch.uint8).contiguous(), g
 
 
+def quantize_fp8_rows(w: torch.Tensor):
+    """Encode a float32 matrix [N, K] as FP8 with one scale per row: scale =
+    row amax / 448 (1 for a zero row), codes = E4M3(w / scale) by torch's
+    cast (nearest, ties to even).  Returns (codes float8_e4m3fn [N, K],
+    scales float32 [N])."""
+    w = w.float()
+    amax = w.abs().amax(1)
+    scale = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax))
+    codes = (w / scale[:, None]).clamp(-448.0, 448.0).to(torch.float8_e4m3fn)
+    return codes.contiguous(), scale.contiguous()
+
+
 # ---------------------------------------------------------------------------
 # Generation
 # ---------------------------------------------------------------------------
@@ -143,7 +159,8 @@ def generate(wl: Workload, device="cpu", *, experts=True):
     Returns a dict with x [T,H], router_w [E,H] f32, bias [E] f32 or None and,
     when ``experts``: gate/up [E,I,H], down [E,H,I] (f32 or bf16) or, for
     NVFP4, gate/up/down packed uint8, gate_sf/up_sf/down_sf uint8 E4M3 and
-    gate_gs/up_gs/down_gs float32 [E].
+    gate_gs/up_gs/down_gs float32 [E]; for FP8, gate/up/down float8_e4m3fn
+    and gate_rs/up_rs/down_rs float32 row scales [E, I] / [E, H].
     """
     gen = torch.Generator(device=device)
     gen.manual_seed(wl.seed)
@@ -168,6 +185,15 @@ def generate(wl: Workload, device="cpu", *, experts=True):
             out[name] = packed
             out[name + "_sf"] = sf
             out[name + "_gs"] = gs.to(device)
+        elif wl.w_dtype == "fp8":
+            codes = torch.empty((wl.E, n, k), dtype=torch.float8_e4m3fn, device=device)
+            rs = torch.empty((wl.E, n), dtype=torch.float32, device=device)
+            for e in range(wl.E):
+                c, r = quantize_fp8_rows(_randn((n, k), gen, device, std=0.02))
+                codes[e].copy_(c)
+                rs[e].copy_(r)
+            out[name] = codes
+            out[name + "_rs"] = rs
         else:
             dt = torch.float32 if wl.w_dtype == "f32" else torch.bfloat16
             w = torch.empty((wl.E, n, k), dtype=dt, device=device)

@@ -52,7 +52,7 @@ typedef enum {
   BEAM_ERR_DEVICE_CHECK = 6  /* device: a kernel's own consistency check failed */
 } beam_status_t;
 
-typedef enum { BEAM_F32 = 0, BEAM_BF16 = 1, BEAM_NVFP4 = 2 } beam_dtype_t;
+typedef enum { BEAM_F32 = 0, BEAM_BF16 = 1, BEAM_NVFP4 = 2, BEAM_FP8 = 3 } beam_dtype_t;
 
 /* Layer shape.  T tokens, hidden H, expert intermediate I, E experts in
  * n_group contiguous groups (group j = experts [j*E/n_group, (j+1)*E/n_group)),
@@ -68,8 +68,9 @@ typedef struct {
  *   BEAM_LAYOUT_TILED: the same bytes regrouped so that every tile the GEMMs
  *     load is contiguous: the matrix of R = E*N rows (N = I for gate / up, H
  *     for down) and B bytes per row is cut into tiles of 128 rows x b bytes,
- *     b = 128 for BF16 (64 elements), 32 for E2M1 codes (64 elements), 16 for
- *     E4M3 scales (256 elements); tile (i, j) (rows 128i.., bytes bj..) is
+ *     b = 128 for BF16 (64 elements) and FP8 (128 elements), 32 for E2M1
+ *     codes (64 elements), 16 for E4M3 scales (256 elements); the FP8 row
+ *     scales keep their order; tile (i, j) (rows 128i.., bytes bj..) is
  *     stored at byte (i * B/b + j) * 128 * b, its rows b bytes apart.  Made by
  *     beam_moe_pack_weights; streams ~3% faster from HBM (each tile is one
  *     contiguous block instead of 128 pieces). */
@@ -82,6 +83,17 @@ typedef enum { BEAM_LAYOUT_ROWS = 0, BEAM_LAYOUT_TILED = 1 } beam_weight_layout_
  *          [E, I, H/16] / [E, H, I/16], one per 16 consecutive K elements;
  *          *_gs = FP32 global scale per expert and matrix [E].
  *          Element value = e2m1 * e4m3 * global.
+ *   FP8  : gate/up [E, I, H], down [E, H, I] E4M3 bytes (OCP FP8 E4M3: bias 7,
+ *          no infinities, largest finite 448); *_rs = FP32 scale per output
+ *          row [E, I] / [E, H].  Element value = e4m3 * row scale.  The
+ *          launch post (section "Mixture of Experts") lists an FP8 checkpoint
+ *          without its layout; this per-row layout is the library's reading.
+ *          The GEMM inputs are quantised per row to E4M3 at run time (x
+ *          rows before gate/up, h rows before down): scale = row amax / 448
+ *          (1 for a zero row), code = E4M3(a / scale), round to nearest even,
+ *          saturating, both divisions in FP32; the MMAs run E4M3 x E4M3 with
+ *          FP32 accumulation and both scales are applied in FP32 after the
+ *          sum.  Supported when I <= H (h's codes share the x-code buffer).
  * (in `layout` order; BEAM_LAYOUT_ROWS when the field is zero-initialised).
  * Pointers the dtype does not use must be NULL. */
 typedef struct {
@@ -96,6 +108,9 @@ typedef struct {
   const float* up_gs;
   const float* down_gs;
   beam_weight_layout_t layout;
+  const float* gate_rs; /* FP8 only */
+  const float* up_rs;
+  const float* down_rs;
 } beam_expert_weights_t;
 
 /* Where the intermediates of the last call live inside the workspace (byte
@@ -108,9 +123,14 @@ typedef struct {
  *   xp bf16[T*top_k, H]    token rows in perm order
  *   h bf16[T*top_k, I]     SwiGLU activations in perm order
  *   yr bf16[T*top_k, H]    expert outputs in perm order (before weighting)
- *   status uint32[4]       device status word (code, where, 0, 0) */
+ *   status uint32[4]       device status word (code, where, 0, 0)
+ * FP8 weights only (the GEMM inputs quantised per row):
+ *   xq u8[T*top_k, H]      E4M3 codes of the token rows, perm order (inside xp)
+ *   hq u8[T*top_k, I]      E4M3 codes of h, perm order (inside xp, after xq)
+ *   xs, hs f32[T*top_k]    their row scales */
 typedef struct {
   size_t status, counts, offsets, perm, pos, xp, h, yr, total;
+  size_t xq, hq, xs, hs;
 } beam_ws_layout_t;
 
 /* Bytes of workspace beam_moe_forward / beam_moe_experts need for `shape`
@@ -165,9 +185,11 @@ beam_status_t beam_moe_forward(const beam_moe_shape_t* shape, const void* x, bea
 typedef enum {
   BEAM_STAGE_ROUTE = 0,    /* router GEMV + selection (+ per-tile histogram) */
   BEAM_STAGE_DISPATCH = 1, /* counts, offsets, perm, pos from the histograms */
-  BEAM_STAGE_GATHER = 2,   /* token rows into route order (BF16) */
+  BEAM_STAGE_GATHER = 2,   /* token rows into route order (BF16; FP8 weights:
+                              E4M3 codes and row scales) */
   BEAM_STAGE_GATE_UP = 3,  /* grouped gate/up GEMM with the SwiGLU epilogue */
-  BEAM_STAGE_DOWN = 4,     /* grouped down GEMM */
+  BEAM_STAGE_DOWN = 4,     /* grouped down GEMM (FP8 weights: after h is
+                              quantised per row) */
   BEAM_STAGE_COMBINE = 5,  /* weighted sum of each token's expert outputs
                               (+ the residual update when args->residual) */
   BEAM_STAGE_COUNT = 6
@@ -230,22 +252,27 @@ beam_status_t beam_moe_forward_stage(const beam_moe_shape_t* shape, const beam_m
                                      beam_stage_t stage, void* workspace, size_t workspace_bytes,
                                      void* stream);
 
-/* Number of kernels stage `stage` launches for `shape` and activations of
- * type `xdtype` on the current device: the router adds a selection kernel
- * when it splits its reduction across CTAs, and its tensor-core path (BF16
- * x, T >= 512) a kernel that splits the router weight into BF16 terms; the
- * dispatch is two kernels; -1 on an unsupported shape or stage. */
-int32_t beam_moe_stage_kernel_count(const beam_moe_shape_t* shape, beam_dtype_t xdtype, beam_stage_t stage);
+/* Number of kernels stage `stage` launches for `shape`, activations of type
+ * `xdtype` and expert weights of type `wdtype` on the current device: the
+ * router adds a selection kernel when it splits its reduction across CTAs,
+ * and its tensor-core path (BF16 x, T >= 512) a kernel that splits the
+ * router weight into BF16 terms; the dispatch is two kernels; with FP8
+ * weights the down stage first quantises h (two kernels); -1 on an
+ * unsupported shape, dtype or stage. */
+int32_t beam_moe_stage_kernel_count(const beam_moe_shape_t* shape, beam_dtype_t xdtype, beam_dtype_t wdtype,
+                                    beam_stage_t stage);
 
 /* Regroup row-major expert weights into BEAM_LAYOUT_TILED (a one-time step
  * when loading a model; not part of the Beam post's method, which fixes the
  * arithmetic, not the storage).  `src`: layout BEAM_LAYOUT_ROWS; `dst`: the
  * same dtype, caller-allocated arrays of the same sizes (gate, up, down and,
  * for NVFP4, the three scale arrays; dst's global-scale pointers are used as
- * given and may alias src's); dst->layout is set to BEAM_LAYOUT_TILED.  The
- * arrays must not overlap.  Async on `stream`.  Errors as for the forward
- * call's weights; BEAM_ERR_UNSUPPORTED unless N and K are multiples of 128 / 64
- * elements (BF16) or 128 / 256 (NVFP4). */
+ * given and may alias src's; for FP8, dst's row-scale pointers must be src's,
+ * as the row scales keep their order); dst->layout is set to
+ * BEAM_LAYOUT_TILED.  The arrays must not overlap.  Async on `stream`.
+ * Errors as for the forward call's weights; BEAM_ERR_UNSUPPORTED unless N and
+ * K are multiples of 128 / 64 elements (BF16), 128 / 256 (NVFP4) or
+ * 128 / 128 (FP8). */
 beam_status_t beam_moe_pack_weights(const beam_moe_shape_t* shape, const beam_expert_weights_t* src,
                                     beam_expert_weights_t* dst, void* stream);
 

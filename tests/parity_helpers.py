@@ -8,8 +8,8 @@ Comparison rules (the same everywhere):
     gap) -- exceeds 1e-5; tokens at or below that margin are near-ties, which
     FP32 rounding may legitimately flip, and are counted, not compared;
   * weights: |w - w_ref| <= 1e-5 * |w_ref| + 1e-6 for the compared tokens;
-  * outputs: max|y - y_ref| / max|y_ref| <= 1e-2 (BF16 experts) or 3e-2
-    (NVFP4 experts) over the compared tokens.
+  * outputs: max|y - y_ref| / max|y_ref| <= 1e-2 (BF16 and FP8 experts) or
+    3e-2 (NVFP4 experts) over the compared tokens.
 """
 from __future__ import annotations
 
@@ -19,7 +19,7 @@ import torch
 import oracle
 
 MARGIN = 1e-5
-Y_TOL = {"bf16": 1e-2, "f32": 1e-2, "nvfp4": 3e-2}
+Y_TOL = {"bf16": 1e-2, "f32": 1e-2, "nvfp4": 3e-2, "fp8": 1e-2}
 
 
 def host_act(t: torch.Tensor) -> np.ndarray:
@@ -33,7 +33,11 @@ def host_act(t: torch.Tensor) -> np.ndarray:
 
 
 def host_expert(d: dict, e: int):
-    """Host copies of expert e's weights in a form oracle.expert_ffn takes."""
+    """Host copies of expert e's weights in a form oracle.expert_ffn takes
+    (for FP8: the E4M3 codes as bytes and the row scales, oracle.expert_ffn_fp8)."""
+    if d["gate"].dtype == torch.float8_e4m3fn:
+        mats = [d[n][e].cpu().view(torch.uint8).numpy() for n in ("gate", "up", "down")]
+        return mats, dict(fp8_rs=[d[n + "_rs"][e].cpu().numpy() for n in ("gate", "up", "down")])
     if d["gate"].dtype == torch.uint8:
         mats = [d[n][e].cpu().numpy() for n in ("gate", "up", "down")]
         scales = [d[n + "_sf"][e].cpu().numpy() for n in ("gate", "up", "down")]
@@ -62,7 +66,10 @@ def oracle_y(d: dict, tokens, ids, weights, *, oracle_weights=None):
             mats, kw = [oracle_weights[k][e] for k in ("gate", "up", "down")], {}
         else:
             mats, kw = host_expert(d, int(e))
-        o[rows, ks] = oracle.expert_ffn(x[rows], *mats, **kw)
+        if "fp8_rs" in kw:
+            o[rows, ks] = oracle.expert_ffn_fp8(x[rows], *mats, *kw["fp8_rs"])
+        else:
+            o[rows, ks] = oracle.expert_ffn(x[rows], *mats, **kw)
     return oracle.combine(weights, o)
 
 

@@ -217,3 +217,30 @@ def test_forward_residual_argument_errors(lib):
     # without a residual, the plain stages still need y
     assert lib.beam_moe_forward_stage(ctypes.byref(sh), ctypes.byref(a), 0, 0x100000, n, None) == \
         moe.BEAM_ERR_INVALID_ARG
+
+
+def test_fp8_weight_rules(lib):
+    sh = _shape(T=16, H=256, I=256)
+    n = moe.workspace_size(sh, "fp8")
+    assert n == moe.workspace_size(sh, "bf16") > 0
+    lay = moe.workspace_layout(sh, "fp8")
+    R_pad = 16 * 8
+    assert lay["xq"] == lay["xp"] and lay["hq"] >= lay["xq"] + R_pad * 256
+    assert lay["hq"] + R_pad * 256 <= lay["xp"] + R_pad * 256 * 2  # h's codes fit in the BF16 row buffer
+    ew = moe._ExpertWeights()
+    ew.dtype = moe.BEAM_FP8
+    ew.gate, ew.up, ew.down = 0x1000, 0x2000, 0x3000
+    ew.gate_rs, ew.up_rs, ew.down_rs = 0x4000, 0x5000, None
+
+    def call(shape):
+        return lib.beam_moe_experts(ctypes.byref(shape), 0x10000, moe.BEAM_BF16, ctypes.byref(ew), 0x30000,
+                                    0x40000, 0x50000, 0x100000, moe.workspace_size(shape, "fp8"), None)
+
+    assert call(sh) == moe.BEAM_ERR_INVALID_ARG  # a row-scale array missing
+    ew.down_rs = 0x6000
+    ew.gate_sf = 0x7000  # an NVFP4 array with FP8 weights
+    assert call(sh) == moe.BEAM_ERR_INVALID_ARG
+    ew.gate_sf = None
+    assert call(_shape(T=16, H=256, I=384)) == moe.BEAM_ERR_UNSUPPORTED  # I > H
+    ew.dtype = moe.BEAM_BF16  # row scales with BF16 weights
+    assert call(sh) == moe.BEAM_ERR_INVALID_ARG

@@ -223,6 +223,49 @@ def measure(wl, steps, warmup, dev, world, sampler_index, state=None, residual_s
     return out, state
 
 
+def measure_dense(wl, steps, warmup, dev, pk):
+    """The dense SwiGLU MLP (one expert taking every row) through
+    beam_dense_mlp_forward, device-timed per call; weights in the tiled layout."""
+    import group_limited_routing_03_b300 as moe
+    from group_limited_routing_03_b300 import inputs
+
+    d = inputs.generate(wl, dev)
+    w = {k: d[k] for k in ("gate", "up", "down")}
+    mlp = moe.DenseMLP(w, max_tokens=wl.T, pack=True)
+    x = d["x"]
+    y = torch.empty_like(x)
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        mlp(x, y)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        e0.record(stream)
+        for _ in range(steps):
+            mlp(x, y)
+        e1.record(stream)
+        torch.cuda.synchronize()
+    code, where = moe.beam_moe_read_device_status(mlp.workspace)
+    if code != 0:
+        raise RuntimeError(f"device status {code} at {where} in the dense MLP")
+    ms = e0.elapsed_time(e1) / steps
+    wbytes = 3 * wl.H * wl.I * 2
+    flops = 2.0 * wl.T * 3 * wl.H * wl.I
+    gbs = (wbytes + 2 * wl.T * wl.H * 2 + 2 * wl.T * wl.I * 2) / (ms * 1e-3) / 1e9
+    tfs = flops / (ms * 1e-3) / 1e12
+    out = dict(value=wl.T / (ms * 1e-3), unit="tokens/s", ms_per_call=round(ms, 4), steps=steps,
+               config={"workload": f"{wl.name} T={wl.T} H={wl.H} I={wl.I} dense SwiGLU MLP, BF16", "T": wl.T},
+               gpu_launches=steps * 3, clocks=clk.summary())
+    if wl.T <= 256:
+        out["roofline"] = dict(bound="hbm", achieved=round(gbs, 1), peak=pk["hbm"], unit="GB/s",
+                               frac=round(gbs / pk["hbm"], 4), peak_source=pk["source"])
+    else:
+        out["roofline"] = dict(bound="tensor", achieved=round(tfs, 1), peak=pk["bf16"], unit="TFLOP/s",
+                               frac=round(tfs / pk["bf16"], 4), peak_source=pk["source"])
+    del d, mlp
+    return out
+
+
 def residual_numbers(wl, m_plain, m_res, steps, pk, k):
     """The post-norm residual update fused into the combine: its stage time
     against the plain combine's in the same step, and its own HBM roofline.
@@ -469,6 +512,8 @@ def main():
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-dense", action="store_true",
+                    help="skip the dense SwiGLU MLP (decode T=64 and prefill T=8192, I=20480)")
     ap.add_argument("--no-fp8", action="store_true",
                     help="skip the FP8-weight layers (decode T=64 and prefill T=8192)")
     ap.add_argument("--no-residual", action="store_true",
@@ -556,6 +601,12 @@ def main():
             del fstate
             torch.cuda.empty_cache()
 
+    dense = None
+    if not args.no_dense and not args.small:
+        dense = {name: measure_dense(inputs.workload(name), args.steps if name == "dense_dec" else max(3, args.steps // 2),
+                                     args.warmup, dev, pk) for name in ("dense_dec", "dense")}
+        torch.cuda.empty_cache()
+
     if rank != 0:
         return
     line = {
@@ -569,7 +620,7 @@ def main():
                          f"({m['touched']} x {weight_bytes_per_expert(wl) / 1e6:.1f} MB), far larger than L2"},
         "roofline": hbm, "roofline_tensor": tc, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": m["launches_per_step"] * args.steps, "clocks": m["clocks"],
-        "step": sn, "residual_epilogue": residual, "prefill": prefill, "fp8": fp8,
+        "step": sn, "residual_epilogue": residual, "prefill": prefill, "fp8": fp8, "dense": dense,
     }
     print(json.dumps(line), flush=True)
 

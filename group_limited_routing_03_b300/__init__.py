@@ -46,6 +46,10 @@ class Shape(ctypes.Structure):
                 ("routed_scale", ctypes.c_float)]
 
 
+class DenseShape(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int32), ("H", ctypes.c_int32), ("I", ctypes.c_int32)]
+
+
 class _ExpertWeights(ctypes.Structure):
     _fields_ = [("dtype", ctypes.c_int), ("gate", ctypes.c_void_p), ("up", ctypes.c_void_p),
                 ("down", ctypes.c_void_p), ("gate_sf", ctypes.c_void_p), ("up_sf", ctypes.c_void_p),
@@ -110,12 +114,17 @@ def load():
     lib.beam_moe_stage_kernel_count.restype = ctypes.c_int32
     lib.beam_moe_debug_timeout.argtypes = [vp, sz, u32, vp]
     lib.beam_moe_pack_weights.argtypes = [sp, ctypes.POINTER(_ExpertWeights), ctypes.POINTER(_ExpertWeights), vp]
+    dp = ctypes.POINTER(DenseShape)
+    lib.beam_dense_workspace_size.argtypes = [dp, i32]
+    lib.beam_dense_workspace_size.restype = sz
+    lib.beam_dense_mlp_forward.argtypes = [dp, vp, i32, ctypes.POINTER(_ExpertWeights), vp, vp, sz, vp]
+    lib.beam_dense_pack_weights.argtypes = [dp, ctypes.POINTER(_ExpertWeights), ctypes.POINTER(_ExpertWeights), vp]
     lib.beam_status_string.argtypes = [i32]
     lib.beam_status_string.restype = ctypes.c_char_p
     for n in ("beam_moe_workspace_layout", "beam_moe_route", "beam_moe_dispatch", "beam_moe_experts",
               "beam_moe_forward", "beam_moe_forward_stage", "beam_moe_forward_residual",
               "beam_moe_read_device_status",
-              "beam_moe_debug_timeout"):
+              "beam_moe_debug_timeout", "beam_dense_mlp_forward", "beam_dense_pack_weights"):
         getattr(lib, n).restype = i32
     _lib = lib
     return lib
@@ -346,6 +355,63 @@ def beam_moe_read_device_status(workspace, stream=None):
 def beam_moe_debug_timeout(workspace, timeout_us: int, stream=None):
     _check(load().beam_moe_debug_timeout(_ptr(workspace), workspace.numel(), int(timeout_us), _stream(stream)),
            "beam_moe_debug_timeout")
+
+
+# --------------------------------------------------------------------------
+# dense SwiGLU MLP (the first layers of the model)
+# --------------------------------------------------------------------------
+def dense_shape(T, H, I) -> DenseShape:
+    return DenseShape(T, H, I)
+
+
+def dense_workspace_size(sh: DenseShape, wdtype="bf16") -> int:
+    return int(load().beam_dense_workspace_size(ctypes.byref(sh), _wdtype(wdtype)))
+
+
+def beam_dense_mlp_forward(sh: DenseShape, x, weights: dict, y, workspace, stream=None):
+    """y = Wd (silu(Wg x) * (Wu x)) with one expert's worth of weights
+    (gate/up [1, I, H], down [1, H, I] and the per-expert arrays)."""
+    ew = _weights(weights)
+    _check(load().beam_dense_mlp_forward(ctypes.byref(sh), _ptr(x), _act_dtype(x), ctypes.byref(ew), _ptr(y),
+                                         _ptr(workspace), workspace.numel(), _stream(stream)),
+           "beam_dense_mlp_forward")
+
+
+def dense_pack_weights(sh: DenseShape, weights: dict, stream=None) -> dict:
+    """The dense MLP's weights regrouped into the tiled layout (new arrays)."""
+    out = {k: v for k, v in weights.items()}
+    for name in ("gate", "up", "down", "gate_sf", "up_sf", "down_sf"):
+        if weights.get(name) is not None:
+            out[name] = torch.empty_like(weights[name])
+    src, dst = _weights(weights), _weights(out)
+    _check(load().beam_dense_pack_weights(ctypes.byref(sh), ctypes.byref(src), ctypes.byref(dst), _stream(stream)),
+           "beam_dense_pack_weights")
+    out["layout"] = "tiled"
+    return out
+
+
+class DenseMLP:
+    """One dense SwiGLU MLP with its weights and a workspace for up to
+    ``max_tokens`` rows (caller-owned torch device tensors)."""
+
+    def __init__(self, weights: dict, max_tokens: int, pack=False):
+        self.I, self.H = weights["gate"].shape[1], weights["down"].shape[1]
+        self.max_tokens = max_tokens
+        if pack and weights.get("layout", "rows") == "rows":
+            weights = dense_pack_weights(dense_shape(max_tokens, self.H, self.I), weights)
+        self.weights = weights
+        n = dense_workspace_size(dense_shape(max_tokens, self.H, self.I), _wdtype(weights))
+        if n == 0:
+            raise BeamError(BEAM_ERR_UNSUPPORTED, "beam_dense_workspace_size")
+        self.workspace = torch.zeros(n, dtype=torch.uint8, device=weights["gate"].device)
+
+    def __call__(self, x, y=None, stream=None):
+        T = x.shape[0]
+        if T > self.max_tokens:
+            raise ValueError(f"{T} rows > workspace capacity {self.max_tokens}")
+        y = torch.empty((T, self.H), dtype=torch.bfloat16, device=x.device) if y is None else y
+        beam_dense_mlp_forward(dense_shape(T, self.H, self.I), x, self.weights, y, self.workspace, stream)
+        return y
 
 
 # --------------------------------------------------------------------------

@@ -169,13 +169,57 @@ beam_status_t check_shape(const beam_moe_shape_t* s) {
   return BEAM_OK;
 }
 
+// Dense MLP workspace: status, unit counters, the one-expert schedule, h, and
+// for FP8 weights the codes of x and h with their row scales.
+struct DenseLayout {
+  size_t status, sched, counts, offsets, chunk_prefix, h, xq, hq, xs, hs, total;
+};
+
+void make_dense_layout(const beam_dense_shape_t& s, DenseLayout& L) {
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align256(off + bytes);
+    return o;
+  };
+  const size_t T = static_cast<size_t>(s.T), H = static_cast<size_t>(s.H), I = static_cast<size_t>(s.I);
+  const size_t T_pad = (T + kBoxRows - 1) / kBoxRows * kBoxRows;
+  L.status = take(16);
+  L.sched = take(16);
+  L.counts = take(kExperts * 4);
+  L.offsets = take((kExperts + 1) * 4);
+  L.chunk_prefix = take((kExperts + 1) * 4);
+  L.h = take(T_pad * I * 2);
+  L.xq = take(T_pad * H);
+  L.hq = take(T_pad * I);
+  L.xs = take((T_pad + 32) * 4);
+  L.hs = take((T_pad + 32) * 4);
+  L.total = off;
+}
+
+// The dense shape as a block shape (the block's constants; only T, H, I are read).
+beam_moe_shape_t dense_as_moe(const beam_dense_shape_t& s) {
+  beam_moe_shape_t m;
+  m.T = s.T;
+  m.H = s.H;
+  m.I = s.I;
+  m.E = kExperts;
+  m.n_group = kGroups;
+  m.topk_group = kGroupsKept;
+  m.top_k = kTopK;
+  m.routed_scale = 1.0f;
+  return m;
+}
+
 beam_status_t check_workspace(const beam_moe_shape_t* s, const void* ws, size_t bytes, Layout& L) {
   make_layout(*s, L);
   if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0 || bytes < L.total) return BEAM_ERR_WORKSPACE;
   return BEAM_OK;
 }
 
-beam_status_t check_weights(const beam_moe_shape_t* s, const beam_expert_weights_t* w) {
+// shared_codes: FP8 h codes live in the x-code buffer (the block's workspace),
+// which needs I <= H; the dense MLP's workspace has its own.
+beam_status_t check_weights(const beam_moe_shape_t* s, const beam_expert_weights_t* w, bool shared_codes = true) {
   if (w == nullptr) return BEAM_ERR_INVALID_ARG;
   if (w->layout != BEAM_LAYOUT_ROWS && w->layout != BEAM_LAYOUT_TILED) return BEAM_ERR_INVALID_ARG;
   if (w->dtype == BEAM_FP8) {
@@ -185,7 +229,7 @@ beam_status_t check_weights(const beam_moe_shape_t* s, const beam_expert_weights
       return BEAM_ERR_INVALID_ARG;
     if (w->gate_sf || w->up_sf || w->down_sf || w->gate_gs || w->up_gs || w->down_gs) return BEAM_ERR_INVALID_ARG;
     // h's codes share the x-code buffer (I <= H); the k-block is 128 elements
-    if (s->I > s->H) return BEAM_ERR_UNSUPPORTED;
+    if (shared_codes && s->I > s->H) return BEAM_ERR_UNSUPPORTED;
     return BEAM_OK;
   }
   if (w->gate_rs || w->up_rs || w->down_rs) return BEAM_ERR_INVALID_ARG;
@@ -294,23 +338,65 @@ beam_status_t run_gather(const beam_moe_shape_t& s, const void* x, bool x_bf16, 
 }
 
 // mode 0: gate/up (+SwiGLU) -> h; mode 1: down -> yr.
-beam_status_t run_gemm(int mode, const beam_moe_shape_t& s, const beam_expert_weights_t* wts, void* ws,
-                       const Layout& L, const DeviceInfo& d, cudaStream_t stream) {
-  const int R = s.T * kTopK;
+// The buffers and sizes one pair of grouped GEMMs works on: the MoE block
+// (T*8 route rows over 256 experts, in the workspace) or the dense MLP (T
+// rows, one "expert", x itself as the gate/up input).
+struct GemmIO {
+  int R;                // route rows
+  int nmax;             // routes per unit at most
+  uint64_t n_exp;       // experts stacked in the weight arrays
+  const void* xp;       // BF16 gate/up input rows [xp_rows, H]
+  uint64_t xp_rows;     // rows of that tensor (whole TMA boxes past R read zeros or unused rows)
+  __nv_bfloat16* h;     // [R_pad, I]
+  __nv_bfloat16* out;   // down output [R, H]
+  uint8_t* xq;          // FP8: codes of the gate/up input rows [R_pad, H]
+  uint8_t* hq;          // FP8: codes of h [R_pad, I]
+  float* xs;            // FP8: their row scales [R_pad + 32]
+  float* hs;
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* chunk_prefix;
+  int* sched;           // two unit counters (gate/up, down)
+  uint32_t* status;
+};
+
+GemmIO moe_io(const beam_moe_shape_t& s, void* ws, const Layout& L, bool fp4) {
+  GemmIO io;
+  io.R = s.T * kTopK;
+  io.nmax = chunk_rows(s.T, fp4);
+  io.n_exp = kExperts;
+  io.xp = at<__nv_bfloat16>(ws, L.xp);
+  io.xp_rows = static_cast<uint64_t>((io.R + kBoxRows - 1) / kBoxRows * kBoxRows);
+  io.h = at<__nv_bfloat16>(ws, L.h);
+  io.out = at<__nv_bfloat16>(ws, L.yr);
+  io.xq = at<uint8_t>(ws, L.xq);
+  io.hq = at<uint8_t>(ws, L.hq);
+  io.xs = at<float>(ws, L.xs);
+  io.hs = at<float>(ws, L.hs);
+  io.counts = at<int32_t>(ws, L.counts);
+  io.offsets = at<int32_t>(ws, L.offsets);
+  io.chunk_prefix = at<int32_t>(ws, L.chunk_prefix);
+  io.sched = at<int>(ws, L.sched);
+  io.status = at<uint32_t>(ws, L.status);
+  return io;
+}
+
+beam_status_t run_gemm(int mode, const beam_moe_shape_t& s, const beam_expert_weights_t* wts, const GemmIO& io,
+                       const DeviceInfo& d, cudaStream_t stream) {
+  const int R = io.R;
   const uint64_t R_pad = static_cast<uint64_t>((R + kBoxRows - 1) / kBoxRows * kBoxRows);
   const bool fp4 = wts->dtype == BEAM_NVFP4;
   const bool fp8 = wts->dtype == BEAM_FP8;
-  const int nmax = chunk_rows(s.T, fp4);
+  const int nmax = io.nmax;
   // FP8: h's row quantisation comes first (its scales need whole rows of h)
   if (fp8 && mode == 1) {
-    const cudaError_t e = launch_quantize_rows(at<__nv_bfloat16>(ws, L.h), s.T * kTopK, s.I, at<uint8_t>(ws, L.hq),
-                                               at<float>(ws, L.hs), stream);
+    const cudaError_t e = launch_quantize_rows(io.h, R, s.I, io.hq, io.hs, stream);
     if (e != cudaSuccess) return BEAM_ERR_CUDA;
   }
-  __nv_bfloat16* xp = at<__nv_bfloat16>(ws, L.xp);
-  __nv_bfloat16* h = at<__nv_bfloat16>(ws, L.h);
-  __nv_bfloat16* yr = at<__nv_bfloat16>(ws, L.yr);
-  const uint64_t E = kExperts, H = s.H, I = s.I;
+  const void* xp = io.xp;
+  __nv_bfloat16* h = io.h;
+  __nv_bfloat16* yr = io.out;
+  const uint64_t E = io.n_exp, H = s.H, I = s.I;
   GemmMaps maps;
   std::memset(&maps, 0, sizeof(maps));
   bool ok;
@@ -334,8 +420,8 @@ beam_status_t run_gemm(int mode, const beam_moe_shape_t& s, const beam_expert_we
   auto wmap_f8 = [&](CUtensorMap* m, const void* base, uint64_t N, uint64_t K) {
     return tiled ? make_u8_sw128_map(m, base, 128, E * N * (K / 128), kBlockM) : make_u8_sw128_map(m, base, K, E * N, kBlockM);
   };
-  uint8_t* xq = at<uint8_t>(ws, L.xq);
-  uint8_t* hq = at<uint8_t>(ws, L.hq);
+  uint8_t* xq = io.xq;
+  uint8_t* hq = io.hq;
   if (fp8) {
     if (mode == 0)
       ok = make_u8_sw128_map(&maps.b, xq, H, R_pad, kBoxRows) && wmap_f8(&maps.a0, wts->gate, I, H) &&
@@ -344,7 +430,7 @@ beam_status_t run_gemm(int mode, const beam_moe_shape_t& s, const beam_expert_we
       ok = make_u8_sw128_map(&maps.b, hq, I, R_pad, kBoxRows) && wmap_f8(&maps.a0, wts->down, H, I);
     if (mode == 1) maps.a1 = maps.a0;
   } else if (mode == 0) {
-    ok = make_bf16_map(&maps.b, xp, H, R_pad, kBoxRows);
+    ok = make_bf16_map(&maps.b, xp, H, io.xp_rows, kBoxRows);
     if (fp4)
       ok = ok && wmap_codes(&maps.a0, wts->gate, I, H) && wmap_codes(&maps.a1, wts->up, I, H) &&
            wmap_scales(&maps.s0, wts->gate_sf, I, H) && wmap_scales(&maps.s1, wts->up_sf, I, H);
@@ -384,9 +470,9 @@ beam_status_t run_gemm(int mode, const beam_moe_shape_t& s, const beam_expert_we
   const int rows_per_unit =
       pair ? (mode == 0 ? 2 * kBlockM : 4 * kBlockM) : ((fp4 || wide) && mode == 1 ? 2 * kBlockM : kBlockM);
   GemmParams p;
-  p.counts = at<int32_t>(ws, L.counts);
-  p.offsets = at<int32_t>(ws, L.offsets);
-  p.chunk_prefix = at<int32_t>(ws, L.chunk_prefix);
+  p.counts = io.counts;
+  p.offsets = io.offsets;
+  p.chunk_prefix = io.chunk_prefix;
   p.m_tiles = (mode == 0 ? s.I : s.H) / rows_per_unit;
   p.a_rows_per_expert = mode == 0 ? s.I : s.H;
   p.k_blocks = (mode == 0 ? s.H : s.I) / (fp8 ? 2 * kBlockK : kBlockK);
@@ -421,15 +507,15 @@ beam_status_t run_gemm(int mode, const beam_moe_shape_t& s, const beam_expert_we
     if (p.a_stages < 2) return BEAM_ERR_UNSUPPORTED;   // the converter groups alternate
     p.tmem_cols = 512;
   }
-  p.sched = at<int>(ws, L.sched) + mode;
+  p.sched = io.sched + mode;
   p.out = mode == 0 ? h : yr;
   p.out_ld = mode == 0 ? s.I : s.H;
   p.gs0 = fp4 ? (mode == 0 ? wts->gate_gs : wts->down_gs) : nullptr;
   p.gs1 = fp4 && mode == 0 ? wts->up_gs : nullptr;
   p.rs0 = fp8 ? (mode == 0 ? wts->gate_rs : wts->down_rs) : nullptr;
   p.rs1 = fp8 && mode == 0 ? wts->up_rs : nullptr;
-  p.bscale = fp8 ? at<float>(ws, mode == 0 ? L.xs : L.hs) : nullptr;
-  p.status = at<uint32_t>(ws, L.status);
+  p.bscale = fp8 ? (mode == 0 ? io.xs : io.hs) : nullptr;
+  p.status = io.status;
   p.timeout_ns = kDefaultTimeoutNs;
   const size_t smem = gemm_smem_bytes(stages, acc_stages, sb);
   // persistent: one CTA per SM, or as many pairs as can be resident at once
@@ -440,8 +526,8 @@ beam_status_t run_gemm(int mode, const beam_moe_shape_t& s, const beam_expert_we
   if (fp8) {
     if (!make_u8_sw128_map(&maps.bb, mode == 0 ? xq : hq, mode == 0 ? H : I, R_pad, static_cast<uint32_t>(p.b_big_rows)))
       return BEAM_ERR_CUDA;
-  } else if (!make_bf16_map(&maps.bb, mode == 0 ? static_cast<const void*>(xp) : static_cast<const void*>(h),
-                            mode == 0 ? H : I, R_pad, static_cast<uint32_t>(p.b_big_rows))) {
+  } else if (!make_bf16_map(&maps.bb, mode == 0 ? xp : static_cast<const void*>(h), mode == 0 ? H : I,
+                            mode == 0 ? io.xp_rows : R_pad, static_cast<uint32_t>(p.b_big_rows))) {
     return BEAM_ERR_CUDA;
   }
   if (cudaMemsetAsync(p.sched, 0, sizeof(int), stream) != cudaSuccess) return BEAM_ERR_CUDA;
@@ -459,8 +545,8 @@ beam_status_t run_experts(const beam_moe_shape_t& s, const void* x, bool x_bf16,
                           const DeviceInfo& d, bool hist_ready, cudaStream_t stream) {
   beam_status_t st = run_dispatch(s, ids, ws, L, chunk_rows(s.T, wts->dtype == BEAM_NVFP4), hist_ready, stream);
   if (st == BEAM_OK) st = run_gather(s, x, x_bf16, wts->dtype == BEAM_FP8, ws, L, d, stream);
-  if (st == BEAM_OK) st = run_gemm(0, s, wts, ws, L, d, stream);
-  if (st == BEAM_OK) st = run_gemm(1, s, wts, ws, L, d, stream);
+  if (st == BEAM_OK) st = run_gemm(0, s, wts, moe_io(s, ws, L, wts->dtype == BEAM_NVFP4), d, stream);
+  if (st == BEAM_OK) st = run_gemm(1, s, wts, moe_io(s, ws, L, wts->dtype == BEAM_NVFP4), d, stream);
   if (st == BEAM_OK) st = run_combine(s, w, y, x_bf16, ws, L, stream);
   return st;
 }
@@ -531,9 +617,9 @@ beam_status_t run_stage(const beam_moe_shape_t& s, const beam_moe_args_t& a, int
     case BEAM_STAGE_GATHER:
       return run_gather(s, a.x, xb, a.weights->dtype == BEAM_FP8, ws, L, d, cs);
     case BEAM_STAGE_GATE_UP:
-      return run_gemm(0, s, a.weights, ws, L, d, cs);
+      return run_gemm(0, s, a.weights, moe_io(s, ws, L, a.weights->dtype == BEAM_NVFP4), d, cs);
     case BEAM_STAGE_DOWN:
-      return run_gemm(1, s, a.weights, ws, L, d, cs);
+      return run_gemm(1, s, a.weights, moe_io(s, ws, L, a.weights->dtype == BEAM_NVFP4), d, cs);
     case BEAM_STAGE_COMBINE:
       if (a.residual) return run_combine_residual(s, a.topk_w, *a.residual, a.y, xb, ws, L, cs);
       return run_combine(s, a.topk_w, a.y, xb, ws, L, cs);
@@ -707,18 +793,20 @@ beam_status_t beam_moe_read_device_status(void* workspace, uint32_t* where, void
   return static_cast<beam_status_t>(word[0]);
 }
 
-beam_status_t beam_moe_pack_weights(const beam_moe_shape_t* shape, const beam_expert_weights_t* src,
-                                    beam_expert_weights_t* dst, void* stream) {
+// Weight packing for n_exp stacked experts (256 for the block, 1 for the
+// dense MLP).
+static beam_status_t pack_impl(const beam_moe_shape_t* shape, size_t n_exp, const beam_expert_weights_t* src,
+                               beam_expert_weights_t* dst, void* stream) {
   beam_status_t st = check_shape(shape);
   if (st != BEAM_OK) return st;
   if (src == nullptr || dst == nullptr || src->layout != BEAM_LAYOUT_ROWS || dst->dtype != src->dtype)
     return BEAM_ERR_INVALID_ARG;
   beam_expert_weights_t probe = *dst;
   probe.layout = BEAM_LAYOUT_TILED;
-  st = check_weights(shape, src);
-  if (st == BEAM_OK) st = check_weights(shape, &probe);
+  st = check_weights(shape, src, n_exp == kExperts);
+  if (st == BEAM_OK) st = check_weights(shape, &probe, n_exp == kExperts);
   if (st != BEAM_OK) return st;
-  const size_t E = kExperts, H = shape->H, I = shape->I;
+  const size_t E = n_exp, H = shape->H, I = shape->I;
   const bool fp4 = src->dtype == BEAM_NVFP4, fp8 = src->dtype == BEAM_FP8;
   // FP8 row scales keep their order: the same arrays serve both layouts
   if (fp8 && (dst->gate_rs != src->gate_rs || dst->up_rs != src->up_rs || dst->down_rs != src->down_rs))
@@ -759,6 +847,75 @@ beam_status_t beam_moe_pack_weights(const beam_moe_shape_t* shape, const beam_ex
   }
   dst->layout = BEAM_LAYOUT_TILED;
   return BEAM_OK;
+}
+
+beam_status_t beam_moe_pack_weights(const beam_moe_shape_t* shape, const beam_expert_weights_t* src,
+                                    beam_expert_weights_t* dst, void* stream) {
+  return pack_impl(shape, kExperts, src, dst, stream);
+}
+
+beam_status_t beam_dense_pack_weights(const beam_dense_shape_t* shape, const beam_expert_weights_t* src,
+                                      beam_expert_weights_t* dst, void* stream) {
+  if (shape == nullptr) return BEAM_ERR_INVALID_ARG;
+  const beam_moe_shape_t ms = dense_as_moe(*shape);
+  return pack_impl(&ms, 1, src, dst, stream);
+}
+
+size_t beam_dense_workspace_size(const beam_dense_shape_t* shape, beam_dtype_t wdtype) {
+  if (shape == nullptr) return 0;
+  const beam_moe_shape_t ms = dense_as_moe(*shape);
+  if (check_shape(&ms) != BEAM_OK) return 0;
+  if (wdtype != BEAM_BF16 && wdtype != BEAM_NVFP4 && wdtype != BEAM_FP8) return 0;
+  DenseLayout L;
+  make_dense_layout(*shape, L);
+  return L.total;
+}
+
+beam_status_t beam_dense_mlp_forward(const beam_dense_shape_t* shape, const void* x, beam_dtype_t xdtype,
+                                     const beam_expert_weights_t* weights, void* y, void* workspace,
+                                     size_t workspace_bytes, void* stream) {
+  if (shape == nullptr) return BEAM_ERR_INVALID_ARG;
+  const beam_moe_shape_t ms = dense_as_moe(*shape);
+  beam_status_t st = check_shape(&ms);
+  if (st != BEAM_OK) return st;
+  if (!x || !y || !aligned16(x) || !aligned16(y)) return BEAM_ERR_INVALID_ARG;
+  st = check_weights(&ms, weights, false);
+  if (st != BEAM_OK) return st;
+  const bool fp8 = weights->dtype == BEAM_FP8;
+  if (xdtype != BEAM_BF16 && !(fp8 && xdtype == BEAM_F32)) return BEAM_ERR_UNSUPPORTED;
+  DenseLayout L;
+  make_dense_layout(*shape, L);
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < L.total)
+    return BEAM_ERR_WORKSPACE;
+  DeviceInfo d;
+  if (!device_info(d)) return BEAM_ERR_CUDA;
+  if (d.cc_major < 10) return BEAM_ERR_UNSUPPORTED;
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  void* ws = workspace;
+  GemmIO io;
+  io.R = shape->T;
+  io.nmax = chunk_rows(shape->T, weights->dtype == BEAM_NVFP4);
+  io.n_exp = 1;
+  io.xp = x;  // BF16 x is the gate/up input itself, rows in token order
+  io.xp_rows = static_cast<uint64_t>(shape->T);
+  io.h = at<__nv_bfloat16>(ws, L.h);
+  io.out = static_cast<__nv_bfloat16*>(y);
+  io.xq = at<uint8_t>(ws, L.xq);
+  io.hq = at<uint8_t>(ws, L.hq);
+  io.xs = at<float>(ws, L.xs);
+  io.hs = at<float>(ws, L.hs);
+  io.counts = at<int32_t>(ws, L.counts);
+  io.offsets = at<int32_t>(ws, L.offsets);
+  io.chunk_prefix = at<int32_t>(ws, L.chunk_prefix);
+  io.sched = at<int>(ws, L.sched);
+  io.status = at<uint32_t>(ws, L.status);
+  if (launch_dense_dispatch(io.R, io.nmax, io.counts, io.offsets, io.chunk_prefix, cs) != cudaSuccess)
+    return BEAM_ERR_CUDA;
+  if (fp8 && launch_gather_q8(x, xdtype == BEAM_BF16, shape->H, nullptr, shape->T, io.xq, io.xs, cs) != cudaSuccess)
+    return BEAM_ERR_CUDA;
+  st = run_gemm(0, ms, weights, io, d, cs);
+  if (st == BEAM_OK) st = run_gemm(1, ms, weights, io, d, cs);
+  return st;
 }
 
 beam_status_t beam_moe_debug_timeout(void* workspace, size_t workspace_bytes, uint32_t timeout_us, void* stream) {

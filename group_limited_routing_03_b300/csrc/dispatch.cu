@@ -186,6 +186,25 @@ cudaError_t launch_dispatch(const int32_t* ids, int R, int n_tiles, int32_t* til
   return cudaGetLastError();
 }
 
+namespace {
+// The dense MLP as one "expert" that takes every row: counts = (R, 0, ...),
+// offsets = (0, R, ..., R), chunk_prefix = (0, n, ..., n) with n = ceil(R / nmax).
+__global__ void __launch_bounds__(288) dense_dispatch_kernel(int R, int nmax, int32_t* counts, int32_t* offsets,
+                                                             int32_t* chunk_prefix) {
+  const int e = threadIdx.x;
+  if (e > kExperts) return;
+  if (e < kExperts) counts[e] = e == 0 ? R : 0;
+  offsets[e] = e == 0 ? 0 : R;
+  chunk_prefix[e] = e == 0 ? 0 : (R + nmax - 1) / nmax;
+}
+}  // namespace
+
+cudaError_t launch_dense_dispatch(int R, int nmax, int32_t* counts, int32_t* offsets, int32_t* chunk_prefix,
+                                  cudaStream_t stream) {
+  dense_dispatch_kernel<<<1, 288, 0, stream>>>(R, nmax, counts, offsets, chunk_prefix);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_gather(const void* x, bool x_bf16, int H, const int32_t* pos, int T, __nv_bfloat16* xp,
                           int num_sms, cudaStream_t stream) {
   const size_t n = static_cast<size_t>(T) * (H / 8);

@@ -120,11 +120,15 @@ cudaError_t launch_tile_hist(const int32_t* ids, int R, int n_tiles, int32_t* ti
 cudaError_t launch_dispatch(const int32_t* ids, int R, int n_tiles, int32_t* tile_hist,
                             int32_t* counts, int32_t* offsets, int32_t* chunk_prefix, int nmax,
                             int32_t* perm, int32_t* pos, cudaStream_t stream);
+// Dense MLP: the unit schedule of one expert holding all R rows.
+cudaError_t launch_dense_dispatch(int R, int nmax, int32_t* counts, int32_t* offsets, int32_t* chunk_prefix,
+                                  cudaStream_t stream);
 cudaError_t launch_gather(const void* x, bool x_bf16, int H, const int32_t* pos, int T,
                           __nv_bfloat16* xp, int num_sms, cudaStream_t stream);
 // FP8 weights: token rows (x in BF16 or FP32) to E4M3 codes in route order,
 // one FP32 scale per row (amax / 448, 1 for a zero row); every token's codes
-// are written to its 8 route rows (xq [R_pad, H], xs [R_pad]).
+// are written to its 8 route rows (xq [R_pad, H], xs [R_pad]); pos == NULL
+// (dense MLP): row t to row t.
 cudaError_t launch_gather_q8(const void* x, bool x_bf16, int H, const int32_t* pos, int T, uint8_t* xq, float* xs,
                              cudaStream_t stream);
 // FP8 weights: rows of h (BF16 [R, I]) to E4M3 codes hq [R_pad, I] and row

@@ -78,8 +78,9 @@ __device__ __forceinline__ uint4 codes16(const void* row, int g, float s) {
   return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// One warp per token: its codes go to the token's 8 route rows.
-template <bool kBf16>
+// One warp per token: its codes go to the token's kRoutes route rows (8 for
+// the MoE block, at pos[t*8 + k]; 1 for the dense MLP, row t).
+template <bool kBf16, int kRoutes>
 __global__ void __launch_bounds__(32 * kWarpsPerCta) gather_q8_kernel(const void* x, int H, const int32_t* pos,
                                                                       int T, uint8_t* xq, float* xs) {
   const int lane = threadIdx.x & 31;
@@ -89,14 +90,14 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta) gather_q8_kernel(const void
                           : static_cast<const void*>(static_cast<const float*>(x) + static_cast<size_t>(t) * H);
   const int groups = H / 16;
   const float s = row_scale<kBf16>(row, groups, lane);
-  int p[kTopK];
+  int p[kRoutes];
 #pragma unroll
-  for (int k = 0; k < kTopK; ++k) p[k] = __ldg(&pos[static_cast<size_t>(t) * kTopK + k]);
-  if (lane < kTopK) xs[p[lane]] = s;
+  for (int k = 0; k < kRoutes; ++k) p[k] = kRoutes == 1 ? t : __ldg(&pos[static_cast<size_t>(t) * kTopK + k]);
+  if (lane < kRoutes) xs[p[lane]] = s;
   for (int g = lane; g < groups; g += 32) {
     const uint4 c = codes16<kBf16>(row, g, s);
 #pragma unroll
-    for (int k = 0; k < kTopK; ++k) *reinterpret_cast<uint4*>(xq + static_cast<size_t>(p[k]) * H + 16 * g) = c;
+    for (int k = 0; k < kRoutes; ++k) *reinterpret_cast<uint4*>(xq + static_cast<size_t>(p[k]) * H + 16 * g) = c;
   }
 }
 
@@ -118,10 +119,16 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta) quantize_rows_kernel(const 
 cudaError_t launch_gather_q8(const void* x, bool x_bf16, int H, const int32_t* pos, int T, uint8_t* xq, float* xs,
                              cudaStream_t stream) {
   const int grid = (T + kWarpsPerCta - 1) / kWarpsPerCta;
-  if (x_bf16)
-    gather_q8_kernel<true><<<grid, 32 * kWarpsPerCta, 0, stream>>>(x, H, pos, T, xq, xs);
-  else
-    gather_q8_kernel<false><<<grid, 32 * kWarpsPerCta, 0, stream>>>(x, H, pos, T, xq, xs);
+  if (pos == nullptr) {  // dense MLP: row t to row t
+    if (x_bf16)
+      gather_q8_kernel<true, 1><<<grid, 32 * kWarpsPerCta, 0, stream>>>(x, H, pos, T, xq, xs);
+    else
+      gather_q8_kernel<false, 1><<<grid, 32 * kWarpsPerCta, 0, stream>>>(x, H, pos, T, xq, xs);
+  } else if (x_bf16) {
+    gather_q8_kernel<true, kTopK><<<grid, 32 * kWarpsPerCta, 0, stream>>>(x, H, pos, T, xq, xs);
+  } else {
+    gather_q8_kernel<false, kTopK><<<grid, 32 * kWarpsPerCta, 0, stream>>>(x, H, pos, T, xq, xs);
+  }
   return cudaGetLastError();
 }
 

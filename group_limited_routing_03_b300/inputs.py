@@ -20,11 +20,17 @@ nvfp4      4096    5120   2560   BF16 x, NVFP4 experts, FP32 router
 skew       32768   5120   2560   BF16, Zipf(1.1) router bias scaled to [0, 3]
 fp8        8192    5120   2560   BF16 x, FP8 experts (E4M3 + row scales, ~10 GB)
 fp8_decode 64      5120   2560   same as fp8
+dense      8192    5120   20480  dense SwiGLU MLP (one "expert"), BF16 (0.63 GB)
+dense_dec  64      5120   20480  same as dense
 =========  ======  =====  =====  ============================================
+
+The dense MLP's width is not given on the pages; 20480 = 8 x 2560 gives it
+the per-token work of the MoE block's eight experts.
 
 Distributions: x ~ N(0, 1) (a post-RMSNorm hidden state); router weight
 ~ N(0, variance 1/H), so logits are ~N(0, 1); expert weights ~ N(0, std 0.02).
-Seeds: tiny 0, decode 1, prefill 2, nvfp4 3, skew 4, fp8 5, fp8_decode 6.  Draw order: x, router
+Seeds: tiny 0, decode 1, prefill 2, nvfp4 3, skew 4, fp8 5, fp8_decode 6,
+dense 7, dense_dec 8.  Draw order: x, router
 weight, bias, gate (expert by expert), up, down.
 """
 from __future__ import annotations
@@ -66,6 +72,8 @@ WORKLOADS = {
     "skew": Workload("skew", 32768, 5120, 2560, "bf16", "bf16", 4, "zipf"),
     "fp8": Workload("fp8", 8192, 5120, 2560, "bf16", "fp8", 5, "none"),
     "fp8_decode": Workload("fp8_decode", 64, 5120, 2560, "bf16", "fp8", 6, "none"),
+    "dense": Workload("dense", 8192, 5120, 20480, "bf16", "bf16", 7, "none", E=1),
+    "dense_dec": Workload("dense_dec", 64, 5120, 20480, "bf16", "bf16", 8, "none", E=1),
 }
 
 

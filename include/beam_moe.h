@@ -309,6 +309,33 @@ beam_status_t beam_moe_route_noalloc(const beam_moe_shape_t* shape, const void* 
                                      const float* router_w, const float* router_bias, int32_t* topk_ids,
                                      float* topk_w, void* stream);
 
+/* Dense SwiGLU MLP.  Source: the Beam post, section "Mixture of Experts":
+ * the first 3 of the 52 layers use a dense SwiGLU MLP in place of the MoE
+ * block (its width is not given; I is the caller's).  Same arithmetic as one
+ * expert of the block:
+ *   y[t,:] = Wd (silu(Wg x[t,:]) * (Wu x[t,:])),  SwiGLU product in FP32,
+ *   FP32 accumulation, h rounded to BF16 between the matmuls,
+ * run by the block's grouped GEMMs as a single expert that takes every row.
+ * x and y: BF16 [T, H] (FP32 x only with FP8 weights, whose first step
+ * re-encodes x).  Weights: a beam_expert_weights_t of one expert (gate/up
+ * [1, I, H], down [1, H, I], the per-expert arrays of NVFP4 / FP8 with one
+ * entry), any dtype and layout the block takes.  Shape limits as for the
+ * block (H % 128, I % 128, 1 <= T <= 1048576; NVFP4 H, I % 256). */
+typedef struct {
+  int32_t T, H, I;
+} beam_dense_shape_t;
+
+/* Workspace bytes of beam_dense_mlp_forward (0 on an unsupported shape). */
+size_t beam_dense_workspace_size(const beam_dense_shape_t* shape, beam_dtype_t wdtype);
+
+beam_status_t beam_dense_mlp_forward(const beam_dense_shape_t* shape, const void* x, beam_dtype_t xdtype,
+                                     const beam_expert_weights_t* weights, void* y, void* workspace,
+                                     size_t workspace_bytes, void* stream);
+
+/* beam_moe_pack_weights for the dense MLP's one-expert weight arrays. */
+beam_status_t beam_dense_pack_weights(const beam_dense_shape_t* shape, const beam_expert_weights_t* src,
+                                      beam_expert_weights_t* dst, void* stream);
+
 /* Static description of a status code. */
 const char* beam_status_string(beam_status_t status);
 

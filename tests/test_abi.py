@@ -244,3 +244,23 @@ def test_fp8_weight_rules(lib):
     assert call(_shape(T=16, H=256, I=384)) == moe.BEAM_ERR_UNSUPPORTED  # I > H
     ew.dtype = moe.BEAM_BF16  # row scales with BF16 weights
     assert call(sh) == moe.BEAM_ERR_INVALID_ARG
+
+
+def test_dense_mlp_argument_errors(lib):
+    sh = moe.dense_shape(64, 256, 512)
+    n = moe.dense_workspace_size(sh, "bf16")
+    assert n > 0 and moe.dense_workspace_size(moe.dense_shape(64, 200, 512)) == 0
+    ew = moe._ExpertWeights()
+    ew.dtype = moe.BEAM_BF16
+    ew.gate, ew.up, ew.down = 0x1000, 0x2000, 0x3000
+
+    def call(x, xdt, y, ws, nbytes):
+        return lib.beam_dense_mlp_forward(ctypes.byref(sh), x, xdt, ctypes.byref(ew), y, ws, nbytes, None)
+
+    assert call(None, moe.BEAM_BF16, 0x20000, 0x100000, n) == moe.BEAM_ERR_INVALID_ARG
+    assert call(0x10008, moe.BEAM_BF16, 0x20000, 0x100000, n) == moe.BEAM_ERR_INVALID_ARG  # misaligned x
+    assert call(0x10000, moe.BEAM_F32, 0x20000, 0x100000, n) == moe.BEAM_ERR_UNSUPPORTED  # FP32 x, BF16 weights
+    assert call(0x10000, moe.BEAM_BF16, 0x20000, 0x100000, n - 1) == moe.BEAM_ERR_WORKSPACE
+    assert call(0x10000, moe.BEAM_BF16, 0x20000, 0x100080, n) == moe.BEAM_ERR_WORKSPACE  # not 256-byte aligned
+    assert lib.beam_dense_mlp_forward(None, 0x10000, moe.BEAM_BF16, ctypes.byref(ew), 0x20000, 0x100000, n,
+                                      None) == moe.BEAM_ERR_INVALID_ARG

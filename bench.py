@@ -515,7 +515,7 @@ def main():
     ap.add_argument("--no-dense", action="store_true",
                     help="skip the dense SwiGLU MLP (decode T=64 and prefill T=8192, I=20480)")
     ap.add_argument("--no-fp8", action="store_true",
-                    help="skip the FP8-weight layers (decode T=64 and prefill T=8192)")
+                    help="skip the FP8-weight layers (decode T=64 and prefill T=8192) and the NVFP4 decode layer")
     ap.add_argument("--no-residual", action="store_true",
                     help="skip the extra steps with the post-norm residual update fused into the combine")
     ap.add_argument("--small", action="store_true",
@@ -588,14 +588,15 @@ def main():
     fp8 = None
     if not args.no_fp8 and not args.small:
         fp8 = {}
-        for name, steps in (("fp8_decode", args.steps), ("fp8", max(3, args.steps // 2))):
+        for name, steps in (("fp8_decode", args.steps), ("fp8", max(3, args.steps // 2)), ("nvfp4_dec", args.steps)):
             fw = inputs.workload(name)
             fm, fstate = measure(fw, steps, args.warmup, dev, world, torch.cuda.current_device())
             f_ms = max_over_ranks(fm["total_ms"], world)
             fhbm, ftc = roofline(fw, fm, pk)
             fp8[name] = dict(value=fw.T * steps * world / (f_ms * 1e-3), unit="tokens/s",
-                             config={"workload": f"{name} T={fw.T} H={fw.H} I={fw.I} E=256 fp8 experts "
-                                                 "(E4M3 + row scales), E4M3 activations per row", "T": fw.T},
+                             config={"workload": f"{name} T={fw.T} H={fw.H} I={fw.I} E=256 " + (
+                                 "fp8 experts (E4M3 + row scales), E4M3 activations per row" if fw.w_dtype == "fp8"
+                                 else "nvfp4 experts (W4A16)"), "T": fw.T},
                              roofline_hbm=fhbm, roofline=ftc, clocks=fm["clocks"],
                              gpu_launches=fm["launches_per_step"] * steps, **step_numbers(fw, fm, steps))
             del fstate
@@ -620,7 +621,7 @@ def main():
                          f"({m['touched']} x {weight_bytes_per_expert(wl) / 1e6:.1f} MB), far larger than L2"},
         "roofline": hbm, "roofline_tensor": tc, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": m["launches_per_step"] * args.steps, "clocks": m["clocks"],
-        "step": sn, "residual_epilogue": residual, "prefill": prefill, "fp8": fp8, "dense": dense,
+        "step": sn, "residual_epilogue": residual, "prefill": prefill, "weight_formats": fp8, "dense": dense,
     }
     print(json.dumps(line), flush=True)
 

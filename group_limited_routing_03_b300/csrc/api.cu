@@ -6,6 +6,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -169,10 +170,13 @@ beam_status_t check_shape(const beam_moe_shape_t* s) {
   return BEAM_OK;
 }
 
+int chunk_rows(int T, bool fp4);
+int split_parts(int units, int k_blocks);
+
 // Dense MLP workspace: status, unit counters, the one-expert schedule, h, and
 // for FP8 weights the codes of x and h with their row scales.
 struct DenseLayout {
-  size_t status, sched, counts, offsets, chunk_prefix, h, xq, hq, xs, hs, total;
+  size_t status, sched, counts, offsets, chunk_prefix, h, xq, hq, xs, hs, partial, total;
 };
 
 void make_dense_layout(const beam_dense_shape_t& s, DenseLayout& L) {
@@ -194,6 +198,15 @@ void make_dense_layout(const beam_dense_shape_t& s, DenseLayout& L) {
   L.hq = take(T_pad * I);
   L.xs = take((T_pad + 32) * 4);
   L.hs = take((T_pad + 32) * 4);
+  // K-split partial planes: the larger of gate/up (two planes of T x I per
+  // part) and down (one of T x H), parts as run_gemm picks them for BF16
+  // weights (FP8 has half the k-blocks, so never more parts)
+  const int nmax = chunk_rows(s.T, false);
+  const int chunks = (s.T + nmax - 1) / nmax;
+  const size_t gu = static_cast<size_t>(split_parts(chunks * (s.I / kBlockM), s.H / kBlockK));
+  const size_t dn = static_cast<size_t>(split_parts(chunks * (s.H / kBlockM), s.I / kBlockK));
+  const size_t need = std::max(gu > 1 ? gu * 2 * T * I : 0, dn > 1 ? dn * T * H : 0);
+  L.partial = take(need * 4);
   L.total = off;
 }
 
@@ -358,7 +371,21 @@ struct GemmIO {
   int32_t* chunk_prefix;
   int* sched;           // two unit counters (gate/up, down)
   uint32_t* status;
+  int split_chunks;     // K split allowed: the number of token chunks (known on the host), else 0
+  float* partial;       // K split: FP32 partial planes (see split_parts)
 };
+
+// K split of a grouped GEMM with few units: enough parts for about four
+// units per SM of a 148-SM B300, each part at least four k-blocks, at most
+// 16 parts.  1: no split.
+constexpr int kSplitTargetUnits = 592;
+int split_parts(int units, int k_blocks) {
+  if (units <= 0 || units >= kSplitTargetUnits) return 1;
+  int ks = (kSplitTargetUnits + units - 1) / units;
+  if (ks > 16) ks = 16;
+  if (ks > k_blocks / 4) ks = k_blocks / 4;
+  return ks < 2 ? 1 : ks;
+}
 
 GemmIO moe_io(const beam_moe_shape_t& s, void* ws, const Layout& L, bool fp4) {
   GemmIO io;
@@ -378,6 +405,8 @@ GemmIO moe_io(const beam_moe_shape_t& s, void* ws, const Layout& L, bool fp4) {
   io.chunk_prefix = at<int32_t>(ws, L.chunk_prefix);
   io.sched = at<int>(ws, L.sched);
   io.status = at<uint32_t>(ws, L.status);
+  io.split_chunks = 0;  // the block's chunk count is known only on the device
+  io.partial = nullptr;
   return io;
 }
 
@@ -466,7 +495,12 @@ beam_status_t run_gemm(int mode, const beam_moe_shape_t& s, const beam_expert_we
   // Down on one CTA per unit: 256 features (two weight tiles, two
   // accumulators: two MMA chains per k-block) for NVFP4, and for BF16 when H
   // allows ("wide"); else 128.
-  const bool wide = mode == 1 && !pair && !fp4 && s.H % 256 == 0;
+  // K split (host-known chunk count, one CTA per unit, BF16 / FP8): 128-row units
+  const int k_blocks = (mode == 0 ? s.H : s.I) / (fp8 ? 2 * kBlockK : kBlockK);
+  int k_splits = 1;
+  if (io.split_chunks > 0 && io.partial != nullptr && !pair && !fp4)
+    k_splits = split_parts(io.split_chunks * ((mode == 0 ? s.I : s.H) / kBlockM), k_blocks);
+  const bool wide = mode == 1 && !pair && !fp4 && s.H % 256 == 0 && k_splits == 1;
   const int rows_per_unit =
       pair ? (mode == 0 ? 2 * kBlockM : 4 * kBlockM) : ((fp4 || wide) && mode == 1 ? 2 * kBlockM : kBlockM);
   GemmParams p;
@@ -475,7 +509,10 @@ beam_status_t run_gemm(int mode, const beam_moe_shape_t& s, const beam_expert_we
   p.chunk_prefix = io.chunk_prefix;
   p.m_tiles = (mode == 0 ? s.I : s.H) / rows_per_unit;
   p.a_rows_per_expert = mode == 0 ? s.I : s.H;
-  p.k_blocks = (mode == 0 ? s.H : s.I) / (fp8 ? 2 * kBlockK : kBlockK);
+  p.k_blocks = k_blocks;
+  p.k_splits = k_splits;
+  p.rows = R;
+  p.partial = k_splits > 1 ? io.partial : nullptr;
   p.a_tiled = tiled ? 1 : 0;
   p.nmax = nmax;
   const int num_a = (mode == 0 || pair || fp4 || wide) ? 2 : 1;  // weight tiles per stage
@@ -531,7 +568,10 @@ beam_status_t run_gemm(int mode, const beam_moe_shape_t& s, const beam_expert_we
     return BEAM_ERR_CUDA;
   }
   if (cudaMemsetAsync(p.sched, 0, sizeof(int), stream) != cudaSuccess) return BEAM_ERR_CUDA;
-  return cuda_status(launch_gemm(mode, fp4, pair, wide, fp8, maps, p, grid, smem, stream));
+  if (launch_gemm(mode, fp4, pair, wide, fp8, maps, p, grid, smem, stream) != cudaSuccess) return BEAM_ERR_CUDA;
+  if (k_splits > 1)
+    return cuda_status(launch_splitk_finish(mode, io.partial, k_splits, R, p.out_ld, mode == 0 ? h : yr, stream));
+  return BEAM_OK;
 }
 
 beam_status_t run_combine(const beam_moe_shape_t& s, const float* w, void* y, bool y_bf16, void* ws, const Layout& L,
@@ -909,6 +949,8 @@ beam_status_t beam_dense_mlp_forward(const beam_dense_shape_t* shape, const void
   io.chunk_prefix = at<int32_t>(ws, L.chunk_prefix);
   io.sched = at<int>(ws, L.sched);
   io.status = at<uint32_t>(ws, L.status);
+  io.split_chunks = (io.R + io.nmax - 1) / io.nmax;
+  io.partial = at<float>(ws, L.partial);
   if (launch_dense_dispatch(io.R, io.nmax, io.counts, io.offsets, io.chunk_prefix, cs) != cudaSuccess)
     return BEAM_ERR_CUDA;
   if (fp8 && launch_gather_q8(x, xdtype == BEAM_BF16, shape->H, nullptr, shape->T, io.xq, io.xs, cs) != cudaSuccess)

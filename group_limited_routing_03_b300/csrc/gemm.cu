@@ -72,11 +72,18 @@ constexpr int kSchedRing = 8;                               // scheduled unit in
 
 struct Unit {
   int e, m, start, n;
+  int ks, kb0, kb1;  // K split: part ks covers k-blocks [kb0, kb1)
 };
 
 __device__ __forceinline__ Unit unit_at(const GemmParams& p, int u) {
-  const int q = u / p.m_tiles;
   Unit U;
+  // K split (p.k_splits > 1: few units for many SMs): the parts of one tile
+  // are adjacent unit indices
+  U.ks = u % p.k_splits;
+  u /= p.k_splits;
+  U.kb0 = U.ks * p.k_blocks / p.k_splits;
+  U.kb1 = (U.ks + 1) * p.k_blocks / p.k_splits;
+  const int q = u / p.m_tiles;
   U.m = u - q * p.m_tiles;
   // expert e with chunk_prefix[e] <= q < chunk_prefix[e+1]
   int lo = 0, hi = kExperts;  // invariant: chunk_prefix[lo] <= q < chunk_prefix[hi]
@@ -305,7 +312,7 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       const uint64_t pol_x = l2_policy_evict_last();
-      const int total_units = __ldg(&p.chunk_prefix[kExperts]) * p.m_tiles;
+      const int total_units = __ldg(&p.chunk_prefix[kExperts]) * p.m_tiles * p.k_splits;
       int stage = 0;
       uint32_t phase = 0;
       long long issued = 0;
@@ -335,7 +342,7 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
             a_bytes + (big ? static_cast<uint32_t>(p.b_big_rows) * (kBlockK * 2) : static_cast<uint32_t>(nbox) * kBoxBytes);
         const CUtensorMap* bmap = big ? &maps.bb : &maps.b;
         const int box_rows = big ? 0 : kBoxRows;  // row step between boxes
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
+        for (int kb = U.kb0; kb < U.kb1; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, p.timeout_ns, abort_flag, p.status, kWhereProducerEmpty)) {
             ok = false;
             break;
@@ -407,7 +414,7 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
         tc_fence_after();
         const uint32_t d0 = tmem_base + static_cast<uint32_t>(acc) * p.acc_cols;
         const uint32_t d1 = d0 + static_cast<uint32_t>(p.nmax);
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
+        for (int kb = U.kb0; kb < U.kb1; ++kb) {
           // BF16: the TMA bytes of the stage.  NVFP4: the converters' BF16
           // tile in TMEM; they arrive after observing the stage's TMA bytes.
           if (!mbar_wait(kFp4 ? &afull[astage] : &full[stage], kFp4 ? aphase : phase, p.timeout_ns, abort_flag,
@@ -421,7 +428,7 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
             const uint32_t ta = tmem_base + p.a_col0 + static_cast<uint32_t>(astage * kNumA * (kBlockK / 2));
 #pragma unroll
             for (int k = 0; k < kBlockK / 16; ++k) {
-              const uint32_t accumulate = (kb | k) != 0 ? 1u : 0u;
+              const uint32_t accumulate = (kb != U.kb0 || k != 0) ? 1u : 0u;
               mma_bf16_ts(issuer == 0 ? d0 : d1, ta + static_cast<uint32_t>(issuer * (kBlockK / 2)) + 8u * k,
                           db + 2u * k, idesc, accumulate);
             }
@@ -430,7 +437,7 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
             const uint64_t da1 = sdesc_k_sw128(smem_u32(a_tile(stage, kNumA - 1)));
 #pragma unroll
             for (int k = 0; k < kBlockK / 16; ++k) {
-              const uint32_t accumulate = (kb | k) != 0 ? 1u : 0u;
+              const uint32_t accumulate = (kb != U.kb0 || k != 0) ? 1u : 0u;
               if (kPair && kFp8) {
                 mma_f8_pair(d0, da0 + 2u * k, db + 2u * k, idesc, accumulate);
                 mma_f8_pair(d1, da1 + 2u * k, db + 2u * k, idesc, accumulate);
@@ -506,6 +513,42 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
         s1 = (kMode == 0 && p.gs1 != nullptr) ? __ldg(&p.gs1[U.e]) : 1.0f;
       }
       const int ncols = (U.n + 15) & ~15;
+      if (p.partial != nullptr) {
+        // K split: FP32 partial sums (row scales applied, they are linear)
+        // of this part, stored as they are read; the finishing kernel adds
+        // the parts and applies SwiGLU / the BF16 rounding.
+        const size_t plane = static_cast<size_t>(p.rows) * p.out_ld;
+        float* part0 = p.partial + static_cast<size_t>(U.ks) * (kMode == 0 ? 2 : 1) * plane + feat;
+        for (int c0 = 16 * half; c0 < ncols; c0 += 32) {
+          float g[16], g2[16];
+          tmem_ld16(tbase + static_cast<uint32_t>(c0), g);
+          if (kNumA == 2) tmem_ld16(tbase + static_cast<uint32_t>(p.nmax + c0), g2);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float cs = kFp8 ? __ldg(&p.bscale[U.start + c0 + j]) : 1.0f;
+            if (c0 + j < U.n) {
+              float* dst = part0 + static_cast<size_t>(U.start + c0 + j) * p.out_ld;
+              dst[0] = g[j] * cs * s0;
+              if (kMode == 0) dst[plane] = g2[j] * cs * s1;            // up: the second plane
+              if (kMode == 1 && kOut == 2) dst[kHalfRows] = g2[j] * cs * s1;
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (kPair)
+            mbar_arrive_cluster(mapa_shared(&acc_empty[acc], 0));
+          else
+            mbar_arrive(&acc_empty[acc]);
+        }
+        if (++acc == p.acc_stages) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+        continue;
+      }
       __nv_bfloat16* out = p.out + static_cast<size_t>(U.start) * p.out_ld + feat;
       // 1) TMEM -> packed BF16 results in registers (this warp's 16-column
       //    chunks), 2) release the accumulator so the next unit's MMAs start,

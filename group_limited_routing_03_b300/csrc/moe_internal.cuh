@@ -74,6 +74,9 @@ struct GemmParams {
   const float* rs0;             // FP8 row scales (gate or down) [E * rows], else null
   const float* rs1;             // FP8 row scales (up) [E * I], else null
   const float* bscale;          // FP8 token-row scales [R_pad + 32] (x or h rows, perm order), else null
+  int k_splits;                 // parts of the K range per tile (1: none); > 1 only without CTA pairs / NVFP4
+  int rows;                     // route rows R (K split: rows of one partial plane)
+  float* partial;               // K split: FP32 sums [k_splits][planes][R][out_ld] (planes: 2 gate/up, 1 down), else null
   uint32_t* status;
   uint64_t timeout_ns;
 };
@@ -143,6 +146,10 @@ size_t gemm_smem_bytes(int stages, int acc_stages, size_t stage_bytes);
 int gemm_pair_max_clusters(int mode, size_t smem_bytes);
 cudaError_t launch_combine(const __nv_bfloat16* yr, const int32_t* pos, const float* w, int T, int H,
                            void* y, bool y_bf16, cudaStream_t stream);
+// K split: add the k_splits FP32 partial planes in part order; mode 0: h =
+// BF16(silu(sum gate) * sum up) [R, N]; mode 1: out = BF16(sum) [R, N].
+cudaError_t launch_splitk_finish(int mode, const float* partial, int k_splits, int R, int N, __nv_bfloat16* out,
+                                 cudaStream_t stream);
 // Post-norm residual update fused into the combine (see combine.cu).
 struct ResidualParams {
   const void* stream;   // [T, H] residual stream, the activations' dtype

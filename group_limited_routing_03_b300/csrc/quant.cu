@@ -84,7 +84,7 @@ template <bool kBf16, int kRoutes>
 __global__ void __launch_bounds__(32 * kWarpsPerCta) gather_q8_kernel(const void* x, int H, const int32_t* pos,
                                                                       int T, uint8_t* xq, float* xs) {
   const int lane = threadIdx.x & 31;
-  const int t = blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
+  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= T) return;
   const void* row = kBf16 ? static_cast<const void*>(static_cast<const __nv_bfloat16*>(x) + static_cast<size_t>(t) * H)
                           : static_cast<const void*>(static_cast<const float*>(x) + static_cast<size_t>(t) * H);
@@ -118,16 +118,19 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta) quantize_rows_kernel(const 
 
 cudaError_t launch_gather_q8(const void* x, bool x_bf16, int H, const int32_t* pos, int T, uint8_t* xq, float* xs,
                              cudaStream_t stream) {
-  const int grid = (T + kWarpsPerCta - 1) / kWarpsPerCta;
+  // few tokens (decode): two warps per CTA, so the rows spread over more SMs
+  const int warps = T <= 4096 ? 2 : kWarpsPerCta;
+  const int grid = (T + warps - 1) / warps;
+  const int threads = 32 * warps;
   if (pos == nullptr) {  // dense MLP: row t to row t
     if (x_bf16)
-      gather_q8_kernel<true, 1><<<grid, 32 * kWarpsPerCta, 0, stream>>>(x, H, pos, T, xq, xs);
+      gather_q8_kernel<true, 1><<<grid, threads, 0, stream>>>(x, H, pos, T, xq, xs);
     else
-      gather_q8_kernel<false, 1><<<grid, 32 * kWarpsPerCta, 0, stream>>>(x, H, pos, T, xq, xs);
+      gather_q8_kernel<false, 1><<<grid, threads, 0, stream>>>(x, H, pos, T, xq, xs);
   } else if (x_bf16) {
-    gather_q8_kernel<true, kTopK><<<grid, 32 * kWarpsPerCta, 0, stream>>>(x, H, pos, T, xq, xs);
+    gather_q8_kernel<true, kTopK><<<grid, threads, 0, stream>>>(x, H, pos, T, xq, xs);
   } else {
-    gather_q8_kernel<false, kTopK><<<grid, 32 * kWarpsPerCta, 0, stream>>>(x, H, pos, T, xq, xs);
+    gather_q8_kernel<false, kTopK><<<grid, threads, 0, stream>>>(x, H, pos, T, xq, xs);
   }
   return cudaGetLastError();
 }

@@ -17,6 +17,7 @@ tiny       128     256    128    FP32 x / router / experts (seed 0)
 decode     64      5120   2560   BF16 x, BF16 experts (~20 GB), FP32 router
 prefill    8192    5120   2560   same as decode, no router bias
 nvfp4      4096    5120   2560   BF16 x, NVFP4 experts, FP32 router
+nvfp4_dec  64      5120   2560   same as nvfp4 (decode)
 skew       32768   5120   2560   BF16, Zipf(1.1) router bias scaled to [0, 3]
 fp8        8192    5120   2560   BF16 x, FP8 experts (E4M3 + row scales, ~10 GB)
 fp8_decode 64      5120   2560   same as fp8
@@ -30,7 +31,7 @@ the per-token work of the MoE block's eight experts.
 Distributions: x ~ N(0, 1) (a post-RMSNorm hidden state); router weight
 ~ N(0, variance 1/H), so logits are ~N(0, 1); expert weights ~ N(0, std 0.02).
 Seeds: tiny 0, decode 1, prefill 2, nvfp4 3, skew 4, fp8 5, fp8_decode 6,
-dense 7, dense_dec 8.  Draw order: x, router
+dense 7, dense_dec 8, nvfp4_dec 9.  Draw order: x, router
 weight, bias, gate (expert by expert), up, down.
 """
 from __future__ import annotations
@@ -72,6 +73,7 @@ WORKLOADS = {
     "skew": Workload("skew", 32768, 5120, 2560, "bf16", "bf16", 4, "zipf"),
     "fp8": Workload("fp8", 8192, 5120, 2560, "bf16", "fp8", 5, "none"),
     "fp8_decode": Workload("fp8_decode", 64, 5120, 2560, "bf16", "fp8", 6, "none"),
+    "nvfp4_dec": Workload("nvfp4_dec", 64, 5120, 2560, "bf16", "nvfp4", 9, "none"),
     "dense": Workload("dense", 8192, 5120, 20480, "bf16", "bf16", 7, "none", E=1),
     "dense_dec": Workload("dense_dec", 64, 5120, 20480, "bf16", "bf16", 8, "none", E=1),
 }

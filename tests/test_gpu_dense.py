@@ -53,11 +53,15 @@ def _weights(d):
 
 
 # one CTA per unit and CTA pairs (T >= 256, H % 512, I % 256), both layouts,
-# FP8 with I > H (the dense workspace keeps h's codes apart), NVFP4, T = 1
+# FP8 with I > H (the dense workspace keeps h's codes apart), NVFP4, T = 1;
+# K split across CTAs (few units: T <= 128 with enough k-blocks): 64 x 512 x
+# 1024 (gate/up 2 parts, down 4), 100 x 768 x 512 (3 parts over a ragged chunk,
+# down 2), FP8 48 x 1024 x 2048 (2 / 4 parts)
 @pytest.mark.parametrize("T,H,I,w_dtype,pack", [
     (1, 256, 128, "f32", False), (33, 256, 384, "f32", True), (300, 512, 256, "f32", False),
     (600, 1024, 768, "f32", True), (300, 512, 1024, "fp8", False), (200, 256, 512, "fp8", True),
-    (100, 512, 256, "nvfp4", False), (257, 512, 512, "nvfp4", True)])
+    (100, 512, 256, "nvfp4", False), (257, 512, 512, "nvfp4", True),
+    (64, 512, 1024, "f32", False), (100, 768, 512, "f32", True), (48, 1024, 2048, "fp8", False)])
 def test_dense_all_rows(T, H, I, w_dtype, pack):
     wl, d = _dense_inputs(T, H, I, w_dtype, T + I, "cpu")
     dg = {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in d.items()}

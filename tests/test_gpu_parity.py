@@ -232,7 +232,8 @@ def _sample_tokens(T, ids_ref, n, seed, hot_expert=None):
     return np.array(sorted(pick))
 
 
-@pytest.mark.parametrize("name,n_sample", [("decode", 8), ("prefill", 4), ("nvfp4", 4), ("skew", 4)])
+@pytest.mark.parametrize("name,n_sample", [("decode", 8), ("prefill", 4), ("nvfp4", 4), ("skew", 4),
+                                           ("nvfp4_dec", 8)])
 def test_full_size_workloads(name, n_sample):
     wl = inputs.workload(name)
     torch.cuda.empty_cache()

@@ -255,7 +255,8 @@ def measure_dense(wl, steps, warmup, dev, pk):
     tfs = flops / (ms * 1e-3) / 1e12
     out = dict(value=wl.T / (ms * 1e-3), unit="tokens/s", ms_per_call=round(ms, 4), steps=steps,
                config={"workload": f"{wl.name} T={wl.T} H={wl.H} I={wl.I} dense SwiGLU MLP, BF16", "T": wl.T},
-               gpu_launches=steps * 3, clocks=clk.summary())
+               gpu_launches=steps * moe.dense_kernel_count(moe.dense_shape(wl.T, wl.H, wl.I), "bf16"),
+               clocks=clk.summary())
     if wl.T <= 256:
         out["roofline"] = dict(bound="hbm", achieved=round(gbs, 1), peak=pk["hbm"], unit="GB/s",
                                frac=round(gbs / pk["hbm"], 4), peak_source=pk["source"])

@@ -119,6 +119,8 @@ def load():
     lib.beam_dense_workspace_size.restype = sz
     lib.beam_dense_mlp_forward.argtypes = [dp, vp, i32, ctypes.POINTER(_ExpertWeights), vp, vp, sz, vp]
     lib.beam_dense_pack_weights.argtypes = [dp, ctypes.POINTER(_ExpertWeights), ctypes.POINTER(_ExpertWeights), vp]
+    lib.beam_dense_kernel_count.argtypes = [dp, i32]
+    lib.beam_dense_kernel_count.restype = ctypes.c_int32
     lib.beam_status_string.argtypes = [i32]
     lib.beam_status_string.restype = ctypes.c_char_p
     for n in ("beam_moe_workspace_layout", "beam_moe_route", "beam_moe_dispatch", "beam_moe_experts",
@@ -375,6 +377,14 @@ def beam_dense_mlp_forward(sh: DenseShape, x, weights: dict, y, workspace, strea
     _check(load().beam_dense_mlp_forward(ctypes.byref(sh), _ptr(x), _act_dtype(x), ctypes.byref(ew), _ptr(y),
                                          _ptr(workspace), workspace.numel(), _stream(stream)),
            "beam_dense_mlp_forward")
+
+
+def dense_kernel_count(sh: DenseShape, wdtype="bf16") -> int:
+    """Kernels one beam_dense_mlp_forward launches for ``sh`` on this device."""
+    n = int(load().beam_dense_kernel_count(ctypes.byref(sh), _wdtype(wdtype)))
+    if n < 0:
+        raise BeamError(BEAM_ERR_UNSUPPORTED, "beam_dense_kernel_count")
+    return n
 
 
 def dense_pack_weights(sh: DenseShape, weights: dict, stream=None) -> dict:

@@ -410,6 +410,36 @@ GemmIO moe_io(const beam_moe_shape_t& s, void* ws, const Layout& L, bool fp4) {
   return io;
 }
 
+// The GEMM variant run_gemm launches.  CTA pairs (one M=256 MMA per unit over
+// two SMs) halve each SM's shared-memory operand traffic; used for BF16 / FP8
+// weights when chunks reach 256 routes and a pair fits on the device (a pair
+// tile's stage is fixed: two weight tiles, 128 token rows per CTA, one 2 x
+// 256-column accumulator).  K split: only with a host-known chunk count
+// (split_chunks > 0), one CTA per unit, BF16 / FP8.
+struct GemmChoice {
+  bool pair;
+  int clusters;
+  int k_splits;
+};
+
+GemmChoice choose_gemm(int mode, const beam_moe_shape_t& s, bool fp4, bool fp8, int nmax, int split_chunks,
+                       const DeviceInfo& d) {
+  GemmChoice c{false, 0, 1};
+  const size_t budget = static_cast<size_t>(d.smem_optin) - 1024 - 512;
+  c.pair = !fp4 && nmax == 256 && s.H % 512 == 0 && s.I % 256 == 0 && d.sms >= 2;
+  if (c.pair) {
+    const size_t sbp = gemm_stage_bytes(2, false, nmax / 2);
+    int stp = static_cast<int>(budget / sbp);
+    if (stp > kMaxStages) stp = kMaxStages;
+    c.clusters = stp >= 2 ? gemm_pair_max_clusters(mode, gemm_smem_bytes(stp, 1, sbp)) : 0;
+    if (c.clusters <= 0) c.pair = false;
+  }
+  const int k_blocks = (mode == 0 ? s.H : s.I) / (fp8 ? 2 * kBlockK : kBlockK);
+  if (split_chunks > 0 && !c.pair && !fp4)
+    c.k_splits = split_parts(split_chunks * ((mode == 0 ? s.I : s.H) / kBlockM), k_blocks);
+  return c;
+}
+
 beam_status_t run_gemm(int mode, const beam_moe_shape_t& s, const beam_expert_weights_t* wts, const GemmIO& io,
                        const DeviceInfo& d, cudaStream_t stream) {
   const int R = io.R;
@@ -482,24 +512,15 @@ beam_status_t run_gemm(int mode, const beam_moe_shape_t& s, const beam_expert_we
   // CTA, one 2 x 256-column accumulator), and if no pair fits on the device
   // the GEMM runs one CTA per unit.
   const size_t budget = static_cast<size_t>(d.smem_optin) - 1024 - 512;
-  bool pair = !fp4 && nmax == 256 && s.H % 512 == 0 && s.I % 256 == 0 && d.sms >= 2;
-  int clusters = 0;
-  if (pair) {
-    const size_t sbp = gemm_stage_bytes(2, false, nmax / 2);
-    int stp = static_cast<int>(budget / sbp);
-    if (stp > kMaxStages) stp = kMaxStages;
-    clusters = stp >= 2 ? gemm_pair_max_clusters(mode, gemm_smem_bytes(stp, 1, sbp)) : 0;
-    if (clusters <= 0) pair = false;
-  }
+  const GemmChoice gc = choose_gemm(mode, s, fp4, fp8, nmax, io.partial != nullptr ? io.split_chunks : 0, d);
+  const bool pair = gc.pair;
+  const int clusters = gc.clusters;
   // pair units: gate/up 256 features (gate and up tiles), down 512 features.
   // Down on one CTA per unit: 256 features (two weight tiles, two
   // accumulators: two MMA chains per k-block) for NVFP4, and for BF16 when H
-  // allows ("wide"); else 128.
-  // K split (host-known chunk count, one CTA per unit, BF16 / FP8): 128-row units
+  // allows ("wide"); else 128.  K split: 128-row units.
   const int k_blocks = (mode == 0 ? s.H : s.I) / (fp8 ? 2 * kBlockK : kBlockK);
-  int k_splits = 1;
-  if (io.split_chunks > 0 && io.partial != nullptr && !pair && !fp4)
-    k_splits = split_parts(io.split_chunks * ((mode == 0 ? s.I : s.H) / kBlockM), k_blocks);
+  const int k_splits = gc.k_splits;
   const bool wide = mode == 1 && !pair && !fp4 && s.H % 256 == 0 && k_splits == 1;
   const int rows_per_unit =
       pair ? (mode == 0 ? 2 * kBlockM : 4 * kBlockM) : ((fp4 || wide) && mode == 1 ? 2 * kBlockM : kBlockM);
@@ -899,6 +920,23 @@ beam_status_t beam_dense_pack_weights(const beam_dense_shape_t* shape, const bea
   if (shape == nullptr) return BEAM_ERR_INVALID_ARG;
   const beam_moe_shape_t ms = dense_as_moe(*shape);
   return pack_impl(&ms, 1, src, dst, stream);
+}
+
+int32_t beam_dense_kernel_count(const beam_dense_shape_t* shape, beam_dtype_t wdtype) {
+  if (shape == nullptr) return -1;
+  const beam_moe_shape_t ms = dense_as_moe(*shape);
+  if (check_shape(&ms) != BEAM_OK) return -1;
+  if (wdtype != BEAM_BF16 && wdtype != BEAM_NVFP4 && wdtype != BEAM_FP8) return -1;
+  DeviceInfo d;
+  if (!device_info(d)) return -1;
+  const bool fp4 = wdtype == BEAM_NVFP4, fp8 = wdtype == BEAM_FP8;
+  const int nmax = chunk_rows(shape->T, fp4);
+  const int chunks = (shape->T + nmax - 1) / nmax;
+  int n = 1 + 1 + 1;        // schedule, gate/up, down
+  if (fp8) n += 2;          // x codes, h codes
+  for (int mode = 0; mode < 2; ++mode)
+    if (choose_gemm(mode, ms, fp4, fp8, nmax, chunks, d).k_splits > 1) n += 1;  // the finishing kernel
+  return n;
 }
 
 size_t beam_dense_workspace_size(const beam_dense_shape_t* shape, beam_dtype_t wdtype) {

@@ -332,6 +332,13 @@ beam_status_t beam_dense_mlp_forward(const beam_dense_shape_t* shape, const void
                                      const beam_expert_weights_t* weights, void* y, void* workspace,
                                      size_t workspace_bytes, void* stream);
 
+/* Kernels one beam_dense_mlp_forward launches on the current device: the
+ * one-expert schedule, the gate/up and down GEMMs, with FP8 weights the two
+ * row quantisations, and a finishing kernel after each GEMM whose K range is
+ * split across CTAs (few rows: the partial sums are added in part order);
+ * -1 on an unsupported shape or dtype. */
+int32_t beam_dense_kernel_count(const beam_dense_shape_t* shape, beam_dtype_t wdtype);
+
 /* beam_moe_pack_weights for the dense MLP's one-expert weight arrays. */
 beam_status_t beam_dense_pack_weights(const beam_dense_shape_t* shape, const beam_expert_weights_t* src,
                                       beam_expert_weights_t* dst, void* stream);

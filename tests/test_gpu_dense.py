@@ -92,3 +92,12 @@ def test_dense_full_size(name, n_sample):
     del dg, y, mlp
     gc.collect()
     torch.cuda.empty_cache()
+
+
+def test_dense_kernel_count():
+    """K split after each GEMM at decode size (a finishing kernel each), none
+    at prefill size (CTA pairs); FP8 adds the two row quantisations."""
+    assert moe.dense_kernel_count(moe.dense_shape(64, 5120, 20480), "bf16") == 5
+    assert moe.dense_kernel_count(moe.dense_shape(64, 5120, 20480), "fp8") == 7
+    assert moe.dense_kernel_count(moe.dense_shape(8192, 5120, 20480), "bf16") == 3
+    assert moe.dense_kernel_count(moe.dense_shape(64, 5120, 20480), "nvfp4") == 3

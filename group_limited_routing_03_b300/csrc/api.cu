@@ -521,6 +521,8 @@ beam_status_t run_gemm(int mode, const beam_moe_shape_t& s, const beam_expert_we
   // allows ("wide"); else 128.  K split: 128-row units.
   const int k_blocks = (mode == 0 ? s.H : s.I) / (fp8 ? 2 * kBlockK : kBlockK);
   const int k_splits = gc.k_splits;
+  // NVFP4 with chunks of at most 64 routes (decode): more converter warps
+  const bool dec = fp4 && nmax <= kDecChunkRows;
   const bool wide = mode == 1 && !pair && !fp4 && s.H % 256 == 0 && k_splits == 1;
   const int rows_per_unit =
       pair ? (mode == 0 ? 2 * kBlockM : 4 * kBlockM) : ((fp4 || wide) && mode == 1 ? 2 * kBlockM : kBlockM);
@@ -562,7 +564,7 @@ beam_status_t run_gemm(int mode, const beam_moe_shape_t& s, const beam_expert_we
     p.a_stages = static_cast<int>((512 - p.a_col0) / a_cols);
     if (p.a_stages > kMaxAStages) p.a_stages = kMaxAStages;
     if (p.a_stages > p.stages) p.a_stages = p.stages;  // a tile is freed through the smem ring's empty barriers
-    if (p.a_stages < 2) return BEAM_ERR_UNSUPPORTED;   // the converter groups alternate
+    if (p.a_stages < (dec ? 3 : 2)) return BEAM_ERR_UNSUPPORTED;  // one tile per converter group at least
     p.tmem_cols = 512;
   }
   p.sched = io.sched + mode;
@@ -589,7 +591,7 @@ beam_status_t run_gemm(int mode, const beam_moe_shape_t& s, const beam_expert_we
     return BEAM_ERR_CUDA;
   }
   if (cudaMemsetAsync(p.sched, 0, sizeof(int), stream) != cudaSuccess) return BEAM_ERR_CUDA;
-  if (launch_gemm(mode, fp4, pair, wide, fp8, maps, p, grid, smem, stream) != cudaSuccess) return BEAM_ERR_CUDA;
+  if (launch_gemm(mode, fp4, pair, wide, fp8, dec, maps, p, grid, smem, stream) != cudaSuccess) return BEAM_ERR_CUDA;
   if (k_splits > 1)
     return cuda_status(launch_splitk_finish(mode, io.partial, k_splits, R, p.out_ld, mode == 0 ? h : yr, stream));
   return BEAM_OK;

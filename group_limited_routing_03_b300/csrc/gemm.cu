@@ -165,9 +165,19 @@ __device__ __forceinline__ void e2m1x8_to_bf16(uint32_t w, uint32_t scale2, uint
 // kFp8: E4M3 weights and E4M3 activations (kind::f8f6f4): the same tiles of
 // 128-byte rows, now 128 K elements per k-block; the epilogue multiplies each
 // accumulator element by its weight row's scale and its token row's scale.
-template <int kMode, bool kFp4, bool kPair, bool kWide = false, bool kFp8 = false>
+// kDec (NVFP4 at decode sizes, chunks of at most 64 routes): the MMAs are
+// tiny and the conversion of the weights sets the pace, so the same 19 warps
+// are split 4 epilogue warps (enough for 64 columns) and 12 converter warps in
+// three groups that take every third k-block.
+template <int kMode, bool kFp4, bool kPair, bool kWide = false, bool kFp8 = false, bool kDec = false>
 __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
     moe_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
+  static_assert(!kDec || kFp4, "the decode split of warps is for NVFP4");
+  constexpr int kEpi = kDec ? 4 : kEpilogueWarps;            // epilogue warps
+  constexpr int kConv = kDec ? 12 : kConvertWarps;           // converter warps (NVFP4)
+  constexpr int kGroups = kConv / 4;                         // converter groups, one k-block each
+  constexpr int kEpiHalves = kEpi / 4;                       // epilogue warps per TMEM lane quarter
+  static_assert(2 + kEpi + kConv == kMma2Warp, "NVFP4 warp layout");
   // Weight tiles per stage: gate/up always two (gate, up); down two on CTA
   // pairs (two 256-row halves of a 512-row unit sharing the token tile) and
   // for NVFP4 (two 128-row halves of a 256-row unit), so that every k-block
@@ -182,7 +192,7 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
   // Roles that read every scheduled unit index (they release ring slots).
   constexpr uint32_t kRingConsumers =
       kPair ? (1 + kEpilogueWarps) + (1 + kEpilogueWarps)  // even CTA: MMA + epilogue; odd: producer + epilogue
-            : 1 + kEpilogueWarps + (kFp4 ? kConvertWarps + 1 : 0);
+            : 1 + kEpi + (kFp4 ? kConv + 1 : 0);
   constexpr uint32_t kIssuers = kFp4 ? 2 : 1;  // MMA-issuing threads: commits per k-block / unit
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -218,10 +228,10 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kIssuers);
     }
-    for (int a = 0; a < kMaxAStages; ++a) mbar_init(&afull[a], kConvertWarps / 2);  // one converter group per k-block
+    for (int a = 0; a < kMaxAStages; ++a) mbar_init(&afull[a], kConv / kGroups);  // one converter group per k-block
     for (int a = 0; a < p.acc_stages; ++a) {
       mbar_init(&acc_full[a], kIssuers);
-      mbar_init(&acc_empty[a], kPair ? 2 * kEpilogueWarps : kEpilogueWarps);
+      mbar_init(&acc_empty[a], kPair ? 2 * kEpilogueWarps : kEpi);
     }
     mbar_init(drain, kIssuers);
     for (int r = 0; r < kSchedRing; ++r) {
@@ -481,7 +491,7 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
         mma_commit(drain);
       mbar_wait(drain, 0, p.timeout_ns, nullptr, p.status, kWhereDrain);
     }
-  } else if (warp < 2 + kEpilogueWarps) {
+  } else if (warp < 2 + kEpi) {
     // ------------------------------------------------------------ epilogue
     const int quad = warp & 3;               // TMEM lanes this warp may read
     const int half = (warp - 2) >> 2;        // which 16-column chunks (even / odd)
@@ -513,13 +523,13 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
         s1 = (kMode == 0 && p.gs1 != nullptr) ? __ldg(&p.gs1[U.e]) : 1.0f;
       }
       const int ncols = (U.n + 15) & ~15;
-      if (p.partial != nullptr) {
+      if (!kFp4 && !kPair && !kWide && p.partial != nullptr) {  // K split: 128-row units, BF16 / FP8
         // K split: FP32 partial sums (row scales applied, they are linear)
         // of this part, stored as they are read; the finishing kernel adds
         // the parts and applies SwiGLU / the BF16 rounding.
         const size_t plane = static_cast<size_t>(p.rows) * p.out_ld;
         float* part0 = p.partial + static_cast<size_t>(U.ks) * (kMode == 0 ? 2 : 1) * plane + feat;
-        for (int c0 = 16 * half; c0 < ncols; c0 += 32) {
+        for (int c0 = 16 * half; c0 < ncols; c0 += 16 * kEpiHalves) {
           float g[16], g2[16];
           tmem_ld16(tbase + static_cast<uint32_t>(c0), g);
           if (kNumA == 2) tmem_ld16(tbase + static_cast<uint32_t>(p.nmax + c0), g2);
@@ -553,11 +563,12 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
       // 1) TMEM -> packed BF16 results in registers (this warp's 16-column
       //    chunks), 2) release the accumulator so the next unit's MMAs start,
       //    3) global stores.
-      constexpr int kMaxChunks = (kFp4 ? kChunkRowsFp4 : kChunkRowsBf16) / 32;  // columns / (2 x 16)
+      // this warp's 16-column chunks: columns / (kEpiHalves x 16)
+      constexpr int kMaxChunks = (kDec ? 64 : (kFp4 ? kChunkRowsFp4 : kChunkRowsBf16)) / (16 * kEpiHalves);
       uint32_t hp[kOut][kMaxChunks][8];
 #pragma unroll
       for (int ci = 0; ci < kMaxChunks; ++ci) {
-        const int c0 = 16 * half + 32 * ci;
+        const int c0 = 16 * half + 16 * kEpiHalves * ci;
         if (c0 < ncols) {
           float g[16], g2[16];
           tmem_ld16(tbase + static_cast<uint32_t>(c0), g);
@@ -606,7 +617,7 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
       }
 #pragma unroll
       for (int ci = 0; ci < kMaxChunks; ++ci) {
-        const int c0 = 16 * half + 32 * ci;
+        const int c0 = 16 * half + 16 * kEpiHalves * ci;
         if (c0 < ncols) {
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
@@ -635,28 +646,28 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
     // units), warps 14-17 the odd ones, so two k-blocks are expanded at once;
     // a thread expands its row of every weight matrix of the unit (gate and
     // up, or down): 64 K elements = 32 TMEM columns each.
-    const int cw = warp - (2 + kEpilogueWarps);
+    const int cw = warp - (2 + kEpi);
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const int group = cw >> 2;
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
-    // This group's k-blocks i = group, group+2, ...: smem stage / phase of i,
-    // TMEM tile of i, and smem stage / phase of i - a_stages (the k-block that
-    // last read that tile; its empty barrier completing frees the tile).  The
-    // host keeps 2 <= a_stages <= stages.
+    // This group's k-blocks i = group, group+G, ... (G = kGroups): smem stage
+    // / phase of i, TMEM tile of i, and smem stage / phase of i - a_stages (the
+    // k-block that last read that tile; its empty barrier completing frees the
+    // tile).  The host keeps G <= a_stages <= stages.
     int stage = group, astage = group;
     uint32_t phase = 0;
     int rstage = group - p.a_stages + p.stages;
     uint32_t rphase = 1;
     int i = group;
-    uint32_t parity = 0;                // k-blocks seen so far, modulo 2
+    int turn = 0;                       // k-blocks seen so far, modulo G
     bool ok = true;
     while (ok) {
       int u;
       if (!warp_take(u) || u < 0) break;
       for (int kb = 0; kb < p.k_blocks; ++kb) {
-        const bool mine = parity == static_cast<uint32_t>(group);
-        parity ^= 1u;
+        const bool mine = turn == group;
+        if (++turn == kGroups) turn = 0;
         if (!mine) continue;
         int good = 1;
         if (lane == 0)
@@ -697,16 +708,16 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&afull[astage]);
-        if ((stage += 2) >= p.stages) {
+        if ((stage += kGroups) >= p.stages) {
           stage -= p.stages;
           phase ^= 1u;
         }
-        if ((astage += 2) >= p.a_stages) astage -= p.a_stages;
-        if ((rstage += 2) >= p.stages) {
+        if ((astage += kGroups) >= p.a_stages) astage -= p.a_stages;
+        if ((rstage += kGroups) >= p.stages) {
           rstage -= p.stages;
           rphase ^= 1u;
         }
-        i += 2;
+        i += kGroups;
       }
     }
   }
@@ -725,9 +736,9 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
   }
 }
 
-template <int kMode, bool kFp4, bool kPair, bool kWide = false, bool kFp8 = false>
+template <int kMode, bool kFp4, bool kPair, bool kWide = false, bool kFp8 = false, bool kDec = false>
 cudaError_t launch_one(const GemmMaps& maps, const GemmParams& p, int grid, size_t smem_bytes, cudaStream_t stream) {
-  auto kern = moe_gemm_kernel<kMode, kFp4, kPair, kWide, kFp8>;
+  auto kern = moe_gemm_kernel<kMode, kFp4, kPair, kWide, kFp8, kDec>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_bytes));
   if (err != cudaSuccess) return err;
   if (!kPair) {
@@ -783,8 +794,13 @@ int gemm_pair_max_clusters(int mode, size_t smem_bytes) {
   return n;
 }
 
-cudaError_t launch_gemm(int mode, bool fp4, bool pair, bool wide, bool fp8, const GemmMaps& maps, const GemmParams& p,
-                        int grid, size_t smem_bytes, cudaStream_t stream) {
+cudaError_t launch_gemm(int mode, bool fp4, bool pair, bool wide, bool fp8, bool dec, const GemmMaps& maps,
+                        const GemmParams& p, int grid, size_t smem_bytes, cudaStream_t stream) {
+  if (dec) {
+    if (!fp4 || pair || fp8) return cudaErrorInvalidValue;
+    return mode == 0 ? launch_one<0, true, false, false, false, true>(maps, p, grid, smem_bytes, stream)
+                     : launch_one<1, true, false, false, false, true>(maps, p, grid, smem_bytes, stream);
+  }
   if (fp8) {
     if (fp4) return cudaErrorInvalidValue;
     if (pair)

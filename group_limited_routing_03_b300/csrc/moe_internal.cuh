@@ -138,9 +138,11 @@ cudaError_t launch_gather_q8(const void* x, bool x_bf16, int H, const int32_t* p
 // scales hs [R_pad], the same rule.
 cudaError_t launch_quantize_rows(const __nv_bfloat16* h, int R, int I, uint8_t* hq, float* hs, cudaStream_t stream);
 // wide: BF16 / FP8 down on one CTA per unit with 256-row units (two tiles per
-// k-block); fp8: E4M3 weights and activations (kind::f8f6f4)
-cudaError_t launch_gemm(int mode, bool fp4, bool pair, bool wide, bool fp8, const GemmMaps& maps, const GemmParams& p,
-                        int grid, size_t smem_bytes, cudaStream_t stream);
+// k-block); fp8: E4M3 weights and activations (kind::f8f6f4); dec: NVFP4 with
+// chunks of at most 64 routes (4 epilogue warps, 12 converter warps)
+cudaError_t launch_gemm(int mode, bool fp4, bool pair, bool wide, bool fp8, bool dec, const GemmMaps& maps,
+                        const GemmParams& p, int grid, size_t smem_bytes, cudaStream_t stream);
+constexpr int kDecChunkRows = 64;  // NVFP4 decode variant: routes per unit at most
 size_t gemm_smem_bytes(int stages, int acc_stages, size_t stage_bytes);
 // Clusters of two CTAs of the pair kernel that can be resident at once (0: none).
 int gemm_pair_max_clusters(int mode, size_t smem_bytes);

@@ -101,3 +101,16 @@ def test_dense_kernel_count():
     assert moe.dense_kernel_count(moe.dense_shape(64, 5120, 20480), "fp8") == 7
     assert moe.dense_kernel_count(moe.dense_shape(8192, 5120, 20480), "bf16") == 3
     assert moe.dense_kernel_count(moe.dense_shape(64, 5120, 20480), "nvfp4") == 3
+
+
+def test_dense_fp8_with_fp32_x():
+    """FP8 weights take FP32 x too (its first step re-encodes x as E4M3)."""
+    wl = inputs.workload("tiny", T=70, H=512, I=768, x_dtype="f32", w_dtype="fp8", seed=31, E=1)
+    dg = inputs.generate(wl, DEV)
+    mlp = moe.DenseMLP(_weights(dg), max_tokens=wl.T)
+    y = torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device=DEV)
+    moe.beam_dense_mlp_forward(moe.dense_shape(wl.T, wl.H, wl.I), dg["x"], mlp.weights, y, mlp.workspace)
+    code, where = moe.beam_moe_read_device_status(mlp.workspace)
+    assert code == 0, f"device status {code} where {where}"
+    err = rel_err(y.cpu().double().numpy(), _oracle(dg, np.arange(wl.T)))
+    assert err <= Y_TOL["fp8"], err

@@ -121,3 +121,21 @@ def test_fp8_full_size(name, n_sample):
     del dg, y, ws
     gc.collect()
     torch.cuda.empty_cache()
+
+
+def test_fp8_stages_equal_forward():
+    """The FP8 forward issued stage by stage (the h quantisation inside the
+    down stage) gives the bits of beam_moe_forward."""
+    wl = inputs.workload("tiny", T=150, H=512, I=256, x_dtype="bf16", w_dtype="fp8", seed=8)
+    dg = inputs.generate(wl, DEV)
+    sh = moe.shape(wl.T, wl.H, wl.I)
+    weights = _weights(dg, "tiled", sh)
+    y, ids, w, _ = _forward(wl, dg, weights)
+    ws = moe.alloc_workspace(sh, "fp8")
+    y2 = torch.empty_like(y)
+    ids2, w2 = torch.empty_like(ids), torch.empty_like(w)
+    call = moe.ForwardCall(sh, dg["x"], dg["router_w"], None, weights, y2, ids2, w2, ws)
+    for i in range(len(moe.STAGES)):
+        call.stage(i)
+    torch.cuda.synchronize()
+    assert torch.equal(ids2, ids) and torch.equal(w2, w) and torch.equal(y2, y)

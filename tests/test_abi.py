@@ -264,3 +264,31 @@ def test_dense_mlp_argument_errors(lib):
     assert call(0x10000, moe.BEAM_BF16, 0x20000, 0x100080, n) == moe.BEAM_ERR_WORKSPACE  # not 256-byte aligned
     assert lib.beam_dense_mlp_forward(None, 0x10000, moe.BEAM_BF16, ctypes.byref(ew), 0x20000, 0x100000, n,
                                       None) == moe.BEAM_ERR_INVALID_ARG
+
+
+def test_pack_weights_fp8_row_scales_must_be_shared(lib):
+    sh = _shape(T=16, H=256, I=256)
+    src = moe._ExpertWeights()
+    src.dtype = moe.BEAM_FP8
+    src.gate, src.up, src.down = 0x100000, 0x2000000, 0x4000000
+    src.gate_rs, src.up_rs, src.down_rs = 0x7000000, 0x7100000, 0x7200000
+    dst = moe._ExpertWeights()
+    dst.dtype = moe.BEAM_FP8
+    dst.gate, dst.up, dst.down = 0x10000000, 0x12000000, 0x14000000
+    dst.gate_rs, dst.up_rs, dst.down_rs = 0x7000000, 0x7100000, 0x7300000  # down_rs differs
+    assert lib.beam_moe_pack_weights(ctypes.byref(sh), ctypes.byref(src), ctypes.byref(dst), None) == \
+        moe.BEAM_ERR_INVALID_ARG
+    dsh = moe.dense_shape(16, 256, 256)
+    assert lib.beam_dense_pack_weights(None, ctypes.byref(src), ctypes.byref(dst), None) == moe.BEAM_ERR_INVALID_ARG
+    assert lib.beam_dense_pack_weights(ctypes.byref(dsh), ctypes.byref(src), ctypes.byref(dst), None) == \
+        moe.BEAM_ERR_INVALID_ARG
+
+
+def test_dense_workspace_grows_with_k_split_planes(lib):
+    """At decode sizes the dense workspace holds the K-split partial planes
+    (parts x planes x T x N FP32); at prefill sizes none are needed."""
+    small = moe.dense_workspace_size(moe.dense_shape(64, 5120, 20480))
+    h_and_codes = 64 * 20480 * 2 + 64 * 5120 + 64 * 20480
+    assert small > h_and_codes + 4 * 2 * 64 * 20480 * 4  # four gate/up parts, two planes
+    big = moe.dense_workspace_size(moe.dense_shape(8192, 5120, 20480))
+    assert big < 8192 * 20480 * 2 + 8192 * 5120 + 8192 * 20480 + (1 << 20)

@@ -139,3 +139,37 @@ def test_fp8_stages_equal_forward():
         call.stage(i)
     torch.cuda.synchronize()
     assert torch.equal(ids2, ids) and torch.equal(w2, w) and torch.equal(y2, y)
+
+
+def test_fp8_maximum_token_count():
+    """T = 2^20 (8M routes) at H = I = 128: routing and y of sampled tokens
+    against the oracle, and the x codes of sampled route rows byte for byte."""
+    T = 1 << 20
+    wl = inputs.workload("fp8", T=T, H=128, I=128, seed=92)
+    torch.cuda.empty_cache()
+    dg = inputs.generate(wl, DEV)
+    sh = moe.shape(wl.T, wl.H, wl.I)
+    y, ids, w, ws = _forward(wl, dg, _weights(dg, "tiled", sh))
+    rng = np.random.default_rng(92)
+    tok = np.unique(np.concatenate([[0, T - 1], rng.integers(0, T, 2000)]))
+    x_h = host_act(dg["x"])
+    ref = oracle.route(x_h[tok], dg["router_w"].cpu().numpy(), None, want_scores=True)
+    safe = compare_routing(ids.cpu().numpy()[tok], w.cpu().numpy()[tok], ref)
+    few = tok[safe][:24]
+    y_ref = oracle_y(dg, few, ref["ids"][safe][:24], ref["weights"][safe][:24])
+    err = rel_err(y.cpu()[few].double().numpy(), y_ref)
+    assert err <= Y_TOL["fp8"], err
+    # x codes of sampled route rows (perm order in the workspace)
+    lay = moe.workspace_layout(sh, "fp8")
+    R = T * 8
+    rows = np.unique(np.concatenate([[0, R - 1], rng.integers(0, R, 3000)]))
+    perm = ws[lay["perm"]:lay["perm"] + 4 * R].view(torch.int32)[torch.as_tensor(rows, device=DEV)].cpu().numpy()
+    xq = ws[lay["xq"]:lay["xq"] + R * wl.H].view(R, wl.H)[torch.as_tensor(rows, device=DEV)].cpu().numpy()
+    xs = ws[lay["xs"]:lay["xs"] + 4 * R].view(torch.float32)[torch.as_tensor(rows, device=DEV)].cpu().numpy()
+    rows32 = (x_h[perm // 8].astype(np.uint32) << 16).view(np.float32)
+    codes, scales = oracle.quantize_e4m3_rows(rows32)
+    np.testing.assert_array_equal(xq, codes)
+    np.testing.assert_array_equal(xs, scales)
+    del dg, y, ws
+    gc.collect()
+    torch.cuda.empty_cache()

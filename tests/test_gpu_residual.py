@@ -160,3 +160,28 @@ def test_residual_full_size(name, k, n_sample):
     del dg, out, stream
     gc.collect()
     torch.cuda.empty_cache()
+
+
+def test_residual_maximum_token_count():
+    """T = 2^20 at H = I = 128 (one CTA per row): the new stream of sampled
+    tokens against the oracle."""
+    T = 1 << 20
+    wl = inputs.workload("prefill", T=T, H=128, I=128, seed=93)
+    torch.cuda.empty_cache()
+    dg = inputs.generate(wl, DEV)
+    stream, g = inputs.residual_inputs(wl, DEV)
+    out, _, ids, w = _run(wl, dg, dg, stream, g, 105, want_y=False)
+    rng = np.random.default_rng(93)
+    tok = np.unique(np.concatenate([[0, T - 1], rng.integers(0, T, 2000)]))
+    x_h = host_act(dg["x"])
+    ref = oracle.route(x_h[tok], dg["router_w"].cpu().numpy(), None, want_scores=True)
+    safe = compare_routing(ids.cpu().numpy()[tok], w.cpu().numpy()[tok], ref)
+    few = tok[safe][:24]
+    y_ref = oracle_y(dg, few, ref["ids"][safe][:24], ref["weights"][safe][:24])
+    idx = torch.as_tensor(few, device=DEV)
+    out_ref = oracle.residual_update(y_ref, host_act(stream[idx]), g.cpu().numpy(), EPS, 105)
+    err = rel_err(out[idx].cpu().double().numpy(), out_ref)
+    assert err <= _tol(wl.x_dtype, wl.w_dtype), err
+    del dg, out, stream
+    gc.collect()
+    torch.cuda.empty_cache()

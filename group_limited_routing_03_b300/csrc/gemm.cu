@@ -3,9 +3,11 @@
 //
 // Beam launch post, section "Mixture of Experts": every expert is a SwiGLU MLP
 // (hidden 5120, intermediate 2560); section "Residual Stream": the SwiGLU
-// product is computed in FP32.  The same post names NVFP4 as the Blackwell
-// checkpoint format (4-bit weights); here those weights are expanded to BF16
-// in shared memory and multiplied with BF16 activations (W4A16).
+// product is computed in FP32.  The same post names three checkpoint formats:
+// BF16; NVFP4 for Blackwell (4-bit weights), here expanded to BF16 in TMEM
+// and multiplied with BF16 activations (W4A16); and FP8, here E4M3 weights
+// with per-row scales multiplied with per-row-quantised E4M3 activations on
+// kind::f8f6f4 MMAs.
 //
 //   mode 0 (gate/up):  h[r, i]  = silu(x_r . Wg[e,i,:]) * (x_r . Wu[e,i,:])
 //   mode 1 (down):     yr[r, j] = h_r . Wd[e,j,:]
@@ -15,37 +17,44 @@
 // routed tokens are its N side ("swap AB"): an expert sees 1..3 tokens at
 // decode and ~256 at prefill, and N can be any multiple of 16 up to 256,
 // while M is 128 per CTA.  A work unit is (expert, token chunk of <= nmax
-// routes, weight row tile): 128 rows, or on CTA pairs 256 (gate/up) / 512
-// (down) rows, and 256 rows for NVFP4 down; each k-block issues its MMAs into
-// two accumulators (gate and up, or two row halves).  Units are numbered in
-// the order (expert, chunk, row tile) and taken from a global counter in that
+// routes, weight row tile[, part of the K range]): 128 rows, or on CTA pairs
+// 256 (gate/up) / 512 (down) rows, and 256 rows for two-tile down units; each
+// k-block issues its MMAs into two accumulators (gate and up, or two row
+// halves) where the unit has two tiles.  Units are numbered in the order
+// (expert, chunk, row tile, K part) and taken from a global counter in that
 // order by a persistent grid (one CTA, or CTA pair, per SM), so CTAs running
 // side by side share the token chunk (and, for several chunks of one expert,
-// the weight tiles) through L2.
+// the weight tiles) through L2.  A K range split into parts (few units for
+// many SMs) leaves FP32 partial sums that splitk.cu adds up.
 //
-// Warp roles:
-//   warp 0       TMA producer: weight tile(s) 128x64 and the chunk's token
-//                rows x 64 (one box of the tile's height, or 32-row boxes for
-//                a small chunk) per stage, 128-byte swizzle (NVFP4: the
-//                packed 128x32-byte tiles and their E4M3 scales);
-//   warp 1       TMEM allocator and MMA issuer (one thread):
-//                tcgen05.mma kind::f16, M=128, N=round_up(n,16), K=16 steps;
-//   warps 2-9    epilogue: tcgen05.ld of the accumulators (warp w reads TMEM
-//                lanes 32*(w%4)..+31; warps 2-5 take the even 16-column
-//                chunks, warps 6-9 the odd ones), NVFP4 global scale, SwiGLU
-//                in FP32 (mode 0), BF16 stores;
-//   warps 10-17  (NVFP4 only) converters: packed E2M1 x E4M3 -> BF16 weight
-//                tile, written straight into TMEM (tcgen05.st; the thread of
-//                TMEM lane m expands weight row m), where the MMA reads its A
-//                operand.  Shared memory then carries only the packed bytes
-//                and the activations, and its bandwidth stays with the MMA's
-//                B operand.
+// Warp roles (BF16 / FP8: 10 warps; NVFP4: 19 warps):
+//   warp 0       TMA producer: weight tile(s) of 128 rows x 128 bytes and the
+//                chunk's token rows x 128 bytes (one box of the tile's
+//                height, or 32-row boxes for a small chunk) per stage,
+//                128-byte swizzle (NVFP4: the packed 128x32-byte tiles and
+//                their E4M3 scales);
+//   warp 1       TMEM allocator and MMA issuer (one thread): tcgen05.mma
+//                kind::f16 (BF16, K=16 steps) or kind::f8f6f4 (E4M3, K=32
+//                steps), M=128 (256 on pairs), N=round_up(n,16);
+//   warps 2..    epilogue (8 warps; 4 in the NVFP4 decode variant):
+//                tcgen05.ld of the accumulators (warp w reads TMEM lanes
+//                32*(w%4)..+31 and every (warps/4)-th 16-column chunk),
+//                NVFP4 global scale or FP8 row x token-row scales, SwiGLU in
+//                FP32 (mode 0), BF16 stores (K parts: FP32 partial stores);
+//   then         (NVFP4 only) converters, 8 warps in two groups (12 in three
+//                groups in the decode variant) taking alternate k-blocks:
+//                packed E2M1 x E4M3 -> BF16 weight tile, written straight
+//                into TMEM (tcgen05.st; the thread of TMEM lane m expands
+//                weight row m), where the MMA reads its A operand.  Shared
+//                memory then carries only the packed bytes and the
+//                activations, and its bandwidth stays with the MMA's B operand;
+//   last         (NVFP4 only) a second MMA issuer for the second tile.
 // Shared-memory stages are recycled through full/empty mbarriers, TMEM
 // accumulator buffers through acc_full/acc_empty.  NVFP4: the converters wait
 // for the TMA bytes of a stage before expanding its weights, and the MMA
-// thread waits only for the converters (afull), whose arrival follows their
+// threads wait only for the converters (afull), whose arrival follows their
 // observation of the TMA completion; a TMEM weight tile is reused once the
-// empty barrier of the k-block that last read it has completed, so the single
+// empty barrier of the k-block that last read it has completed, so each
 // MMA-issuing thread waits once and commits once per k-block.  Every wait is
 // bounded; waits after the first poll let the thread sleep (see mbar_wait).
 #include <cuda.h>

@@ -1,7 +1,10 @@
 // api.cu -- the C ABI declared in include/beam_moe.h: argument validation,
 // workspace carve-up, TMA descriptors and the launch sequence
-//   router -> [tile histogram] -> scan -> scatter -> gather -> gate/up GEMM
-//   -> down GEMM -> combine
+//   router -> [tile histogram] -> scan -> scatter -> gather (FP8 weights: E4M3
+//   codes of x) -> gate/up GEMM -> [FP8: E4M3 codes of h] -> down GEMM ->
+//   combine (or the combine fused with the post-norm residual update)
+// and, for the dense MLP, schedule -> [FP8: codes of x] -> gate/up GEMM
+// [-> K-split finish] -> [FP8: codes of h] -> down GEMM [-> K-split finish],
 // all on the caller's stream, with no host synchronisation and no allocation.
 #include <cuda.h>
 #include <cuda_runtime.h>

@@ -18,7 +18,7 @@ constexpr int kRouterTile = 32;    // tokens per router CTA (= one dispatch tile
 constexpr int kRouterKChunk = 32;  // hidden elements per router k-step
 constexpr int kTileRoutes = kRouterTile * kTopK;  // routes per dispatch tile (256)
 constexpr int kBlockM = 128;       // weight rows per MMA tile (TMEM lanes)
-constexpr int kBlockK = 64;        // K elements per pipeline stage (128 bytes of bf16)
+constexpr int kBlockK = 64;        // K elements per pipeline stage (128 bytes of bf16; FP8 stages hold 128)
 constexpr int kBoxRows = 32;       // token rows per TMA box of the activation operand
 constexpr int kMaxSmsForSizing = 256;  // bound on the SM count used to size the workspace
 constexpr uint32_t kPackedTileBytes = kBlockM * kBlockK / 2;  // NVFP4: 128 rows x 32 bytes

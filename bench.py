@@ -223,6 +223,34 @@ def measure(wl, steps, warmup, dev, world, sampler_index, state=None, residual_s
     return out, state
 
 
+def measure_graph(wl, state, steps, warmup):
+    """The same step recorded once in a CUDA graph (GraphedForward) and
+    replayed: x copied into the graph's input, then one graph launch."""
+    import group_limited_routing_03_b300 as moe
+
+    d, sh, ws, y, ids, w, call = state
+    layer = moe.BeamMoE(d["router_w"], d.get("bias"), call.weights, max_tokens=wl.T)
+    graphed = moe.GraphedForward(layer, wl.T, dtype=d["x"].dtype)
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        graphed(d["x"])
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        graphed(d["x"])
+    e1.record(stream)
+    torch.cuda.synchronize()
+    code, where = moe.beam_moe_read_device_status(layer.workspace)
+    if code != 0:
+        raise RuntimeError(f"device status {code} at {where} in the graph replays")
+    ms = e0.elapsed_time(e1) / steps
+    out = dict(value=wl.T / (ms * 1e-3), unit="tokens/s", ms_per_step=round(ms, 4), steps=steps,
+               note="one CUDA-graph replay per step (the library's launches recorded once), x copied in first")
+    del graphed, layer
+    return out
+
+
 def measure_dense(wl, steps, warmup, dev, pk):
     """The dense SwiGLU MLP (one expert taking every row) through
     beam_dense_mlp_forward, device-timed per call; weights in the tiled layout."""
@@ -566,6 +594,10 @@ def main():
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = oracle_sample(wl, state[0])
+    try:
+        graph = measure_graph(wl, state, args.steps, args.warmup)
+    except Exception as e:  # an auxiliary number: record why it is missing
+        graph = {"unavailable": f"{type(e).__name__}: {e}"[:300]}
     residual = None
     if not args.no_residual:
         rm, _ = measure(wl, args.steps, args.warmup, dev, world, torch.cuda.current_device(), state=state,
@@ -628,7 +660,7 @@ def main():
                          f"({m['touched']} x {weight_bytes_per_expert(wl) / 1e6:.1f} MB), far larger than L2"},
         "roofline": hbm, "roofline_tensor": tc, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": m["launches_per_step"] * args.steps, "clocks": m["clocks"],
-        "step": sn, "residual_epilogue": residual, "prefill": prefill, "weight_formats": fp8, "dense": dense,
+        "step": sn, "graph": graph, "residual_epilogue": residual, "prefill": prefill, "weight_formats": fp8, "dense": dense,
     }
     print(json.dumps(line), flush=True)
 

@@ -359,6 +359,42 @@ def beam_moe_debug_timeout(workspace, timeout_us: int, stream=None):
            "beam_moe_debug_timeout")
 
 
+class GraphedForward:
+    """One forward of ``layer`` for a fixed token count, recorded once in a
+    CUDA graph and replayed with one launch (a decode serving loop): the
+    library's kernel launches, its tensor-map arguments and the workspace
+    addresses are fixed at capture; each call copies x into the graph's
+    static input and replays.  Shares ``layer.workspace``: do not run the
+    layer and the graph at the same time."""
+
+    def __init__(self, layer, T: int, dtype=torch.bfloat16):
+        if T > layer.max_tokens:
+            raise ValueError(f"{T} tokens > workspace capacity {layer.max_tokens}")
+        dev = layer.router_w.device
+        self.x = torch.zeros((T, layer.H), dtype=dtype, device=dev)
+        self.y = torch.empty_like(self.x)
+        self.ids = torch.empty((T, 8), dtype=torch.int32, device=dev)
+        self.w = torch.empty((T, 8), dtype=torch.float32, device=dev)
+        sh = layer.shape(T)
+        args = (sh, self.x, layer.router_w, layer.router_bias, layer.weights, self.y, self.ids, self.w,
+                layer.workspace)
+        side = torch.cuda.Stream(device=dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):  # warm-up outside the capture (kernel attributes, driver entry points)
+            ForwardCall(*args, stream=side).run()
+        torch.cuda.current_stream(dev).wait_stream(side)
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            self._call = ForwardCall(*args, stream=torch.cuda.current_stream(dev))
+            self._call.run()
+        self.workspace = layer.workspace
+
+    def __call__(self, x):
+        self.x.copy_(x)
+        self.graph.replay()
+        return self.y, self.ids, self.w
+
+
 # --------------------------------------------------------------------------
 # dense SwiGLU MLP (the first layers of the model)
 # --------------------------------------------------------------------------

@@ -9,6 +9,11 @@ The block (Beam launch post, "Willkommen Beam ..." (spke.com), section
 "Mixture of Experts"): sigmoid router over 256 experts, 8 groups of 32 ranked
 by the sum of their two best scores, best 4 groups kept, top-8 experts inside
 them, weights normalised and scaled by 2.5, SwiGLU experts, no shared expert.
+Expert weights in BF16, NVFP4 (W4A16) or FP8 (E4M3 with row scales, E4M3
+activations); the block may be followed by the post-norm residual update of
+section "Residual Stream" (``beam_moe_forward_residual``); the first layers'
+dense SwiGLU MLP runs on the same GEMMs (``DenseMLP``); a decode-size forward
+can be recorded in a CUDA graph (``GraphedForward``).
 """
 from __future__ import annotations
 
@@ -23,7 +28,10 @@ __all__ = [
     "ForwardCall", "STAGES", "beam_moe_stage_kernel_count", "beam_moe_route_noalloc", "pack_weights",
     "BEAM_LAYOUT_ROWS", "BEAM_LAYOUT_TILED",
     "beam_moe_read_device_status", "beam_moe_debug_timeout", "beam_status_string", "BeamMoE",
-    "library_path", "load",
+    "library_path", "load", "BEAM_F32", "BEAM_BF16", "BEAM_NVFP4", "BEAM_FP8",
+    "beam_moe_forward_residual", "GraphedForward",
+    "DenseShape", "dense_shape", "dense_workspace_size", "dense_kernel_count", "beam_dense_mlp_forward",
+    "dense_pack_weights", "DenseMLP",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))

@@ -292,3 +292,37 @@ def test_dense_workspace_grows_with_k_split_planes(lib):
     assert small > h_and_codes + 4 * 2 * 64 * 20480 * 4  # four gate/up parts, two planes
     big = moe.dense_workspace_size(moe.dense_shape(8192, 5120, 20480))
     assert big < 8192 * 20480 * 2 + 8192 * 5120 + 8192 * 20480 + (1 << 20)
+
+
+def test_plain_c_program_uses_the_boundary(lib, tmp_path):
+    """The header is C99 and the library is usable from a C program with no
+    Python or torch: workspace sizing and argument errors, no GPU needed."""
+    import shutil
+    import subprocess
+
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "use_boundary.c"
+    src.write_text(r'''
+#include <stdio.h>
+#include "beam_moe.h"
+int main(void) {
+  beam_moe_shape_t s = {64, 5120, 2560, 256, 8, 4, 8, 2.5f};
+  size_t n = beam_moe_workspace_size(&s, BEAM_BF16);
+  size_t n8 = beam_moe_workspace_size(&s, BEAM_FP8);
+  beam_dense_shape_t d = {64, 5120, 20480};
+  size_t nd = beam_dense_workspace_size(&d, BEAM_BF16);
+  beam_moe_shape_t bad = s;
+  bad.E = 128;
+  int rc = beam_moe_route(&bad, 0, BEAM_BF16, 0, 0, 0, 0, 0, 0, 0);
+  printf("%zu %zu %zu %d %s\n", n, n8, nd, rc, beam_status_string((beam_status_t)rc));
+  return (n == 0 || n8 != n || nd == 0 || rc != BEAM_ERR_UNSUPPORTED) ? 1 : 0;
+}
+''')
+    exe = tmp_path / "use_boundary"
+    libdir = os.path.dirname(moe.library_path())
+    subprocess.run([gcc, "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), str(src), "-L", libdir,
+                    "-lbeam_moe", "-Wl,-rpath," + libdir, "-o", str(exe)], check=True)
+    r = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stdout + r.stderr

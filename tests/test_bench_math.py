@@ -1,0 +1,70 @@
+"""The measurement arithmetic of bench.py (no GPU): algorithmic bytes and
+FLOPs per launch, the peaks they are divided by, and the committed traffic
+record lookup."""
+import pytest
+
+import bench
+from group_limited_routing_03_b300 import inputs
+
+PK = dict(hbm=6500.0, bf16=1800.0, bf16_sustained=1400.0, source="test")
+
+
+def _m(ms_gate_up, touched):
+    st = [0.0] * len(bench.STAGES)
+    st[bench.STAGES.index("gate_up")] = ms_gate_up
+    return {"stage_ms": st, "touched": touched}
+
+
+def test_weight_bytes_per_expert():
+    wl = inputs.workload("decode")
+    assert bench.weight_bytes_per_expert(wl) == 3 * 5120 * 2560 * 2
+    assert bench.weight_bytes_per_expert(inputs.workload("fp8")) == 3 * 5120 * 2560 + 4 * (2 * 2560 + 5120)
+    nv = bench.weight_bytes_per_expert(inputs.workload("nvfp4"))
+    assert nv == 3 * 5120 * 2560 // 2 + 3 * 5120 * 2560 // 16 + 12
+
+
+def test_roofline_bf16_decode_bytes_and_fraction():
+    wl = inputs.workload("decode")
+    hbm, tc = bench.roofline(wl, _m(1.5, 222), PK)
+    R = 64 * 8
+    wbytes = 222 * 2 * 2560 * 5120 * 2
+    act = R * 5120 * 2 + R * 2560 * 2
+    assert hbm["algorithmic_bytes"] == wbytes + act
+    assert hbm["achieved"] == pytest.approx((wbytes + act) / 1.5e-3 / 1e9, rel=1e-3)
+    assert hbm["frac"] == pytest.approx(hbm["achieved"] / 6500.0, rel=1e-3)
+    assert tc["algorithmic_flops"] == 2.0 * R * 2 * 2560 * 5120
+    assert tc["peak"] == 1800.0 and tc["peak_sustained"] == 1400.0
+
+
+def test_roofline_fp8_uses_twice_the_bf16_peak_and_one_byte_weights():
+    wl = inputs.workload("fp8")
+    hbm, tc = bench.roofline(wl, _m(1.6, 256), PK)
+    R = 8192 * 8
+    wbytes = 256 * 2 * 2560 * 5120 + 256 * 2 * 2560 * 4
+    act = R * 5120 * 1 + R * 2560 * 2
+    assert hbm["algorithmic_bytes"] == wbytes + act
+    assert tc["peak"] == 3600.0 and tc["peak_sustained"] == 2800.0
+    assert tc["frac"] == pytest.approx(tc["achieved"] / 3600.0, rel=1e-3)
+
+
+def test_residual_numbers_bytes():
+    wl = inputs.workload("prefill")
+    st = [0.0] * len(bench.STAGES)
+    c = bench.STAGES.index("combine")
+    st[c] = 0.15
+    plain = {"stage_ms": list(st), "total_ms": 50.0}
+    res = {"stage_ms": list(st), "total_ms": 50.0, "clocks": {}}
+    out = bench.residual_numbers(wl, plain, res, 10, PK, 105)
+    T, H = 8192, 5120
+    assert out["roofline"]["algorithmic_bytes"] == T * 8 * H * 2 + 2 * T * H * 2 + H * 4 + T * 8 * 8
+    assert out["step_k"] == 105 and out["in_place"]
+
+
+def test_job_throughput_counts_every_rank():
+    assert bench.job_throughput(64, 50, 4, 100.0) == pytest.approx(64 * 50 * 4 / 0.1)
+
+
+def test_traffic_record_lookup():
+    assert bench.traffic_record("moe_gemm_gate_up", "no_such_workload") is None
+    v = bench.traffic_record("moe_gemm_gate_up", "decode")
+    assert v is None or v > 1e9  # bytes per launch, or None once the kernel source changed

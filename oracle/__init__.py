@@ -50,6 +50,15 @@ Parity status of each function (what pins it is in ``tests/test_oracle_*``):
 * ``expert_ffn_fp8`` pinned: numpy matmuls on values decoded and quantised by
                    torch (float8_e4m3fn), independent of the oracle's encoder,
                    with h rounded to BF16 by torch.
+* ``encode_e2m1``  pinned: brute-force nearest E2M1 magnitude with the
+                   even-code tie rule, the generator's independent storage
+                   encoder, saturation.
+* ``quantize_nvfp4_rows`` pinned: scales against torch's E4M3 cast of the
+                   FP32 block value, codes against a brute-force nearest
+                   search, zero rows, error bounds.
+* ``expert_ffn_w4a4`` pinned: numpy matmuls on weights decoded by the pinned
+                   decoders and activations from the pinned quantiser (the
+                   NVFP4-activation reading for a W4A4 path; no kernel yet).
 * ``round_bf16``   pinned: torch's float32 -> bfloat16 cast on float inputs
                    (every tie of a random sample), closed forms on doubles.
 """
@@ -95,6 +104,13 @@ def _load():
         lib.oracle_expert_ffn.restype = i32
         lib.oracle_expert_ffn_fp8.argtypes = [i64, i64, i64, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, i32]
         lib.oracle_expert_ffn_fp8.restype = i32
+        lib.oracle_encode_e2m1.argtypes = [ctypes.c_float]
+        lib.oracle_encode_e2m1.restype = ctypes.c_uint8
+        lib.oracle_quantize_nvfp4_row.argtypes = [vp, i64, vp, vp, vp]
+        lib.oracle_quantize_nvfp4_row.restype = None
+        lib.oracle_expert_ffn_w4a4.argtypes = [i64, i64, i64, vp, i32, vp, vp, vp, vp, vp, vp, dbl, dbl, dbl, vp, vp,
+                                               i32]
+        lib.oracle_expert_ffn_w4a4.restype = i32
         lib.oracle_round_bf16.argtypes = [dbl]
         lib.oracle_round_bf16.restype = ctypes.c_float
         lib.oracle_encode_e4m3.argtypes = [ctypes.c_float]
@@ -262,6 +278,50 @@ def quantize_e4m3_rows(a):
         row = a[r]
         lib.oracle_quantize_e4m3_row(_ptr(row), K, _ptr(codes[r]), scales[r:r + 1].ctypes.data_as(ctypes.c_void_p))
     return codes, scales
+
+
+def encode_e2m1(v) -> int:
+    """E2M1 code (4 bits) of one float32 value: nearest, ties to even, saturating at 6."""
+    return int(_load().oracle_encode_e2m1(float(np.float32(v))))
+
+
+def quantize_nvfp4_rows(a):
+    """Per-row NVFP4 quantisation of float32 rows a [n, K] (K % 16 == 0):
+    (codes uint8 [n, K] one E2M1 code per byte, scales uint8 [n, K/16] E4M3
+    bits, global float32 [n]) with global = amax / (6 * 448)."""
+    lib = _load()
+    a = np.ascontiguousarray(a, dtype=np.float32)
+    n, K = a.shape
+    assert K % 16 == 0
+    codes = np.zeros((n, K), np.uint8)
+    scales = np.zeros((n, K // 16), np.uint8)
+    glob = np.zeros(n, np.float32)
+    for r in range(n):
+        row = a[r]
+        lib.oracle_quantize_nvfp4_row(_ptr(row), K, _ptr(codes[r]), _ptr(scales[r]),
+                                      glob[r:r + 1].ctypes.data_as(ctypes.c_void_p))
+    return codes, scales, glob
+
+
+def expert_ffn_w4a4(x, wg, wu, wd, *, scales, global_scales, want_h=False, threads=None):
+    """One expert with NVFP4 weights (as expert_ffn) whose GEMM inputs are
+    quantised per row to NVFP4 (quantize_nvfp4_rows; h rounded to BF16
+    first).  Returns f64[n, H] (and h f64[n, I] before rounding)."""
+    lib = _load()
+    x, xd = _act(x)
+    n, H = x.shape
+    I = wg.shape[0]
+    assert wg.shape == (I, H // 2) and wu.shape == (I, H // 2) and wd.shape == (H, I // 2)
+    wg, wu, wd = (np.ascontiguousarray(m, dtype=np.uint8) for m in (wg, wu, wd))
+    sg, su, sd = (np.ascontiguousarray(m, dtype=np.uint8) for m in scales)
+    gg, gu, gd = (float(v) for v in global_scales)
+    out = np.zeros((n, H), np.float64)
+    h = np.zeros((n, I), np.float64) if want_h else None
+    rc = lib.oracle_expert_ffn_w4a4(H, I, n, _ptr(x), xd, _ptr(wg), _ptr(wu), _ptr(wd), _ptr(sg), _ptr(su),
+                                    _ptr(sd), gg, gu, gd, _ptr(out), _ptr(h), threads or default_threads())
+    if rc != 0:
+        raise ValueError(f"oracle_expert_ffn_w4a4 failed ({rc})")
+    return (out, h) if want_h else out
 
 
 def expert_ffn_fp8(x, wg, wu, wd, rg, ru, rd, *, want_h=False, threads=None):

@@ -161,6 +161,66 @@ float oracle_round_bf16(double v) {
   return (float)(v < 0 ? -r : r);
 }
 
+/* Float -> E2M1 code (layout at oracle_decode_e2m1): the nearest of the
+ * eight magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6, ties to the even code,
+ * magnitudes above 6 giving 6 (no infinity in the format); a search over the
+ * magnitudes in code order. */
+uint8_t oracle_encode_e2m1(float v) {
+  const uint8_t sign = signbit(v) ? 0x8 : 0x0;
+  const double a = fabs((double)v);
+  int best = 0;
+  double bd = INFINITY;
+  for (int c = 0; c < 8; ++c) {
+    const double d = fabs(a - oracle_decode_e2m1((uint8_t)c));
+    if (d < bd || (d == bd && c % 2 == 0)) {
+      best = c;
+      bd = d;
+    }
+  }
+  return sign | (uint8_t)best;
+}
+
+/* Per-row dynamic NVFP4 quantisation of a GEMM input row -- the reading used
+ * for NVFP4 activations (W4A4; the launch post names NVFP4 only as a weight
+ * format): the row's global scale g = amax / (6 * 448) in FP32 (1 when amax is
+ * 0), the same recipe as the weights' per-matrix scale but per row; each
+ * block of 16 consecutive elements the E4M3 scale s = E4M3((bmax / 6) / g)
+ * (FP32 divisions, nearest even, saturating at 448); each element the E2M1
+ * code of a / (s * g) (FP32 product and division; code 0 when s is 0).  The
+ * element stands for e2m1 * s * g.  codes: one code per byte, [K]. */
+void oracle_quantize_nvfp4_row(const float* a, int64_t K, uint8_t* codes, uint8_t* scales, float* global) {
+  float amax = 0.0f;
+  for (int64_t j = 0; j < K; ++j) {
+    const float m = fabsf(a[j]);
+    if (m > amax) amax = m;
+  }
+  volatile float g = amax / (6.0f * 448.0f);
+  float gf = g;
+  if (gf == 0.0f) gf = 1.0f;
+  for (int64_t b = 0; b < K / 16; ++b) {
+    float bmax = 0.0f;
+    for (int j = 0; j < 16; ++j) {
+      const float m = fabsf(a[b * 16 + j]);
+      if (m > bmax) bmax = m;
+    }
+    volatile float t = bmax / 6.0f;
+    volatile float q = t / gf;
+    const uint8_t sc = oracle_encode_e4m3(q);
+    scales[b] = sc;
+    volatile float sv = (float)oracle_decode_e4m3(sc);
+    volatile float d = sv * gf;
+    for (int j = 0; j < 16; ++j) {
+      if (sv == 0.0f || d == 0.0f) {
+        codes[b * 16 + j] = 0;
+        continue;
+      }
+      volatile float e = a[b * 16 + j] / d;
+      codes[b * 16 + j] = oracle_encode_e2m1(e);
+    }
+  }
+  *global = gf;
+}
+
 /* One element [row, k] of a weight matrix with `cols` columns (K). */
 typedef struct {
   int dtype;            /* ORACLE_F32 / ORACLE_BF16 / ORACLE_NVFP4 / ORACLE_FP8 */
@@ -499,6 +559,71 @@ int oracle_expert_ffn_fp8(int64_t H, int64_t I, int64_t n, const void* x, int x_
 done:
   free(rowf);
   free(codes);
+  free(xq);
+  free(hq);
+  if (!h_out) free(h);
+  return rc;
+}
+
+/*
+ * oracle_expert_ffn_w4a4: one expert with NVFP4 weights (layout as in
+ * oracle_expert_ffn) whose GEMM inputs are quantised per row to NVFP4 at run
+ * time (oracle_quantize_nvfp4_row): x as given before gate/up, h rounded to
+ * BF16 before down.  Values are decoded exactly and summed in double in
+ * index order.  h_out (nullable) receives h before rounding.
+ */
+int oracle_expert_ffn_w4a4(int64_t H, int64_t I, int64_t n, const void* x, int x_dtype, const uint8_t* wg,
+                           const uint8_t* wu, const uint8_t* wd, const uint8_t* sg, const uint8_t* su,
+                           const uint8_t* sd, double gg, double gu, double gd, double* out, double* h_out,
+                           int nthreads) {
+  if (H <= 0 || I <= 0 || n < 0 || H % 16 != 0 || I % 16 != 0 || !sg || !su || !sd) return -1;
+  const int64_t nn = n > 0 ? n : 1, KM = H > I ? H : I;
+  float* rowf = (float*)malloc(sizeof(float) * (size_t)KM);
+  uint8_t* codes = (uint8_t*)malloc((size_t)KM);
+  uint8_t* scales = (uint8_t*)malloc((size_t)(KM / 16));
+  double* xq = (double*)malloc(sizeof(double) * (size_t)(nn * H));
+  double* hq = (double*)malloc(sizeof(double) * (size_t)(nn * I));
+  double* h = h_out ? h_out : (double*)malloc(sizeof(double) * (size_t)(nn * I));
+  int rc = 0;
+  if (!rowf || !codes || !scales || !xq || !hq || !h) {
+    rc = -2;
+    goto done;
+  }
+  for (int64_t r = 0; r < n; ++r) {
+    float g;
+    for (int64_t j = 0; j < H; ++j) rowf[j] = (float)act_elem(x, x_dtype, r * H + j);
+    oracle_quantize_nvfp4_row(rowf, H, codes, scales, &g);
+    for (int64_t j = 0; j < H; ++j)
+      xq[r * H + j] = oracle_decode_e2m1(codes[j]) * oracle_decode_e4m3(scales[j / 16]) * (double)g;
+  }
+  {
+    ffn_args_t a;
+    a.H = H;
+    a.I = I;
+    a.n = n;
+    a.x = NULL;
+    a.x_dtype = -1;
+    a.wg = (oracle_matrix_t){ORACLE_NVFP4, wg, sg, gg, H, NULL};
+    a.wu = (oracle_matrix_t){ORACLE_NVFP4, wu, su, gu, H, NULL};
+    a.wd = (oracle_matrix_t){ORACLE_NVFP4, wd, sd, gd, I, NULL};
+    a.h = h;
+    a.out = out;
+    a.xq = xq;
+    parallel_for(n * I, nthreads, ffn_hidden, &a);
+    for (int64_t r = 0; r < n; ++r) {
+      float g;
+      for (int64_t i = 0; i < I; ++i) rowf[i] = oracle_round_bf16(h[r * I + i]);
+      oracle_quantize_nvfp4_row(rowf, I, codes, scales, &g);
+      for (int64_t i = 0; i < I; ++i)
+        hq[r * I + i] = oracle_decode_e2m1(codes[i]) * oracle_decode_e4m3(scales[i / 16]) * (double)g;
+    }
+    a.h = hq;
+    parallel_for(n * H, nthreads, ffn_down, &a);
+  }
+done:
+  free(rowf);
+  free(codes);
+  free(scales);
   free(xq);
   free(hq);
   if (!h_out) free(h);

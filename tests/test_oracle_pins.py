@@ -531,3 +531,97 @@ def test_round_bf16():
     assert oracle.round_bf16(m + 2.0 ** -40) == 1.0 + 2.0 ** -7  # above the midpoint (FP32 would round it to m)
     assert oracle.round_bf16(-(m + 2.0 ** -40)) == -(1.0 + 2.0 ** -7)
     assert oracle.round_bf16(1.0 + 3 * 2.0 ** -8) == 1.0 + 2 * 2.0 ** -7  # tie between odd and even: to even
+
+
+# ---------------------------------------------------------------------------
+# NVFP4 activations (the reading for a W4A4 path): E2M1 encoder, per-row
+# quantiser, the W4A4 expert
+# ---------------------------------------------------------------------------
+E2M1_MAG = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+
+
+def _nearest_e2m1(v):
+    """Brute force: the nearest magnitude, ties to the even code."""
+    a = abs(float(v))
+    d = np.abs(E2M1_MAG - a)
+    best = [c for c in range(8) if d[c] == d.min()]
+    c = min(best, key=lambda c: (c % 2, c))  # an even code wins a tie
+    return (8 if np.signbit(np.float32(v)) else 0) | c
+
+
+def test_encode_e2m1_nearest_ties_to_even():
+    for c in range(16):
+        v = np.float32(oracle.decode_e2m1(c))
+        assert oracle.encode_e2m1(v) == c
+    mids = (E2M1_MAG[:-1] + E2M1_MAG[1:]) / 2
+    for m in mids:
+        for v in (m, -m):
+            assert oracle.encode_e2m1(v) == _nearest_e2m1(v), v
+    rng = np.random.default_rng(41)
+    vals = (rng.standard_normal(3000) * 3).astype(np.float32)
+    got = np.array([oracle.encode_e2m1(v) for v in vals])
+    np.testing.assert_array_equal(got, [_nearest_e2m1(v) for v in vals])
+    # the input generator's storage encoder (written separately) agrees; it
+    # writes zero with a clear sign bit where the oracle keeps the sign (both
+    # are zero), so the codes are compared with the sign of zero dropped
+    gen = inputs._e2m1_codes(torch.from_numpy(vals)).numpy()
+    np.testing.assert_array_equal(np.where(got & 7 == 0, 0, got), gen)
+    assert oracle.encode_e2m1(7.5) == 7 and oracle.encode_e2m1(-1e9) == 15  # saturation at 6
+
+
+def test_quantize_nvfp4_rows_scales_codes_and_bounds():
+    rng = np.random.default_rng(42)
+    a = (rng.standard_normal((5, 64)) * np.exp2(rng.integers(-6, 6, (5, 1)))).astype(np.float32)
+    a[3] = 0.0
+    codes, scales, glob = oracle.quantize_nvfp4_rows(a)
+    assert glob[3] == 1.0 and (codes[3] == 0).all() and (scales[3] == 0).all()
+    for r in (0, 1, 2, 4):
+        g = np.float32(np.abs(a[r]).max()) / np.float32(6 * 448)
+        assert glob[r] == g
+        for b in range(4):
+            blk = a[r, 16 * b:16 * b + 16]
+            q = (np.float32(np.abs(blk).max()) / np.float32(6)) / g
+            want = torch.tensor([q], dtype=torch.float32).to(torch.float8_e4m3fn).view(torch.uint8).item()
+            assert scales[r, b] == want
+            s = np.float32(torch.tensor([scales[r, b]], dtype=torch.uint8).view(torch.float8_e4m3fn).float().item())
+            d = np.float32(s * g)
+            for j in range(16):
+                assert codes[r, 16 * b + j] == _nearest_e2m1(blk[j] / d)
+            # reconstruction: within half the widest E2M1 step (1.0) of s * g,
+            # values beyond 6 * s * g saturate
+            back = E2M1_MAG[codes[r, 16 * b:16 * b + 16] & 7] * np.where(codes[r, 16 * b:16 * b + 16] & 8, -1, 1)
+            err = np.abs(back * float(d) - blk.astype(np.float64))
+            assert (err <= float(d) * 1.0 + np.maximum(np.abs(blk) - 6 * float(d), 0) + 1e-12).all()
+
+
+def test_expert_ffn_w4a4_matches_numpy():
+    rng = np.random.default_rng(43)
+    n, H, I = 4, 64, 32
+    x = rng.standard_normal((n, H)).astype(np.float32)
+    w32 = {k: torch.from_numpy((rng.standard_normal(s) * 0.02).astype(np.float32))
+           for k, s in (("gate", (I, H)), ("up", (I, H)), ("down", (H, I)))}
+    enc = {k: inputs.quantize_nvfp4(v) for k, v in w32.items()}
+
+    def dec_w(p, sf, g):
+        N, K2 = p.shape
+        c = np.stack([p.numpy() & 0xF, p.numpy() >> 4], -1).reshape(N, 2 * K2)
+        sc = np.array([oracle.decode_e4m3(int(b)) for b in sf.numpy().reshape(-1)]).reshape(sf.shape)
+        return np.array([[oracle.decode_e2m1(int(v)) for v in row] for row in c]) * np.repeat(sc, 16, 1) * g
+
+    def dec_a(a32):
+        c, s, g = oracle.quantize_nvfp4_rows(a32)
+        vals = np.array([[oracle.decode_e2m1(int(v)) for v in row] for row in c])
+        sc = np.array([[oracle.decode_e4m3(int(v)) for v in row] for row in s])
+        return vals * np.repeat(sc, 16, 1) * g[:, None].astype(np.float64)
+
+    wg, wu, wd = (dec_w(*enc[k]) for k in ("gate", "up", "down"))
+    xq = dec_a(x)
+    ga, ua = xq @ wg.T, xq @ wu.T
+    h = ga / (1 + np.exp(-ga)) * ua
+    hb = torch.from_numpy(h.astype(np.float32)).to(torch.bfloat16).float().numpy()
+    ref = dec_a(hb) @ wd.T
+    got, h_got = oracle.expert_ffn_w4a4(x, enc["gate"][0].numpy(), enc["up"][0].numpy(), enc["down"][0].numpy(),
+                                        scales=[enc[k][1].numpy() for k in ("gate", "up", "down")],
+                                        global_scales=[enc[k][2] for k in ("gate", "up", "down")], want_h=True)
+    np.testing.assert_allclose(h_got, h, rtol=1e-12, atol=1e-12 * np.abs(h).max())
+    np.testing.assert_allclose(got, ref, rtol=1e-10, atol=1e-12 * np.abs(ref).max())

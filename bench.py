@@ -4,8 +4,11 @@
 One step = one forward of the whole block (router, dispatch, gather, gate/up
 GEMM + SwiGLU, down GEMM, combine) over one batch of synthetic tokens, with
 every input already resident in HBM.  The headline workload is the decode
-layer (T=64, H=5120, I=2560, 256 BF16 experts); the prefill layer (T=8192)
-is measured the same way and reported under "prefill".
+layer (T=64, H=5120, I=2560, 256 BF16 experts); the prefill layer (T=8192),
+the NVFP4-expert layer (T=4096) and the skewed-routing layer (T=32768, Zipf
+router bias) are measured the same way and reported under "prefill", "nvfp4"
+and "skew", each with its rooflines, per-stage times and a bounded oracle
+sample with the workload's near-tie count.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -296,6 +299,70 @@ def measure_dense(wl, steps, warmup, dev, pk):
     return out
 
 
+def workload_record(name, steps, warmup, dev, world, pk, small, cpu_budget_s=None, note="", residual=False):
+    """One more workload measured like the headline: device-timed steps
+    through the per-stage calls, the gate/up kernel's HBM and tensor
+    rooflines, the whole step's numbers, optionally the same steps with the
+    residual update fused into the combine, and, on rank 0 of a 1-GPU run, a
+    bounded sample of the oracle (with the workload's near-tie count)."""
+    from group_limited_routing_03_b300 import inputs
+
+    wl = inputs.workload(name, **small)
+    m, state = measure(wl, steps, warmup, dev, world, torch.cuda.current_device())
+    t_ms = max_over_ranks(m["total_ms"], world)
+    hbm, tc = roofline(wl, m, pk)
+    desc = {"bf16": "bf16 experts", "nvfp4": "nvfp4 experts (W4A16)",
+            "fp8": "fp8 experts (E4M3 + row scales), E4M3 activations per row"}[wl.w_dtype]
+    rec = dict(value=wl.T * steps * world / (t_ms * 1e-3), unit="tokens/s",
+               config={"workload": f"{name} T={wl.T} H={wl.H} I={wl.I} E=256 {desc}" + (f", {note}" if note else ""),
+                       "T": wl.T},
+               roofline=tc, roofline_hbm=hbm, clocks=m["clocks"], gpu_launches=m["launches_per_step"] * steps,
+               **step_numbers(wl, m, steps, pk))
+    if residual:
+        rm, _ = measure(wl, steps, warmup, dev, world, torch.cuda.current_device(), state=state,
+                        residual_step=RESIDUAL_STEP)
+        rec["residual_epilogue"] = residual_numbers(wl, m, rm, steps, pk, RESIDUAL_STEP)
+    if cpu_budget_s is not None and world == 1 and int(os.environ.get("RANK", "0")) == 0:
+        rec["cpu_baseline"] = oracle_sample(wl, state[0], budget_s=cpu_budget_s)
+    del state
+    torch.cuda.empty_cache()
+    return rec
+
+
+def measure_route_noalloc(dev, steps=50):
+    """beam_moe_route (workspace) against beam_moe_route_noalloc (static
+    scratch, hidden dimension split across at most 4096 / T CTAs per tile):
+    device time per call at H=5120, BF16 x, FP32 router."""
+    import group_limited_routing_03_b300 as moe
+    from group_limited_routing_03_b300 import inputs
+
+    out = {}
+    stream = torch.cuda.current_stream()
+    for T in (64, 2048, 4096):
+        wl = inputs.workload("prefill", T=T)
+        d = inputs.generate(wl, dev, experts=False)
+        sh = moe.shape(T, wl.H, wl.I)
+        ws = moe.alloc_workspace(sh, "bf16", dev)
+        ids = torch.empty((T, 8), dtype=torch.int32, device=dev)
+        w = torch.empty((T, 8), dtype=torch.float32, device=dev)
+        res = {}
+        for label, fn in (("route_ms", lambda: moe.beam_moe_route(sh, d["x"], d["router_w"], None, ids, w, ws)),
+                          ("noalloc_ms", lambda: moe.beam_moe_route_noalloc(sh, d["x"], d["router_w"], None, ids, w))):
+            for _ in range(5):
+                fn()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(steps):
+                fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            res[label] = round(e0.elapsed_time(e1) / steps, 4)
+        out[f"T={T}"] = res
+        del d, ws
+    torch.cuda.empty_cache()
+    return out
+
+
 def residual_numbers(wl, m_plain, m_res, steps, pk, k):
     """The post-norm residual update fused into the combine: its stage time
     against the plain combine's in the same step, and its own HBM roofline.
@@ -422,16 +489,28 @@ def roofline(wl, m, pk):
     return hbm, tc
 
 
-def step_numbers(wl, m, steps):
+def step_numbers(wl, m, steps, pk=None):
+    """Whole-step numbers: algorithmic bytes (touched experts' weights, x in,
+    y out, router weight) and FLOPs (three expert GEMMs per route, the router
+    GEMV per token) over the device time of one step, and, with the peaks,
+    their fractions of the HBM and tensor peaks."""
     R = wl.T * 8
     ms = m["total_ms"] / steps
     wbytes = m["touched"] * weight_bytes_per_expert(wl)
     xb = 2 if wl.x_dtype == "bf16" else 4
     bytes_alg = wbytes + wl.T * wl.H * xb * 2 + wl.E * wl.H * 4
     flops = 2.0 * R * 3 * wl.I * wl.H + 2.0 * wl.T * wl.E * wl.H
-    return dict(ms_per_step=round(ms, 4), tokens_per_s=wl.T / (ms * 1e-3),
-                step_gbs=round(bytes_alg / (ms * 1e-3) / 1e9, 1), step_tflops=round(flops / (ms * 1e-3) / 1e12, 1),
-                touched_experts=m["touched"], stage_ms={s: round(v, 4) for s, v in zip(STAGES, m["stage_ms"])})
+    gbs = bytes_alg / (ms * 1e-3) / 1e9
+    tfs = flops / (ms * 1e-3) / 1e12
+    out = dict(ms_per_step=round(ms, 4), tokens_per_s=wl.T / (ms * 1e-3),
+               step_gbs=round(gbs, 1), step_tflops=round(tfs, 1),
+               touched_experts=m["touched"], stage_ms={s: round(v, 4) for s, v in zip(STAGES, m["stage_ms"])})
+    if pk is not None:
+        ratio = 2.0 if wl.w_dtype == "fp8" else 1.0
+        out["step_frac_hbm"] = round(gbs / pk["hbm"], 4)
+        out["step_frac_tensor"] = round(tfs / (pk["bf16"] * ratio), 4)
+        out["step_frac_tensor_sustained"] = round(tfs / (pk["bf16_sustained"] * ratio), 4)
+    return out
 
 
 # ---------------------------------------------------------------------------
@@ -440,7 +519,8 @@ def step_numbers(wl, m, steps):
 def oracle_sample(wl, d, budget_s=12.0, max_tokens=None):
     """Time the FP64 oracle on a bounded sample of the workload: routing of all
     T tokens, then whole tokens (8 experts + combine) one by one until the
-    budget is spent.  Host copies of the inputs are made outside the timing."""
+    budget is spent.  Host copies of the inputs are made outside the timing.
+    Also counts the workload's near-tie tokens (oracle margin <= 1e-5)."""
     import numpy as np
 
     import oracle
@@ -480,7 +560,8 @@ def oracle_sample(wl, d, budget_s=12.0, max_tokens=None):
     sec = t_route * done / wl.T + t_ffn
     return dict(value=done / sec, unit="tokens/s", cores=threads, kind="oracle",
                 sample=f"{wl.name}: routing of all {wl.T} tokens (time pro-rated to the sample), then "
-                       f"{done} whole tokens (8 experts each, FP64) on {threads} threads; {sec:.2f} s of CPU time")
+                       f"{done} whole tokens (8 experts each, FP64) on {threads} threads; {sec:.2f} s of CPU time",
+                near_ties=int((r["margin"] <= 1e-5).sum()), near_tie_tokens_of=wl.T)
 
 
 def run_reference(args, rank, world):
@@ -545,6 +626,8 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default="decode")
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-more", action="store_true",
+                    help="skip the NVFP4 layer (T=4096) and the skewed-routing layer (T=32768)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-dense", action="store_true",
@@ -581,7 +664,7 @@ def main():
     wl = inputs.workload(args.workload, **small)
     m, state = measure(wl, args.steps, args.warmup, dev, world, torch.cuda.current_device())
     total_ms = max_over_ranks(m["total_ms"], world)
-    sn = step_numbers(wl, m, args.steps)
+    sn = step_numbers(wl, m, args.steps, pk)
     value = job_throughput(wl.T, args.steps, world, total_ms)
     hbm, tc = roofline(wl, m, pk)
 
@@ -608,38 +691,28 @@ def main():
 
     prefill = None
     if not args.no_prefill:
-        pw = inputs.workload("prefill", **small)
-        pm, pstate = measure(pw, max(3, args.steps // 2), args.warmup, dev, world, torch.cuda.current_device())
-        p_ms = max_over_ranks(pm["total_ms"], world)
-        psn = step_numbers(pw, pm, max(3, args.steps // 2))
-        phbm, ptc = roofline(pw, pm, pk)
-        presidual = None
-        if not args.no_residual:
-            rm, _ = measure(pw, max(3, args.steps // 2), args.warmup, dev, world, torch.cuda.current_device(),
-                            state=pstate, residual_step=RESIDUAL_STEP)
-            presidual = residual_numbers(pw, pm, rm, max(3, args.steps // 2), pk, RESIDUAL_STEP)
-        prefill = dict(value=pw.T * max(3, args.steps // 2) * world / (p_ms * 1e-3), unit="tokens/s",
-                       config={"workload": f"prefill T={pw.T} H={pw.H} I={pw.I} E=256 bf16 experts", "T": pw.T},
-                       roofline=ptc, roofline_hbm=phbm, clocks=pm["clocks"], residual_epilogue=presidual, **psn)
-        del pstate
-        torch.cuda.empty_cache()
+        psteps = max(3, args.steps // 2)
+        prefill = workload_record("prefill", psteps, args.warmup, dev, world, pk, small,
+                                  cpu_budget_s=None if args.no_cpu_baseline else 3.0,
+                                  residual=not args.no_residual)
+
+    # the NVFP4 layer (T=4096) and the skewed-routing stress layer (T=32768)
+    more = {}
+    if not args.no_more:
+        for name, steps, note in (("nvfp4", max(3, args.steps // 2), ""),
+                                  ("skew", max(3, args.steps // 4), "Zipf(1.1) router bias in [0, 3]")):
+            more[name] = workload_record(name, steps, args.warmup, dev, world, pk, small,
+                                         cpu_budget_s=None if args.no_cpu_baseline else 3.0, note=note)
 
     fp8 = None
     if not args.no_fp8 and not args.small:
         fp8 = {}
         for name, steps in (("fp8_decode", args.steps), ("fp8", max(3, args.steps // 2)), ("nvfp4_dec", args.steps)):
-            fw = inputs.workload(name)
-            fm, fstate = measure(fw, steps, args.warmup, dev, world, torch.cuda.current_device())
-            f_ms = max_over_ranks(fm["total_ms"], world)
-            fhbm, ftc = roofline(fw, fm, pk)
-            fp8[name] = dict(value=fw.T * steps * world / (f_ms * 1e-3), unit="tokens/s",
-                             config={"workload": f"{name} T={fw.T} H={fw.H} I={fw.I} E=256 " + (
-                                 "fp8 experts (E4M3 + row scales), E4M3 activations per row" if fw.w_dtype == "fp8"
-                                 else "nvfp4 experts (W4A16)"), "T": fw.T},
-                             roofline_hbm=fhbm, roofline=ftc, clocks=fm["clocks"],
-                             gpu_launches=fm["launches_per_step"] * steps, **step_numbers(fw, fm, steps))
-            del fstate
-            torch.cuda.empty_cache()
+            fp8[name] = workload_record(name, steps, args.warmup, dev, world, pk, {})
+
+    route_noalloc = None
+    if not args.small:
+        route_noalloc = measure_route_noalloc(dev)
 
     dense = None
     if not args.no_dense and not args.small:
@@ -660,7 +733,9 @@ def main():
                          f"({m['touched']} x {weight_bytes_per_expert(wl) / 1e6:.1f} MB), far larger than L2"},
         "roofline": hbm, "roofline_tensor": tc, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": m["launches_per_step"] * args.steps, "clocks": m["clocks"],
-        "step": sn, "graph": graph, "residual_epilogue": residual, "prefill": prefill, "weight_formats": fp8, "dense": dense,
+        "step": sn, "graph": graph, "residual_epilogue": residual, "prefill": prefill,
+        "nvfp4": more.get("nvfp4"), "skew": more.get("skew"), "weight_formats": fp8, "dense": dense,
+        "route_noalloc": route_noalloc,
     }
     print(json.dumps(line), flush=True)
 

@@ -162,17 +162,6 @@ void make_layout(const beam_moe_shape_t& s, Layout& L) {
 // ------------------------------------------------------------------ checks
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-beam_status_t check_shape(const beam_moe_shape_t* s) {
-  if (s == nullptr) return BEAM_ERR_INVALID_ARG;
-  if (s->T < 1 || s->H < 1 || s->I < 1) return BEAM_ERR_INVALID_ARG;
-  if (s->E != kExperts || s->n_group != kGroups || s->topk_group != kGroupsKept || s->top_k != kTopK)
-    return BEAM_ERR_UNSUPPORTED;
-  if (s->H % 128 != 0 || s->I % 128 != 0 || s->H > 65536 || s->I > 65536 || s->T > (1 << 20))
-    return BEAM_ERR_UNSUPPORTED;
-  if (!std::isfinite(s->routed_scale)) return BEAM_ERR_INVALID_ARG;
-  return BEAM_OK;
-}
-
 int chunk_rows(int T, bool fp4);
 int split_parts(int units, int k_blocks);
 
@@ -694,6 +683,28 @@ beam_status_t run_stage(const beam_moe_shape_t& s, const beam_moe_args_t& a, int
 }
 
 }  // namespace
+
+beam_status_t check_shape(const beam_moe_shape_t* s) {
+  if (s == nullptr) return BEAM_ERR_INVALID_ARG;
+  if (s->T < 1 || s->H < 1 || s->I < 1) return BEAM_ERR_INVALID_ARG;
+  if (s->E != kExperts || s->n_group != kGroups || s->topk_group != kGroupsKept || s->top_k != kTopK)
+    return BEAM_ERR_UNSUPPORTED;
+  if (s->H % 128 != 0 || s->I % 128 != 0 || s->H > 65536 || s->I > 65536 || s->T > (1 << 20))
+    return BEAM_ERR_UNSUPPORTED;
+  if (!std::isfinite(s->routed_scale)) return BEAM_ERR_INVALID_ARG;
+  return BEAM_OK;
+}
+
+beam_status_t check_route_args(const void* x, beam_dtype_t xdtype, const float* router_w, const float* router_bias,
+                               const int32_t* topk_ids, const float* topk_w) {
+  if (!x || !router_w || !topk_ids || !topk_w) return BEAM_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(router_w) || !aligned16(topk_ids) || !aligned16(topk_w) ||
+      (router_bias && !aligned16(router_bias)))
+    return BEAM_ERR_INVALID_ARG;
+  if (xdtype != BEAM_F32 && xdtype != BEAM_BF16) return BEAM_ERR_UNSUPPORTED;
+  return BEAM_OK;
+}
+
 }  // namespace beam
 
 using namespace beam;
@@ -736,11 +747,8 @@ beam_status_t beam_moe_route(const beam_moe_shape_t* shape, const void* x, beam_
                              void* workspace, size_t workspace_bytes, void* stream) {
   beam_status_t st = check_shape(shape);
   if (st != BEAM_OK) return st;
-  if (!x || !router_w || !topk_ids || !topk_w) return BEAM_ERR_INVALID_ARG;
-  if (!aligned16(x) || !aligned16(router_w) || !aligned16(topk_ids) || !aligned16(topk_w) ||
-      (router_bias && !aligned16(router_bias)))
-    return BEAM_ERR_INVALID_ARG;
-  if (xdtype != BEAM_F32 && xdtype != BEAM_BF16) return BEAM_ERR_UNSUPPORTED;
+  st = check_route_args(x, xdtype, router_w, router_bias, topk_ids, topk_w);
+  if (st != BEAM_OK) return st;
   Layout L;
   st = check_workspace(shape, workspace, workspace_bytes, L);
   if (st != BEAM_OK) return st;

@@ -8,6 +8,8 @@
 #include <cstddef>
 #include <cstdint>
 
+#include "beam_moe.h"
+
 namespace beam {
 
 constexpr int kExperts = 256;      // E
@@ -28,6 +30,17 @@ constexpr int kMaxAStages = 8;     // NVFP4: BF16 weight tiles in TMEM in flight
 constexpr int kMaxStages = 8;      // shared-memory ring depth
 constexpr int kChunkRowsBf16 = 256;  // routes per GEMM unit (BF16 weights)
 constexpr int kChunkRowsFp4 = 160;   // NVFP4: TMEM holds the accumulators and the weight tiles
+
+// ---------------------------------------------------------------------------
+// Argument checks shared by the entry points (api.cu)
+// ---------------------------------------------------------------------------
+// The layer shape: BEAM_OK, BEAM_ERR_INVALID_ARG (null, non-positive size,
+// non-finite scale) or BEAM_ERR_UNSUPPORTED (outside the supported set).
+beam_status_t check_shape(const beam_moe_shape_t* s);
+// The routing call's tensors: set, 16-byte aligned (bias may be null), x FP32
+// or BF16.
+beam_status_t check_route_args(const void* x, beam_dtype_t xdtype, const float* router_w, const float* router_bias,
+                               const int32_t* topk_ids, const float* topk_w);
 
 // ---------------------------------------------------------------------------
 // Router

@@ -11,9 +11,13 @@
 //
 // Limits: at most kNoAllocMaxTokens tokens; the split of the hidden
 // dimension across CTAs is reduced so that the partial logits fit in
-// kNoAllocPartRows rows of E floats.  Nothing in the scratch has to start at
-// zero (every call writes every element it later reads), but every call
-// shares it, so two calls that overlap on the GPU race.
+// kNoAllocPartRows rows of E floats: at most 4096 / T splits, so every
+// T > 2048 runs one split per 32-token tile (beam_moe_route splits the
+// hidden dimension up to T = 4704 on a 148-SM B300), and the selection is
+// fused into the logits kernel.  Nothing in the scratch has to start at zero
+// (every call writes every element it later reads), but every call shares
+// it, so two calls that overlap on the GPU race.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -33,25 +37,79 @@ constexpr size_t kScratchBytes = kHistBytes + kPartBytes;                       
 
 static __device__ __align__(256) unsigned char g_route_scratch[kScratchBytes];
 
-std::mutex g_scratch_mu;
-void* g_scratch_ptr[64] = {};
+// Device address of g_route_scratch, per CUDA context.  Host code only sees
+// a host-side stand-in under that name, so the address is looked up with
+// cudaGetSymbolAddress in the context that will run the kernels.  The cache
+// is keyed by the context's unique id (cuCtxGetId), which no later context
+// reuses: after cudaDeviceReset, or under another context of the same device,
+// the address is looked up afresh instead of reusing one that belongs to a
+// dead or different context.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
 
-// Device address of g_route_scratch on the current device (looked up once
-// per device, with that device current).
-beam_status_t scratch_address(void** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return BEAM_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (g_scratch_ptr[dev] == nullptr) {
+struct DriverFns {
+  CtxGetCurrentFn get_current = nullptr;
+  CtxGetIdFn get_id = nullptr;
+};
+
+const DriverFns& driver_fns() {
+  static DriverFns fns;
+  static std::once_flag once;
+  std::call_once(once, [] {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess || p == nullptr) return BEAM_ERR_CUDA;
-    g_scratch_ptr[dev] = p;
-  }
-  *out = g_scratch_ptr[dev];
-  return BEAM_OK;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fns.get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fns.get_id = reinterpret_cast<CtxGetIdFn>(p);
+  });
+  return fns;
 }
 
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+constexpr int kCacheSlots = 64;
+struct CacheEntry {
+  unsigned long long ctx_id;
+  void* ptr;
+};
+std::mutex g_scratch_mu;
+CacheEntry g_scratch_cache[kCacheSlots] = {};
+int g_scratch_next = 0;
+
+// Unique id of the context current to this thread (false: none yet, or the
+// driver does not report it).
+bool current_context_id(unsigned long long* id) {
+  const DriverFns& fns = driver_fns();
+  CUcontext ctx = nullptr;
+  return fns.get_current != nullptr && fns.get_id != nullptr && fns.get_current(&ctx) == CUDA_SUCCESS &&
+         ctx != nullptr && fns.get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+beam_status_t scratch_address(void** out) {
+  unsigned long long id = 0;
+  bool keyed = current_context_id(&id);
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (keyed) {
+    for (int i = 0; i < kCacheSlots; ++i)
+      if (g_scratch_cache[i].ptr != nullptr && g_scratch_cache[i].ctx_id == id) {
+        *out = g_scratch_cache[i].ptr;
+        return BEAM_OK;
+      }
+  }
+  // set-up for this context (the runtime binds its primary context to the
+  // thread here if none was current)
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess || p == nullptr) return BEAM_ERR_CUDA;
+  if (!keyed) keyed = current_context_id(&id);
+  if (keyed) {  // replaces the oldest entry once every slot is taken
+    g_scratch_cache[g_scratch_next] = CacheEntry{id, p};
+    g_scratch_next = (g_scratch_next + 1) % kCacheSlots;
+  }
+  *out = p;
+  return BEAM_OK;
+}
 
 }  // namespace
 }  // namespace beam
@@ -61,23 +119,14 @@ using namespace beam;
 extern "C" beam_status_t beam_moe_route_noalloc(const beam_moe_shape_t* shape, const void* x, beam_dtype_t xdtype,
                                                 const float* router_w, const float* router_bias, int32_t* topk_ids,
                                                 float* topk_w, void* stream) {
-  if (shape == nullptr) return BEAM_ERR_INVALID_ARG;
-  if (shape->T < 1 || shape->H < 1 || shape->I < 1) return BEAM_ERR_INVALID_ARG;
-  if (shape->E != kExperts || shape->n_group != kGroups || shape->topk_group != kGroupsKept ||
-      shape->top_k != kTopK || shape->H % 128 != 0 || shape->H > 65536)
-    return BEAM_ERR_UNSUPPORTED;
-  if (shape->T > kNoAllocMaxTokens) return BEAM_ERR_UNSUPPORTED;  // beyond the static scratch
-  if (!(shape->routed_scale == shape->routed_scale) || shape->routed_scale > 3.4e38f ||
-      shape->routed_scale < -3.4e38f)
-    return BEAM_ERR_INVALID_ARG;
-  if (!x || !router_w || !topk_ids || !topk_w) return BEAM_ERR_INVALID_ARG;
-  if (!aligned16(x) || !aligned16(router_w) || !aligned16(topk_ids) || !aligned16(topk_w) ||
-      (router_bias && !aligned16(router_bias)))
-    return BEAM_ERR_INVALID_ARG;
-  if (xdtype != BEAM_F32 && xdtype != BEAM_BF16) return BEAM_ERR_UNSUPPORTED;
+  beam_status_t st = check_shape(shape);  // the rules of beam_moe_route ...
+  if (st != BEAM_OK) return st;
+  if (shape->T > kNoAllocMaxTokens) return BEAM_ERR_UNSUPPORTED;  // ... and the static scratch's limit
+  st = check_route_args(x, xdtype, router_w, router_bias, topk_ids, topk_w);
+  if (st != BEAM_OK) return st;
 
   void* scratch = nullptr;
-  const beam_status_t st = scratch_address(&scratch);
+  st = scratch_address(&scratch);
   if (st != BEAM_OK) return st;
   int sms = 0, dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||

@@ -294,14 +294,18 @@ beam_status_t beam_moe_debug_timeout(void* workspace, size_t workspace_bytes, ui
  * allocation can stall the device).  The Beam post has no counterpart: this
  * is an integration convenience.  Same result as beam_moe_route (the hidden
  * dimension may be split across fewer CTAs, so FP32 logits can differ in the
- * last bits).  Arguments as beam_moe_route, without the workspace.
+ * last bits).  Arguments and shape rules as beam_moe_route, without the
+ * workspace.
  *   - Scratch: a library-owned static device buffer of 6 MiB (2 MiB of tile
  *     histograms + 4 MiB of partial logits) on every GPU that loads the
  *     library, held until the process exits.  No allocation in any call.
- *   - Limit: T <= 65536, else BEAM_ERR_UNSUPPORTED.
- *   - The first call on a device looks up the buffer's device address (once
- *     per device, with that device current); make that first call before any
- *     stream capture.
+ *   - Limit: T <= 65536, else BEAM_ERR_UNSUPPORTED.  The hidden dimension is
+ *     split across at most 4096 / T CTAs per 32-token tile, so every T > 2048
+ *     runs one split per tile (beam_moe_route splits it up to T = 4704 on a
+ *     148-SM B300, and runs BF16 x with T >= 512 on the tensor cores).
+ *   - The first call in each CUDA context (per device, or per driver context
+ *     a caller makes current) looks up the buffer's device address in that
+ *     context; make that first call before any stream capture.
  *   - All calls share the buffer and it keeps the last call's contents
  *     (nothing in it needs to start at zero); calls that overlap on the GPU,
  *     on any stream or thread, race and must be serialised by the caller. */

@@ -1,3 +1,4 @@
+import json
 import os
 import sys
 
@@ -28,3 +29,17 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    """One JSON line per workload whose routing the GPU parity tests checked:
+    its token count, how many tokens were near-ties (oracle margin <= 1e-5,
+    validity-checked instead of compared id by id) and how many outputs were
+    compared with the oracle."""
+    helpers = sys.modules.get("parity_helpers")
+    records = getattr(helpers, "NEAR_TIES", None) if helpers is not None else None
+    if not records:
+        return
+    terminalreporter.section("routing near-ties per workload")
+    for rec in records:
+        terminalreporter.write_line("near_ties " + json.dumps(rec))

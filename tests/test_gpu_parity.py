@@ -9,8 +9,8 @@ import torch
 import group_limited_routing_03_b300 as moe
 import oracle
 from group_limited_routing_03_b300 import inputs
-from parity_helpers import (Y_TOL, compare_routing, host_act, oracle_route, oracle_y, rel_err,
-                            seeded_routing)
+from parity_helpers import (Y_TOL, chunk_rows, compare_routing, full_size_tokens, host_act, oracle_route,
+                            oracle_y, record_near_ties, rel_err, seeded_routing)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -55,34 +55,46 @@ def _run_forward(wl, d, weights):
 # ---------------------------------------------------------------------------
 # whole block, small shapes (every token compared)
 # ---------------------------------------------------------------------------
+def _small_forward_vs_oracle(wl, *, fp32_originals):
+    """Forward of a small workload; routing checked on every token, y of every
+    token (near-ties with the GPU's ids) against the oracle."""
+    dg, dc = _gpu_inputs(wl, cpu_gen=True)
+    weights = _bf16_weights(dg) if fp32_originals else dg
+    y, ids, w, _ = _run_forward(wl, dg, weights)
+    ref = oracle_route(dg)
+    r = compare_routing(ids.cpu().numpy(), w.cpu().numpy(), ref)
+    tok = np.arange(wl.T)
+    # FP32 workloads: the oracle runs the FP32 originals (the GPU gets BF16 copies)
+    ow = {k: dc[k].numpy() for k in ("gate", "up", "down")} if fp32_originals else None
+    y_ref = oracle_y(dg, tok, r.ids, r.weights, oracle_weights=ow)
+    err = rel_err(y.cpu().double().numpy(), y_ref)
+    return r, err
+
+
+def test_tiny_workload_as_specified():
+    """The tiny layer exactly as specified: T=128, H=256, I=128, 256 experts,
+    FP32 x / router / experts drawn with seed 0; every token compared."""
+    wl = inputs.workload("tiny")
+    assert (wl.T, wl.H, wl.I, wl.x_dtype, wl.w_dtype, wl.seed) == (128, 256, 128, "f32", "f32", 0)
+    r, err = _small_forward_vs_oracle(wl, fp32_originals=True)
+    record_near_ties("tiny", wl.T, r, wl.T)
+    assert err <= Y_TOL["f32"], err
+
+
 @pytest.mark.parametrize("T,H,I,x_dtype", [(128, 256, 128, "f32"), (1, 256, 128, "bf16"), (33, 256, 128, "bf16"),
                                            (300, 384, 256, "bf16"), (77, 1024, 512, "f32")])
 def test_forward_small_all_tokens(T, H, I, x_dtype):
     wl = inputs.workload("tiny", T=T, H=H, I=I, x_dtype=x_dtype, seed=T + H)
-    dg, dc = _gpu_inputs(wl, cpu_gen=True)
-    y, ids, w, _ = _run_forward(wl, dg, _bf16_weights(dg))
-    ref = oracle_route(dg)
-    safe = compare_routing(ids.cpu().numpy(), w.cpu().numpy(), ref)
-    tok = np.nonzero(safe)[0]
-    # oracle on the FP32 originals of the expert weights (the GPU gets BF16 copies)
-    ow = {k: dc[k].numpy() for k in ("gate", "up", "down")}
-    y_ref = oracle_y(dg, tok, ref["ids"][tok], ref["weights"][tok], oracle_weights=ow)
-    err = rel_err(y.cpu().double().numpy()[tok], y_ref)
+    _, err = _small_forward_vs_oracle(wl, fp32_originals=True)
     assert err <= Y_TOL["bf16"], err
 
 
 @pytest.mark.parametrize("T,H,I", [(300, 512, 256), (40, 256, 512), (1, 256, 256), (257, 256, 256)])
 def test_forward_nvfp4_small_all_tokens(T, H, I):
     """NVFP4 experts (E2M1 codes, E4M3 block scales, FP32 global scale),
-    dequantised in shared memory, BF16 activations."""
+    expanded exactly to BF16 in TMEM, BF16 activations."""
     wl = inputs.workload("nvfp4", T=T, H=H, I=I, seed=31 + T)
-    dg, _ = _gpu_inputs(wl, cpu_gen=True)
-    y, ids, w, _ = _run_forward(wl, dg, dg)
-    ref = oracle_route(dg)
-    safe = compare_routing(ids.cpu().numpy(), w.cpu().numpy(), ref)
-    tok = np.nonzero(safe)[0]
-    y_ref = oracle_y(dg, tok, ref["ids"][tok], ref["weights"][tok])
-    err = rel_err(y.cpu().double().numpy()[tok], y_ref)
+    _, err = _small_forward_vs_oracle(wl, fp32_originals=False)
     assert err <= Y_TOL["nvfp4"], err
 
 
@@ -100,7 +112,8 @@ def test_route_tensor_core_path(name, T, H):
     assert moe.beam_moe_read_device_status(ws)[0] == 0
     ref = oracle_route(d)
     bias = None if d.get("bias") is None else d["bias"].cpu().numpy()
-    compare_routing(ids.cpu().numpy(), w.cpu().numpy(), ref, bias=bias)
+    r = compare_routing(ids.cpu().numpy(), w.cpu().numpy(), ref, bias=bias)
+    record_near_ties(f"{name} route T={T} H={H} (tensor-core router)", T, r, 0)
     # dispatch histograms written by the router agree with the ids
     moe.beam_moe_dispatch(sh, ids, ws)
     lay = moe.workspace_layout(sh)
@@ -222,35 +235,29 @@ def test_bounded_wait_reports_timeout_and_context_survives():
 # ---------------------------------------------------------------------------
 # full-size workloads: routing on every token, outputs on sampled tokens
 # ---------------------------------------------------------------------------
-def _sample_tokens(T, ids_ref, n, seed, hot_expert=None):
-    rng = np.random.default_rng(seed)
-    pick = {0, T - 1}
-    if hot_expert is not None:
-        pick.add(int(np.nonzero((ids_ref == hot_expert).any(1))[0][0]))
-    while len(pick) < n:
-        pick.add(int(rng.integers(0, T)))
-    return np.array(sorted(pick))
-
-
-@pytest.mark.parametrize("name,n_sample", [("decode", 8), ("prefill", 4), ("nvfp4", 4), ("skew", 4),
-                                           ("nvfp4_dec", 8)])
-def test_full_size_workloads(name, n_sample):
+@pytest.mark.parametrize("name", ["decode", "prefill", "nvfp4", "skew", "nvfp4_dec"])
+def test_full_size_workloads(name):
+    """Routing of every token against the oracle; outputs of every token at
+    decode sizes, else of tokens covering every touched expert and every
+    unit of work (token chunk) of the three most-loaded experts, plus every
+    near-tie token (with the GPU's ids)."""
     wl = inputs.workload(name)
     torch.cuda.empty_cache()
     dg = inputs.generate(wl, DEV)
     y, ids, w, ws = _run_forward(wl, dg, dg)
     ref = oracle_route(dg)
     bias = None if dg.get("bias") is None else dg["bias"].cpu().numpy()
-    safe = compare_routing(ids.cpu().numpy(), w.cpu().numpy(), ref, bias=bias)
-    counts = np.bincount(ref["ids"].reshape(-1), minlength=256)
+    ids_h = ids.cpu().numpy()
+    r = compare_routing(ids_h, w.cpu().numpy(), ref, bias=bias)
+    counts = np.bincount(ids_h.reshape(-1), minlength=256)
     if name == "skew":
         assert counts.max() > 10 * counts.mean()
-    hot = int(np.argmax(counts))
-    tok = _sample_tokens(wl.T, ref["ids"], n_sample, seed=wl.seed, hot_expert=hot)
-    tok = tok[safe[tok]]
-    y_ref = oracle_y(dg, tok, ref["ids"][tok], ref["weights"][tok])
+    tok = full_size_tokens(ids_h, chunk_rows(wl.T, wl.w_dtype), extra=np.nonzero(~r.safe)[0][:64])
+    y_ref = oracle_y(dg, tok, r.ids[tok], r.weights[tok])
     err = rel_err(y.cpu()[tok].double().numpy(), y_ref)
-    print(f"{name}: near-ties {(~safe).sum()} of {wl.T}; sampled {len(tok)} tokens; rel err {err:.3e}")
+    record_near_ties(name, wl.T, r, len(tok))
+    print(f"{name}: near-ties {r.near_ties} of {wl.T}; compared {len(tok)} tokens "
+          f"({int((counts > 0).sum())} experts touched); rel err {err:.3e}")
     assert err <= Y_TOL[wl.w_dtype], err
     del dg, y, ws
     gc.collect()
@@ -294,9 +301,9 @@ def test_maximum_token_count():
     x_h = host_act(dg["x"])
     bias = None if dg.get("bias") is None else dg["bias"].cpu().numpy()
     ref = oracle.route(x_h[tok], dg["router_w"].cpu().numpy(), bias, want_scores=True)
-    safe = compare_routing(ids_h[tok], w.cpu().numpy()[tok], ref, bias=bias)
-    few = tok[safe][:24]
-    y_ref = oracle_y(dg, few, ref["ids"][safe][:24], ref["weights"][safe][:24])
+    r = compare_routing(ids_h[tok], w.cpu().numpy()[tok], ref, bias=bias)
+    few = tok[:24]
+    y_ref = oracle_y(dg, few, r.ids[:24], r.weights[:24])
     err = rel_err(y.cpu()[few].double().numpy(), y_ref)
     assert err <= Y_TOL["bf16"], err
     del dg, y, ws

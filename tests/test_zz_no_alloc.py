@@ -55,6 +55,30 @@ def test_noalloc_route_matches_workspace_route_twice(name, T, H):
         assert ((ids_b >= 0) & (ids_b < 256)).all()
 
 
+@pytest.mark.parametrize("name,T,H,x_dtype", [
+    ("prefill", 600, 1024, "bf16"),    # BF16, T >= 512: the workspace route runs on the tensor cores
+    ("prefill", 4097, 1024, "bf16"),   # T > 2048: one hidden-dimension split per tile
+    ("skew", 5000, 1024, "f32"),       # past both split regimes, FP32 x, router bias
+    ("prefill", 65536, 1024, "bf16"),  # the largest T: the 2 MiB histogram region exactly full
+    ("prefill", 65536, 512, "f32"),
+])
+def test_noalloc_route_at_its_limits(name, T, H, x_dtype):
+    """Both routing entry points against the oracle on the tokens whose margin
+    is clear (ids exact, weights to 1e-5) and against each other."""
+    wl = inputs.workload(name, T=T, H=H, x_dtype=x_dtype, seed=7 * T + H)
+    d = inputs.generate(wl, "cuda", experts=False)
+    (ids_a, w_a), (ids_b, w_b) = _route_both(wl, d)
+    b = None if d.get("bias") is None else d["bias"].cpu().numpy()
+    ref = oracle.route(host_act(d["x"]), d["router_w"].cpu().numpy(), b)
+    safe = ref["margin"] > MARGIN
+    assert safe.mean() > 0.5
+    for ids, w in ((ids_a, w_a), (ids_b, w_b)):
+        np.testing.assert_array_equal(np.sort(ids[safe], 1), np.sort(ref["ids"][safe], 1))
+        np.testing.assert_allclose(np.sort(w[safe], 1), np.sort(ref["weights"][safe], 1), rtol=1e-5, atol=1e-6)
+        assert ((ids >= 0) & (ids < 256)).all()
+    np.testing.assert_array_equal(ids_b[safe], ids_a[safe])
+
+
 def test_noalloc_rejects_sizes_beyond_its_buffer():
     sh = moe.shape(65537, 256, 128)
     x = torch.zeros((16, 256), dtype=torch.bfloat16, device="cuda")  # never read: rejected on the host
@@ -64,3 +88,9 @@ def test_noalloc_rejects_sizes_beyond_its_buffer():
     with pytest.raises(moe.BeamError) as ei:
         moe.beam_moe_route_noalloc(sh, x, wr, None, ids, w)
     assert ei.value.code == moe.BEAM_ERR_UNSUPPORTED
+    # the shape rules of beam_moe_route apply too (one validation for both)
+    for bad, code in ((moe.shape(16, 256, 100), moe.BEAM_ERR_UNSUPPORTED),
+                      (moe.shape(16, 256, 128, routed_scale=float("inf")), moe.BEAM_ERR_INVALID_ARG)):
+        with pytest.raises(moe.BeamError) as ei:
+            moe.beam_moe_route_noalloc(bad, x, wr, None, ids, w)
+        assert ei.value.code == code

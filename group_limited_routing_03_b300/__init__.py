@@ -27,7 +27,7 @@ __all__ = [
     "beam_moe_route", "beam_moe_dispatch", "beam_moe_experts", "beam_moe_forward", "beam_moe_forward_stage",
     "ForwardCall", "STAGES", "beam_moe_stage_kernel_count", "beam_moe_route_noalloc", "pack_weights",
     "BEAM_LAYOUT_ROWS", "BEAM_LAYOUT_TILED",
-    "beam_moe_read_device_status", "beam_moe_debug_timeout", "beam_status_string", "BeamMoE",
+    "beam_moe_read_device_status", "beam_moe_debug_timeout", "beam_debug_nvfp4_expand", "beam_status_string", "BeamMoE",
     "library_path", "load", "BEAM_F32", "BEAM_BF16", "BEAM_NVFP4", "BEAM_FP8",
     "beam_moe_forward_residual", "GraphedForward",
     "DenseShape", "dense_shape", "dense_workspace_size", "dense_kernel_count", "beam_dense_mlp_forward",
@@ -121,6 +121,7 @@ def load():
     lib.beam_moe_stage_kernel_count.argtypes = [sp, i32, i32, i32]
     lib.beam_moe_stage_kernel_count.restype = ctypes.c_int32
     lib.beam_moe_debug_timeout.argtypes = [vp, sz, u32, vp]
+    lib.beam_debug_nvfp4_expand.argtypes = [vp, vp, i32, vp, vp]
     lib.beam_moe_pack_weights.argtypes = [sp, ctypes.POINTER(_ExpertWeights), ctypes.POINTER(_ExpertWeights), vp]
     dp = ctypes.POINTER(DenseShape)
     lib.beam_dense_workspace_size.argtypes = [dp, i32]
@@ -134,7 +135,8 @@ def load():
     for n in ("beam_moe_workspace_layout", "beam_moe_route", "beam_moe_dispatch", "beam_moe_experts",
               "beam_moe_forward", "beam_moe_forward_stage", "beam_moe_forward_residual",
               "beam_moe_read_device_status",
-              "beam_moe_debug_timeout", "beam_dense_mlp_forward", "beam_dense_pack_weights"):
+              "beam_moe_debug_timeout", "beam_debug_nvfp4_expand", "beam_dense_mlp_forward",
+              "beam_dense_pack_weights"):
         getattr(lib, n).restype = i32
     _lib = lib
     return lib
@@ -360,6 +362,17 @@ def beam_moe_read_device_status(workspace, stream=None):
     where = ctypes.c_uint32(0)
     code = load().beam_moe_read_device_status(_ptr(workspace), ctypes.byref(where), _stream(stream))
     return int(code), int(where.value)
+
+
+def beam_debug_nvfp4_expand(codes, scales, out, stream=None):
+    """Expand NVFP4 blocks with the GEMM converters' device code: codes uint8
+    [n_blocks * 8], scales uint8 [n_blocks] (E4M3), out int16/float16
+    [n_blocks * 16] (FP16 bits)."""
+    n_blocks = scales.numel()
+    if codes.numel() != 8 * n_blocks or out.numel() != 16 * n_blocks:
+        raise ValueError("codes must hold 8 bytes and out 16 values per block")
+    _check(load().beam_debug_nvfp4_expand(_ptr(codes), _ptr(scales), n_blocks, _ptr(out), _stream(stream)),
+           "beam_debug_nvfp4_expand")
 
 
 def beam_moe_debug_timeout(workspace, timeout_us: int, stream=None):

@@ -69,17 +69,19 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 2-D row-major bf16 matrix [rows, inner]; boxes of box_rows x 64 elements,
-// 128-byte swizzle.
-bool make_bf16_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows) {
+// 2-D row-major matrix of 16-bit elements [rows, inner] (BF16, or FP16 for
+// the NVFP4 path's activations); boxes of box_rows x 64 elements, 128-byte
+// swizzle.
+bool make_bf16_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows,
+                   CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   EncodeTiledFn enc = encode_fn();
   if (enc == nullptr) return false;
   const cuuint64_t dims[2] = {inner, rows};
   const cuuint64_t strides[1] = {inner * 2};
   const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBlockK), box_rows};
   const cuuint32_t estr[2] = {1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+  return enc(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -168,10 +170,11 @@ int split_parts(int units, int k_blocks);
 // Dense MLP workspace: status, unit counters, the one-expert schedule, h, and
 // for FP8 weights the codes of x and h with their row scales.
 struct DenseLayout {
-  size_t status, sched, counts, offsets, chunk_prefix, h, xq, hq, xs, hs, partial, total;
+  size_t status, sched, counts, offsets, chunk_prefix, h, xq, hq, xs, hs, x16, partial, total;
 };
 
-void make_dense_layout(const beam_dense_shape_t& s, DenseLayout& L) {
+// NVFP4 weights also need x as FP16 rows (x16, T_pad x H).
+void make_dense_layout(const beam_dense_shape_t& s, beam_dtype_t wdtype, DenseLayout& L) {
   size_t off = 0;
   auto take = [&](size_t bytes) {
     const size_t o = off;
@@ -190,6 +193,7 @@ void make_dense_layout(const beam_dense_shape_t& s, DenseLayout& L) {
   L.hq = take(T_pad * I);
   L.xs = take((T_pad + 32) * 4);
   L.hs = take((T_pad + 32) * 4);
+  L.x16 = take(wdtype == BEAM_NVFP4 ? T_pad * H * 2 : 0);
   // K-split partial planes: the larger of gate/up (two planes of T x I per
   // part) and down (one of T x H), parts as run_gemm picks them for BF16
   // weights (FP8 has half the k-blocks, so never more parts)
@@ -333,11 +337,16 @@ uint32_t pow2_at_least(uint32_t v) {
   return p;
 }
 
-beam_status_t run_gather(const beam_moe_shape_t& s, const void* x, bool x_bf16, bool fp8, void* ws, const Layout& L,
-                         const DeviceInfo& d, cudaStream_t stream) {
-  if (fp8)
+// Token rows into route order: BF16 (BF16 weights), E4M3 codes with row
+// scales (FP8 weights) or FP16 rows times a power of two (NVFP4 weights).
+beam_status_t run_gather(const beam_moe_shape_t& s, const void* x, bool x_bf16, beam_dtype_t wdtype, void* ws,
+                         const Layout& L, const DeviceInfo& d, cudaStream_t stream) {
+  if (wdtype == BEAM_FP8)
     return cuda_status(launch_gather_q8(x, x_bf16, s.H, at<int32_t>(ws, L.pos), s.T, at<uint8_t>(ws, L.xq),
                                         at<float>(ws, L.xs), stream));
+  if (wdtype == BEAM_NVFP4)
+    return cuda_status(launch_gather_f16(x, x_bf16, s.H, at<int32_t>(ws, L.pos), s.T, at<__half>(ws, L.xp),
+                                         at<float>(ws, L.xs), stream));
   return cuda_status(launch_gather(x, x_bf16, s.H, at<int32_t>(ws, L.pos), s.T, at<__nv_bfloat16>(ws, L.xp), d.sms,
                                    stream));
 }
@@ -439,11 +448,19 @@ beam_status_t run_gemm(int mode, const beam_moe_shape_t& s, const beam_expert_we
   const bool fp4 = wts->dtype == BEAM_NVFP4;
   const bool fp8 = wts->dtype == BEAM_FP8;
   const int nmax = io.nmax;
-  // FP8: h's row quantisation comes first (its scales need whole rows of h)
+  // FP8 / NVFP4: h's row conversion comes first (its scales need whole rows
+  // of h): E4M3 codes into hq, or FP16 in place
   if (fp8 && mode == 1) {
     const cudaError_t e = launch_quantize_rows(io.h, R, s.I, io.hq, io.hs, stream);
     if (e != cudaSuccess) return BEAM_ERR_CUDA;
   }
+  if (fp4 && mode == 1) {
+    const cudaError_t e = launch_rows_to_f16(io.h, R, s.I, io.hs, stream);
+    if (e != cudaSuccess) return BEAM_ERR_CUDA;
+  }
+  // NVFP4: the activation operand holds FP16 rows (kind::f16 takes A and B
+  // of one type)
+  const CUtensorMapDataType act_dt = fp4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const void* xp = io.xp;
   __nv_bfloat16* h = io.h;
   __nv_bfloat16* yr = io.out;
@@ -481,14 +498,14 @@ beam_status_t run_gemm(int mode, const beam_moe_shape_t& s, const beam_expert_we
       ok = make_u8_sw128_map(&maps.b, hq, I, R_pad, kBoxRows) && wmap_f8(&maps.a0, wts->down, H, I);
     if (mode == 1) maps.a1 = maps.a0;
   } else if (mode == 0) {
-    ok = make_bf16_map(&maps.b, xp, H, io.xp_rows, kBoxRows);
+    ok = make_bf16_map(&maps.b, xp, H, io.xp_rows, kBoxRows, act_dt);
     if (fp4)
       ok = ok && wmap_codes(&maps.a0, wts->gate, I, H) && wmap_codes(&maps.a1, wts->up, I, H) &&
            wmap_scales(&maps.s0, wts->gate_sf, I, H) && wmap_scales(&maps.s1, wts->up_sf, I, H);
     else
       ok = ok && wmap_bf16(&maps.a0, wts->gate, I, H) && wmap_bf16(&maps.a1, wts->up, I, H);
   } else {
-    ok = make_bf16_map(&maps.b, h, I, R_pad, kBoxRows);
+    ok = make_bf16_map(&maps.b, h, I, R_pad, kBoxRows, act_dt);
     if (fp4)
       ok = ok && wmap_codes(&maps.a0, wts->down, H, I) && wmap_scales(&maps.s0, wts->down_sf, H, I);  // a1 / s1 = a0 / s0
     else
@@ -566,7 +583,7 @@ beam_status_t run_gemm(int mode, const beam_moe_shape_t& s, const beam_expert_we
   p.gs1 = fp4 && mode == 0 ? wts->up_gs : nullptr;
   p.rs0 = fp8 ? (mode == 0 ? wts->gate_rs : wts->down_rs) : nullptr;
   p.rs1 = fp8 && mode == 0 ? wts->up_rs : nullptr;
-  p.bscale = fp8 ? (mode == 0 ? io.xs : io.hs) : nullptr;
+  p.bscale = (fp8 || fp4) ? (mode == 0 ? io.xs : io.hs) : nullptr;
   p.status = io.status;
   p.timeout_ns = kDefaultTimeoutNs;
   const size_t smem = gemm_smem_bytes(stages, acc_stages, sb);
@@ -579,7 +596,7 @@ beam_status_t run_gemm(int mode, const beam_moe_shape_t& s, const beam_expert_we
     if (!make_u8_sw128_map(&maps.bb, mode == 0 ? xq : hq, mode == 0 ? H : I, R_pad, static_cast<uint32_t>(p.b_big_rows)))
       return BEAM_ERR_CUDA;
   } else if (!make_bf16_map(&maps.bb, mode == 0 ? xp : static_cast<const void*>(h), mode == 0 ? H : I,
-                            mode == 0 ? io.xp_rows : R_pad, static_cast<uint32_t>(p.b_big_rows))) {
+                            mode == 0 ? io.xp_rows : R_pad, static_cast<uint32_t>(p.b_big_rows), act_dt)) {
     return BEAM_ERR_CUDA;
   }
   if (cudaMemsetAsync(p.sched, 0, sizeof(int), stream) != cudaSuccess) return BEAM_ERR_CUDA;
@@ -599,7 +616,7 @@ beam_status_t run_experts(const beam_moe_shape_t& s, const void* x, bool x_bf16,
                           const int32_t* ids, const float* w, void* y, void* ws, const Layout& L,
                           const DeviceInfo& d, bool hist_ready, cudaStream_t stream) {
   beam_status_t st = run_dispatch(s, ids, ws, L, chunk_rows(s.T, wts->dtype == BEAM_NVFP4), hist_ready, stream);
-  if (st == BEAM_OK) st = run_gather(s, x, x_bf16, wts->dtype == BEAM_FP8, ws, L, d, stream);
+  if (st == BEAM_OK) st = run_gather(s, x, x_bf16, wts->dtype, ws, L, d, stream);
   if (st == BEAM_OK) st = run_gemm(0, s, wts, moe_io(s, ws, L, wts->dtype == BEAM_NVFP4), d, stream);
   if (st == BEAM_OK) st = run_gemm(1, s, wts, moe_io(s, ws, L, wts->dtype == BEAM_NVFP4), d, stream);
   if (st == BEAM_OK) st = run_combine(s, w, y, x_bf16, ws, L, stream);
@@ -670,7 +687,7 @@ beam_status_t run_stage(const beam_moe_shape_t& s, const beam_moe_args_t& a, int
     case BEAM_STAGE_DISPATCH:
       return run_dispatch(s, a.topk_ids, ws, L, chunk_rows(s.T, a.weights->dtype == BEAM_NVFP4), true, cs);
     case BEAM_STAGE_GATHER:
-      return run_gather(s, a.x, xb, a.weights->dtype == BEAM_FP8, ws, L, d, cs);
+      return run_gather(s, a.x, xb, a.weights->dtype, ws, L, d, cs);
     case BEAM_STAGE_GATE_UP:
       return run_gemm(0, s, a.weights, moe_io(s, ws, L, a.weights->dtype == BEAM_NVFP4), d, cs);
     case BEAM_STAGE_DOWN:
@@ -848,7 +865,7 @@ int32_t beam_moe_stage_kernel_count(const beam_moe_shape_t* shape, beam_dtype_t 
       return sp > 1 ? 2 : 1;
     }
     case BEAM_STAGE_DISPATCH: return 2;
-    case BEAM_STAGE_DOWN: return wdtype == BEAM_FP8 ? 2 : 1;  // FP8: h quantised first
+    case BEAM_STAGE_DOWN: return wdtype == BEAM_BF16 ? 1 : 2;  // FP8 / NVFP4: h's rows converted first
     case BEAM_STAGE_GATHER:
     case BEAM_STAGE_GATE_UP:
     case BEAM_STAGE_COMBINE: return 1;
@@ -946,7 +963,7 @@ int32_t beam_dense_kernel_count(const beam_dense_shape_t* shape, beam_dtype_t wd
   const int nmax = chunk_rows(shape->T, fp4);
   const int chunks = (shape->T + nmax - 1) / nmax;
   int n = 1 + 1 + 1;        // schedule, gate/up, down
-  if (fp8) n += 2;          // x codes, h codes
+  if (fp8 || fp4) n += 2;   // x and h rows converted (E4M3 codes / FP16)
   for (int mode = 0; mode < 2; ++mode)
     if (choose_gemm(mode, ms, fp4, fp8, nmax, chunks, d).k_splits > 1) n += 1;  // the finishing kernel
   return n;
@@ -958,7 +975,7 @@ size_t beam_dense_workspace_size(const beam_dense_shape_t* shape, beam_dtype_t w
   if (check_shape(&ms) != BEAM_OK) return 0;
   if (wdtype != BEAM_BF16 && wdtype != BEAM_NVFP4 && wdtype != BEAM_FP8) return 0;
   DenseLayout L;
-  make_dense_layout(*shape, L);
+  make_dense_layout(*shape, wdtype, L);
   return L.total;
 }
 
@@ -975,7 +992,7 @@ beam_status_t beam_dense_mlp_forward(const beam_dense_shape_t* shape, const void
   const bool fp8 = weights->dtype == BEAM_FP8;
   if (xdtype != BEAM_BF16 && !(fp8 && xdtype == BEAM_F32)) return BEAM_ERR_UNSUPPORTED;
   DenseLayout L;
-  make_dense_layout(*shape, L);
+  make_dense_layout(*shape, weights->dtype, L);
   if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < L.total)
     return BEAM_ERR_WORKSPACE;
   DeviceInfo d;
@@ -1006,6 +1023,11 @@ beam_status_t beam_dense_mlp_forward(const beam_dense_shape_t* shape, const void
     return BEAM_ERR_CUDA;
   if (fp8 && launch_gather_q8(x, xdtype == BEAM_BF16, shape->H, nullptr, shape->T, io.xq, io.xs, cs) != cudaSuccess)
     return BEAM_ERR_CUDA;
+  if (weights->dtype == BEAM_NVFP4) {  // x as FP16 rows times a power of two
+    io.xp = at<__half>(ws, L.x16);
+    if (launch_gather_f16(x, true, shape->H, nullptr, shape->T, at<__half>(ws, L.x16), io.xs, cs) != cudaSuccess)
+      return BEAM_ERR_CUDA;
+  }
   st = run_gemm(0, ms, weights, io, d, cs);
   if (st == BEAM_OK) st = run_gemm(1, ms, weights, io, d, cs);
   return st;

@@ -61,6 +61,7 @@
 #include <cuda_bf16.h>
 
 #include "moe_internal.cuh"
+#include "nvfp4.cuh"
 #include "tc.cuh"
 
 namespace beam {
@@ -115,52 +116,6 @@ __device__ __forceinline__ Unit unit_at(const GemmParams& p, int u) {
   U.start = __ldg(&p.offsets[lo]) + c * base + (c < rem ? c : rem);
   U.n = base + (c < rem ? 1 : 0);
   return U;
-}
-
-// ---------------------------------------------------------------------------
-// NVFP4 -> BF16 (exact): an E2M1 magnitude has at most 2 significant bits and
-// an E4M3 scale at most 4, so their product fits BF16's 8 bits, and every
-// such product (>= 2^-10, <= 2688) is a normal BF16 number.
-// ---------------------------------------------------------------------------
-// E4M3 code (low 8 bits) -> BF16 bits in both halves.  The 7 magnitude bits
-// placed at FP32 bits 20..26 read as the E4M3 value times 2^-120 (E4M3
-// subnormals become FP32 subnormals), and the product with 2^120 is exact.
-__device__ __forceinline__ uint32_t e4m3_to_bf16x2(uint32_t code) {
-  const float f = __fmul_rn(__uint_as_float((code & 0x7Fu) << 20), 0x1p120f);
-  const uint32_t b = (__float_as_uint(f) >> 16) | ((code & 0x80u) << 8);
-  return b | (b << 16);
-}
-
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
-  uint32_t r;
-  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
-  return r;
-}
-
-// Eight E2M1 codes (one 32-bit word, element i in bits 4i..4i+3) times a
-// BF16 scale pair -> four BF16x2 words (element 2j in the low half of word
-// j).  Magnitudes come from byte-permute lookups into the high and low bytes
-// of the BF16 patterns of 0, .5, 1, 1.5, 2, 3, 4, 6; the signs are moved to
-// bit 7 of the high bytes by one more permute per four elements; a final
-// permute interleaves low and high bytes.  No branches.
-__device__ __forceinline__ void e2m1x8_to_bf16(uint32_t w, uint32_t scale2, uint32_t* o) {
-  constexpr uint32_t kHi0 = 0x3F3F3F00u, kHi1 = 0x40404040u;  // high bytes of codes 0..7
-  constexpr uint32_t kLo0 = 0xC0800000u, kLo1 = 0xC0804000u;  // low bytes of codes 0..7
-  const uint32_t m = w & 0x77777777u;      // magnitude codes (a selector uses its low 16 bits)
-  const uint32_t mb = __umulhi(m, 0x10000u);  // m >> 16, on the multiply pipe
-  const uint32_t w4 = w * 16u;                // w << 4, on the multiply pipe
-  // bit 7 of byte i = sign of element i: (w4.b0, w.b0, w4.b1, w.b1), then bytes 2, 3
-  const uint32_t ha = prmt(kHi0, kHi1, m) | (prmt(w, w4, 0x1504u) & 0x80808080u);
-  const uint32_t hb = prmt(kHi0, kHi1, mb) | (prmt(w, w4, 0x3726u) & 0x80808080u);
-  const uint32_t la = prmt(kLo0, kLo1, m), lb = prmt(kLo0, kLo1, mb);
-  uint32_t q[4] = {prmt(la, ha, 0x5140u), prmt(la, ha, 0x7362u), prmt(lb, hb, 0x5140u), prmt(lb, hb, 0x7362u)};
-  const __nv_bfloat162 s2 = *reinterpret_cast<const __nv_bfloat162*>(&scale2);
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&q[j]);
-    v = __hmul2(v, s2);  // exact: at most 6 significant bits
-    o[j] = *reinterpret_cast<uint32_t*>(&v);
-  }
 }
 
 // kPair: a cluster of two CTAs runs each unit as one M=256 pair MMA
@@ -426,8 +381,9 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
         if (!ring_take(u) || u < 0) break;
         const Unit U = unit_at(p, u);
         const uint32_t n_mma = static_cast<uint32_t>((U.n + 15) & ~15);
-        const uint32_t idesc = kFp8 ? idesc_e4m3_f32(kPair ? 2 * kBlockM : kBlockM, n_mma)
-                                    : idesc_bf16_f32(kPair ? 2 * kBlockM : kBlockM, n_mma);
+        const uint32_t idesc = kFp8   ? idesc_e4m3_f32(kPair ? 2 * kBlockM : kBlockM, n_mma)
+                               : kFp4 ? idesc_f16_f32(kBlockM, n_mma)
+                                      : idesc_bf16_f32(kPair ? 2 * kBlockM : kBlockM, n_mma);
         if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1u, p.timeout_ns, abort_flag, p.status, kWhereMmaAccEmpty))
           break;
         tc_fence_after();
@@ -448,7 +404,7 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
 #pragma unroll
             for (int k = 0; k < kBlockK / 16; ++k) {
               const uint32_t accumulate = (kb != U.kb0 || k != 0) ? 1u : 0u;
-              mma_bf16_ts(issuer == 0 ? d0 : d1, ta + static_cast<uint32_t>(issuer * (kBlockK / 2)) + 8u * k,
+              mma_f16_ts(issuer == 0 ? d0 : d1, ta + static_cast<uint32_t>(issuer * (kBlockK / 2)) + 8u * k,
                           db + 2u * k, idesc, accumulate);
             }
           } else {
@@ -583,9 +539,11 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
           tmem_ld16(tbase + static_cast<uint32_t>(c0), g);
           if (kNumA == 2) tmem_ld16(tbase + static_cast<uint32_t>(p.nmax + c0), g2);
           tmem_ld_wait();
-          if (kFp8) {
-            // token row scales of these 16 columns (the scale array is padded
-            // past the last route, so columns beyond the chunk read in bounds)
+          if (kFp8 || kFp4) {
+            // token row scales of these 16 columns (FP8: the E4M3 rows';
+            // NVFP4: the inverse powers of two of the FP16 rows; the scale
+            // array is padded past the last route, so columns beyond the
+            // chunk read in bounds)
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
               const float cs = __ldg(&p.bscale[U.start + c0 + j]);
@@ -701,15 +659,14 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
           const uint32_t wv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
           const uint32_t sc4 =
               *reinterpret_cast<const uint32_t*>(s_tile(stage, mat) + row * kScaleBoxCols + 4 * (kb & 3));
+          uint32_t sp[4];
+          scales4_to_f16_pairs(sc4, sp);
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             uint32_t out[16];
 #pragma unroll
-            for (int g = 0; g < 2; ++g) {  // 16 elements per scale
-              const uint32_t s2 = e4m3_to_bf16x2((sc4 >> (8 * (2 * h + g))) & 0xFFu);
-              e2m1x8_to_bf16(wv[4 * h + 2 * g], s2, out + 8 * g);
-              e2m1x8_to_bf16(wv[4 * h + 2 * g + 1], s2, out + 8 * g + 4);
-            }
+            for (int g = 0; g < 2; ++g)  // 16 elements per scale
+              nvfp4x16_to_f16(wv[4 * h + 2 * g], wv[4 * h + 2 * g + 1], sp[2 * h + g], out + 8 * g);
             tmem_st16(ta0 + static_cast<uint32_t>(mat * (kBlockK / 2) + 16 * h), out);
           }
         }

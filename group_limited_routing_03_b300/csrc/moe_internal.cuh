@@ -3,6 +3,7 @@
 #pragma once
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <cstddef>
@@ -150,6 +151,15 @@ cudaError_t launch_gather_q8(const void* x, bool x_bf16, int H, const int32_t* p
 // FP8 weights: rows of h (BF16 [R, I]) to E4M3 codes hq [R_pad, I] and row
 // scales hs [R_pad], the same rule.
 cudaError_t launch_quantize_rows(const __nv_bfloat16* h, int R, int I, uint8_t* hq, float* hs, cudaStream_t stream);
+// NVFP4 weights (FP16 tensor cores): token rows (x in BF16 or FP32, the
+// latter rounded to BF16 first) to FP16 times a power of two per row, in
+// route order (xh [R_pad, H]), the inverse power of two per row in xs
+// [R_pad]; pos == NULL (dense MLP): row t to row t.  Exact (see quant.cu).
+cudaError_t launch_gather_f16(const void* x, bool x_bf16, int H, const int32_t* pos, int T, __half* xh, float* xs,
+                              cudaStream_t stream);
+// NVFP4 weights: rows of h (BF16 [R, I]) to FP16 in place, the same rule,
+// inverse scales in hs [R_pad].
+cudaError_t launch_rows_to_f16(void* h, int R, int I, float* hs, cudaStream_t stream);
 // wide: BF16 / FP8 down on one CTA per unit with 256-row units (two tiles per
 // k-block); fp8: E4M3 weights and activations (kind::f8f6f4); dec: NVFP4 with
 // chunks of at most 64 routes (4 epilogue warps, 12 converter warps)

@@ -214,10 +214,11 @@ __device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
-// D[tmem] (+)= A[tmem] x B[smem]^T: the A tile sits in tensor memory, row m
-// in lane m, two BF16 K elements per 32-bit column (the even one in the low
+// D[tmem] (+)= A[tmem] x B[smem]^T (kind::f16: BF16 or FP16 operands, as the
+// instruction descriptor says): the A tile sits in tensor memory, row m in
+// lane m, two 16-bit K elements per 32-bit column (the even one in the low
 // half), so one K=16 step spans 8 columns.
-__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
                                             uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
@@ -381,6 +382,12 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N) {
   return (1u << 4)                 // D format: F32
          | (1u << 7)               // A format: BF16
          | (1u << 10)              // B format: BF16
+         | ((N >> 3) << 17)        // N >> 3
+         | ((M >> 4) << 24);       // M >> 4
+}
+// kind::f16 with FP16 A and B (format code 0), FP32 D.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(uint32_t M, uint32_t N) {
+  return (1u << 4)                 // D format: F32
          | ((N >> 3) << 17)        // N >> 3
          | ((M >> 4) << 24);       // M >> 4
 }

@@ -288,6 +288,18 @@ beam_status_t beam_moe_read_device_status(void* workspace, uint32_t* where, void
 beam_status_t beam_moe_debug_timeout(void* workspace, size_t workspace_bytes, uint32_t timeout_us,
                                      void* stream);
 
+/* Test hook for the NVFP4 weight expansion (not part of the Beam post's
+ * method): expands n_blocks blocks of 16 E2M1 elements with the same device
+ * code the grouped GEMMs' converter warps run.  codes: device, n_blocks * 8
+ * bytes (block b in bytes 8b..8b+7, element 2j in the low nibble of byte j);
+ * scales: device, n_blocks E4M3 codes (block b's at byte b); out: device,
+ * n_blocks * 16 FP16 values (bit patterns), element i of block b at 16b + i,
+ * = e2m1 * e4m3 exactly (NaN for the E4M3 NaN codes).  n_blocks a positive
+ * multiple of 4, all pointers 16-byte aligned, else BEAM_ERR_INVALID_ARG.
+ * Async on `stream`. */
+beam_status_t beam_debug_nvfp4_expand(const uint8_t* codes, const uint8_t* scales, int32_t n_blocks, uint16_t* out,
+                                      void* stream);
+
 /* Routing without a workspace, for callers that cannot allocate device memory
  * (a host framework that owns all device memory and hands a plugin only its
  * inputs and outputs, or a serving loop that must never allocate, since an

@@ -100,7 +100,7 @@ def test_dense_kernel_count():
     assert moe.dense_kernel_count(moe.dense_shape(64, 5120, 20480), "bf16") == 5
     assert moe.dense_kernel_count(moe.dense_shape(64, 5120, 20480), "fp8") == 7
     assert moe.dense_kernel_count(moe.dense_shape(8192, 5120, 20480), "bf16") == 3
-    assert moe.dense_kernel_count(moe.dense_shape(64, 5120, 20480), "nvfp4") == 3
+    assert moe.dense_kernel_count(moe.dense_shape(64, 5120, 20480), "nvfp4") == 5  # + x and h to FP16 rows
 
 
 def test_dense_fp8_with_fp32_x():

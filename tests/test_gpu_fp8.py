@@ -100,6 +100,7 @@ def test_fp8_activation_codes():
     xdt = moe.BEAM_BF16
     assert moe.beam_moe_stage_kernel_count(sh, 4, xdt, "fp8") == 2  # down: quantise h, then the GEMM
     assert moe.beam_moe_stage_kernel_count(sh, 4, xdt, "bf16") == 1
+    assert moe.beam_moe_stage_kernel_count(sh, 4, xdt, "nvfp4") == 2  # down: h to FP16 rows, then the GEMM
 
 
 @pytest.mark.parametrize("name", ["fp8_decode", "fp8"])

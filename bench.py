@@ -630,6 +630,7 @@ def main():
                     help="skip the NVFP4 layer (T=4096) and the skewed-routing layer (T=32768)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay of the headline step")
     ap.add_argument("--no-dense", action="store_true",
                     help="skip the dense SwiGLU MLP (decode T=64 and prefill T=8192, I=20480)")
     ap.add_argument("--no-fp8", action="store_true",
@@ -677,8 +678,10 @@ def main():
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = oracle_sample(wl, state[0])
+    graph = None
     try:
-        graph = measure_graph(wl, state, args.steps, args.warmup)
+        if not args.no_graph:
+            graph = measure_graph(wl, state, args.steps, args.warmup)
     except Exception as e:  # an auxiliary number: record why it is missing
         graph = {"unavailable": f"{type(e).__name__}: {e}"[:300]}
     residual = None

@@ -100,6 +100,20 @@ bool make_u8_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t ro
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D view of a tensor: dims d (innermost first), byte strides of dims 1 and
+// 2 (any order: the innermost dimension is contiguous), box b.
+bool make_3d_map(CUtensorMap* map, CUtensorMapDataType dt, const void* base, const uint64_t (&d)[3],
+                 const uint64_t (&stride)[2], const uint32_t (&b)[3], CUtensorMapSwizzle swz) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[3] = {d[0], d[1], d[2]};
+  const cuuint64_t strides[2] = {stride[0], stride[1]};
+  const cuuint32_t box[3] = {b[0], b[1], b[2]};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 2-D row-major byte matrix [rows, inner], boxes box_rows x 128 bytes with the
 // 128-byte swizzle the MMA descriptors expect (FP8 operand tiles).
 bool make_u8_sw128_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows) {
@@ -326,6 +340,9 @@ beam_status_t run_dispatch(const beam_moe_shape_t& s, const int32_t* ids, void* 
 // Routes per GEMM unit: all of an expert's routes up to a cap (BF16 256, the
 // widest MMA; NVFP4 160, so that TMEM also holds three BF16 weight tiles).
 int chunk_rows(int T, bool fp4) {
+  // NVFP4 with few routes per expert (T <= 256: 8 on average): chunks of 16
+  // leave TMEM room for the decode variant's accumulators and tile rings
+  if (fp4 && T <= kFp4SmallT) return kDecChunkRows;
   const int cap = fp4 ? kChunkRowsFp4 : kChunkRowsBf16;
   int n = ((T + kBoxRows - 1) / kBoxRows) * kBoxRows;
   return n > cap ? cap : n;
@@ -548,12 +565,17 @@ beam_status_t run_gemm(int mode, const beam_moe_shape_t& s, const beam_expert_we
   p.a_tiled = tiled ? 1 : 0;
   p.nmax = nmax;
   const int num_a = (mode == 0 || pair || fp4 || wide) ? 2 : 1;  // weight tiles per stage
-  const size_t sb = gemm_stage_bytes(num_a, fp4, pair ? nmax / 2 : nmax);
+  // NVFP4 in the tiled layout: several k-blocks per stage (four with small
+  // chunks, two otherwise), so one stage is five TMA loads (codes and scales
+  // of both matrices, the activations as a 3-D box) for several k-blocks
+  const int sub = (fp4 && tiled) ? (nmax <= kDecChunkRows ? 4 : 2) : 1;
+  const size_t sb = gemm_stage_bytes(num_a, fp4, pair ? nmax / 2 : nmax, sub);
   int stages = static_cast<int>(budget / sb);
   if (stages > kMaxStages) stages = kMaxStages;
   if (stages < 2) return BEAM_ERR_UNSUPPORTED;
   p.stages = stages;
-  p.acc_cols = static_cast<uint32_t>(num_a * nmax);
+  // NVFP4 decode variant: two accumulators per matrix (alternate K steps)
+  p.acc_cols = static_cast<uint32_t>(num_a * nmax * (dec ? 2 : 1));
   int acc_stages = static_cast<int>(512 / p.acc_cols);
   if (acc_stages > 4) acc_stages = 4;
   if (acc_stages < 1) acc_stages = 1;
@@ -572,10 +594,12 @@ beam_status_t run_gemm(int mode, const beam_moe_shape_t& s, const beam_expert_we
     p.a_col0 = static_cast<uint32_t>(acc_stages) * p.acc_cols;
     p.a_stages = static_cast<int>((512 - p.a_col0) / a_cols);
     if (p.a_stages > kMaxAStages) p.a_stages = kMaxAStages;
-    if (p.a_stages > p.stages) p.a_stages = p.stages;  // a tile is freed through the smem ring's empty barriers
-    if (p.a_stages < (dec ? 3 : 2)) return BEAM_ERR_UNSUPPORTED;  // one tile per converter group at least
+    // converter groups G = 3 (decode) or 2; a group's consecutive k-blocks
+    // lie at most 2G - 1 apart, and a tile must come back to it no sooner
+    if (p.a_stages < (dec ? 5 : 3)) return BEAM_ERR_UNSUPPORTED;
     p.tmem_cols = 512;
   }
+  p.sub_blocks = sub;
   p.sched = io.sched + mode;
   p.out = mode == 0 ? h : yr;
   p.out_ld = mode == 0 ? s.I : s.H;
@@ -598,6 +622,26 @@ beam_status_t run_gemm(int mode, const beam_moe_shape_t& s, const beam_expert_we
   } else if (!make_bf16_map(&maps.bb, mode == 0 ? xp : static_cast<const void*>(h), mode == 0 ? H : I,
                             mode == 0 ? io.xp_rows : R_pad, static_cast<uint32_t>(p.b_big_rows), act_dt)) {
     return BEAM_ERR_CUDA;
+  }
+  if (sub > 1) {
+    // packed codes: the tiled layout as (byte, row, tile), boxes of `sub`
+    // consecutive tiles; activations as (element, row, k-block), boxes of the
+    // chunk's rows for `sub` k-blocks (their B tiles one after another)
+    const uint64_t N = mode == 0 ? I : H, K = mode == 0 ? H : I;
+    const uint64_t tiles = E * N / kBlockM * (K / kBlockK);
+    const uint64_t cd[3] = {kBlockK / 2, kBlockM, tiles};
+    const uint64_t cs[2] = {kBlockK / 2, kPackedTileBytes};
+    const uint32_t cb[3] = {kBlockK / 2, kBlockM, static_cast<uint32_t>(sub)};
+    const void* c0 = mode == 0 ? wts->gate : wts->down;
+    const void* c1 = mode == 0 ? wts->up : wts->down;
+    const void* act = mode == 0 ? xp : static_cast<const void*>(h);
+    const uint64_t ad[3] = {kBlockK, mode == 0 ? io.xp_rows : R_pad, K / kBlockK};
+    const uint64_t as[2] = {K * 2, kBlockK * 2};
+    const uint32_t ab[3] = {kBlockK, static_cast<uint32_t>(p.b_big_rows), static_cast<uint32_t>(sub)};
+    if (!make_3d_map(&maps.a0, CU_TENSOR_MAP_DATA_TYPE_UINT8, c0, cd, cs, cb, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_3d_map(&maps.a1, CU_TENSOR_MAP_DATA_TYPE_UINT8, c1, cd, cs, cb, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_3d_map(&maps.bb, act_dt, act, ad, as, ab, CU_TENSOR_MAP_SWIZZLE_128B))
+      return BEAM_ERR_CUDA;
   }
   if (cudaMemsetAsync(p.sched, 0, sizeof(int), stream) != cudaSuccess) return BEAM_ERR_CUDA;
   if (launch_gemm(mode, fp4, pair, wide, fp8, dec, maps, p, grid, smem, stream) != cudaSuccess) return BEAM_ERR_CUDA;

@@ -161,12 +161,16 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t b_tile_bytes = static_cast<uint32_t>(kPair ? p.nmax / 2 : p.nmax) * kBlockK * 2;
-  const uint32_t stage_bytes = static_cast<uint32_t>(gemm_stage_bytes(kNumA, kFp4, kPair ? p.nmax / 2 : p.nmax));
+  // NVFP4: k-blocks per pipeline stage (1, 2 or 4; K loaded as a whole
+  // number of stages per unit)
+  const int S = kFp4 ? p.sub_blocks : 1;
+  const uint32_t stage_bytes = static_cast<uint32_t>(gemm_stage_bytes(kNumA, kFp4, kPair ? p.nmax / 2 : p.nmax, S));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(p.stages) * stage_bytes);
   uint64_t* full = bars;
   uint64_t* empty = full + p.stages;
-  uint64_t* afull = empty + p.stages;        // NVFP4: BF16 weight tile written to TMEM
-  uint64_t* acc_full = afull + kMaxAStages;
+  uint64_t* afull = empty + p.stages;        // NVFP4: FP16 weight tile written to TMEM
+  uint64_t* aempty = afull + kMaxAStages;    // NVFP4: the MMAs reading that tile have completed
+  uint64_t* acc_full = aempty + kMaxAStages;
   uint64_t* acc_empty = acc_full + p.acc_stages;
   uint64_t* drain = acc_empty + p.acc_stages;
   uint64_t* ufull = drain + 1;        // unit ring: index published
@@ -177,14 +181,19 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = kPair ? cluster_ctarank() : 0u;  // 0: the CTA that issues the MMAs
-  // Stage layout: BF16 weights [A x kNumA][B]; NVFP4 [B][packed x kNumA][scales x kNumA]
+  // Stage layout: BF16 weights [A x kNumA][B]; NVFP4 [B x S][packed x kNumA x S][scales x kNumA]
+  // (k-block `sub` of the stage: B at b_tile + sub * b_tile_bytes, packed
+  // codes of matrix `which` at p_tile(s, which, sub); one scale tile per
+  // matrix covers four k-blocks)
   auto a_tile = [&](int s, int which) { return smem + static_cast<size_t>(s) * stage_bytes + which * kATileBytes; };
   auto b_tile = [&](int s) {
     return smem + static_cast<size_t>(s) * stage_bytes + (kFp4 ? 0u : kNumA * kATileBytes);
   };
-  auto p_tile = [&](int s, int which) { return b_tile(s) + b_tile_bytes + which * kPackedTileBytes; };
+  auto p_tile = [&](int s, int which, int sub) {
+    return b_tile(s) + S * b_tile_bytes + (which * S + sub) * kPackedTileBytes;
+  };
   auto s_tile = [&](int s, int which) {
-    return b_tile(s) + b_tile_bytes + kNumA * kPackedTileBytes + which * kScaleTileBytes;
+    return b_tile(s) + S * b_tile_bytes + kNumA * S * kPackedTileBytes + which * kScaleTileBytes;
   };
 
   if (threadIdx.x == 0) {
@@ -192,7 +201,10 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kIssuers);
     }
-    for (int a = 0; a < kMaxAStages; ++a) mbar_init(&afull[a], kConv / kGroups);  // one converter group per k-block
+    for (int a = 0; a < kMaxAStages; ++a) {
+      mbar_init(&afull[a], kConv / kGroups);  // one converter group per k-block
+      mbar_init(&aempty[a], kIssuers);
+    }
     for (int a = 0; a < p.acc_stages; ++a) {
       mbar_init(&acc_full[a], kIssuers);
       mbar_init(&acc_empty[a], kPair ? 2 * kEpilogueWarps : kEpi);
@@ -308,15 +320,16 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
         const int b_row0 = U.start + static_cast<int>(rank) * n_local;
         // activations: one box of the tile's full height when the chunk fills
         // more than half of it (rows past the chunk are loaded and not read),
-        // else ceil(n / 32) boxes of 32 rows
-        const bool big = 2 * n_local > p.b_big_rows;
+        // else ceil(n / 32) boxes of 32 rows; NVFP4 stages of several
+        // k-blocks always load the full height
+        const bool big = 2 * n_local > p.b_big_rows || S > 1 || p.b_big_rows < kBoxRows;
         const int nbox = big ? 1 : (n_local + kBoxRows - 1) / kBoxRows;
-        const uint32_t a_bytes = kFp4 ? kNumA * (kPackedTileBytes + kScaleTileBytes) : kNumA * kATileBytes;
+        const uint32_t a_bytes = kFp4 ? kNumA * (S * kPackedTileBytes + kScaleTileBytes) : kNumA * kATileBytes;
         const uint32_t bytes =
-            a_bytes + (big ? static_cast<uint32_t>(p.b_big_rows) * (kBlockK * 2) : static_cast<uint32_t>(nbox) * kBoxBytes);
+            a_bytes + (big ? static_cast<uint32_t>(S * p.b_big_rows) * (kBlockK * 2) : static_cast<uint32_t>(nbox) * kBoxBytes);
         const CUtensorMap* bmap = big ? &maps.bb : &maps.b;
         const int box_rows = big ? 0 : kBoxRows;  // row step between boxes
-        for (int kb = U.kb0; kb < U.kb1; ++kb) {
+        for (int kb = U.kb0; kb < U.kb1; kb += S) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, p.timeout_ns, abort_flag, p.status, kWhereProducerEmpty)) {
             ok = false;
             break;
@@ -339,9 +352,16 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
               const int sx = a_x((kb >> 2) * static_cast<int>(kScaleBoxCols));
               // gate/up: gate and up tiles of the same rows; down: rows a_row and a_row + 128
               const int a_row1 = kMode == 0 ? a_row : a_row + kHalfRows;
-              tma_load_2d_nohint(p_tile(stage, 0), &maps.a0, &full[stage], a_x(kx / 2), a_y(a_row, kb));
+              // packed codes of S k-blocks: S consecutive tiles of the tiled
+              // layout's 3-D view (bytes, row, tile), or one 2-D box when S = 1
+              if (S > 1) {
+                tma_load_3d(p_tile(stage, 0, 0), &maps.a0, &full[stage], 0, 0, (a_row >> 7) * p.k_blocks + kb);
+                tma_load_3d(p_tile(stage, 1, 0), &maps.a1, &full[stage], 0, 0, (a_row1 >> 7) * p.k_blocks + kb);
+              } else {
+                tma_load_2d_nohint(p_tile(stage, 0, 0), &maps.a0, &full[stage], a_x(kx / 2), a_y(a_row, kb));
+                tma_load_2d_nohint(p_tile(stage, 1, 0), &maps.a1, &full[stage], a_x(kx / 2), a_y(a_row1, kb));
+              }
               tma_load_2d_nohint(s_tile(stage, 0), &maps.s0, &full[stage], sx, s_y(a_row, kb));
-              tma_load_2d_nohint(p_tile(stage, 1), &maps.a1, &full[stage], a_x(kx / 2), a_y(a_row1, kb));
               tma_load_2d_nohint(s_tile(stage, 1), &maps.s1, &full[stage], sx, s_y(a_row1, kb));
             } else {
               tma_load_2d_nohint(a_tile(stage, 0), &maps.a0, &full[stage], a_x(kx), a_y(a_row, kb));
@@ -350,8 +370,11 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
                 tma_load_2d_nohint(a_tile(stage, 1), &maps.a1, &full[stage], a_x(kx),
                                    a_y(kMode == 0 ? a_row : a_row + kHalfRows, kb));
             }
-            for (int b = 0; b < nbox; ++b)
-              tma_load_2d(b_tile(stage) + b * kBoxBytes, bmap, &full[stage], kx, U.start + b * box_rows, pol_x);
+            if (kFp4 && S > 1)  // the chunk's rows for S k-blocks: 3-D view (element, row, k-block)
+              tma_load_3d_hint(b_tile(stage), bmap, &full[stage], 0, U.start, kb, pol_x);
+            else
+              for (int b = 0; b < nbox; ++b)
+                tma_load_2d(b_tile(stage) + b * kBoxBytes, bmap, &full[stage], kx, U.start + b * box_rows, pol_x);
           }
           ++issued;
           if (++stage == p.stages) {
@@ -369,45 +392,100 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
         mbar_wait(&full[s], par, p.timeout_ns, nullptr, p.status, kWhereDrain);
       }
     }
-  } else if (warp == 1 || (kFp4 && warp == kMma2Warp)) {
-    // ------------------------------------------------------------ MMA issuer
-    const int issuer = warp == 1 ? 0 : 1;  // NVFP4: which tile's MMAs this thread issues
-    if (lane == 0 && rank == 0) {
+  } else if (kFp4 && (warp == 1 || warp == kMma2Warp)) {
+    // ------------------------------------------------------------ MMA issuers (NVFP4)
+    // One thread per weight matrix of the unit (gate / up, or the two row
+    // halves of a down unit), each its own accumulator chain, A (the FP16
+    // tile the converters wrote) from TMEM, B from the stage's activation
+    // tile of that k-block; descriptors formed once per stage.  In the decode
+    // variant each matrix has two accumulators taking alternate K steps, so
+    // consecutive MMAs of a thread do not wait on one another (the epilogue
+    // adds the two).  Per k-block: wait for the converters, four MMAs, a
+    // commit that frees the TMEM tile; per stage a commit that frees the
+    // shared-memory stage.
+    const int issuer = warp == 1 ? 0 : 1;
+    if (lane == 0) {
       int stage = 0, acc = 0, astage = 0;
       uint32_t phase = 0, acc_phase = 0, aphase = 0;
+      constexpr uint32_t kAStep = kNumA * (kBlockK / 2);  // TMEM columns of one expanded k-block
+      const uint32_t b_step = b_tile_bytes >> 4;          // descriptor address units per k-block of a stage
+      bool ok = true;
+      while (ok) {
+        int u;
+        if (!ring_take(u) || u < 0) break;
+        const Unit U = unit_at(p, u);
+        const uint32_t idesc = idesc_f16_f32(kBlockM, static_cast<uint32_t>((U.n + 15) & ~15));
+        if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1u, p.timeout_ns, abort_flag, p.status, kWhereMmaAccEmpty))
+          break;
+        tc_fence_after();
+        const uint32_t d = tmem_base + static_cast<uint32_t>(acc) * p.acc_cols + static_cast<uint32_t>(issuer * p.nmax);
+        const uint32_t d_odd = kDec ? d + static_cast<uint32_t>(2 * p.nmax) : d;
+        for (int kb = U.kb0; kb < U.kb1 && ok; kb += S) {
+          const uint64_t db0 = sdesc_k_sw128(smem_u32(b_tile(stage)));
+          for (int sub = 0; sub < S; ++sub) {
+            if (!mbar_wait(&afull[astage], aphase, p.timeout_ns, abort_flag, p.status, kWhereMmaFull)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint64_t db = db0 + static_cast<uint64_t>(sub) * b_step;
+            const uint32_t ta = tmem_base + p.a_col0 + static_cast<uint32_t>(astage) * kAStep +
+                                static_cast<uint32_t>(issuer * (kBlockK / 2));
+            const uint32_t first = (kb + sub == U.kb0) ? 1u : 0u;  // the unit's first k-block starts the sum
+            mma_f16_ts(d, ta, db, idesc, first ^ 1u);
+            mma_f16_ts(d_odd, ta + 8u, db + 2u, idesc, kDec ? (first ^ 1u) : 1u);
+            mma_f16_ts(d, ta + 16u, db + 4u, idesc, 1u);
+            mma_f16_ts(d_odd, ta + 24u, db + 6u, idesc, 1u);
+            mma_commit(&aempty[astage]);  // the TMEM tile is free once these MMAs complete
+            if (++astage == p.a_stages) {
+              astage = 0;
+              aphase ^= 1u;
+            }
+          }
+          if (!ok) break;
+          mma_commit(&empty[stage]);  // the stage is free once its last k-block's MMAs complete
+          if (++stage == p.stages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit(&acc_full[acc]);
+        if (++acc == p.acc_stages) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      // Every MMA issued by this thread has completed before TMEM is freed.
+      mma_commit(drain);
+      mbar_wait(drain, 0, p.timeout_ns, nullptr, p.status, kWhereDrain);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && rank == 0) {
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
       while (ok) {
         int u;
         if (!ring_take(u) || u < 0) break;
         const Unit U = unit_at(p, u);
         const uint32_t n_mma = static_cast<uint32_t>((U.n + 15) & ~15);
-        const uint32_t idesc = kFp8   ? idesc_e4m3_f32(kPair ? 2 * kBlockM : kBlockM, n_mma)
-                               : kFp4 ? idesc_f16_f32(kBlockM, n_mma)
-                                      : idesc_bf16_f32(kPair ? 2 * kBlockM : kBlockM, n_mma);
+        const uint32_t idesc = kFp8 ? idesc_e4m3_f32(kPair ? 2 * kBlockM : kBlockM, n_mma)
+                                    : idesc_bf16_f32(kPair ? 2 * kBlockM : kBlockM, n_mma);
         if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1u, p.timeout_ns, abort_flag, p.status, kWhereMmaAccEmpty))
           break;
         tc_fence_after();
         const uint32_t d0 = tmem_base + static_cast<uint32_t>(acc) * p.acc_cols;
         const uint32_t d1 = d0 + static_cast<uint32_t>(p.nmax);
         for (int kb = U.kb0; kb < U.kb1; ++kb) {
-          // BF16: the TMA bytes of the stage.  NVFP4: the converters' BF16
-          // tile in TMEM; they arrive after observing the stage's TMA bytes.
-          if (!mbar_wait(kFp4 ? &afull[astage] : &full[stage], kFp4 ? aphase : phase, p.timeout_ns, abort_flag,
-                         p.status, kWhereMmaFull)) {
+          if (!mbar_wait(&full[stage], phase, p.timeout_ns, abort_flag, p.status, kWhereMmaFull)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint64_t db = sdesc_k_sw128(smem_u32(b_tile(stage)));
-          if (kFp4) {
-            const uint32_t ta = tmem_base + p.a_col0 + static_cast<uint32_t>(astage * kNumA * (kBlockK / 2));
-#pragma unroll
-            for (int k = 0; k < kBlockK / 16; ++k) {
-              const uint32_t accumulate = (kb != U.kb0 || k != 0) ? 1u : 0u;
-              mma_f16_ts(issuer == 0 ? d0 : d1, ta + static_cast<uint32_t>(issuer * (kBlockK / 2)) + 8u * k,
-                          db + 2u * k, idesc, accumulate);
-            }
-          } else {
+          {
             const uint64_t da0 = sdesc_k_sw128(smem_u32(a_tile(stage, 0)));
             const uint64_t da1 = sdesc_k_sw128(smem_u32(a_tile(stage, kNumA - 1)));
 #pragma unroll
@@ -434,10 +512,6 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
             mma_commit(&empty[stage]);
           stage = stage + 1 == p.stages ? 0 : stage + 1;
           phase ^= stage == 0 ? 1u : 0u;
-          if (kFp4) {
-            astage = astage + 1 == p.a_stages ? 0 : astage + 1;
-            aphase ^= astage == 0 ? 1u : 0u;
-          }
         }
         if (!ok) break;
         if (kPair)
@@ -529,7 +603,7 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
       //    chunks), 2) release the accumulator so the next unit's MMAs start,
       //    3) global stores.
       // this warp's 16-column chunks: columns / (kEpiHalves x 16)
-      constexpr int kMaxChunks = (kDec ? 64 : (kFp4 ? kChunkRowsFp4 : kChunkRowsBf16)) / (16 * kEpiHalves);
+      constexpr int kMaxChunks = (kDec ? kDecChunkRows : (kFp4 ? kChunkRowsFp4 : kChunkRowsBf16)) / (16 * kEpiHalves);
       uint32_t hp[kOut][kMaxChunks][8];
 #pragma unroll
       for (int ci = 0; ci < kMaxChunks; ++ci) {
@@ -538,6 +612,17 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
           float g[16], g2[16];
           tmem_ld16(tbase + static_cast<uint32_t>(c0), g);
           if (kNumA == 2) tmem_ld16(tbase + static_cast<uint32_t>(p.nmax + c0), g2);
+          if (kDec) {  // the odd-K-step accumulators of both matrices
+            float o[16], o2[16];
+            tmem_ld16(tbase + static_cast<uint32_t>(2 * p.nmax + c0), o);
+            tmem_ld16(tbase + static_cast<uint32_t>(3 * p.nmax + c0), o2);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              g[j] += o[j];
+              g2[j] += o2[j];
+            }
+          }
           tmem_ld_wait();
           if (kFp8 || kFp4) {
             // token row scales of these 16 columns (FP8: the E4M3 rows';
@@ -609,8 +694,8 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
   } else if (kFp4 && warp < kMma2Warp) {
     // ------------------------------------------------------------ converters
     // Warp w may write TMEM lanes 32*(w%4)..+31, so its lane i expands weight
-    // row 32*(w%4)+i.  Warps 10-13 take the even k-blocks (counted over all
-    // units), warps 14-17 the odd ones, so two k-blocks are expanded at once;
+    // row 32*(w%4)+i.  The converter groups (4 warps each) take the k-blocks
+    // in turn (counted over all units), so G k-blocks are expanded at once;
     // a thread expands its row of every weight matrix of the unit (gate and
     // up, or down): 64 K elements = 32 TMEM columns each.
     const int cw = warp - (2 + kEpi);
@@ -618,29 +703,46 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
     const int row = quarter * 32 + lane;
     const int group = cw >> 2;
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
-    // This group's k-blocks i = group, group+G, ... (G = kGroups): smem stage
-    // / phase of i, TMEM tile of i, and smem stage / phase of i - a_stages (the
-    // k-block that last read that tile; its empty barrier completing frees the
-    // tile).  The host keeps G <= a_stages <= stages.
-    int stage = group, astage = group;
-    uint32_t phase = 0;
-    int rstage = group - p.a_stages + p.stages;
-    uint32_t rphase = 1;
-    int i = group;
-    int turn = 0;                       // k-blocks seen so far, modulo G
+    // This group's k-blocks: kb = group, group + G, ... of every unit (G =
+    // kGroups; the same split in every unit, so a unit's sums do not depend
+    // on which units the CTA ran before).  For the CTA's running k-block
+    // index i: the stage holding it (S k-blocks per stage), its phase and its
+    // place `sub` in the stage; its TMEM tile (i mod a_stages) and the parity
+    // of that tile's previous release (aempty: the MMAs of k-block
+    // i - a_stages completed; the MMA threads issue the k-blocks in order, so
+    // the release of k-block i - 2*a_stages has completed by then and the
+    // wait cannot be mistaken for it).  The host keeps G <= a_stages.
+    int sub = 0, stage = 0, astage = 0, i = 0;
+    uint32_t phase = 0, aphase = 1;
+    auto advance_to = [&](int target) {  // target >= i
+      const int by = target - i;
+      sub += by;
+      while (sub >= S) {
+        sub -= S;
+        if (++stage == p.stages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      astage += by;
+      while (astage >= p.a_stages) {
+        astage -= p.a_stages;
+        aphase ^= 1u;
+      }
+      i = target;
+    };
+    int unit_base = 0;  // running index of the current unit's first k-block
     bool ok = true;
     while (ok) {
       int u;
       if (!warp_take(u) || u < 0) break;
-      for (int kb = 0; kb < p.k_blocks; ++kb) {
-        const bool mine = turn == group;
-        if (++turn == kGroups) turn = 0;
-        if (!mine) continue;
+      for (int kb = group; kb < p.k_blocks; kb += kGroups) {
+        advance_to(unit_base + kb);
         int good = 1;
         if (lane == 0)
           good = (mbar_wait(&full[stage], phase, p.timeout_ns, abort_flag, p.status, kWhereConvert) &&
                   (i < p.a_stages ||
-                   mbar_wait(&empty[rstage], rphase, p.timeout_ns, abort_flag, p.status, kWhereConvert)))
+                   mbar_wait(&aempty[astage], aphase, p.timeout_ns, abort_flag, p.status, kWhereConvert)))
                      ? 1
                      : 0;
         good = __shfl_sync(0xFFFFFFFFu, good, 0);
@@ -654,7 +756,7 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
         for (int mat = 0; mat < kNumA; ++mat) {
           // packed row: 32 bytes (64 elements); scale row: this k-block's 4
           // E4M3 codes at byte 4*(kb%4), one per 16 elements
-          const uint4* src = reinterpret_cast<const uint4*>(p_tile(stage, mat) + row * (kBlockK / 2));
+          const uint4* src = reinterpret_cast<const uint4*>(p_tile(stage, mat, sub) + row * (kBlockK / 2));
           const uint4 v0 = src[0], v1 = src[1];
           const uint32_t wv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
           const uint32_t sc4 =
@@ -674,17 +776,8 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&afull[astage]);
-        if ((stage += kGroups) >= p.stages) {
-          stage -= p.stages;
-          phase ^= 1u;
-        }
-        if ((astage += kGroups) >= p.a_stages) astage -= p.a_stages;
-        if ((rstage += kGroups) >= p.stages) {
-          rstage -= p.stages;
-          rphase ^= 1u;
-        }
-        i += kGroups;
       }
+      unit_base += p.k_blocks;
     }
   }
 
@@ -732,7 +825,7 @@ cudaError_t launch_one(const GemmMaps& maps, const GemmParams& p, int grid, size
 
 size_t gemm_smem_bytes(int stages, int acc_stages, size_t stage_bytes) {
   return 1024 + static_cast<size_t>(stages) * stage_bytes +
-         (2 * stages + 2 * kMaxAStages + 2 * acc_stages + 1 + 2 * kSchedRing) * 8 + kSchedRing * 4 + 16;
+         (2 * stages + 3 * kMaxAStages + 2 * acc_stages + 1 + 2 * kSchedRing) * 8 + kSchedRing * 4 + 16;
 }
 
 int gemm_pair_max_clusters(int mode, size_t smem_bytes) {

@@ -31,6 +31,7 @@ constexpr int kMaxAStages = 8;     // NVFP4: BF16 weight tiles in TMEM in flight
 constexpr int kMaxStages = 8;      // shared-memory ring depth
 constexpr int kChunkRowsBf16 = 256;  // routes per GEMM unit (BF16 weights)
 constexpr int kChunkRowsFp4 = 160;   // NVFP4: TMEM holds the accumulators and the weight tiles
+constexpr int kFp4SmallT = 256;      // NVFP4: up to this many tokens, the decode variant (chunks of kDecChunkRows)
 
 // ---------------------------------------------------------------------------
 // Argument checks shared by the entry points (api.cu)
@@ -78,7 +79,8 @@ struct GemmParams {
   uint32_t tmem_cols;           // TMEM columns allocated (power of two)
   int b_big_rows;               // rows of the bb box (the B tile's capacity: nmax, or nmax / 2 for CTA pairs)
   int a_tiled;                  // weights (codes, scales) in BEAM_LAYOUT_TILED: every box is one contiguous tile
-  int a_stages;                 // NVFP4: BF16 weight tiles in TMEM (ring depth)
+  int sub_blocks;               // NVFP4: k-blocks per pipeline stage (1, 2 or 4; divides k_blocks)
+  int a_stages;                 // NVFP4: FP16 weight tiles in TMEM (ring depth)
   uint32_t a_col0;              // NVFP4: first TMEM column of that ring
   int* sched;                   // unit counter (zeroed before the launch)
   __nv_bfloat16* out;           // h [R, I] or yr [R, H], perm order
@@ -104,10 +106,11 @@ struct GemmMaps {
 
 // Bytes of one pipeline stage: the activation boxes plus, for BF16 weights,
 // the weight tile(s), or for NVFP4 the packed tile(s) and scale tile(s) that
-// the converters expand into TMEM.
-__host__ __device__ inline size_t gemm_stage_bytes(int num_a, bool fp4, int nmax) {
-  const size_t b = static_cast<size_t>(nmax) * kBlockK * 2;
-  if (fp4) return b + static_cast<size_t>(num_a) * (kPackedTileBytes + kScaleTileBytes);
+// the converters expand into TMEM; NVFP4 stages may hold `sub` consecutive
+// k-blocks (activations and packed tiles of each, one scale tile per matrix).
+__host__ __device__ inline size_t gemm_stage_bytes(int num_a, bool fp4, int nmax, int sub = 1) {
+  const size_t b = static_cast<size_t>(sub) * nmax * kBlockK * 2;
+  if (fp4) return b + static_cast<size_t>(num_a) * (sub * kPackedTileBytes + kScaleTileBytes);
   return b + static_cast<size_t>(num_a) * kBlockM * kBlockK * 2;
 }
 
@@ -165,7 +168,7 @@ cudaError_t launch_rows_to_f16(void* h, int R, int I, float* hs, cudaStream_t st
 // chunks of at most 64 routes (4 epilogue warps, 12 converter warps)
 cudaError_t launch_gemm(int mode, bool fp4, bool pair, bool wide, bool fp8, bool dec, const GemmMaps& maps,
                         const GemmParams& p, int grid, size_t smem_bytes, cudaStream_t stream);
-constexpr int kDecChunkRows = 64;  // NVFP4 decode variant: routes per unit at most
+constexpr int kDecChunkRows = 16;  // NVFP4 decode variant: routes per unit at most
 size_t gemm_smem_bytes(int stages, int acc_stages, size_t stage_bytes);
 // Clusters of two CTAs of the pair kernel that can be resident at once (0: none).
 int gemm_pair_max_clusters(int mode, size_t smem_bytes);

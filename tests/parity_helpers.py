@@ -185,7 +185,9 @@ def rel_err(y_gpu: np.ndarray, y_ref: np.ndarray) -> float:
 
 def chunk_rows(T: int, w_dtype: str) -> int:
     """Routes per GEMM unit at most (the library's rule): a multiple of 32
-    covering T, capped at 256 (160 for NVFP4 weights)."""
+    covering T, capped at 256 (NVFP4 weights: 160; 16 up to T = 256)."""
+    if w_dtype == "nvfp4" and T <= 256:
+        return 16
     cap = 160 if w_dtype == "nvfp4" else 256
     return min(cap, (T + 31) // 32 * 32)
 

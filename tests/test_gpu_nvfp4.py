@@ -87,3 +87,58 @@ def test_fp16_activation_rows_against_the_oracle(T, H, I):
         ref = np.abs(y_ref[t]).max()
         err = np.abs(yg[t] - y_ref[t]).max() / ref
         assert err <= Y_TOL["nvfp4"], (t, err, ref)
+
+
+@pytest.mark.parametrize("T,H,I,hot", [(200, 512, 256, (3, 100)), (1, 256, 256, None), (96, 1024, 512, (7,)),
+                                       (256, 256, 768, None)])
+def test_tiled_weights_four_kblocks_per_stage(T, H, I, hot):
+    """Few tokens (chunks of at most 32 routes) with packed weights: each
+    pipeline stage carries four k-blocks (3-D boxes of consecutive tiles and
+    of the chunk's activation rows).  Same bits as the row-major weights (one
+    k-block per stage), and the oracle's output on a seeded routing whose hot
+    experts take every token (several chunks of one expert)."""
+    wl = inputs.workload("nvfp4", T=T, H=H, I=I, seed=300 + T)
+    dg = inputs.generate(wl, DEV)
+    sh = moe.shape(T, H, I)
+    packed = moe.pack_weights(sh, dg)
+    ids, w = seeded_routing(T, seed=T + 3, hot=hot)
+    ys = []
+    for wts in (dg, packed):
+        ws = moe.alloc_workspace(sh, "nvfp4")
+        y = torch.empty((T, H), dtype=torch.bfloat16, device=DEV)
+        moe.beam_moe_experts(sh, dg["x"], wts, ids.to(DEV), w.to(DEV), y, ws)
+        code, where = moe.beam_moe_read_device_status(ws)
+        assert code == 0, (code, where)
+        ys.append(y)
+    assert torch.equal(ys[0].view(torch.int16), ys[1].view(torch.int16))
+    y_ref = oracle_y(dg, np.arange(T), ids.numpy(), w.numpy().astype(np.float64))
+    err = float(np.abs(ys[1].cpu().double().numpy() - y_ref).max() / np.abs(y_ref).max())
+    assert err <= Y_TOL["nvfp4"], err
+
+
+@pytest.mark.parametrize("name", ["nvfp4_dec", "nvfp4"])
+def test_full_size_tiled_equals_rows(name):
+    """The full-size NVFP4 layers as the benchmark runs them (packed weights)
+    give the bits of the row-major weights, whose output the full-size parity
+    test checks against the oracle."""
+    wl = inputs.workload(name)
+    torch.cuda.empty_cache()
+    dg = inputs.generate(wl, DEV)
+    sh = moe.shape(wl.T, wl.H, wl.I)
+    packed = moe.pack_weights(sh, dg)
+    outs = []
+    for wts in (dg, packed):
+        ws = moe.alloc_workspace(sh, "nvfp4")
+        y = torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device=DEV)
+        ids = torch.empty((wl.T, 8), dtype=torch.int32, device=DEV)
+        w = torch.empty((wl.T, 8), dtype=torch.float32, device=DEV)
+        moe.beam_moe_forward(sh, dg["x"], dg["router_w"], None, wts, y, ids, w, ws)
+        code, where = moe.beam_moe_read_device_status(ws)
+        assert code == 0, (code, where)
+        outs.append((y, ids))
+        del ws
+    assert torch.equal(outs[0][1], outs[1][1])
+    assert torch.equal(outs[0][0].view(torch.int16), outs[1][0].view(torch.int16))
+    del dg, packed, outs
+    gc.collect()
+    torch.cuda.empty_cache()

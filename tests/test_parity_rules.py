@@ -154,4 +154,5 @@ def test_full_size_tokens_cover_experts_and_hot_chunks():
 
 def test_chunk_rows_rule():
     assert chunk_rows(64, "bf16") == 64 and chunk_rows(8192, "bf16") == 256
-    assert chunk_rows(4096, "nvfp4") == 160 and chunk_rows(64, "nvfp4") == 64 and chunk_rows(1, "fp8") == 32
+    assert chunk_rows(4096, "nvfp4") == 160 and chunk_rows(64, "nvfp4") == 16 and chunk_rows(1, "fp8") == 32
+    assert chunk_rows(257, "nvfp4") == 160 and chunk_rows(64, "bf16") == 64

@@ -28,7 +28,7 @@ __all__ = [
     "ForwardCall", "STAGES", "beam_moe_stage_kernel_count", "beam_moe_route_noalloc", "pack_weights",
     "BEAM_LAYOUT_ROWS", "BEAM_LAYOUT_TILED",
     "beam_moe_read_device_status", "beam_moe_debug_timeout", "beam_debug_nvfp4_expand", "beam_status_string", "BeamMoE",
-    "library_path", "load", "BEAM_F32", "BEAM_BF16", "BEAM_NVFP4", "BEAM_FP8",
+    "library_path", "load", "load_debug", "BEAM_F32", "BEAM_BF16", "BEAM_NVFP4", "BEAM_FP8",
     "beam_moe_forward_residual", "GraphedForward",
     "DenseShape", "dense_shape", "dense_workspace_size", "dense_kernel_count", "beam_dense_mlp_forward",
     "dense_pack_weights", "DenseMLP",
@@ -96,14 +96,11 @@ def library_path() -> str:
     return _LIB_PATH
 
 
-def load():
-    """Load libbeam_moe.so (built in-tree by ``__graft_entry__.build()``)."""
-    global _lib
-    if _lib is not None:
-        return _lib
-    if not os.path.exists(_LIB_PATH):
-        raise ImportError(f"{_LIB_PATH} is missing: build the CUDA library first (__graft_entry__.build())")
-    lib = ctypes.CDLL(_LIB_PATH)
+_LIB_DEBUG_PATH = os.path.join(_PKG, "libbeam_moe_debug.so")
+_lib_debug = None
+
+
+def _configure(lib):
     vp, sz, i32, u32 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_uint32
     sp = ctypes.POINTER(Shape)
     lib.beam_moe_workspace_size.argtypes = [sp, i32]
@@ -122,6 +119,8 @@ def load():
     lib.beam_moe_stage_kernel_count.restype = ctypes.c_int32
     lib.beam_moe_debug_timeout.argtypes = [vp, sz, u32, vp]
     lib.beam_debug_nvfp4_expand.argtypes = [vp, vp, i32, vp, vp]
+    lib.beam_moe_debug_build.argtypes = []
+    lib.beam_moe_debug_build.restype = ctypes.c_int32
     lib.beam_moe_pack_weights.argtypes = [sp, ctypes.POINTER(_ExpertWeights), ctypes.POINTER(_ExpertWeights), vp]
     dp = ctypes.POINTER(DenseShape)
     lib.beam_dense_workspace_size.argtypes = [dp, i32]
@@ -138,8 +137,30 @@ def load():
               "beam_moe_debug_timeout", "beam_debug_nvfp4_expand", "beam_dense_mlp_forward",
               "beam_dense_pack_weights"):
         getattr(lib, n).restype = i32
-    _lib = lib
     return lib
+
+
+def load():
+    """Load libbeam_moe.so (built in-tree by ``__graft_entry__.build()``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise ImportError(f"{_LIB_PATH} is missing: build the CUDA library first (__graft_entry__.build())")
+    _lib = _configure(ctypes.CDLL(_LIB_PATH))
+    return _lib
+
+
+def load_debug():
+    """Load libbeam_moe_debug.so, the build with device-side checks of every
+    workspace index (same C ABI; ``beam_moe_debug_build()`` returns 1)."""
+    global _lib_debug
+    if _lib_debug is not None:
+        return _lib_debug
+    if not os.path.exists(_LIB_DEBUG_PATH):
+        raise ImportError(f"{_LIB_DEBUG_PATH} is missing: build it first (__graft_entry__.build())")
+    _lib_debug = _configure(ctypes.CDLL(_LIB_DEBUG_PATH))
+    return _lib_debug
 
 
 # --------------------------------------------------------------------------

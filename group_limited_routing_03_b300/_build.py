@@ -1,8 +1,10 @@
-"""Compile the CUDA sources in ``csrc/`` into ``libbeam_moe.so`` (in-tree).
+"""Compile the CUDA sources in ``csrc/`` into ``libbeam_moe.so`` (in-tree),
+and with ``debug=True`` into ``libbeam_moe_debug.so`` (BEAM_DEBUG=1: device
+checks of every index a kernel takes from the workspace).
 
 nvcc cross-compiles for sm_103a (B300) without a GPU.  Objects go to
-``_build/`` next to this file; the shared library is written next to this
-file so that it travels with the package.
+``_build/`` (``_build_debug/``) next to this file; the shared libraries are
+written next to this file so that they travel with the package.
 """
 from __future__ import annotations
 
@@ -17,6 +19,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libbeam_moe.so")
+BUILD_DEBUG = os.path.join(PKG, "_build_debug")
+LIB_DEBUG = os.path.join(PKG, "libbeam_moe_debug.so")
 
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",
@@ -50,14 +54,18 @@ def _stale(target, deps):
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Build (if stale) and return the path of libbeam_moe.so."""
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=(), debug: bool = False) -> str:
+    """Build (if stale) and return the path of libbeam_moe.so (debug=True:
+    libbeam_moe_debug.so)."""
+    build_dir, lib_path = (BUILD_DEBUG, LIB_DEBUG) if debug else (BUILD, LIB)
+    if debug:
+        extra_flags = (*extra_flags, "-DBEAM_DEBUG=1")
+    os.makedirs(build_dir, exist_ok=True)
     nvcc = _nvcc()
     hdrs = _headers()
     objs, jobs = [], []
     for src in sources():
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         objs.append(obj)
         if force or _stale(obj, [src] + hdrs):
             cmd = [nvcc, *NVCC_FLAGS, *extra_flags, "-I", INCLUDE, "-I", CSRC, "-c", src, "-o", obj]
@@ -74,14 +82,15 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     if jobs:
         with cf.ThreadPoolExecutor(max_workers=min(len(jobs), os.cpu_count() or 4)) as ex:
             list(ex.map(run, jobs))
-    if force or jobs or _stale(LIB, objs):
-        tmp = LIB + f".tmp{os.getpid()}"
+    if force or jobs or _stale(lib_path, objs):
+        tmp = lib_path + f".tmp{os.getpid()}"
         run([nvcc, "-shared", *NVCC_FLAGS[:2], "-o", tmp, *objs])
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":
     import sys
 
     print(build(force="--force" in sys.argv, verbose=True))
+    print(build(force="--force" in sys.argv, verbose=True, debug=True))

@@ -21,6 +21,11 @@ namespace beam {
 namespace {
 
 constexpr uint64_t kDefaultTimeoutNs = 1000000000ull;  // 1 s per bounded wait
+#if defined(BEAM_DEBUG) && BEAM_DEBUG
+constexpr bool kDebugBuild = true;  // device checks of every workspace index (see tc.cuh)
+#else
+constexpr bool kDebugBuild = false;
+#endif
 
 // ------------------------------------------------------------------ device
 struct DeviceInfo {
@@ -333,7 +338,7 @@ beam_status_t run_dispatch(const beam_moe_shape_t& s, const int32_t* ids, void* 
   }
   e = launch_dispatch(ids, R, L.n_tiles, at<int32_t>(ws, L.tile_hist), at<int32_t>(ws, L.counts),
                       at<int32_t>(ws, L.offsets), at<int32_t>(ws, L.chunk_prefix), nmax, at<int32_t>(ws, L.perm),
-                      at<int32_t>(ws, L.pos), stream);
+                      at<int32_t>(ws, L.pos), at<uint32_t>(ws, L.status), stream);
   return cuda_status(e);
 }
 
@@ -360,12 +365,12 @@ beam_status_t run_gather(const beam_moe_shape_t& s, const void* x, bool x_bf16, 
                          const Layout& L, const DeviceInfo& d, cudaStream_t stream) {
   if (wdtype == BEAM_FP8)
     return cuda_status(launch_gather_q8(x, x_bf16, s.H, at<int32_t>(ws, L.pos), s.T, at<uint8_t>(ws, L.xq),
-                                        at<float>(ws, L.xs), stream));
+                                        at<float>(ws, L.xs), at<uint32_t>(ws, L.status), stream));
   if (wdtype == BEAM_NVFP4)
     return cuda_status(launch_gather_f16(x, x_bf16, s.H, at<int32_t>(ws, L.pos), s.T, at<__half>(ws, L.xp),
-                                         at<float>(ws, L.xs), stream));
+                                         at<float>(ws, L.xs), at<uint32_t>(ws, L.status), stream));
   return cuda_status(launch_gather(x, x_bf16, s.H, at<int32_t>(ws, L.pos), s.T, at<__nv_bfloat16>(ws, L.xp), d.sms,
-                                   stream));
+                                   at<uint32_t>(ws, L.status), stream));
 }
 
 // mode 0: gate/up (+SwiGLU) -> h; mode 1: down -> yr.
@@ -644,6 +649,9 @@ beam_status_t run_gemm(int mode, const beam_moe_shape_t& s, const beam_expert_we
       return BEAM_ERR_CUDA;
   }
   if (cudaMemsetAsync(p.sched, 0, sizeof(int), stream) != cudaSuccess) return BEAM_ERR_CUDA;
+  if (kDebugBuild &&
+      launch_validate_schedule(io.counts, io.offsets, io.chunk_prefix, R, nmax, io.status, stream) != cudaSuccess)
+    return BEAM_ERR_CUDA;
   if (launch_gemm(mode, fp4, pair, wide, fp8, dec, maps, p, grid, smem, stream) != cudaSuccess) return BEAM_ERR_CUDA;
   if (k_splits > 1)
     return cuda_status(launch_splitk_finish(mode, io.partial, k_splits, R, p.out_ld, mode == 0 ? h : yr, stream));
@@ -653,7 +661,8 @@ beam_status_t run_gemm(int mode, const beam_moe_shape_t& s, const beam_expert_we
 beam_status_t run_combine(const beam_moe_shape_t& s, const float* w, void* y, bool y_bf16, void* ws, const Layout& L,
                           cudaStream_t stream) {
   return cuda_status(
-      launch_combine(at<__nv_bfloat16>(ws, L.yr), at<int32_t>(ws, L.pos), w, s.T, s.H, y, y_bf16, stream));
+      launch_combine(at<__nv_bfloat16>(ws, L.yr), at<int32_t>(ws, L.pos), w, s.T, s.H, y, y_bf16,
+                     at<uint32_t>(ws, L.status), stream));
 }
 
 beam_status_t run_experts(const beam_moe_shape_t& s, const void* x, bool x_bf16, const beam_expert_weights_t* wts,
@@ -695,7 +704,7 @@ beam_status_t run_combine_residual(const beam_moe_shape_t& s, const float* w, co
   r.keep = static_cast<float>(std::sqrt(static_cast<double>(res.step - 1) / res.step));
   r.add = static_cast<float>(1.0 / std::sqrt(static_cast<double>(res.step)));
   return cuda_status(launch_combine_residual(at<__nv_bfloat16>(ws, L.yr), at<int32_t>(ws, L.pos), w, s.T, s.H, r, y,
-                                             bf16, stream));
+                                             bf16, at<uint32_t>(ws, L.status), stream));
 }
 
 // Validation shared by beam_moe_forward, beam_moe_forward_stage and
@@ -909,9 +918,10 @@ int32_t beam_moe_stage_kernel_count(const beam_moe_shape_t* shape, beam_dtype_t 
       return sp > 1 ? 2 : 1;
     }
     case BEAM_STAGE_DISPATCH: return 2;
-    case BEAM_STAGE_DOWN: return wdtype == BEAM_BF16 ? 1 : 2;  // FP8 / NVFP4: h's rows converted first
+    // FP8 / NVFP4: h's rows converted first; debug builds check the schedule before each GEMM
+    case BEAM_STAGE_DOWN: return (wdtype == BEAM_BF16 ? 1 : 2) + (kDebugBuild ? 1 : 0);
+    case BEAM_STAGE_GATE_UP: return 1 + (kDebugBuild ? 1 : 0);
     case BEAM_STAGE_GATHER:
-    case BEAM_STAGE_GATE_UP:
     case BEAM_STAGE_COMBINE: return 1;
     default: return -1;
   }
@@ -1007,6 +1017,7 @@ int32_t beam_dense_kernel_count(const beam_dense_shape_t* shape, beam_dtype_t wd
   const int nmax = chunk_rows(shape->T, fp4);
   const int chunks = (shape->T + nmax - 1) / nmax;
   int n = 1 + 1 + 1;        // schedule, gate/up, down
+  if (kDebugBuild) n += 2;  // the schedule checked before each GEMM
   if (fp8 || fp4) n += 2;   // x and h rows converted (E4M3 codes / FP16)
   for (int mode = 0; mode < 2; ++mode)
     if (choose_gemm(mode, ms, fp4, fp8, nmax, chunks, d).k_splits > 1) n += 1;  // the finishing kernel
@@ -1065,11 +1076,13 @@ beam_status_t beam_dense_mlp_forward(const beam_dense_shape_t* shape, const void
   io.partial = at<float>(ws, L.partial);
   if (launch_dense_dispatch(io.R, io.nmax, io.counts, io.offsets, io.chunk_prefix, cs) != cudaSuccess)
     return BEAM_ERR_CUDA;
-  if (fp8 && launch_gather_q8(x, xdtype == BEAM_BF16, shape->H, nullptr, shape->T, io.xq, io.xs, cs) != cudaSuccess)
+  if (fp8 && launch_gather_q8(x, xdtype == BEAM_BF16, shape->H, nullptr, shape->T, io.xq, io.xs, io.status, cs) !=
+                 cudaSuccess)
     return BEAM_ERR_CUDA;
   if (weights->dtype == BEAM_NVFP4) {  // x as FP16 rows times a power of two
     io.xp = at<__half>(ws, L.x16);
-    if (launch_gather_f16(x, true, shape->H, nullptr, shape->T, at<__half>(ws, L.x16), io.xs, cs) != cudaSuccess)
+    if (launch_gather_f16(x, true, shape->H, nullptr, shape->T, at<__half>(ws, L.x16), io.xs, io.status, cs) !=
+        cudaSuccess)
       return BEAM_ERR_CUDA;
   }
   st = run_gemm(0, ms, weights, io, d, cs);
@@ -1084,6 +1097,8 @@ beam_status_t beam_moe_debug_timeout(void* workspace, size_t workspace_bytes, ui
   return cuda_status(launch_debug_timeout(static_cast<uint32_t*>(workspace), static_cast<uint64_t>(timeout_us) * 1000ull,
                                           static_cast<cudaStream_t>(stream)));
 }
+
+int32_t beam_moe_debug_build(void) { return kDebugBuild ? 1 : 0; }
 
 const char* beam_status_string(beam_status_t status) {
   switch (status) {

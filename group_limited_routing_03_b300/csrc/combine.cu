@@ -17,13 +17,17 @@ namespace {
 
 template <bool kBf16Out>
 __global__ void __launch_bounds__(128) combine_kernel(const __nv_bfloat16* yr, const int32_t* pos, const float* w,
-                                                      int H, void* y) {
+                                                      int H, void* y, uint32_t* status) {
   __shared__ int ps[kTopK];
   __shared__ float ws[kTopK];
   const int t = blockIdx.x;
 
   if (threadIdx.x < kTopK) {
-    ps[threadIdx.x] = pos[static_cast<size_t>(t) * kTopK + threadIdx.x];
+    int q = pos[static_cast<size_t>(t) * kTopK + threadIdx.x];
+    // route rows: T * 8, one CTA row per token
+    if (q >= 0 && !dcheck(q < static_cast<int>(gridDim.x) * kTopK, blockIdx.y == 0 ? status : nullptr, kCheckCombinePos))
+      q = -1;
+    ps[threadIdx.x] = q;
     ws[threadIdx.x] = w[static_cast<size_t>(t) * kTopK + threadIdx.x];
   }
   __syncthreads();
@@ -76,7 +80,7 @@ __global__ void __launch_bounds__(128) combine_kernel(const __nv_bfloat16* yr, c
 template <bool kBf16, int kClusterY>
 __global__ void __launch_bounds__(128) combine_residual_kernel(const __nv_bfloat16* yr, const int32_t* pos,
                                                                const float* w, int H, ResidualParams r,
-                                                               void* y_out) {
+                                                               void* y_out, uint32_t* status) {
   extern __shared__ float4 ys4[];  // this CTA's part of y[t,:], 8 floats per group
   float* ys = reinterpret_cast<float*>(ys4);
   __shared__ int ps[kTopK];
@@ -88,7 +92,10 @@ __global__ void __launch_bounds__(128) combine_residual_kernel(const __nv_bfloat
   const int G = H / 8, step = kClusterY * 128;
 
   if (threadIdx.x < kTopK) {
-    ps[threadIdx.x] = pos[static_cast<size_t>(t) * kTopK + threadIdx.x];
+    int q = pos[static_cast<size_t>(t) * kTopK + threadIdx.x];
+    if (q >= 0 && !dcheck(q < static_cast<int>(gridDim.x) * kTopK, rank == 0 ? status : nullptr, kCheckResidualPos))
+      q = -1;
+    ps[threadIdx.x] = q;
     ws[threadIdx.x] = w[static_cast<size_t>(t) * kTopK + threadIdx.x];
   }
   __syncthreads();
@@ -197,12 +204,12 @@ __global__ void debug_timeout_kernel(uint32_t* status, uint64_t timeout_ns) {
 }  // namespace
 
 cudaError_t launch_combine(const __nv_bfloat16* yr, const int32_t* pos, const float* w, int T, int H, void* y,
-                           bool y_bf16, cudaStream_t stream) {
+                           bool y_bf16, uint32_t* status, cudaStream_t stream) {
   const dim3 grid(T, T >= 1024 ? 1 : (H / 8 + 127) / 128);
   if (y_bf16)
-    combine_kernel<true><<<grid, 128, 0, stream>>>(yr, pos, w, H, y);
+    combine_kernel<true><<<grid, 128, 0, stream>>>(yr, pos, w, H, y, status);
   else
-    combine_kernel<false><<<grid, 128, 0, stream>>>(yr, pos, w, H, y);
+    combine_kernel<false><<<grid, 128, 0, stream>>>(yr, pos, w, H, y, status);
   return cudaGetLastError();
 }
 
@@ -223,7 +230,7 @@ size_t residual_smem_bytes(int T, int H) {
 namespace {
 template <bool kBf16, int kCY>
 cudaError_t launch_residual_t(const __nv_bfloat16* yr, const int32_t* pos, const float* w, int T, int H,
-                              const ResidualParams& r, void* y_out, size_t smem, cudaStream_t stream) {
+                              const ResidualParams& r, void* y_out, uint32_t* status, size_t smem, cudaStream_t stream) {
   auto kern = combine_residual_kernel<kBf16, kCY>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (err != cudaSuccess) return err;
@@ -239,28 +246,29 @@ cudaError_t launch_residual_t(const __nv_bfloat16* yr, const int32_t* pos, const
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = kCY > 1 ? 1 : 0;
-  err = cudaLaunchKernelEx(&cfg, kern, yr, pos, w, H, r, y_out);
+  err = cudaLaunchKernelEx(&cfg, kern, yr, pos, w, H, r, y_out, status);
   if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
 
 template <bool kBf16>
 cudaError_t launch_residual_d(const __nv_bfloat16* yr, const int32_t* pos, const float* w, int T, int H,
-                              const ResidualParams& r, void* y_out, cudaStream_t stream) {
+                              const ResidualParams& r, void* y_out, uint32_t* status, cudaStream_t stream) {
   const size_t smem = residual_smem_bytes(T, H);
   switch (residual_cluster_y(T, H)) {
-    case 1: return launch_residual_t<kBf16, 1>(yr, pos, w, T, H, r, y_out, smem, stream);
-    case 2: return launch_residual_t<kBf16, 2>(yr, pos, w, T, H, r, y_out, smem, stream);
-    case 4: return launch_residual_t<kBf16, 4>(yr, pos, w, T, H, r, y_out, smem, stream);
-    default: return launch_residual_t<kBf16, 8>(yr, pos, w, T, H, r, y_out, smem, stream);
+    case 1: return launch_residual_t<kBf16, 1>(yr, pos, w, T, H, r, y_out, status, smem, stream);
+    case 2: return launch_residual_t<kBf16, 2>(yr, pos, w, T, H, r, y_out, status, smem, stream);
+    case 4: return launch_residual_t<kBf16, 4>(yr, pos, w, T, H, r, y_out, status, smem, stream);
+    default: return launch_residual_t<kBf16, 8>(yr, pos, w, T, H, r, y_out, status, smem, stream);
   }
 }
 }  // namespace
 
 cudaError_t launch_combine_residual(const __nv_bfloat16* yr, const int32_t* pos, const float* w, int T, int H,
-                                    const ResidualParams& r, void* y_out, bool bf16, cudaStream_t stream) {
-  return bf16 ? launch_residual_d<true>(yr, pos, w, T, H, r, y_out, stream)
-              : launch_residual_d<false>(yr, pos, w, T, H, r, y_out, stream);
+                                    const ResidualParams& r, void* y_out, bool bf16, uint32_t* status,
+                                    cudaStream_t stream) {
+  return bf16 ? launch_residual_d<true>(yr, pos, w, T, H, r, y_out, status, stream)
+              : launch_residual_d<false>(yr, pos, w, T, H, r, y_out, status, stream);
 }
 
 cudaError_t launch_debug_timeout(uint32_t* status, uint64_t timeout_ns, cudaStream_t stream) {

@@ -63,7 +63,7 @@ __global__ void __launch_bounds__(256) tile_hist_kernel(const int32_t* ids, int 
     if (e >= 0 && e < kExperts)
       atomicAdd(&hist[e], 1);
     else
-      report_status(status, kStatusDeviceCheck, 20);
+      report_status(status, kStatusDeviceCheck, kCheckTileHistId);
   }
   __syncthreads();
   tile_hist[static_cast<size_t>(threadIdx.x) * n_tiles + blockIdx.x] = hist[threadIdx.x];
@@ -90,7 +90,7 @@ __global__ void __launch_bounds__(256) scan_kernel(int32_t* tile_hist, int n_til
 __global__ void __launch_bounds__(256) scatter_kernel(const int32_t* ids, int R, int n_tiles,
                                                       const int32_t* tile_prefix, const int32_t* counts,
                                                       int nmax, int32_t* offsets, int32_t* chunk_prefix,
-                                                      int32_t* perm, int32_t* pos) {
+                                                      int32_t* perm, int32_t* pos, uint32_t* status) {
   __shared__ int warp_sums[8];
   __shared__ int total;
   __shared__ int off_s[kExperts];
@@ -116,7 +116,10 @@ __global__ void __launch_bounds__(256) scatter_kernel(const int32_t* ids, int R,
   const int r = tile * kTileRoutes + tid;
   const bool valid = r < R;
   int e = valid ? ids[r] : -1;
-  if (e < 0 || e >= kExperts) e = -1;
+  if (e < 0 || e >= kExperts) {
+    if (valid) dcheck(false, status, kCheckScatterId);
+    e = -1;
+  }
   const unsigned peers = __match_any_sync(0xFFFFFFFFu, e);
   const unsigned lt = (1u << lane) - 1u;
   const int rank_in_warp = __popc(peers & lt);
@@ -139,7 +142,8 @@ __global__ void __launch_bounds__(256) scatter_kernel(const int32_t* ids, int R,
 // expert id was out of range, are skipped); 8 elements (16 bytes) per step.
 template <bool kBf16>
 __global__ void __launch_bounds__(256) gather_kernel(const void* x, int H, const int32_t* pos, int T,
-                                                     __nv_bfloat16* xp) {
+                                                     __nv_bfloat16* xp, uint32_t* status) {
+  const int R = T * kTopK;
   const int vecs_per_row = H / 8;
   const size_t n = static_cast<size_t>(T) * vecs_per_row;
 #pragma unroll 2
@@ -165,7 +169,8 @@ __global__ void __launch_bounds__(256) gather_kernel(const void* x, int H, const
     const int dst[kTopK] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
 #pragma unroll
     for (int k = 0; k < kTopK; ++k)
-      if (dst[k] >= 0) *reinterpret_cast<uint4*>(xp + static_cast<size_t>(dst[k]) * H + c * 8) = out;
+      if (dst[k] >= 0 && dcheck(dst[k] < R, status, kCheckGatherPos))
+        *reinterpret_cast<uint4*>(xp + static_cast<size_t>(dst[k]) * H + c * 8) = out;
   }
 }
 
@@ -179,10 +184,10 @@ cudaError_t launch_tile_hist(const int32_t* ids, int R, int n_tiles, int32_t* ti
 
 cudaError_t launch_dispatch(const int32_t* ids, int R, int n_tiles, int32_t* tile_hist, int32_t* counts,
                             int32_t* offsets, int32_t* chunk_prefix, int nmax, int32_t* perm, int32_t* pos,
-                            cudaStream_t stream) {
+                            uint32_t* status, cudaStream_t stream) {
   scan_kernel<<<kExperts, 256, 0, stream>>>(tile_hist, n_tiles, counts);
   scatter_kernel<<<n_tiles, 256, 0, stream>>>(ids, R, n_tiles, tile_hist, counts, nmax, offsets,
-                                              chunk_prefix, perm, pos);
+                                              chunk_prefix, perm, pos, status);
   return cudaGetLastError();
 }
 
@@ -199,6 +204,40 @@ __global__ void __launch_bounds__(288) dense_dispatch_kernel(int R, int nmax, in
 }
 }  // namespace
 
+namespace {
+// Debug builds, before each grouped GEMM: the schedule the GEMM will read
+// must describe R routes in order -- counts >= 0, offsets the exclusive
+// prefix sum of counts ending at most at R, chunk_prefix the prefix sum of
+// ceil(count / nmax).  If it does not, the check is recorded and
+// chunk_prefix[E] is set to 0, so that the GEMM runs no unit (it would
+// otherwise store outside the route rows).
+__global__ void __launch_bounds__(kExperts) validate_schedule_kernel(const int32_t* counts, const int32_t* offsets,
+                                                                     int32_t* chunk_prefix, int R, int nmax,
+                                                                     uint32_t* status) {
+  __shared__ int bad;
+  const int e = threadIdx.x;
+  if (e == 0) bad = 0;
+  __syncthreads();
+  const int c = counts[e];
+  const int o0 = offsets[e], o1 = offsets[e + 1];
+  const int q0 = chunk_prefix[e], q1 = chunk_prefix[e + 1];
+  const bool ok = c >= 0 && o0 >= 0 && o1 == o0 + c && o1 <= R && (e != 0 || (o0 == 0 && q0 == 0)) &&
+                  q1 - q0 == (c + nmax - 1) / nmax;
+  if (!ok) atomicExch(&bad, 1);
+  __syncthreads();
+  if (e == 0 && bad != 0) {
+    report_status(status, kStatusDeviceCheck, kCheckSchedule);
+    chunk_prefix[kExperts] = 0;
+  }
+}
+}  // namespace
+
+cudaError_t launch_validate_schedule(const int32_t* counts, const int32_t* offsets, int32_t* chunk_prefix, int R,
+                                     int nmax, uint32_t* status, cudaStream_t stream) {
+  validate_schedule_kernel<<<1, kExperts, 0, stream>>>(counts, offsets, chunk_prefix, R, nmax, status);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_dense_dispatch(int R, int nmax, int32_t* counts, int32_t* offsets, int32_t* chunk_prefix,
                                   cudaStream_t stream) {
   dense_dispatch_kernel<<<1, 288, 0, stream>>>(R, nmax, counts, offsets, chunk_prefix);
@@ -206,16 +245,16 @@ cudaError_t launch_dense_dispatch(int R, int nmax, int32_t* counts, int32_t* off
 }
 
 cudaError_t launch_gather(const void* x, bool x_bf16, int H, const int32_t* pos, int T, __nv_bfloat16* xp,
-                          int num_sms, cudaStream_t stream) {
+                          int num_sms, uint32_t* status, cudaStream_t stream) {
   const size_t n = static_cast<size_t>(T) * (H / 8);
   size_t blocks = (n + 255) / 256;
   const size_t cap = static_cast<size_t>(num_sms) * 16;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   if (x_bf16)
-    gather_kernel<true><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(x, H, pos, T, xp);
+    gather_kernel<true><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(x, H, pos, T, xp, status);
   else
-    gather_kernel<false><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(x, H, pos, T, xp);
+    gather_kernel<false><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(x, H, pos, T, xp, status);
   return cudaGetLastError();
 }
 

@@ -139,18 +139,23 @@ cudaError_t launch_tile_hist(const int32_t* ids, int R, int n_tiles, int32_t* ti
                              uint32_t* status, cudaStream_t stream);
 cudaError_t launch_dispatch(const int32_t* ids, int R, int n_tiles, int32_t* tile_hist,
                             int32_t* counts, int32_t* offsets, int32_t* chunk_prefix, int nmax,
-                            int32_t* perm, int32_t* pos, cudaStream_t stream);
+                            int32_t* perm, int32_t* pos, uint32_t* status, cudaStream_t stream);
+// Debug builds, before each grouped GEMM: check the schedule (counts,
+// offsets, chunk prefix) describes R routes with chunks of nmax; if not,
+// record it in the status word and leave the GEMM no unit.
+cudaError_t launch_validate_schedule(const int32_t* counts, const int32_t* offsets, int32_t* chunk_prefix, int R,
+                                     int nmax, uint32_t* status, cudaStream_t stream);
 // Dense MLP: the unit schedule of one expert holding all R rows.
 cudaError_t launch_dense_dispatch(int R, int nmax, int32_t* counts, int32_t* offsets, int32_t* chunk_prefix,
                                   cudaStream_t stream);
 cudaError_t launch_gather(const void* x, bool x_bf16, int H, const int32_t* pos, int T,
-                          __nv_bfloat16* xp, int num_sms, cudaStream_t stream);
+                          __nv_bfloat16* xp, int num_sms, uint32_t* status, cudaStream_t stream);
 // FP8 weights: token rows (x in BF16 or FP32) to E4M3 codes in route order,
 // one FP32 scale per row (amax / 448, 1 for a zero row); every token's codes
 // are written to its 8 route rows (xq [R_pad, H], xs [R_pad]); pos == NULL
 // (dense MLP): row t to row t.
 cudaError_t launch_gather_q8(const void* x, bool x_bf16, int H, const int32_t* pos, int T, uint8_t* xq, float* xs,
-                             cudaStream_t stream);
+                             uint32_t* status, cudaStream_t stream);
 // FP8 weights: rows of h (BF16 [R, I]) to E4M3 codes hq [R_pad, I] and row
 // scales hs [R_pad], the same rule.
 cudaError_t launch_quantize_rows(const __nv_bfloat16* h, int R, int I, uint8_t* hq, float* hs, cudaStream_t stream);
@@ -159,7 +164,7 @@ cudaError_t launch_quantize_rows(const __nv_bfloat16* h, int R, int I, uint8_t* 
 // route order (xh [R_pad, H]), the inverse power of two per row in xs
 // [R_pad]; pos == NULL (dense MLP): row t to row t.  Exact (see quant.cu).
 cudaError_t launch_gather_f16(const void* x, bool x_bf16, int H, const int32_t* pos, int T, __half* xh, float* xs,
-                              cudaStream_t stream);
+                              uint32_t* status, cudaStream_t stream);
 // NVFP4 weights: rows of h (BF16 [R, I]) to FP16 in place, the same rule,
 // inverse scales in hs [R_pad].
 cudaError_t launch_rows_to_f16(void* h, int R, int I, float* hs, cudaStream_t stream);
@@ -173,7 +178,7 @@ size_t gemm_smem_bytes(int stages, int acc_stages, size_t stage_bytes);
 // Clusters of two CTAs of the pair kernel that can be resident at once (0: none).
 int gemm_pair_max_clusters(int mode, size_t smem_bytes);
 cudaError_t launch_combine(const __nv_bfloat16* yr, const int32_t* pos, const float* w, int T, int H,
-                           void* y, bool y_bf16, cudaStream_t stream);
+                           void* y, bool y_bf16, uint32_t* status, cudaStream_t stream);
 // K split: add the k_splits FP32 partial planes in part order; mode 0: h =
 // BF16(silu(sum gate) * sum up) [R, N]; mode 1: out = BF16(sum) [R, N].
 cudaError_t launch_splitk_finish(int mode, const float* partial, int k_splits, int R, int N, __nv_bfloat16* out,
@@ -186,7 +191,8 @@ struct ResidualParams {
   float eps, keep, add;
 };
 cudaError_t launch_combine_residual(const __nv_bfloat16* yr, const int32_t* pos, const float* w, int T, int H,
-                                    const ResidualParams& r, void* y_out, bool bf16, cudaStream_t stream);
+                                    const ResidualParams& r, void* y_out, bool bf16, uint32_t* status,
+                                    cudaStream_t stream);
 // Row split (CTAs per token, one cluster) and dynamic shared memory of the
 // fused kernel.
 int residual_cluster_y(int T, int H);

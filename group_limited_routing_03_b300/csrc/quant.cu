@@ -32,6 +32,7 @@
 #include <cuda_fp8.h>
 
 #include "moe_internal.cuh"
+#include "tc.cuh"
 
 namespace beam {
 namespace {
@@ -100,7 +101,7 @@ __device__ __forceinline__ uint4 codes16(const void* row, int g, float s) {
 // range (pos < 0); 1 for the dense MLP, row t).
 template <bool kBf16, int kRoutes>
 __global__ void __launch_bounds__(32 * kWarpsPerCta) gather_q8_kernel(const void* x, int H, const int32_t* pos,
-                                                                      int T, uint8_t* xq, float* xs) {
+                                                                      int T, uint8_t* xq, float* xs, uint32_t* status) {
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= T) return;
@@ -110,7 +111,10 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta) gather_q8_kernel(const void
   const float s = row_scale<kBf16>(row, groups, lane);
   int p[kRoutes];
 #pragma unroll
-  for (int k = 0; k < kRoutes; ++k) p[k] = kRoutes == 1 ? t : __ldg(&pos[static_cast<size_t>(t) * kTopK + k]);
+  for (int k = 0; k < kRoutes; ++k) {
+    p[k] = kRoutes == 1 ? t : __ldg(&pos[static_cast<size_t>(t) * kTopK + k]);
+    if (p[k] >= 0 && !dcheck(p[k] < T * kRoutes, lane == 0 ? status : nullptr, kCheckQ8Pos)) p[k] = -1;
+  }
   if (lane < kRoutes && p[lane] >= 0) xs[p[lane]] = s;
   for (int g = lane; g < groups; g += 32) {
     const uint4 c = codes16<kBf16>(row, g, s);
@@ -187,7 +191,7 @@ __device__ __forceinline__ void f16x16(const void* row, int g, float up, uint4& 
 // are skipped; kRoutes = 1: row t), its row scale 2^-k beside them.
 template <bool kBf16, int kRoutes>
 __global__ void __launch_bounds__(32 * kWarpsPerCta) gather_f16_kernel(const void* x, int H, const int32_t* pos,
-                                                                       int T, __half* xh, float* xs) {
+                                                                       int T, __half* xh, float* xs, uint32_t* status) {
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= T) return;
@@ -198,7 +202,10 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta) gather_f16_kernel(const voi
   const float up = pow2f(k);
   int p[kRoutes];
 #pragma unroll
-  for (int r = 0; r < kRoutes; ++r) p[r] = kRoutes == 1 ? t : __ldg(&pos[static_cast<size_t>(t) * kTopK + r]);
+  for (int r = 0; r < kRoutes; ++r) {
+    p[r] = kRoutes == 1 ? t : __ldg(&pos[static_cast<size_t>(t) * kTopK + r]);
+    if (p[r] >= 0 && !dcheck(p[r] < T * kRoutes, lane == 0 ? status : nullptr, kCheckF16Pos)) p[r] = -1;
+  }
   if (lane < kRoutes && p[lane] >= 0) xs[p[lane]] = pow2f(-k);
   for (int g = lane; g < groups; g += 32) {
     uint4 lo, hi;
@@ -237,19 +244,19 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta) rows_to_f16_kernel(void* h,
 }  // namespace
 
 cudaError_t launch_gather_f16(const void* x, bool x_bf16, int H, const int32_t* pos, int T, __half* xh, float* xs,
-                              cudaStream_t stream) {
+                              uint32_t* status, cudaStream_t stream) {
   const int warps = T <= 4096 ? 2 : kWarpsPerCta;
   const int grid = (T + warps - 1) / warps;
   const int threads = 32 * warps;
   if (pos == nullptr) {  // dense MLP: row t to row t
     if (x_bf16)
-      gather_f16_kernel<true, 1><<<grid, threads, 0, stream>>>(x, H, pos, T, xh, xs);
+      gather_f16_kernel<true, 1><<<grid, threads, 0, stream>>>(x, H, pos, T, xh, xs, status);
     else
-      gather_f16_kernel<false, 1><<<grid, threads, 0, stream>>>(x, H, pos, T, xh, xs);
+      gather_f16_kernel<false, 1><<<grid, threads, 0, stream>>>(x, H, pos, T, xh, xs, status);
   } else if (x_bf16) {
-    gather_f16_kernel<true, kTopK><<<grid, threads, 0, stream>>>(x, H, pos, T, xh, xs);
+    gather_f16_kernel<true, kTopK><<<grid, threads, 0, stream>>>(x, H, pos, T, xh, xs, status);
   } else {
-    gather_f16_kernel<false, kTopK><<<grid, threads, 0, stream>>>(x, H, pos, T, xh, xs);
+    gather_f16_kernel<false, kTopK><<<grid, threads, 0, stream>>>(x, H, pos, T, xh, xs, status);
   }
   return cudaGetLastError();
 }
@@ -261,20 +268,20 @@ cudaError_t launch_rows_to_f16(void* h, int R, int I, float* hs, cudaStream_t st
 }
 
 cudaError_t launch_gather_q8(const void* x, bool x_bf16, int H, const int32_t* pos, int T, uint8_t* xq, float* xs,
-                             cudaStream_t stream) {
+                             uint32_t* status, cudaStream_t stream) {
   // few tokens (decode): two warps per CTA, so the rows spread over more SMs
   const int warps = T <= 4096 ? 2 : kWarpsPerCta;
   const int grid = (T + warps - 1) / warps;
   const int threads = 32 * warps;
   if (pos == nullptr) {  // dense MLP: row t to row t
     if (x_bf16)
-      gather_q8_kernel<true, 1><<<grid, threads, 0, stream>>>(x, H, pos, T, xq, xs);
+      gather_q8_kernel<true, 1><<<grid, threads, 0, stream>>>(x, H, pos, T, xq, xs, status);
     else
-      gather_q8_kernel<false, 1><<<grid, threads, 0, stream>>>(x, H, pos, T, xq, xs);
+      gather_q8_kernel<false, 1><<<grid, threads, 0, stream>>>(x, H, pos, T, xq, xs, status);
   } else if (x_bf16) {
-    gather_q8_kernel<true, kTopK><<<grid, threads, 0, stream>>>(x, H, pos, T, xq, xs);
+    gather_q8_kernel<true, kTopK><<<grid, threads, 0, stream>>>(x, H, pos, T, xq, xs, status);
   } else {
-    gather_q8_kernel<false, kTopK><<<grid, threads, 0, stream>>>(x, H, pos, T, xq, xs);
+    gather_q8_kernel<false, kTopK><<<grid, threads, 0, stream>>>(x, H, pos, T, xq, xs, status);
   }
   return cudaGetLastError();
 }

@@ -33,6 +33,37 @@ __device__ __forceinline__ void report_status(uint32_t* status, uint32_t code, u
   }
 }
 
+// Device-side consistency checks.  Release builds check only what a caller
+// can get wrong through the C ABI at no cost (expert ids out of range); debug
+// builds (BEAM_DEBUG=1, libbeam_moe_debug.so) also check every index a kernel
+// takes from the workspace before using it as an address (route positions,
+// the GEMMs' per-expert schedule).  A failed check records
+// (BEAM_ERR_DEVICE_CHECK, where) in the status word and the access is
+// skipped; nothing traps.
+#if defined(BEAM_DEBUG) && BEAM_DEBUG
+constexpr bool kDebugChecks = true;
+#else
+constexpr bool kDebugChecks = false;
+#endif
+enum : uint32_t {
+  kCheckTileHistId = 20,   // an expert id outside [0, E) given to the dispatch
+  kCheckScatterId = 21,    // the same, met by the scatter (ids from the router's histogram path)
+  kCheckGatherPos = 22,    // a route position outside [-1, R) read by the gather (BF16 rows)
+  kCheckCombinePos = 23,   // ... by the combine
+  kCheckSchedule = 24,     // counts / offsets / chunk prefix inconsistent before a grouped GEMM
+  kCheckQ8Pos = 26,        // ... by the gather of E4M3 codes (FP8 weights)
+  kCheckF16Pos = 27,       // ... by the gather of FP16 rows (NVFP4 weights)
+  kCheckResidualPos = 28,  // ... by the combine fused with the residual update
+};
+// Debug builds: false (and recorded) when `ok` fails; release builds: true.
+__device__ __forceinline__ bool dcheck(bool ok, uint32_t* status, uint32_t where) {
+  if (kDebugChecks && !ok) {
+    report_status(status, kStatusDeviceCheck, where);
+    return false;
+  }
+  return true;
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

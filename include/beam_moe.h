@@ -359,6 +359,20 @@ int32_t beam_dense_kernel_count(const beam_dense_shape_t* shape, beam_dtype_t wd
 beam_status_t beam_dense_pack_weights(const beam_dense_shape_t* shape, const beam_expert_weights_t* src,
                                       beam_expert_weights_t* dst, void* stream);
 
+/* 1 when this library is the debug build (libbeam_moe_debug.so, compiled
+ * with BEAM_DEBUG=1), else 0.  The debug build checks on the device every
+ * index a kernel takes from the workspace before using it as an address --
+ * route positions in the gathers and combines, and, before each grouped GEMM
+ * (one more kernel per GEMM), that counts / offsets / chunk prefixes describe
+ * the routes -- and on a failed check records BEAM_ERR_DEVICE_CHECK in the
+ * status word (second word: where: 21 expert id met by the dispatch, 22 / 26
+ * / 27 route position met by the gather of BF16 rows / E4M3 codes / FP16
+ * rows, 23 / 28 by the combine / the combine with the residual update, 24 the
+ * GEMM schedule), skips the access (a GEMM with a bad schedule runs no work)
+ * and returns normally.  Both builds check expert ids given to the dispatch
+ * (where 20).  Otherwise the two builds compute the same results. */
+int32_t beam_moe_debug_build(void);
+
 /* Static description of a status code. */
 const char* beam_status_string(beam_status_t status);
 

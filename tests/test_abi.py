@@ -38,6 +38,17 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(lib, name), f"{name} declared in beam_moe.h but not exported"
 
 
+def test_debug_build_exports_the_same_boundary(lib):
+    """libbeam_moe_debug.so (device checks of every workspace index) exports
+    every declared entry point too, and says which build it is."""
+    _build.build(debug=True)
+    dbg = moe.load_debug()
+    for name in declared_functions():
+        assert hasattr(dbg, name), f"{name} declared in beam_moe.h but not exported by the debug build"
+    assert dbg.beam_moe_debug_build() == 1
+    assert lib.beam_moe_debug_build() == 0
+
+
 def test_status_strings(lib):
     for code in range(7):
         assert moe.beam_status_string(code)

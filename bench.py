@@ -442,9 +442,41 @@ def weight_bytes_per_expert(wl):
     return 3 * wl.H * wl.I * 2
 
 
-def traffic_record(kernel: str, workload: str):
-    """Per-launch DRAM bytes of `kernel` from the committed ncu summary, if the
-    kernel source is unchanged since the capture (else None)."""
+def code_hash(texts) -> str:
+    """sha256 of C/CUDA sources with comments removed and white space
+    collapsed: it changes with the code the compiler sees, not with its
+    comments.  String and character literals are kept as they are."""
+    out = []
+    for text in texts:
+        i, n = 0, len(text)
+        while i < n:
+            c = text[i]
+            if text.startswith("//", i):
+                j = text.find("\n", i)
+                i = n if j < 0 else j
+            elif text.startswith("/*", i):
+                j = text.find("*/", i + 2)
+                i = n if j < 0 else j + 2
+                out.append(" ")
+            elif c in "\"'":
+                j = i + 1
+                while j < n and text[j] != c:
+                    j += 2 if text[j] == "\\" else 1
+                out.append(text[i:j + 1])
+                i = j + 1
+            else:
+                out.append(c)
+                i += 1
+        out.append("\n")
+    return hashlib.sha256(" ".join("".join(out).split()).encode()).hexdigest()
+
+
+def traffic_record(kernel: str, workload: str, algorithmic_bytes: float):
+    """Per-launch DRAM bytes of `kernel`: the ratio of DRAM to algorithmic
+    bytes ncu measured on a small case of the workload (committed summary),
+    times this launch's algorithmic bytes; None when there is no record or
+    the kernel's code (its sources, comments aside) changed since the
+    capture."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     if not os.path.exists(path):
         return None
@@ -453,10 +485,13 @@ def traffic_record(kernel: str, workload: str):
     ent = rec.get(workload, {}).get(kernel)
     if not ent:
         return None
-    src = os.path.join(ROOT, "group_limited_routing_03_b300", "csrc", ent["source"])
-    if not os.path.exists(src) or hashlib.sha256(open(src, "rb").read()).hexdigest() != ent["sha256"]:
+    csrc = os.path.join(ROOT, "group_limited_routing_03_b300", "csrc")
+    srcs = [os.path.join(csrc, name) for name in ent["sources"]]
+    if not all(os.path.exists(f) for f in srcs):
         return None
-    return float(ent["dram_bytes_per_launch"])
+    if code_hash(open(f).read() for f in srcs) != ent["code_sha256"]:
+        return None
+    return round(float(ent["dram_ratio"]) * algorithmic_bytes, 1)
 
 
 def roofline(wl, m, pk):
@@ -474,7 +509,8 @@ def roofline(wl, m, pk):
     gbs = (wbytes + act_bytes) / (ms * 1e-3) / 1e9
     tfs = flops / (ms * 1e-3) / 1e12
     hbm = dict(bound="hbm", achieved=round(gbs, 1), peak=pk["hbm"], unit="GB/s", frac=round(gbs / pk["hbm"], 4),
-               traffic=traffic_record("moe_gemm_gate_up", wl.name), kernel="moe_gemm_kernel<0> (gate/up + SwiGLU)",
+               traffic=traffic_record("moe_gemm_gate_up", wl.name, wbytes + act_bytes),
+               kernel="moe_gemm_kernel<0> (gate/up + SwiGLU)",
                algorithmic_bytes=wbytes + act_bytes, launch_ms=round(ms, 4), peak_source=pk["source"])
     # FP8 MMAs: the measured BF16 peak times the nominal FP8 / BF16 ratio (2).
     # peak: the burst GEMM figure (the headline fraction); peak_sustained: the

@@ -343,7 +343,7 @@ beam_status_t run_dispatch(const beam_moe_shape_t& s, const int32_t* ids, void* 
 }
 
 // Routes per GEMM unit: all of an expert's routes up to a cap (BF16 256, the
-// widest MMA; NVFP4 160, so that TMEM also holds three BF16 weight tiles).
+// widest MMA; NVFP4 160, so that TMEM also holds a ring of FP16 weight tiles).
 int chunk_rows(int T, bool fp4) {
   // NVFP4 with few routes per expert (T <= 256: 8 on average): chunks of 16
   // leave TMEM room for the decode variant's accumulators and tile rings

@@ -4,8 +4,10 @@
 // Beam launch post, section "Mixture of Experts": every expert is a SwiGLU MLP
 // (hidden 5120, intermediate 2560); section "Residual Stream": the SwiGLU
 // product is computed in FP32.  The same post names three checkpoint formats:
-// BF16; NVFP4 for Blackwell (4-bit weights), here expanded to BF16 in TMEM
-// and multiplied with BF16 activations (W4A16); and FP8, here E4M3 weights
+// BF16; NVFP4 for Blackwell (4-bit weights), here expanded exactly to FP16
+// in TMEM and multiplied with the BF16 activations carried exactly in FP16
+// (each row times a power of two, undone in the epilogue; W4A16); and FP8,
+// here E4M3 weights
 // with per-row scales multiplied with per-row-quantised E4M3 activations on
 // kind::f8f6f4 MMAs.
 //
@@ -43,9 +45,11 @@
 //                FP32 (mode 0), BF16 stores (K parts: FP32 partial stores);
 //   then         (NVFP4 only) converters, 8 warps in two groups (12 in three
 //                groups in the decode variant) taking alternate k-blocks:
-//                packed E2M1 x E4M3 -> BF16 weight tile, written straight
-//                into TMEM (tcgen05.st; the thread of TMEM lane m expands
-//                weight row m), where the MMA reads its A operand.  Shared
+//                packed E2M1 x E4M3 -> FP16 weight tile (hardware cvt of
+//                code pairs and scale pairs, one exact FP16 multiply),
+//                written straight into TMEM (tcgen05.st; the thread of TMEM
+//                lane m expands weight row m), where the MMA (kind::f16, FP16
+//                A and B) reads its A operand.  Shared
 //                memory then carries only the packed bytes and the
 //                activations, and its bandwidth stays with the MMA's B operand;
 //   last         (NVFP4 only) a second MMA issuer for the second tile.
@@ -129,7 +133,7 @@ __device__ __forceinline__ Unit unit_at(const GemmParams& p, int u) {
 // kFp8: E4M3 weights and E4M3 activations (kind::f8f6f4): the same tiles of
 // 128-byte rows, now 128 K elements per k-block; the epilogue multiplies each
 // accumulator element by its weight row's scale and its token row's scale.
-// kDec (NVFP4 at decode sizes, chunks of at most 64 routes): the MMAs are
+// kDec (NVFP4 at decode sizes, chunks of at most 16 routes): the MMAs are
 // tiny and the conversion of the weights sets the pace, so the same 19 warps
 // are split 4 epilogue warps (enough for 64 columns) and 12 converter warps in
 // three groups that take every third k-block.

@@ -65,6 +65,16 @@ def test_job_throughput_counts_every_rank():
 
 
 def test_traffic_record_lookup():
-    assert bench.traffic_record("moe_gemm_gate_up", "no_such_workload") is None
-    v = bench.traffic_record("moe_gemm_gate_up", "decode")
-    assert v is None or v > 1e9  # bytes per launch, or None once the kernel source changed
+    assert bench.traffic_record("moe_gemm_gate_up", "no_such_workload", 1e9) is None
+    assert bench.traffic_record("moe_gemm_gate_up", "prefill", 1e9) is None  # no record for prefill-sized layers
+    v = bench.traffic_record("moe_gemm_gate_up", "decode", 1.128e10)
+    # the small-case ratio times this launch's algorithmic bytes, or None once the kernel source changed
+    assert v is None or 0.95e10 * 1.128 < v < 1.05e10 * 1.128
+
+
+def test_code_hash_ignores_comments_only():
+    a = 'int f() { return 1; }  // one\n/* block */ const char* s = "// kept";\n'
+    b = 'int f() {\n  return 1;\n}\nconst char* s = "// kept";\n'
+    assert bench.code_hash([a]) == bench.code_hash([b])
+    assert bench.code_hash([a]) != bench.code_hash([a.replace("return 1", "return 2")])
+    assert bench.code_hash([a]) != bench.code_hash([a.replace('"// kept"', '""')])

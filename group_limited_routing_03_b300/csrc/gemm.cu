@@ -29,7 +29,7 @@
 // the weight tiles) through L2.  A K range split into parts (few units for
 // many SMs) leaves FP32 partial sums that splitk.cu adds up.
 //
-// Warp roles (BF16 / FP8: 10 warps; NVFP4: 19 warps):
+// Warp roles (BF16 / FP8: 10 warps; NVFP4: 19 warps, 21 in the decode variant):
 //   warp 0       TMA producer: weight tile(s) of 128 rows x 128 bytes and the
 //                chunk's token rows x 128 bytes (one box of the tile's
 //                height, or 32-row boxes for a small chunk) per stage,
@@ -52,7 +52,8 @@
 //                A and B) reads its A operand.  Shared
 //                memory then carries only the packed bytes and the
 //                activations, and its bandwidth stays with the MMA's B operand;
-//   last         (NVFP4 only) a second MMA issuer for the second tile.
+//   last         (NVFP4 only) a second MMA issuer for the second tile (decode
+//                variant: three more, so that two threads share each tile).
 // Shared-memory stages are recycled through full/empty mbarriers, TMEM
 // accumulator buffers through acc_full/acc_empty.  NVFP4: the converters wait
 // for the TMA bytes of a stage before expanding its weights, and the MMA
@@ -80,6 +81,11 @@ constexpr int kThreadsBf16 = 32 * (2 + kEpilogueWarps);
 // thread's instruction rate at N ~ 144.
 constexpr int kMma2Warp = 2 + kEpilogueWarps + kConvertWarps;
 constexpr int kThreadsFp4 = 32 * (kMma2Warp + 1);
+// NVFP4 decode variant: four MMA-issuing threads (warps 1 and kMma2Warp..+2),
+// two per weight matrix, one per accumulator of that matrix.  With chunks of
+// at most 16 routes a tcgen05.mma keeps its issuing thread ~80 cycles while
+// the tensor pipe needs ~33, so one thread per matrix left the pipe idle.
+constexpr int kThreadsFp4Dec = 32 * (kMma2Warp + 3);
 constexpr uint32_t kATileBytes = kBlockM * kBlockK * 2;     // 16 KiB of BF16
 constexpr uint32_t kBoxBytes = kBoxRows * kBlockK * 2;      // 4 KiB
 constexpr int kSchedRing = 8;                               // scheduled unit indices in flight
@@ -138,7 +144,7 @@ __device__ __forceinline__ Unit unit_at(const GemmParams& p, int u) {
 // are split 4 epilogue warps (enough for 64 columns) and 12 converter warps in
 // three groups that take every third k-block.
 template <int kMode, bool kFp4, bool kPair, bool kWide = false, bool kFp8 = false, bool kDec = false>
-__global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
+__global__ void __launch_bounds__(kFp4 ? (kDec ? kThreadsFp4Dec : kThreadsFp4) : kThreadsBf16, 1)
     moe_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
   static_assert(!kDec || kFp4, "the decode split of warps is for NVFP4");
   constexpr int kEpi = kDec ? 4 : kEpilogueWarps;            // epilogue warps
@@ -157,11 +163,12 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
   static_assert(!(kPair && kFp4), "pair MMA path is BF16 / FP8 only");
   static_assert(!(kFp4 && kFp8), "one weight format");
   constexpr int kKElems = kFp8 ? 2 * kBlockK : kBlockK;  // K elements per k-block (128-byte rows)
+  // MMA-issuing threads: commits per k-block / unit
+  constexpr uint32_t kIssuers = kFp4 ? (kDec ? 4 : 2) : 1;
   // Roles that read every scheduled unit index (they release ring slots).
   constexpr uint32_t kRingConsumers =
       kPair ? (1 + kEpilogueWarps) + (1 + kEpilogueWarps)  // even CTA: MMA + epilogue; odd: producer + epilogue
-            : 1 + kEpi + (kFp4 ? kConv + 1 : 0);
-  constexpr uint32_t kIssuers = kFp4 ? 2 : 1;  // MMA-issuing threads: commits per k-block / unit
+            : kIssuers + kEpi + (kFp4 ? kConv : 0);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t b_tile_bytes = static_cast<uint32_t>(kPair ? p.nmax / 2 : p.nmax) * kBlockK * 2;
@@ -396,18 +403,21 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
         mbar_wait(&full[s], par, p.timeout_ns, nullptr, p.status, kWhereDrain);
       }
     }
-  } else if (kFp4 && (warp == 1 || warp == kMma2Warp)) {
+  } else if (kFp4 && (warp == 1 || (warp >= kMma2Warp && warp < kMma2Warp + static_cast<int>(kIssuers) - 1))) {
     // ------------------------------------------------------------ MMA issuers (NVFP4)
     // One thread per weight matrix of the unit (gate / up, or the two row
     // halves of a down unit), each its own accumulator chain, A (the FP16
     // tile the converters wrote) from TMEM, B from the stage's activation
     // tile of that k-block; descriptors formed once per stage.  In the decode
-    // variant each matrix has two accumulators taking alternate K steps, so
-    // consecutive MMAs of a thread do not wait on one another (the epilogue
-    // adds the two).  Per k-block: wait for the converters, four MMAs, a
-    // commit that frees the TMEM tile; per stage a commit that frees the
-    // shared-memory stage.
-    const int issuer = warp == 1 ? 0 : 1;
+    // variant each matrix has two accumulators, one for the K steps 0 and 2
+    // of every k-block and one for the steps 1 and 3 (the epilogue adds the
+    // two), and each accumulator its own issuing thread.  Per k-block: wait
+    // for the converters, the thread's MMAs (four, or two in the decode
+    // variant), a commit that frees the TMEM tile; per stage a commit that
+    // frees the shared-memory stage.
+    const int issuer = warp == 1 ? 0 : warp - kMma2Warp + 1;
+    const int mat = kDec ? (issuer & 1) : issuer;  // the weight matrix (tile) of this thread
+    const uint32_t ks0 = kDec ? static_cast<uint32_t>(issuer >> 1) : 0u;  // decode: K steps ks0, ks0 + 2
     if (lane == 0) {
       int stage = 0, acc = 0, astage = 0;
       uint32_t phase = 0, acc_phase = 0, aphase = 0;
@@ -422,8 +432,9 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
         if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1u, p.timeout_ns, abort_flag, p.status, kWhereMmaAccEmpty))
           break;
         tc_fence_after();
-        const uint32_t d = tmem_base + static_cast<uint32_t>(acc) * p.acc_cols + static_cast<uint32_t>(issuer * p.nmax);
-        const uint32_t d_odd = kDec ? d + static_cast<uint32_t>(2 * p.nmax) : d;
+        // decode: the accumulator of K steps 1 and 3 lies 2 * nmax columns after that of steps 0 and 2
+        const uint32_t d = tmem_base + static_cast<uint32_t>(acc) * p.acc_cols + static_cast<uint32_t>(mat * p.nmax) +
+                           ks0 * static_cast<uint32_t>(2 * p.nmax);
         for (int kb = U.kb0; kb < U.kb1 && ok; kb += S) {
           const uint64_t db0 = sdesc_k_sw128(smem_u32(b_tile(stage)));
           for (int sub = 0; sub < S; ++sub) {
@@ -434,12 +445,17 @@ __global__ void __launch_bounds__(kFp4 ? kThreadsFp4 : kThreadsBf16, 1)
             tc_fence_after();
             const uint64_t db = db0 + static_cast<uint64_t>(sub) * b_step;
             const uint32_t ta = tmem_base + p.a_col0 + static_cast<uint32_t>(astage) * kAStep +
-                                static_cast<uint32_t>(issuer * (kBlockK / 2));
+                                static_cast<uint32_t>(mat * (kBlockK / 2));
             const uint32_t first = (kb + sub == U.kb0) ? 1u : 0u;  // the unit's first k-block starts the sum
-            mma_f16_ts(d, ta, db, idesc, first ^ 1u);
-            mma_f16_ts(d_odd, ta + 8u, db + 2u, idesc, kDec ? (first ^ 1u) : 1u);
-            mma_f16_ts(d, ta + 16u, db + 4u, idesc, 1u);
-            mma_f16_ts(d_odd, ta + 24u, db + 6u, idesc, 1u);
+            if (kDec) {  // K steps ks0 and ks0 + 2 (8 TMEM columns, 2 descriptor units each)
+              mma_f16_ts(d, ta + 8u * ks0, db + 2u * ks0, idesc, first ^ 1u);
+              mma_f16_ts(d, ta + 8u * (ks0 + 2u), db + 2u * (ks0 + 2u), idesc, 1u);
+            } else {
+              mma_f16_ts(d, ta, db, idesc, first ^ 1u);
+              mma_f16_ts(d, ta + 8u, db + 2u, idesc, 1u);
+              mma_f16_ts(d, ta + 16u, db + 4u, idesc, 1u);
+              mma_f16_ts(d, ta + 24u, db + 6u, idesc, 1u);
+            }
             mma_commit(&aempty[astage]);  // the TMEM tile is free once these MMAs complete
             if (++astage == p.a_stages) {
               astage = 0;
@@ -805,7 +821,7 @@ cudaError_t launch_one(const GemmMaps& maps, const GemmParams& p, int grid, size
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_bytes));
   if (err != cudaSuccess) return err;
   if (!kPair) {
-    kern<<<grid, kFp4 ? kThreadsFp4 : kThreadsBf16, smem_bytes, stream>>>(maps, p);
+    kern<<<grid, kFp4 ? (kDec ? kThreadsFp4Dec : kThreadsFp4) : kThreadsBf16, smem_bytes, stream>>>(maps, p);
     return cudaGetLastError();
   }
   cudaLaunchConfig_t cfg = {};

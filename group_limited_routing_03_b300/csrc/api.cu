@@ -448,7 +448,9 @@ struct GemmChoice {
 GemmChoice choose_gemm(int mode, const beam_moe_shape_t& s, bool fp4, bool fp8, int nmax, int split_chunks,
                        const DeviceInfo& d) {
   GemmChoice c{false, 0, 1};
-  const size_t budget = static_cast<size_t>(d.smem_optin) - 1024 - 512;
+  // shared memory for the stages: all but the barriers, unit ring and
+  // alignment slack of the deepest pipeline (gemm_smem_bytes with no stage bytes)
+  const size_t budget = static_cast<size_t>(d.smem_optin) - gemm_smem_bytes(kMaxStages, 4, 0);
   c.pair = !fp4 && nmax == 256 && s.H % 512 == 0 && s.I % 256 == 0 && d.sms >= 2;
   if (c.pair) {
     const size_t sbp = gemm_stage_bytes(2, false, nmax / 2);
@@ -542,7 +544,9 @@ beam_status_t run_gemm(int mode, const beam_moe_shape_t& s, const beam_expert_we
   // runs: a pair tile's stage is fixed (two weight tiles, 128 token rows per
   // CTA, one 2 x 256-column accumulator), and if no pair fits on the device
   // the GEMM runs one CTA per unit.
-  const size_t budget = static_cast<size_t>(d.smem_optin) - 1024 - 512;
+  // shared memory for the stages: all but the barriers, unit ring and
+  // alignment slack of the deepest pipeline (gemm_smem_bytes with no stage bytes)
+  const size_t budget = static_cast<size_t>(d.smem_optin) - gemm_smem_bytes(kMaxStages, 4, 0);
   const GemmChoice gc = choose_gemm(mode, s, fp4, fp8, nmax, io.partial != nullptr ? io.split_chunks : 0, d);
   const bool pair = gc.pair;
   const int clusters = gc.clusters;

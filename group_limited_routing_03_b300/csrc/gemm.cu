@@ -89,6 +89,7 @@ constexpr int kThreadsFp4Dec = 32 * (kMma2Warp + 3);
 constexpr uint32_t kATileBytes = kBlockM * kBlockK * 2;     // 16 KiB of BF16
 constexpr uint32_t kBoxBytes = kBoxRows * kBlockK * 2;      // 4 KiB
 constexpr int kSchedRing = 8;                               // scheduled unit indices in flight
+constexpr int kSlotInts = 8;                                // ints per unit ring slot: index + Unit
 
 struct Unit {
   int e, m, start, n;
@@ -184,10 +185,11 @@ __global__ void __launch_bounds__(kFp4 ? (kDec ? kThreadsFp4Dec : kThreadsFp4) :
   uint64_t* acc_full = aempty + kMaxAStages;
   uint64_t* acc_empty = acc_full + p.acc_stages;
   uint64_t* drain = acc_empty + p.acc_stages;
-  uint64_t* ufull = drain + 1;        // unit ring: index published
-  uint64_t* uempty = ufull + kSchedRing;  // unit ring: index read by every consumer
+  uint64_t* ufull = drain + 1;        // unit ring: unit published
+  uint64_t* uempty = ufull + kSchedRing;  // unit ring: unit read by every consumer
+  // slot r: kSlotInts ints, the unit index and its decoded Unit
   volatile int* ring = reinterpret_cast<volatile int*>(uempty + kSchedRing);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(const_cast<int*>(ring) + kSchedRing);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(const_cast<int*>(ring) + kSchedRing * kSlotInts);
   volatile uint32_t* abort_flag = tmem_slot + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -255,6 +257,15 @@ __global__ void __launch_bounds__(kFp4 ? (kDec ? kThreadsFp4Dec : kThreadsFp4) :
   // global counter in order and publishes each one, or -1 at the end, into a
   // ring read by every role of both CTAs, so units (and the sibling chunks of
   // one expert, which share weight tiles through L2) start in index order.
+  // NVFP4 decode variant: the unit is decoded (unit_at: a binary search over
+  // the chunk prefix in global memory, ~10 dependent loads) once, by the
+  // fetching thread, ahead of its consumers, and every role reads it from the
+  // ring instead of decoding it again at its unit boundary (on the MMA
+  // threads that search cost ~2 us per unit, ~6% of a decode-size launch of
+  // short units).  The other kernels (measured no faster, or slower through
+  // register spills) decode the index in each role.
+  constexpr bool kRingUnits = kDec;
+  constexpr int kStride = kRingUnits ? kSlotInts : 1;  // ints per ring slot in use
   int ring_slot = 0;
   uint32_t ring_phase = 0;
   auto ring_advance = [&]() {
@@ -263,11 +274,22 @@ __global__ void __launch_bounds__(kFp4 ? (kDec ? kThreadsFp4Dec : kThreadsFp4) :
       ring_phase ^= 1u;
     }
   };
-  // One thread: the next unit index (-1: no more); false when a wait gave up.
-  auto ring_take = [&](int& u) -> bool {
+  // One thread: the next unit index (-1: no more) and its Unit; false when a
+  // wait gave up.
+  auto ring_take_raw = [&](int& u, Unit& U) -> bool {
     if (!mbar_wait_cluster(&ufull[ring_slot], ring_phase, p.timeout_ns, abort_flag, p.status, kWhereSchedule))
       return false;
-    u = ring[ring_slot];
+    const volatile int* r = ring + ring_slot * kStride;
+    u = r[0];
+    if (kRingUnits) {
+      U.e = r[1];
+      U.m = r[2];
+      U.start = r[3];
+      U.n = r[4];
+      U.ks = r[5];
+      U.kb0 = r[6];
+      U.kb1 = r[7];
+    }
     if (kPair)
       mbar_arrive_cluster(mapa_shared(&uempty[ring_slot], 0));
     else
@@ -275,13 +297,24 @@ __global__ void __launch_bounds__(kFp4 ? (kDec ? kThreadsFp4Dec : kThreadsFp4) :
     ring_advance();
     return true;
   };
+  auto ring_take = [&](int& u, Unit& U) -> bool {
+    if (!ring_take_raw(u, U)) return false;
+    if (!kRingUnits && u >= 0) U = unit_at(p, u);
+    return true;
+  };
   // Fetching thread only.
-  auto ring_publish = [&](int u) -> bool {
+  auto ring_publish = [&](int u, const Unit& U) -> bool {
     if (!mbar_wait(&uempty[ring_slot], ring_phase ^ 1u, p.timeout_ns, abort_flag, p.status, kWhereSchedule))
       return false;
-    ring[ring_slot] = u;
+    volatile int* r = ring + ring_slot * kStride;
+    constexpr int kInts = kStride;
+    const int v[kSlotInts] = {u, U.e, U.m, U.start, U.n, U.ks, U.kb0, U.kb1};
+#pragma unroll
+    for (int j = 0; j < kInts; ++j) r[j] = v[j];
     if (kPair) {
-      st_shared_cluster_u32(mapa_shared(const_cast<int*>(&ring[ring_slot]), 1), static_cast<uint32_t>(u));
+#pragma unroll
+      for (int j = 0; j < kInts; ++j)
+        st_shared_cluster_u32(mapa_shared(const_cast<int*>(&r[j]), 1), static_cast<uint32_t>(v[j]));
       mbar_arrive_cluster(mapa_shared(&ufull[ring_slot], 1));
     }
     mbar_arrive(&ufull[ring_slot]);
@@ -289,11 +322,23 @@ __global__ void __launch_bounds__(kFp4 ? (kDec ? kThreadsFp4Dec : kThreadsFp4) :
     return true;
   };
   // Warp-wide version of ring_take for the epilogue / converter warps.
-  auto warp_take = [&](int& u) -> bool {
+  auto warp_take = [&](int& u, Unit& U) -> bool {
     int good = 1, v = -1;
-    if (lane == 0) good = ring_take(v) ? 1 : 0;
+    Unit W{};
+    if (lane == 0) good = ring_take_raw(v, W) ? 1 : 0;
     good = __shfl_sync(0xFFFFFFFFu, good, 0);
     u = __shfl_sync(0xFFFFFFFFu, v, 0);
+    if (kRingUnits) {
+      U.e = __shfl_sync(0xFFFFFFFFu, W.e, 0);
+      U.m = __shfl_sync(0xFFFFFFFFu, W.m, 0);
+      U.start = __shfl_sync(0xFFFFFFFFu, W.start, 0);
+      U.n = __shfl_sync(0xFFFFFFFFu, W.n, 0);
+      U.ks = __shfl_sync(0xFFFFFFFFu, W.ks, 0);
+      U.kb0 = __shfl_sync(0xFFFFFFFFu, W.kb0, 0);
+      U.kb1 = __shfl_sync(0xFFFFFFFFu, W.kb1, 0);
+    } else if (u >= 0) {
+      U = unit_at(p, u);
+    }
     return good != 0;
   };
 
@@ -316,15 +361,17 @@ __global__ void __launch_bounds__(kFp4 ? (kDec ? kThreadsFp4Dec : kThreadsFp4) :
       bool ok = true;
       while (ok) {
         int u;
+        Unit U{};
         if (rank == 0) {
           u = atomicAdd(p.sched, 1);
           if (u >= total_units) u = -1;
-          if (!ring_publish(u)) break;
-        } else if (!ring_take(u)) {
+          if (kRingUnits && u >= 0) U = unit_at(p, u);
+          if (!ring_publish(u, U)) break;
+          if (!kRingUnits && u >= 0) U = unit_at(p, u);
+        } else if (!ring_take(u, U)) {
           break;
         }
         if (u < 0) break;
-        const Unit U = unit_at(p, u);
         const int a_row = U.e * p.a_rows_per_expert + U.m * kRowsPerUnit + static_cast<int>(rank) * kBlockM;
         // pair: this CTA loads token rows [start + rank*N/2, +N/2), N = round16(n)
         const int n_local = kPair ? ((U.n + 15) & ~15) / 2 : U.n;
@@ -426,8 +473,8 @@ __global__ void __launch_bounds__(kFp4 ? (kDec ? kThreadsFp4Dec : kThreadsFp4) :
       bool ok = true;
       while (ok) {
         int u;
-        if (!ring_take(u) || u < 0) break;
-        const Unit U = unit_at(p, u);
+        Unit U;
+        if (!ring_take(u, U) || u < 0) break;
         const uint32_t idesc = idesc_f16_f32(kBlockM, static_cast<uint32_t>((U.n + 15) & ~15));
         if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1u, p.timeout_ns, abort_flag, p.status, kWhereMmaAccEmpty))
           break;
@@ -488,8 +535,8 @@ __global__ void __launch_bounds__(kFp4 ? (kDec ? kThreadsFp4Dec : kThreadsFp4) :
       bool ok = true;
       while (ok) {
         int u;
-        if (!ring_take(u) || u < 0) break;
-        const Unit U = unit_at(p, u);
+        Unit U;
+        if (!ring_take(u, U) || u < 0) break;
         const uint32_t n_mma = static_cast<uint32_t>((U.n + 15) & ~15);
         const uint32_t idesc = kFp8 ? idesc_e4m3_f32(kPair ? 2 * kBlockM : kBlockM, n_mma)
                                     : idesc_bf16_f32(kPair ? 2 * kBlockM : kBlockM, n_mma);
@@ -559,8 +606,8 @@ __global__ void __launch_bounds__(kFp4 ? (kDec ? kThreadsFp4Dec : kThreadsFp4) :
     uint32_t acc_phase = 0;
     while (true) {
       int u;
-      if (!warp_take(u) || u < 0) break;
-      const Unit U = unit_at(p, u);
+      Unit U;
+      if (!warp_take(u, U) || u < 0) break;
       int ok = 1;
       if (lane == 0)
         ok = mbar_wait(&acc_full[acc], acc_phase, p.timeout_ns, abort_flag, p.status, kWhereEpiAccFull) ? 1 : 0;
@@ -755,7 +802,8 @@ __global__ void __launch_bounds__(kFp4 ? (kDec ? kThreadsFp4Dec : kThreadsFp4) :
     bool ok = true;
     while (ok) {
       int u;
-      if (!warp_take(u) || u < 0) break;
+      Unit U;
+      if (!warp_take(u, U) || u < 0) break;
       for (int kb = group; kb < p.k_blocks; kb += kGroups) {
         advance_to(unit_base + kb);
         int good = 1;
@@ -845,7 +893,7 @@ cudaError_t launch_one(const GemmMaps& maps, const GemmParams& p, int grid, size
 
 size_t gemm_smem_bytes(int stages, int acc_stages, size_t stage_bytes) {
   return 1024 + static_cast<size_t>(stages) * stage_bytes +
-         (2 * stages + 3 * kMaxAStages + 2 * acc_stages + 1 + 2 * kSchedRing) * 8 + kSchedRing * 4 + 16;
+         (2 * stages + 3 * kMaxAStages + 2 * acc_stages + 1 + 2 * kSchedRing) * 8 + kSchedRing * kSlotInts * 4 + 16;
 }
 
 int gemm_pair_max_clusters(int mode, size_t smem_bytes) {

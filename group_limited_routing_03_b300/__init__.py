@@ -28,7 +28,8 @@ __all__ = [
     "ForwardCall", "STAGES", "beam_moe_stage_kernel_count", "beam_moe_route_noalloc", "pack_weights",
     "BEAM_LAYOUT_ROWS", "BEAM_LAYOUT_TILED",
     "beam_moe_read_device_status", "beam_moe_debug_timeout", "beam_debug_nvfp4_expand", "beam_status_string", "BeamMoE",
-    "library_path", "load", "load_debug", "BEAM_F32", "BEAM_BF16", "BEAM_NVFP4", "BEAM_FP8",
+    "library_path", "load", "load_debug", "BEAM_F32", "BEAM_BF16", "BEAM_NVFP4", "BEAM_FP8", "BEAM_NVFP4_A4",
+    "beam_debug_quantize_nvfp4",
     "beam_moe_forward_residual", "GraphedForward",
     "DenseShape", "dense_shape", "dense_workspace_size", "dense_kernel_count", "beam_dense_mlp_forward",
     "dense_pack_weights", "DenseMLP",
@@ -39,7 +40,7 @@ _LIB_PATH = os.path.join(_PKG, "libbeam_moe.so")
 
 BEAM_OK, BEAM_ERR_INVALID_ARG, BEAM_ERR_UNSUPPORTED, BEAM_ERR_WORKSPACE = 0, 1, 2, 3
 BEAM_ERR_CUDA, BEAM_ERR_TIMEOUT, BEAM_ERR_DEVICE_CHECK = 4, 5, 6
-BEAM_F32, BEAM_BF16, BEAM_NVFP4, BEAM_FP8 = 0, 1, 2, 3
+BEAM_F32, BEAM_BF16, BEAM_NVFP4, BEAM_FP8, BEAM_NVFP4_A4 = 0, 1, 2, 3, 4
 
 
 class BeamError(RuntimeError):
@@ -119,6 +120,7 @@ def _configure(lib):
     lib.beam_moe_stage_kernel_count.restype = ctypes.c_int32
     lib.beam_moe_debug_timeout.argtypes = [vp, sz, u32, vp]
     lib.beam_debug_nvfp4_expand.argtypes = [vp, vp, i32, vp, vp]
+    lib.beam_debug_quantize_nvfp4.argtypes = [vp, i32, i32, i32, vp, vp, vp, vp, vp]
     lib.beam_moe_debug_build.argtypes = []
     lib.beam_moe_debug_build.restype = ctypes.c_int32
     lib.beam_moe_pack_weights.argtypes = [sp, ctypes.POINTER(_ExpertWeights), ctypes.POINTER(_ExpertWeights), vp]
@@ -134,7 +136,7 @@ def _configure(lib):
     for n in ("beam_moe_workspace_layout", "beam_moe_route", "beam_moe_dispatch", "beam_moe_experts",
               "beam_moe_forward", "beam_moe_forward_stage", "beam_moe_forward_residual",
               "beam_moe_read_device_status",
-              "beam_moe_debug_timeout", "beam_debug_nvfp4_expand", "beam_dense_mlp_forward",
+              "beam_moe_debug_timeout", "beam_debug_nvfp4_expand", "beam_debug_quantize_nvfp4", "beam_dense_mlp_forward",
               "beam_dense_pack_weights"):
         getattr(lib, n).restype = i32
     return lib
@@ -201,7 +203,8 @@ def _weights(w: dict) -> _ExpertWeights:
     if w["gate"].dtype == torch.bfloat16:
         ew.dtype = BEAM_BF16
     elif w["gate"].dtype == torch.uint8:
-        ew.dtype = BEAM_NVFP4
+        # "activations": "nvfp4" asks for W4A4 (GEMM inputs quantised to NVFP4)
+        ew.dtype = BEAM_NVFP4_A4 if w.get("activations") == "nvfp4" else BEAM_NVFP4
     elif w["gate"].dtype == torch.float8_e4m3fn:
         ew.dtype = BEAM_FP8
     else:
@@ -224,10 +227,12 @@ def _wdtype(w) -> int:
     if isinstance(w, int):
         return w
     if isinstance(w, str):
-        return {"bf16": BEAM_BF16, "nvfp4": BEAM_NVFP4, "fp8": BEAM_FP8}[w]
+        return {"bf16": BEAM_BF16, "nvfp4": BEAM_NVFP4, "fp8": BEAM_FP8, "nvfp4_a4": BEAM_NVFP4_A4}[w]
     if w["gate"].dtype == torch.float8_e4m3fn:
         return BEAM_FP8
-    return BEAM_NVFP4 if w["gate"].dtype == torch.uint8 else BEAM_BF16
+    if w["gate"].dtype == torch.uint8:
+        return BEAM_NVFP4_A4 if w.get("activations") == "nvfp4" else BEAM_NVFP4
+    return BEAM_BF16
 
 
 # --------------------------------------------------------------------------
@@ -394,6 +399,20 @@ def beam_debug_nvfp4_expand(codes, scales, out, stream=None):
         raise ValueError("codes must hold 8 bytes and out 16 values per block")
     _check(load().beam_debug_nvfp4_expand(_ptr(codes), _ptr(scales), n_blocks, _ptr(out), _stream(stream)),
            "beam_debug_nvfp4_expand")
+
+
+def beam_debug_quantize_nvfp4(a, codes, scales, global_scale, values, stream=None):
+    """Quantise rows of ``a`` (float32 or bfloat16 [rows, K]) with the W4A4
+    forward's device code: codes uint8 [rows, K] (one E2M1 code per byte),
+    scales uint8 [rows, K/16] (E4M3), global_scale float32 [rows], values
+    int16/float16 [rows, K] (FP16 bits of e2m1 * e4m3)."""
+    rows, K = a.shape
+    if codes.numel() != rows * K or scales.numel() != rows * (K // 16) or global_scale.numel() != rows \
+            or values.numel() != rows * K:
+        raise ValueError("output sizes must match a's rows and K")
+    _check(load().beam_debug_quantize_nvfp4(_ptr(a), _act_dtype(a), rows, K, _ptr(codes), _ptr(scales),
+                                            _ptr(global_scale), _ptr(values), _stream(stream)),
+           "beam_debug_quantize_nvfp4")
 
 
 def beam_moe_debug_timeout(workspace, timeout_us: int, stream=None):

@@ -21,6 +21,12 @@ namespace beam {
 namespace {
 
 constexpr uint64_t kDefaultTimeoutNs = 1000000000ull;  // 1 s per bounded wait
+
+// NVFP4 weights, with BF16 activations carried exactly in FP16 (W4A16) or
+// with activations quantised to NVFP4 at run time (W4A4): the same weight
+// arrays, GEMM kernels and workspace; only the activation rows differ.
+inline bool is_nvfp4(beam_dtype_t t) { return t == BEAM_NVFP4 || t == BEAM_NVFP4_A4; }
+inline bool known_wdtype(beam_dtype_t t) { return t == BEAM_BF16 || t == BEAM_FP8 || is_nvfp4(t); }
 #if defined(BEAM_DEBUG) && BEAM_DEBUG
 constexpr bool kDebugBuild = true;  // device checks of every workspace index (see tc.cuh)
 #else
@@ -212,7 +218,7 @@ void make_dense_layout(const beam_dense_shape_t& s, beam_dtype_t wdtype, DenseLa
   L.hq = take(T_pad * I);
   L.xs = take((T_pad + 32) * 4);
   L.hs = take((T_pad + 32) * 4);
-  L.x16 = take(wdtype == BEAM_NVFP4 ? T_pad * H * 2 : 0);
+  L.x16 = take(is_nvfp4(wdtype) ? T_pad * H * 2 : 0);
   // K-split partial planes: the larger of gate/up (two planes of T x I per
   // part) and down (one of T x H), parts as run_gemm picks them for BF16
   // weights (FP8 has half the k-blocks, so never more parts)
@@ -267,7 +273,7 @@ beam_status_t check_weights(const beam_moe_shape_t* s, const beam_expert_weights
     if (w->gate_sf || w->up_sf || w->down_sf || w->gate_gs || w->up_gs || w->down_gs) return BEAM_ERR_INVALID_ARG;
     return BEAM_OK;
   }
-  if (w->dtype == BEAM_NVFP4) {
+  if (is_nvfp4(w->dtype)) {
     if (!w->gate || !w->up || !w->down || !w->gate_sf || !w->up_sf || !w->down_sf || !w->gate_gs || !w->up_gs ||
         !w->down_gs)
       return BEAM_ERR_INVALID_ARG;
@@ -365,6 +371,9 @@ beam_status_t run_gather(const beam_moe_shape_t& s, const void* x, bool x_bf16, 
                          const Layout& L, const DeviceInfo& d, cudaStream_t stream) {
   if (wdtype == BEAM_FP8)
     return cuda_status(launch_gather_q8(x, x_bf16, s.H, at<int32_t>(ws, L.pos), s.T, at<uint8_t>(ws, L.xq),
+                                        at<float>(ws, L.xs), at<uint32_t>(ws, L.status), stream));
+  if (wdtype == BEAM_NVFP4_A4)
+    return cuda_status(launch_gather_a4(x, x_bf16, s.H, at<int32_t>(ws, L.pos), s.T, at<__half>(ws, L.xp),
                                         at<float>(ws, L.xs), at<uint32_t>(ws, L.status), stream));
   if (wdtype == BEAM_NVFP4)
     return cuda_status(launch_gather_f16(x, x_bf16, s.H, at<int32_t>(ws, L.pos), s.T, at<__half>(ws, L.xp),
@@ -469,7 +478,7 @@ beam_status_t run_gemm(int mode, const beam_moe_shape_t& s, const beam_expert_we
                        const DeviceInfo& d, cudaStream_t stream) {
   const int R = io.R;
   const uint64_t R_pad = static_cast<uint64_t>((R + kBoxRows - 1) / kBoxRows * kBoxRows);
-  const bool fp4 = wts->dtype == BEAM_NVFP4;
+  const bool fp4 = is_nvfp4(wts->dtype);
   const bool fp8 = wts->dtype == BEAM_FP8;
   const int nmax = io.nmax;
   // FP8 / NVFP4: h's row conversion comes first (its scales need whole rows
@@ -479,7 +488,8 @@ beam_status_t run_gemm(int mode, const beam_moe_shape_t& s, const beam_expert_we
     if (e != cudaSuccess) return BEAM_ERR_CUDA;
   }
   if (fp4 && mode == 1) {
-    const cudaError_t e = launch_rows_to_f16(io.h, R, s.I, io.hs, stream);
+    const cudaError_t e = wts->dtype == BEAM_NVFP4_A4 ? launch_rows_to_a4(io.h, R, s.I, io.hs, stream)
+                                                       : launch_rows_to_f16(io.h, R, s.I, io.hs, stream);
     if (e != cudaSuccess) return BEAM_ERR_CUDA;
   }
   // NVFP4: the activation operand holds FP16 rows (kind::f16 takes A and B
@@ -672,10 +682,10 @@ beam_status_t run_combine(const beam_moe_shape_t& s, const float* w, void* y, bo
 beam_status_t run_experts(const beam_moe_shape_t& s, const void* x, bool x_bf16, const beam_expert_weights_t* wts,
                           const int32_t* ids, const float* w, void* y, void* ws, const Layout& L,
                           const DeviceInfo& d, bool hist_ready, cudaStream_t stream) {
-  beam_status_t st = run_dispatch(s, ids, ws, L, chunk_rows(s.T, wts->dtype == BEAM_NVFP4), hist_ready, stream);
+  beam_status_t st = run_dispatch(s, ids, ws, L, chunk_rows(s.T, is_nvfp4(wts->dtype)), hist_ready, stream);
   if (st == BEAM_OK) st = run_gather(s, x, x_bf16, wts->dtype, ws, L, d, stream);
-  if (st == BEAM_OK) st = run_gemm(0, s, wts, moe_io(s, ws, L, wts->dtype == BEAM_NVFP4), d, stream);
-  if (st == BEAM_OK) st = run_gemm(1, s, wts, moe_io(s, ws, L, wts->dtype == BEAM_NVFP4), d, stream);
+  if (st == BEAM_OK) st = run_gemm(0, s, wts, moe_io(s, ws, L, is_nvfp4(wts->dtype)), d, stream);
+  if (st == BEAM_OK) st = run_gemm(1, s, wts, moe_io(s, ws, L, is_nvfp4(wts->dtype)), d, stream);
   if (st == BEAM_OK) st = run_combine(s, w, y, x_bf16, ws, L, stream);
   return st;
 }
@@ -742,13 +752,13 @@ beam_status_t run_stage(const beam_moe_shape_t& s, const beam_moe_args_t& a, int
     case BEAM_STAGE_ROUTE:
       return run_route(s, a.x, xb, a.router_w, a.router_bias, a.topk_ids, a.topk_w, ws, L, d, cs);
     case BEAM_STAGE_DISPATCH:
-      return run_dispatch(s, a.topk_ids, ws, L, chunk_rows(s.T, a.weights->dtype == BEAM_NVFP4), true, cs);
+      return run_dispatch(s, a.topk_ids, ws, L, chunk_rows(s.T, is_nvfp4(a.weights->dtype)), true, cs);
     case BEAM_STAGE_GATHER:
       return run_gather(s, a.x, xb, a.weights->dtype, ws, L, d, cs);
     case BEAM_STAGE_GATE_UP:
-      return run_gemm(0, s, a.weights, moe_io(s, ws, L, a.weights->dtype == BEAM_NVFP4), d, cs);
+      return run_gemm(0, s, a.weights, moe_io(s, ws, L, is_nvfp4(a.weights->dtype)), d, cs);
     case BEAM_STAGE_DOWN:
-      return run_gemm(1, s, a.weights, moe_io(s, ws, L, a.weights->dtype == BEAM_NVFP4), d, cs);
+      return run_gemm(1, s, a.weights, moe_io(s, ws, L, is_nvfp4(a.weights->dtype)), d, cs);
     case BEAM_STAGE_COMBINE:
       if (a.residual) return run_combine_residual(s, a.topk_w, *a.residual, a.y, xb, ws, L, cs);
       return run_combine(s, a.topk_w, a.y, xb, ws, L, cs);
@@ -787,7 +797,7 @@ extern "C" {
 
 size_t beam_moe_workspace_size(const beam_moe_shape_t* shape, beam_dtype_t wdtype) {
   if (check_shape(shape) != BEAM_OK) return 0;
-  if (wdtype != BEAM_BF16 && wdtype != BEAM_NVFP4 && wdtype != BEAM_FP8) return 0;
+  if (!known_wdtype(wdtype)) return 0;
   Layout L;
   make_layout(*shape, L);
   return L.total;
@@ -797,7 +807,7 @@ beam_status_t beam_moe_workspace_layout(const beam_moe_shape_t* shape, beam_dtyp
   const beam_status_t st = check_shape(shape);
   if (st != BEAM_OK) return st;
   if (out == nullptr) return BEAM_ERR_INVALID_ARG;
-  if (wdtype != BEAM_BF16 && wdtype != BEAM_NVFP4 && wdtype != BEAM_FP8) return BEAM_ERR_UNSUPPORTED;
+  if (!known_wdtype(wdtype)) return BEAM_ERR_UNSUPPORTED;
   Layout L;
   make_layout(*shape, L);
   out->xq = L.xq;
@@ -908,7 +918,7 @@ int32_t beam_moe_stage_kernel_count(const beam_moe_shape_t* shape, beam_dtype_t 
                                     beam_stage_t stage) {
   if (check_shape(shape) != BEAM_OK) return -1;
   if (xdtype != BEAM_F32 && xdtype != BEAM_BF16) return -1;
-  if (wdtype != BEAM_BF16 && wdtype != BEAM_NVFP4 && wdtype != BEAM_FP8) return -1;
+  if (!known_wdtype(wdtype)) return -1;
   DeviceInfo d;
   if (!device_info(d)) return -1;
   switch (stage) {
@@ -956,7 +966,7 @@ static beam_status_t pack_impl(const beam_moe_shape_t* shape, size_t n_exp, cons
   if (st == BEAM_OK) st = check_weights(shape, &probe, n_exp == kExperts);
   if (st != BEAM_OK) return st;
   const size_t E = n_exp, H = shape->H, I = shape->I;
-  const bool fp4 = src->dtype == BEAM_NVFP4, fp8 = src->dtype == BEAM_FP8;
+  const bool fp4 = is_nvfp4(src->dtype), fp8 = src->dtype == BEAM_FP8;
   // FP8 row scales keep their order: the same arrays serve both layouts
   if (fp8 && (dst->gate_rs != src->gate_rs || dst->up_rs != src->up_rs || dst->down_rs != src->down_rs))
     return BEAM_ERR_INVALID_ARG;
@@ -1014,10 +1024,10 @@ int32_t beam_dense_kernel_count(const beam_dense_shape_t* shape, beam_dtype_t wd
   if (shape == nullptr) return -1;
   const beam_moe_shape_t ms = dense_as_moe(*shape);
   if (check_shape(&ms) != BEAM_OK) return -1;
-  if (wdtype != BEAM_BF16 && wdtype != BEAM_NVFP4 && wdtype != BEAM_FP8) return -1;
+  if (!known_wdtype(wdtype)) return -1;
   DeviceInfo d;
   if (!device_info(d)) return -1;
-  const bool fp4 = wdtype == BEAM_NVFP4, fp8 = wdtype == BEAM_FP8;
+  const bool fp4 = is_nvfp4(wdtype), fp8 = wdtype == BEAM_FP8;
   const int nmax = chunk_rows(shape->T, fp4);
   const int chunks = (shape->T + nmax - 1) / nmax;
   int n = 1 + 1 + 1;        // schedule, gate/up, down
@@ -1032,7 +1042,7 @@ size_t beam_dense_workspace_size(const beam_dense_shape_t* shape, beam_dtype_t w
   if (shape == nullptr) return 0;
   const beam_moe_shape_t ms = dense_as_moe(*shape);
   if (check_shape(&ms) != BEAM_OK) return 0;
-  if (wdtype != BEAM_BF16 && wdtype != BEAM_NVFP4 && wdtype != BEAM_FP8) return 0;
+  if (!known_wdtype(wdtype)) return 0;
   DenseLayout L;
   make_dense_layout(*shape, wdtype, L);
   return L.total;
@@ -1061,7 +1071,7 @@ beam_status_t beam_dense_mlp_forward(const beam_dense_shape_t* shape, const void
   void* ws = workspace;
   GemmIO io;
   io.R = shape->T;
-  io.nmax = chunk_rows(shape->T, weights->dtype == BEAM_NVFP4);
+  io.nmax = chunk_rows(shape->T, is_nvfp4(weights->dtype));
   io.n_exp = 1;
   io.xp = x;  // BF16 x is the gate/up input itself, rows in token order
   io.xp_rows = static_cast<uint64_t>(shape->T);
@@ -1083,11 +1093,13 @@ beam_status_t beam_dense_mlp_forward(const beam_dense_shape_t* shape, const void
   if (fp8 && launch_gather_q8(x, xdtype == BEAM_BF16, shape->H, nullptr, shape->T, io.xq, io.xs, io.status, cs) !=
                  cudaSuccess)
     return BEAM_ERR_CUDA;
-  if (weights->dtype == BEAM_NVFP4) {  // x as FP16 rows times a power of two
+  if (is_nvfp4(weights->dtype)) {  // x as FP16 rows: times a power of two (W4A16) or NVFP4 values (W4A4)
     io.xp = at<__half>(ws, L.x16);
-    if (launch_gather_f16(x, true, shape->H, nullptr, shape->T, at<__half>(ws, L.x16), io.xs, io.status, cs) !=
-        cudaSuccess)
-      return BEAM_ERR_CUDA;
+    const cudaError_t e =
+        weights->dtype == BEAM_NVFP4_A4
+            ? launch_gather_a4(x, true, shape->H, nullptr, shape->T, at<__half>(ws, L.x16), io.xs, io.status, cs)
+            : launch_gather_f16(x, true, shape->H, nullptr, shape->T, at<__half>(ws, L.x16), io.xs, io.status, cs);
+    if (e != cudaSuccess) return BEAM_ERR_CUDA;
   }
   st = run_gemm(0, ms, weights, io, d, cs);
   if (st == BEAM_OK) st = run_gemm(1, ms, weights, io, d, cs);

@@ -1,7 +1,8 @@
-// expand_check.cu -- test hook for the NVFP4 weight expansion: runs the
-// converter warps' own device functions (nvfp4.cuh) over caller-given codes
-// and block scales, so that a test can compare every E2M1 x E4M3 product the
-// grouped GEMMs can form with its exact value.
+// expand_check.cu -- test hooks for the NVFP4 paths: the weight expansion
+// (the converter warps' own device functions, nvfp4.cuh, over caller-given
+// codes and block scales, so that a test can compare every E2M1 x E4M3
+// product the grouped GEMMs can form with its exact value) and the W4A4
+// activation quantiser (quant.cu's, over caller-given rows).
 #include <cuda_runtime.h>
 
 #include "beam_moe.h"
@@ -42,4 +43,19 @@ extern "C" beam_status_t beam_debug_nvfp4_expand(const uint8_t* codes, const uin
   expand_nvfp4_kernel<<<(n_blocks + 255) / 256, 256, 0, static_cast<cudaStream_t>(stream)>>>(
       codes, scales, n_blocks, reinterpret_cast<uint32_t*>(out));
   return cudaGetLastError() == cudaSuccess ? BEAM_OK : BEAM_ERR_CUDA;
+}
+
+extern "C" beam_status_t beam_debug_quantize_nvfp4(const void* a, beam_dtype_t a_dtype, int32_t rows, int32_t K,
+                                                   uint8_t* codes, uint8_t* scales, float* global, uint16_t* values,
+                                                   void* stream) {
+  using namespace beam;
+  if (!a || !codes || !scales || !global || !values || rows < 1 || K < 16 || K % 16 != 0) return BEAM_ERR_INVALID_ARG;
+  if (a_dtype != BEAM_F32 && a_dtype != BEAM_BF16) return BEAM_ERR_UNSUPPORTED;
+  if ((reinterpret_cast<uintptr_t>(a) & 15u) || (reinterpret_cast<uintptr_t>(values) & 15u) ||
+      (reinterpret_cast<uintptr_t>(global) & 3u))
+    return BEAM_ERR_INVALID_ARG;
+  return launch_quantize_a4(a, a_dtype == BEAM_BF16, rows, K, codes, scales, global, reinterpret_cast<__half*>(values),
+                            static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? BEAM_OK
+             : BEAM_ERR_CUDA;
 }

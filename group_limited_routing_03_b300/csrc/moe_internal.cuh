@@ -168,6 +168,19 @@ cudaError_t launch_gather_f16(const void* x, bool x_bf16, int H, const int32_t* 
 // NVFP4 weights: rows of h (BF16 [R, I]) to FP16 in place, the same rule,
 // inverse scales in hs [R_pad].
 cudaError_t launch_rows_to_f16(void* h, int R, int I, float* hs, cudaStream_t stream);
+// NVFP4 activations (W4A4): token rows quantised per row to NVFP4 (x as
+// given), each element written as the FP16 value e2m1 * e4m3 in route order
+// (xh [R_pad, H]), the row's FP32 global scale in xs; pos == NULL: row t to
+// row t (see quant.cu for the rule).
+cudaError_t launch_gather_a4(const void* x, bool x_bf16, int H, const int32_t* pos, int T, __half* xh, float* xs,
+                             uint32_t* status, cudaStream_t stream);
+// W4A4: rows of h (BF16 [R, I]) quantised to NVFP4 in place (as FP16), global
+// scales in hs.
+cudaError_t launch_rows_to_a4(void* h, int R, int I, float* hs, cudaStream_t stream);
+// The W4A4 quantiser on rows [rows, K] (FP32 or BF16): codes (one per byte),
+// block scales, global scales and FP16 values (test hook).
+cudaError_t launch_quantize_a4(const void* a, bool a_bf16, int rows, int K, uint8_t* codes, uint8_t* scales,
+                               float* global, __half* values, cudaStream_t stream);
 // wide: BF16 / FP8 down on one CTA per unit with 256-row units (two tiles per
 // k-block); fp8: E4M3 weights and activations (kind::f8f6f4); dec: NVFP4 with
 // chunks of at most 64 routes (4 epilogue warps, 12 converter warps)

@@ -52,7 +52,18 @@ typedef enum {
   BEAM_ERR_DEVICE_CHECK = 6  /* device: a kernel's own consistency check failed */
 } beam_status_t;
 
-typedef enum { BEAM_F32 = 0, BEAM_BF16 = 1, BEAM_NVFP4 = 2, BEAM_FP8 = 3 } beam_dtype_t;
+/* BEAM_NVFP4_A4 (expert weights only): the NVFP4 weights of BEAM_NVFP4 with
+ * the GEMM inputs quantised to NVFP4 at run time (W4A4): each row of x (as
+ * given) and of h (as stored in BF16) gets the weights' recipe per row:
+ * global scale g = amax / (6 * 448) in FP32 (1 for a zero row), an E4M3 scale
+ * s = E4M3((block max / 6) / g) per 16 consecutive elements and E2M1 codes of
+ * a / (s * g) (FP32 divisions and product, nearest even, saturating; code 0
+ * where s * g is 0), the element standing for e2m1 * s * g.  The launch post
+ * (section "Mixture of Experts") names NVFP4 as a weight format; this
+ * activation recipe is the library's reading.  The GEMMs multiply the
+ * quantised operands exactly (FP16 tensor cores, FP32 accumulation; not the
+ * block-scaled FP4 MMA).  Results move by tens of percent from W4A16's. */
+typedef enum { BEAM_F32 = 0, BEAM_BF16 = 1, BEAM_NVFP4 = 2, BEAM_FP8 = 3, BEAM_NVFP4_A4 = 4 } beam_dtype_t;
 
 /* Layer shape.  T tokens, hidden H, expert intermediate I, E experts in
  * n_group contiguous groups (group j = experts [j*E/n_group, (j+1)*E/n_group)),
@@ -97,7 +108,7 @@ typedef enum { BEAM_LAYOUT_ROWS = 0, BEAM_LAYOUT_TILED = 1 } beam_weight_layout_
  * (in `layout` order; BEAM_LAYOUT_ROWS when the field is zero-initialised).
  * Pointers the dtype does not use must be NULL. */
 typedef struct {
-  beam_dtype_t dtype; /* BEAM_BF16 or BEAM_NVFP4 */
+  beam_dtype_t dtype; /* BEAM_BF16, BEAM_NVFP4, BEAM_NVFP4_A4 (NVFP4 arrays) or BEAM_FP8 */
   const void* gate;
   const void* up;
   const void* down;
@@ -299,6 +310,18 @@ beam_status_t beam_moe_debug_timeout(void* workspace, size_t workspace_bytes, ui
  * Async on `stream`. */
 beam_status_t beam_debug_nvfp4_expand(const uint8_t* codes, const uint8_t* scales, int32_t n_blocks, uint16_t* out,
                                       void* stream);
+
+/* Test hook for the W4A4 activation quantiser (see BEAM_NVFP4_A4): quantises
+ * `rows` rows of K elements (a: device, FP32 or BF16 by a_dtype, row-major)
+ * with the device code the W4A4 forward runs on x and h.  codes: device,
+ * [rows, K] bytes, one E2M1 code per byte (bit 3 the sign); scales: device,
+ * [rows, K/16] E4M3 codes; global: device, [rows] FP32; values: device,
+ * [rows, K] FP16 bit patterns of e2m1 * e4m3 (what the GEMMs multiply; the
+ * global scale is applied after the sums).  K a positive multiple of 16; a and
+ * values 16-byte aligned, else BEAM_ERR_INVALID_ARG; a_dtype other than
+ * BEAM_F32 / BEAM_BF16: BEAM_ERR_UNSUPPORTED.  Async on `stream`. */
+beam_status_t beam_debug_quantize_nvfp4(const void* a, beam_dtype_t a_dtype, int32_t rows, int32_t K, uint8_t* codes,
+                                        uint8_t* scales, float* global, uint16_t* values, void* stream);
 
 /* Routing without a workspace, for callers that cannot allocate device memory
  * (a host framework that owns all device memory and hands a plugin only its

@@ -5,6 +5,7 @@ import os
 import re
 
 import pytest
+import torch
 
 import group_limited_routing_03_b300 as moe
 from group_limited_routing_03_b300 import _build
@@ -337,3 +338,27 @@ int main(void) {
                     "-lbeam_moe", "-Wl,-rpath," + libdir, "-o", str(exe)], check=True)
     r = subprocess.run([str(exe)], capture_output=True, text=True)
     assert r.returncode == 0, r.stdout + r.stderr
+
+
+def test_w4a4_shares_the_nvfp4_arrays_and_workspace(lib):
+    """BEAM_NVFP4_A4 (W4A4) takes the NVFP4 weight arrays and workspace; the
+    binding selects it with "activations": "nvfp4"."""
+    sh = _shape()
+    assert moe.workspace_size(sh, "nvfp4_a4") == moe.workspace_size(sh, "nvfp4") > 0
+    assert moe.workspace_layout(sh, "nvfp4_a4") == moe.workspace_layout(sh, "nvfp4")
+    codes = torch.zeros((256, 4, 8), dtype=torch.uint8)
+    assert moe._wdtype({"gate": codes}) == moe.BEAM_NVFP4
+    assert moe._wdtype({"gate": codes, "activations": "nvfp4"}) == moe.BEAM_NVFP4_A4
+    assert moe._wdtype("nvfp4_a4") == moe.BEAM_NVFP4_A4 == 4
+
+
+def test_quantize_hook_checks_its_arguments(lib):
+    """The W4A4 quantiser hook rejects bad arguments before any launch."""
+    fake = ctypes.c_void_p(1 << 16)  # never dereferenced: every call below fails its checks
+    call = lib.beam_debug_quantize_nvfp4
+    assert call(None, moe.BEAM_BF16, 4, 64, fake, fake, fake, fake, None) == moe.BEAM_ERR_INVALID_ARG
+    assert call(fake, moe.BEAM_BF16, 4, 40, fake, fake, fake, fake, None) == moe.BEAM_ERR_INVALID_ARG
+    assert call(fake, moe.BEAM_BF16, 0, 64, fake, fake, fake, fake, None) == moe.BEAM_ERR_INVALID_ARG
+    assert call(fake, moe.BEAM_FP8, 4, 64, fake, fake, fake, fake, None) == moe.BEAM_ERR_UNSUPPORTED
+    assert call(ctypes.c_void_p((1 << 16) + 8), moe.BEAM_BF16, 4, 64, fake, fake, fake, fake, None) == \
+        moe.BEAM_ERR_INVALID_ARG

@@ -168,6 +168,8 @@ def make_layer(wl, dev, layout=None):
     if (layout or WEIGHTS_LAYOUT) == "tiled":
         weights = moe.pack_weights(sh, d)
         torch.cuda.synchronize()
+    if wl.acts == "nvfp4":  # W4A4: the GEMM inputs quantised to NVFP4 at run time
+        weights = dict(weights, activations="nvfp4")
     ws = moe.alloc_workspace(sh, wl.w_dtype if wl.w_dtype in ("nvfp4", "fp8") else "bf16", dev)
     y = torch.empty((wl.T, wl.H), dtype=d["x"].dtype, device=dev)
     ids = torch.empty((wl.T, 8), dtype=torch.int32, device=dev)
@@ -313,6 +315,8 @@ def workload_record(name, steps, warmup, dev, world, pk, small, cpu_budget_s=Non
     hbm, tc = roofline(wl, m, pk)
     desc = {"bf16": "bf16 experts", "nvfp4": "nvfp4 experts (W4A16)",
             "fp8": "fp8 experts (E4M3 + row scales), E4M3 activations per row"}[wl.w_dtype]
+    if wl.acts == "nvfp4":
+        desc = "nvfp4 experts, NVFP4 activations per row (W4A4; FP16 tensor cores)"
     rec = dict(value=wl.T * steps * world / (t_ms * 1e-3), unit="tokens/s",
                config={"workload": f"{name} T={wl.T} H={wl.H} I={wl.I} E=256 {desc}" + (f", {note}" if note else ""),
                        "T": wl.T},
@@ -586,7 +590,8 @@ def oracle_sample(wl, d, budget_s=12.0, max_tokens=None):
             else:
                 mats[e] = ([host(d[n][e]) for n in ("gate", "up", "down")], {})
         t1 = time.perf_counter()
-        o = np.stack([oracle.expert_ffn(x[t:t + 1], *mats[int(e)][0], threads=threads, **mats[int(e)][1])[0]
+        ffn = oracle.expert_ffn_w4a4 if wl.acts == "nvfp4" else oracle.expert_ffn
+        o = np.stack([ffn(x[t:t + 1], *mats[int(e)][0], threads=threads, **mats[int(e)][1])[0]
                       for e in r["ids"][t]])[None]
         oracle.combine(r["weights"][t:t + 1], o)
         t_ffn += time.perf_counter() - t1
@@ -746,8 +751,10 @@ def main():
     fp8 = None
     if not args.no_fp8 and not args.small:
         fp8 = {}
-        for name, steps in (("fp8_decode", args.steps), ("fp8", max(3, args.steps // 2)), ("nvfp4_dec", args.steps)):
-            fp8[name] = workload_record(name, steps, args.warmup, dev, world, pk, {})
+        for name, steps in (("fp8_decode", args.steps), ("fp8", max(3, args.steps // 2)), ("nvfp4_dec", args.steps),
+                            ("nvfp4_a4", max(3, args.steps // 2))):
+            cpu = None if args.no_cpu_baseline or name != "nvfp4_a4" else 3.0  # the W4A4 oracle timed as well
+            fp8[name] = workload_record(name, steps, args.warmup, dev, world, pk, {}, cpu_budget_s=cpu)
 
     route_noalloc = None
     if not args.small:

@@ -18,6 +18,7 @@ decode     64      5120   2560   BF16 x, BF16 experts (~20 GB), FP32 router
 prefill    8192    5120   2560   same as decode, no router bias
 nvfp4      4096    5120   2560   BF16 x, NVFP4 experts, FP32 router
 nvfp4_dec  64      5120   2560   same as nvfp4 (decode)
+nvfp4_a4   4096    5120   2560   the nvfp4 inputs (seed 3), W4A4 GEMMs
 skew       32768   5120   2560   BF16, Zipf(1.1) router bias scaled to [0, 3]
 fp8        8192    5120   2560   BF16 x, FP8 experts (E4M3 + row scales, ~10 GB)
 fp8_decode 64      5120   2560   same as fp8
@@ -59,6 +60,7 @@ class Workload:
     seed: int
     bias: str  # "none" | "zipf"
     E: int = N_EXPERTS
+    acts: str = "native"  # "nvfp4": the GEMM inputs quantised to NVFP4 at run time (W4A4, NVFP4 weights)
 
     @property
     def routes(self) -> int:
@@ -74,6 +76,8 @@ WORKLOADS = {
     "fp8": Workload("fp8", 8192, 5120, 2560, "bf16", "fp8", 5, "none"),
     "fp8_decode": Workload("fp8_decode", 64, 5120, 2560, "bf16", "fp8", 6, "none"),
     "nvfp4_dec": Workload("nvfp4_dec", 64, 5120, 2560, "bf16", "nvfp4", 9, "none"),
+    # the nvfp4 layer's inputs (same seed) with W4A4 GEMMs
+    "nvfp4_a4": Workload("nvfp4_a4", 4096, 5120, 2560, "bf16", "nvfp4", 3, "none", acts="nvfp4"),
     "dense": Workload("dense", 8192, 5120, 20480, "bf16", "bf16", 7, "none", E=1),
     "dense_dec": Workload("dense_dec", 64, 5120, 20480, "bf16", "bf16", 8, "none", E=1),
 }

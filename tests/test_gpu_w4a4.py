@@ -19,7 +19,8 @@ import torch
 import group_limited_routing_03_b300 as moe
 import oracle
 from group_limited_routing_03_b300 import inputs
-from parity_helpers import Y_TOL, host_act, host_expert, oracle_y, rel_err, seeded_routing
+from parity_helpers import (Y_TOL, chunk_rows, full_size_tokens, host_act, host_expert, oracle_y, rel_err,
+                            seeded_routing)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -237,3 +238,29 @@ def test_w4a4_dense_mlp(T, H, I, pack):
     mats, kw = host_expert(dg, 0)
     y_ref = oracle.expert_ffn_w4a4(host_act(dg["x"]), *mats, **kw)
     assert rel_err(y.cpu().double().numpy(), y_ref) <= Y_TOL["nvfp4"]
+
+
+def test_w4a4_full_size():
+    """The W4A4 layer at the benchmark's size (nvfp4_a4: T=4096, the nvfp4
+    layer's inputs, packed weights as the benchmark runs them): outputs of the
+    tokens covering every touched expert and every chunk of the three most
+    loaded experts against the oracle's W4A4 experts with the GPU's routing
+    (the router, which does not see the expert format, is checked against the
+    oracle on these same inputs by the nvfp4 full-size test)."""
+    wl = inputs.workload("nvfp4_a4")
+    torch.cuda.empty_cache()
+    dg = inputs.generate(wl, DEV)
+    sh = moe.shape(wl.T, wl.H, wl.I)
+    packed = dict(moe.pack_weights(sh, dg), activations="nvfp4")
+    ws = moe.alloc_workspace(sh, "nvfp4_a4")
+    y = torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device=DEV)
+    ids = torch.empty((wl.T, 8), dtype=torch.int32, device=DEV)
+    w = torch.empty((wl.T, 8), dtype=torch.float32, device=DEV)
+    moe.beam_moe_forward(sh, dg["x"], dg["router_w"], None, packed, y, ids, w, ws)
+    code, where = moe.beam_moe_read_device_status(ws)
+    assert code == 0, (code, where)
+    ids_h, w_h = ids.cpu().numpy(), w.cpu().numpy().astype(np.float64)
+    tokens = full_size_tokens(ids_h, chunk_rows(wl.T, "nvfp4"))
+    y_ref = oracle_y_w4a4(dg, tokens, ids_h[tokens], w_h[tokens])
+    assert rel_err(y.cpu().double().numpy()[tokens], y_ref) <= Y_TOL["nvfp4"]
+    print(f"w4a4 full size: {len(tokens)} outputs compared")

@@ -23,10 +23,10 @@
 // 256 (gate/up) / 512 (down) rows, and 256 rows for two-tile down units; each
 // k-block issues its MMAs into two accumulators (gate and up, or two row
 // halves) where the unit has two tiles.  Units are numbered in the order
-// (expert, chunk, row tile, K part) and taken from a global counter in that
+// (expert, row tile, chunk, K part) and taken from a global counter in that
 // order by a persistent grid (one CTA, or CTA pair, per SM), so CTAs running
-// side by side share the token chunk (and, for several chunks of one expert,
-// the weight tiles) through L2.  A K range split into parts (few units for
+// side by side share the weight tile (for several chunks of one expert) and
+// the token chunks through L2.  A K range split into parts (few units for
 // many SMs) leaves FP32 partial sums that splitk.cu adds up.
 //
 // Warp roles (BF16 / FP8: 10 warps; NVFP4: 19 warps, 21 in the decode variant):
@@ -104,8 +104,11 @@ __device__ __forceinline__ Unit unit_at(const GemmParams& p, int u) {
   u /= p.k_splits;
   U.kb0 = U.ks * p.k_blocks / p.k_splits;
   U.kb1 = (U.ks + 1) * p.k_blocks / p.k_splits;
+  // Expert e owns units [chunk_prefix[e], chunk_prefix[e+1]) * m_tiles,
+  // numbered (row tile, chunk): the chunks of one weight tile are adjacent
+  // units, which the schedule starts side by side, so they read the tile's
+  // k-blocks from DRAM once and share them through L2.
   const int q = u / p.m_tiles;
-  U.m = u - q * p.m_tiles;
   // expert e with chunk_prefix[e] <= q < chunk_prefix[e+1]
   int lo = 0, hi = kExperts;  // invariant: chunk_prefix[lo] <= q < chunk_prefix[hi]
   while (hi - lo > 1) {
@@ -118,10 +121,12 @@ __device__ __forceinline__ Unit unit_at(const GemmParams& p, int u) {
   U.e = lo;
   // The expert's routes are cut into nch = ceil(count / nmax) chunks of
   // near-equal size (sizes differ by at most one), so the CTAs that run the
-  // chunks of one weight tile side by side progress in step and share the
-  // weight tile through L2.
-  const int c = q - __ldg(&p.chunk_prefix[lo]);
-  const int nch = __ldg(&p.chunk_prefix[lo + 1]) - __ldg(&p.chunk_prefix[lo]);
+  // chunks of one weight tile side by side progress in step.
+  const int cp0 = __ldg(&p.chunk_prefix[lo]);
+  const int nch = __ldg(&p.chunk_prefix[lo + 1]) - cp0;
+  const int local = u - cp0 * p.m_tiles;
+  U.m = local / nch;
+  const int c = local - U.m * nch;
   const int count = __ldg(&p.counts[lo]);
   const int base = count / nch, rem = count - base * nch;
   U.start = __ldg(&p.offsets[lo]) + c * base + (c < rem ? c : rem);

@@ -605,6 +605,32 @@ def oracle_sample(wl, d, budget_s=12.0, max_tokens=None):
                 near_ties=int((r["margin"] <= 1e-5).sum()), near_tie_tokens_of=wl.T)
 
 
+def line_problems(line: dict, full: bool = True) -> list:
+    """What the printed line lacks of the contract: the top-level keys and
+    their types, the roofline object, and (``full``) the cpu_baseline and e2e
+    objects.  Empty when the line is well formed."""
+    out = []
+    for k, t in (("metric", str), ("value", (int, float)), ("unit", str), ("n_gpus", int), ("steps", int),
+                 ("warmup", int), ("ms_per_step", (int, float)), ("higher_is_better", bool), ("scaling", str),
+                 ("dtype", str), ("data", str), ("config", dict), ("gpu_launches", int), ("clocks", dict)):
+        if not isinstance(line.get(k), t):
+            out.append(f"{k}: {type(line.get(k)).__name__}")
+    if not isinstance(line.get("config", {}).get("workload"), str):
+        out.append("config.workload missing")
+    r = line.get("roofline")
+    if not isinstance(r, dict) or not all(k in r for k in ("bound", "achieved", "peak", "unit", "frac", "traffic")):
+        out.append("roofline malformed")
+    if full:
+        c = line.get("cpu_baseline")
+        if not isinstance(c, dict) or not all(k in c for k in ("value", "unit", "cores", "kind", "sample")):
+            out.append(f"cpu_baseline malformed: {type(c).__name__}")
+        e = line.get("e2e")
+        if not isinstance(e, dict) or not all(k in e for k in ("value", "unit", "h2d_bytes_per_step",
+                                                               "d2h_bytes_per_step")):
+            out.append(f"e2e malformed: {type(e).__name__}")
+    return out
+
+
 def run_reference(args, rank, world):
     """Reference arm: the CPU oracle on the host cores (rank 0 only)."""
     if rank != 0:
@@ -753,8 +779,8 @@ def main():
         fp8 = {}
         for name, steps in (("fp8_decode", args.steps), ("fp8", max(3, args.steps // 2)), ("nvfp4_dec", args.steps),
                             ("nvfp4_a4", max(3, args.steps // 2))):
-            cpu = None if args.no_cpu_baseline or name != "nvfp4_a4" else 3.0  # the W4A4 oracle timed as well
-            fp8[name] = workload_record(name, steps, args.warmup, dev, world, pk, {}, cpu_budget_s=cpu)
+            budget = None if args.no_cpu_baseline or name != "nvfp4_a4" else 3.0  # the W4A4 oracle timed as well
+            fp8[name] = workload_record(name, steps, args.warmup, dev, world, pk, {}, cpu_budget_s=budget)
 
     route_noalloc = None
     if not args.small:
@@ -783,6 +809,9 @@ def main():
         "nvfp4": more.get("nvfp4"), "skew": more.get("skew"), "weight_formats": fp8, "dense": dense,
         "route_noalloc": route_noalloc,
     }
+    problems = line_problems(line, full=not (args.no_cpu_baseline or args.no_e2e))
+    if problems:
+        raise SystemExit("bench line malformed: " + "; ".join(problems))
     print(json.dumps(line), flush=True)
 
 

@@ -78,3 +78,19 @@ def test_code_hash_ignores_comments_only():
     assert bench.code_hash([a]) == bench.code_hash([b])
     assert bench.code_hash([a]) != bench.code_hash([a.replace("return 1", "return 2")])
     assert bench.code_hash([a]) != bench.code_hash([a.replace('"// kept"', '""')])
+
+
+def test_line_contract_check():
+    """bench.py refuses to print a line whose contract objects are malformed
+    (a stray float in cpu_baseline once slipped through)."""
+    good = {"metric": "m", "value": 1.0, "unit": "tokens/s", "n_gpus": 1, "steps": 5, "warmup": 3,
+            "ms_per_step": 2.4, "higher_is_better": True, "scaling": "weak", "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "decode"}, "gpu_launches": 40, "clocks": {"sm_mhz": 2032.0},
+            "roofline": {"bound": "hbm", "achieved": 1.0, "peak": 2.0, "unit": "GB/s", "frac": 0.5, "traffic": None},
+            "cpu_baseline": {"value": 4.0, "unit": "tokens/s", "cores": 16, "kind": "oracle", "sample": "s"},
+            "e2e": {"value": 1.0, "unit": "tokens/s", "h2d_bytes_per_step": 1, "d2h_bytes_per_step": 1}}
+    assert bench.line_problems(good) == []
+    assert bench.line_problems(dict(good, cpu_baseline=3.0)) == ["cpu_baseline malformed: float"]
+    assert bench.line_problems(dict(good, e2e=None), full=False) == []
+    assert bench.line_problems(dict(good, roofline={"bound": "hbm"}))
+    assert bench.line_problems(dict(good, gpu_launches=None))

@@ -39,12 +39,16 @@ def use_debug(debug_lib, monkeypatch):
 
 
 def _setup(w_dtype, T=40, H=512, I=256, seed=3):
-    wl = inputs.workload("nvfp4" if w_dtype == "nvfp4" else "tiny", T=T, H=H, I=I, x_dtype="bf16",
-                         w_dtype=w_dtype, seed=seed)
+    """w_dtype "nvfp4_a4": the NVFP4 weights with W4A4 GEMMs."""
+    fp4 = w_dtype in ("nvfp4", "nvfp4_a4")
+    wl = inputs.workload("nvfp4" if fp4 else "tiny", T=T, H=H, I=I, x_dtype="bf16",
+                         w_dtype="nvfp4" if fp4 else w_dtype, seed=seed)
     d = inputs.generate(wl, DEV)
     keys = ("gate", "up", "down") + (("gate_rs", "up_rs", "down_rs") if w_dtype == "fp8" else ()) + (
-        ("gate_sf", "up_sf", "down_sf", "gate_gs", "up_gs", "down_gs") if w_dtype == "nvfp4" else ())
+        ("gate_sf", "up_sf", "down_sf", "gate_gs", "up_gs", "down_gs") if fp4 else ())
     weights = {k: d[k] for k in keys}
+    if w_dtype == "nvfp4_a4":
+        weights["activations"] = "nvfp4"
     sh = moe.shape(T, H, I)
     ws = moe.alloc_workspace(sh, w_dtype)
     y = torch.empty((T, H), dtype=torch.bfloat16, device=DEV)
@@ -58,7 +62,7 @@ def _i32(ws, off, n):
     return ws[off:off + 4 * n].view(torch.int32)
 
 
-@pytest.mark.parametrize("w_dtype,where", [("bf16", 22), ("fp8", 26), ("nvfp4", 27)])
+@pytest.mark.parametrize("w_dtype,where", [("bf16", 22), ("fp8", 26), ("nvfp4", 27), ("nvfp4_a4", 27)])
 def test_bad_route_positions_before_the_gather(use_debug, w_dtype, where):
     sh, ws, y, call, lay = _setup(w_dtype)
     R = sh.T * 8
@@ -136,7 +140,7 @@ def test_expert_ids_out_of_range(use_debug):
     assert torch.equal(outs[0][0][keep.to(DEV)], outs[1][0][keep.to(DEV)])
 
 
-@pytest.mark.parametrize("w_dtype", ["bf16", "fp8", "nvfp4"])
+@pytest.mark.parametrize("w_dtype", ["bf16", "fp8", "nvfp4", "nvfp4_a4"])
 def test_debug_build_gives_the_release_bits(debug_lib, monkeypatch, w_dtype):
     release, dbg = debug_lib
     res = []

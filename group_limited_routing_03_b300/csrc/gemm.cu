@@ -26,8 +26,9 @@
 // (expert, row tile, chunk, K part) -- (expert, chunk, row tile, K part) for
 // experts with many chunks (see unit_at) -- and taken from a global counter in
 // that order by a persistent grid (one CTA, or CTA pair, per SM), so CTAs
-// running side by side share weight tiles and token chunks through L2.  A K range split into parts (few units for
-// many SMs) leaves FP32 partial sums that splitk.cu adds up.
+// running side by side share weight tiles and token chunks through L2.  A K
+// range split into parts (few units for many SMs) leaves FP32 partial sums
+// that splitk.cu adds up.
 //
 // Warp roles (BF16 / FP8: 10 warps; NVFP4: 19 warps, 21 in the decode variant):
 //   warp 0       TMA producer: weight tile(s) of 128 rows x 128 bytes and the

@@ -17,7 +17,9 @@
  * Conventions for every entry point:
  *   - All tensor pointers are DEVICE pointers, owned by the caller, row-major,
  *     16-byte aligned.  The library allocates no memory and keeps no state
- *     between calls other than a per-device cache of kernel attributes.
+ *     between calls other than a per-device cache of kernel attributes (and,
+ *     for beam_moe_route_noalloc only, a 6 MiB static device buffer whose
+ *     address is cached per CUDA context).
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls
  *     only enqueue work; none synchronises the host except
  *     beam_moe_read_device_status.
